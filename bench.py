@@ -1,0 +1,376 @@
+#!/usr/bin/env python
+"""Throughput of the fused linear logp forward + backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = ll_forward + ll_backward (grad_hidden and an FP32 grad_weight;
+no bias) over one batch of the benchmark workload: 4096 tokens, hidden 2048,
+vocab 32768, bf16 operands, synthetic seeded inputs.  Rank 0 prints one JSON
+line.  Inputs are resident in HBM for `value`; `e2e` adds, every step, the
+host->device copy of the step's hidden states / targets / upstream gradient
+from pinned memory and the device->host read of logp.  L2 is flushed between
+steps (a 512 MiB write outside the timed events).
+
+--impl reference times the FP64 CPU oracle on a bounded sample of the same
+workload (rank 0 only; other ranks exit at once).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tokens/sec fwd+bwd fused linear_logp (1 GB300) and % of BF16 tensor peak"
+WORKLOAD = "bf16_4k_2k_32k"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--token-chunks", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return os.cpu_count() or 1
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region (SM clock, throttle reasons)."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", delete=False, suffix=".csv")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.strip().split(",") for r in self.file.read().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx = float(r[1])
+                for nm, v in zip(names, r[3:7]):
+                    if v.strip().lower() == "active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        busy = [s for s in sm if s > 0.5 * (mx or max(sm))] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "cross_entropy_rl_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(phase: str):
+    """DRAM bytes per launch of `phase` from the committed ncu summary, if it
+    was taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(WORKLOAD, {}).get(phase)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def cpu_baseline(p, rows_target_s=12.0):
+    """The FP64 oracle on a bounded sample of the workload's rows."""
+    import numpy as np
+
+    import oracle
+
+    rows = 32
+    while True:
+        sel = np.arange(rows)
+        t0 = time.perf_counter()
+        oracle.linear_rows(p["gl"], p["h"], p["W"], p["b"], p["y"], p["dtype"], sel)
+        dt = time.perf_counter() - t0
+        if dt * 2 > rows_target_s or rows >= p["N"]:
+            break
+        rows = min(p["N"], max(rows * 2, int(rows * rows_target_s / max(dt, 1e-3) / 2)))
+    return {"value": rows / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{rows} of {p['N']} tokens (full vocab {p['V']}, hidden {p['D']}): "
+                      f"forward, grad_hidden and those tokens' grad_weight/grad_bias, "
+                      f"{dt:.2f} s"}
+
+
+def run_reference(args, rank):
+    """The oracle as the reference arm: each step is a bounded sample."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    from cross_entropy_rl_gb300 import synth
+
+    p = synth.linear_inputs(**synth.WORKLOADS[WORKLOAD], seed=0)
+    rows = 16
+    sel = np.arange(rows)
+    for _ in range(args.warmup):
+        oracle.linear_rows(p["gl"], p["h"], p["W"], p["b"], p["y"], p["dtype"], sel)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        s = (np.arange(rows) + i * rows) % p["N"]
+        oracle.linear_rows(p["gl"], p["h"], p["W"], p["b"], p["y"], p["dtype"], s)
+    t = time.perf_counter() - t0
+    v = rows * args.steps / t
+    out = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "N": p["N"], "D": p["D"], "V": p["V"],
+                      "bias": False, "grad_weight": "fp64",
+                      "step": f"{rows} tokens per step (bounded sample)"},
+           "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": blas_threads(),
+                            "kind": "oracle",
+                            "sample": f"{rows} tokens per step, {args.steps} steps"},
+           "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import cross_entropy_rl_gb300 as ll
+    from cross_entropy_rl_gb300 import synth
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    ll.load()
+    p = synth.linear_inputs(**synth.WORKLOADS[WORKLOAD], seed=rank)
+    N, D, V = p["N"], p["D"], p["V"]
+
+    def to_dev(a, bf16=False):
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if bf16 else torch.from_numpy(a)
+        return t.to(device)
+
+    h, W = to_dev(p["h"], True), to_dev(p["W"], True)
+    y, gl = to_dev(p["y"]), to_dev(p["gl"])
+    logp = torch.empty(N, dtype=torch.float32, device=device)
+    lse = torch.empty_like(logp)
+    dh = torch.empty(N, D, dtype=torch.bfloat16, device=device)
+    dW = torch.empty(V, D, dtype=torch.float32, device=device)
+    ws_f = torch.empty(max(256, ll.workspace_size(N, D, V, torch.bfloat16)),
+                       dtype=torch.uint8, device=device)
+    ws_b = torch.empty(max(256, ll.workspace_size(N, D, V, torch.bfloat16, args.token_chunks,
+                                                  backward=True)),
+                       dtype=torch.uint8, device=device)
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step(hh, yy, gg):
+        ll.forward(hh, W, None, yy, workspace=ws_f, out=(logp, lse))
+        ll.backward(gg, hh, W, None, yy, lse, need_dh=True, need_dw=True, need_db=False,
+                    token_chunks=args.token_chunks, workspace=ws_b, out=(dh, dW, None))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def timed_loop(fn, k):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(k)]
+        barrier()
+        torch.cuda.synchronize()
+        for i in range(k):
+            flush_buf.zero_()
+            evs[i][0].record(stream)
+            fn()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return sum(a.elapsed_time(b) for a, b in evs) / k
+
+    for _ in range(args.warmup):
+        step(h, y, gl)
+    torch.cuda.synchronize()
+    assert ll.check_status() == 0
+
+    clocks = Clocks(local_rank)
+    clocks.start()
+    n0 = ll.launch_count()
+    ms = timed_loop(lambda: step(h, y, gl), args.steps)
+    launches = ll.launch_count() - n0
+    clk = clocks.stop()
+    assert ll.check_status() == 0
+    if dist is not None:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * N / (ms * 1e-3)
+
+    # per-kernel durations: a second pass of the same steps with per-phase events
+    ll.profile(True)
+    timed_loop(lambda: step(h, y, gl), args.steps)
+    prof = ll.profile_summary()
+    ll.profile(False)
+
+    # end to end: per-step inputs from pinned host memory, logp read back
+    h_host = torch.empty(N, D, dtype=torch.bfloat16).pin_memory()
+    h_host.copy_(h.cpu())
+    y_host = y.cpu().pin_memory()
+    g_host = gl.cpu().pin_memory()
+    logp_host = torch.empty(N, dtype=torch.float32).pin_memory()
+    h2, y2, g2 = torch.empty_like(h), torch.empty_like(y), torch.empty_like(gl)
+
+    def e2e_step():
+        h2.copy_(h_host, non_blocking=True)
+        y2.copy_(y_host, non_blocking=True)
+        g2.copy_(g_host, non_blocking=True)
+        step(h2, y2, g2)
+        logp_host.copy_(logp, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    ms_e2e = timed_loop(e2e_step, args.steps)
+    if dist is not None:
+        t = torch.tensor([ms_e2e], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    if rank != 0:
+        return
+    pk, pk_kind = peaks()
+    flops = {"fwd_gemm": 2.0 * N * D * V, "recompute_gemm": 2.0 * N * D * V,
+             "dh_gemm": 2.0 * N * D * V, "dw_gemm": 2.0 * N * D * V}
+    gemms = {k: v for k, v in prof.items() if k in flops}
+    dom = max(gemms, key=lambda k: gemms[k][1])
+    cnt, tot = gemms[dom]
+    avg_ms = tot / cnt
+    achieved = flops[dom] / (avg_ms * 1e-3) / 1e12
+    peak = pk["bf16_tflops"]
+    useful = 6.0 * N * D * V / (ms * 1e-3) / 1e12
+    executed = 8.0 * N * D * V / (ms * 1e-3) / 1e12
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "N": N, "D": D, "V": V, "bias": False,
+                   "grad_weight": "fp32", "grad_hidden": "bf16",
+                   "token_chunks": args.token_chunks or "auto",
+                   "l2": "flushed between steps (512 MiB write outside the timed events)",
+                   "parallelism": f"dp{world}"},
+        "useful_tflops": useful, "useful_frac_of_bf16_peak": useful / peak,
+        "executed_tflops_incl_recompute": executed,
+        "peak_source": pk_kind,
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "frac_of_sustained": achieved / pk.get("bf16_tflops_sustained", peak),
+                     "traffic": ncu_traffic(dom), "avg_launch_ms": avg_ms,
+                     "flops_per_launch": flops[dom]},
+        "kernels_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},
+        "gpu_launches": launches,
+        "e2e": {"value": world * N / (ms_e2e * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h.numel() * 2 + y.numel() * 8 + gl.numel() * 4,
+                "d2h_bytes_per_step": logp.numel() * 4, "ms_per_step": ms_e2e},
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(p)
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,1 +1,247 @@
-"""GB300-native fused linear log-probability (see ``binding`` for the calls)."""
+"""GB300-native fused linear log-probability: thin Python binding.
+
+The computation runs in the CUDA library ``_lib/libll_gb300.so`` built from
+``csrc/`` (C ABI in ``include/ll_linear_logp.h``).  This module only
+marshals arguments: it takes torch tensors, allocates outputs and the scratch
+workspace with torch (the library itself never allocates), and passes raw
+pointers plus the current CUDA stream.  There is no fallback: every call
+raises when the library is missing or a call returns an error status.
+
+    import cross_entropy_rl_gb300 as ll
+    logp, lse = ll.forward(hidden, weight, bias, targets)
+    dh, dW, db = ll.backward(grad_logp, hidden, weight, bias, targets, lse)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "LLError", "load", "lib", "forward", "backward", "logits_fwd", "logits_bwd",
+    "workspace_size", "check_status", "DTYPE_CODES", "EXPORTS",
+]
+
+_LIB = None
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libll_gb300.so")
+
+# ll_dtype codes of the C ABI
+LL_F32, LL_F16, LL_BF16 = 0, 1, 2
+
+_c_i64 = ctypes.c_int64
+_c_p = ctypes.c_void_p
+_c_int = ctypes.c_int
+_c_size = ctypes.c_size_t
+
+# name -> (restype, argtypes): every symbol the header declares
+EXPORTS = {
+    "ll_status_string": (ctypes.c_char_p, [_c_int]),
+    "ll_version": (_c_int, []),
+    "ll_workspace_size": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_int, _c_int]),
+    "ll_forward": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_int,
+                            _c_p, _c_p, _c_p, _c_size, _c_p]),
+    "ll_backward": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64,
+                             _c_int, _c_int, _c_int, _c_int, _c_p, _c_int, _c_p, _c_int,
+                             _c_p, _c_int, _c_p, _c_size, _c_p]),
+    "logits_logp_fwd": (_c_int, [_c_p, _c_i64, _c_int, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_p]),
+    "logits_logp_bwd": (_c_int, [_c_p, _c_p, _c_i64, _c_int, _c_p, _c_p, _c_i64, _c_i64,
+                                 _c_p, _c_p]),
+    "ll_check_status": (_c_int, [_c_p]),
+    "ll_set_wait_limit_ns": (None, [_c_i64]),
+    "ll_debug_unsatisfied_wait": (_c_int, [_c_p, _c_p]),
+    "ll_launch_count": (ctypes.c_longlong, []),
+    "ll_profile_enable": (None, [_c_int]),
+    "ll_profile_summary": (_c_int, [ctypes.c_char_p, _c_size]),
+}
+
+
+class LLError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = "?"
+        if _LIB is not None:
+            msg = _LIB.ll_status_string(status).decode()
+        super().__init__(f"{fn} failed: status {status} ({msg})")
+        self.status = status
+
+
+def load(path: str | None = None):
+    """Load the shared library (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"CUDA library not built: {path} is missing "
+            "(run `python -m cross_entropy_rl_gb300.build`)")
+    lib_ = ctypes.CDLL(path)
+    for name, (res, args) in EXPORTS.items():
+        f = getattr(lib_, name)
+        f.restype = res
+        f.argtypes = args
+    _LIB = lib_
+    return _LIB
+
+
+def lib():
+    return load()
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _code(dtype) -> int:
+    torch = _torch()
+    m = {torch.float32: LL_F32, torch.float16: LL_F16, torch.bfloat16: LL_BF16}
+    if dtype not in m:
+        raise TypeError(f"unsupported dtype {dtype}")
+    return m[dtype]
+
+
+def DTYPE_CODES():
+    torch = _torch()
+    return {torch.float32: LL_F32, torch.float16: LL_F16, torch.bfloat16: LL_BF16}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, st: int):
+    if st != 0:
+        raise LLError(fn, st)
+
+
+def workspace_size(N, D, V, dtype, token_chunks=0, backward=False, need_db=False) -> int:
+    code = dtype if isinstance(dtype, int) else _code(dtype)
+    return int(load().ll_workspace_size(N, D, V, code, token_chunks, int(backward),
+                                        int(bool(need_db))))
+
+
+def _workspace(nbytes, device):
+    torch = _torch()
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def forward(hidden, weight, bias, targets, *, workspace=None, out=None, stream=None):
+    """(logp [N] fp32, lse [N] fp32) of z = hidden . weight^T (+ bias)."""
+    torch = _torch()
+    L = load()
+    N, D = hidden.shape
+    V = weight.shape[0]
+    code = _code(hidden.dtype)
+    if out is None:
+        logp = torch.empty(N, dtype=torch.float32, device=hidden.device)
+        lse = torch.empty(N, dtype=torch.float32, device=hidden.device)
+    else:
+        logp, lse = out
+    ws_need = L.ll_workspace_size(N, D, V, code, 0, 0, 0)
+    if workspace is None:
+        workspace = _workspace(ws_need, hidden.device)
+    st = L.ll_forward(_ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets), N, D, V, code,
+                      _ptr(logp), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("ll_forward", st)
+    return logp, lse
+
+
+def backward(grad_logp, hidden, weight, bias, targets, lse, *, need_dh=True, need_dw=True,
+             need_db=None, dh_dtype=None, dw_dtype=None, token_chunks=0, workspace=None,
+             out=None, stream=None):
+    """(grad_hidden, grad_weight, grad_bias); entries not requested are None.
+
+    dw_dtype defaults to float32; grad_bias uses dw_dtype.
+    """
+    torch = _torch()
+    L = load()
+    N, D = hidden.shape
+    V = weight.shape[0]
+    code = _code(hidden.dtype)
+    if need_db is None:
+        need_db = bias is not None
+    dh_dtype = hidden.dtype if dh_dtype is None else dh_dtype
+    dw_dtype = torch.float32 if dw_dtype is None else dw_dtype
+    dev = hidden.device
+    if out is not None:
+        dh, dW, db = out
+    else:
+        dh = torch.empty(N, D, dtype=dh_dtype, device=dev) if need_dh else None
+        dW = torch.empty(V, D, dtype=dw_dtype, device=dev) if need_dw else None
+        db = torch.empty(V, dtype=dw_dtype, device=dev) if need_db else None
+    ws_need = L.ll_workspace_size(N, D, V, code, token_chunks, 1, int(bool(need_db)))
+    if workspace is None:
+        workspace = _workspace(ws_need, dev)
+    st = L.ll_backward(_ptr(grad_logp), _ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets),
+                       _ptr(lse), N, D, V, code, int(bool(need_dh)), int(bool(need_dw)),
+                       int(bool(need_db)), _ptr(dh), _code(dh_dtype), _ptr(dW), _code(dw_dtype),
+                       _ptr(db), int(token_chunks), _ptr(workspace), workspace.numel(),
+                       _stream(stream))
+    _check("ll_backward", st)
+    return dh, dW, db
+
+
+def logits_fwd(logits, targets, V=None, *, out=None, stream=None):
+    """(logp, lse) from logits [N, ld]; columns >= V (default ld) ignored."""
+    torch = _torch()
+    L = load()
+    N, ld = logits.shape
+    V = ld if V is None else V
+    if logits.stride(1) != 1 or (N > 1 and logits.stride(0) != ld):
+        raise ValueError("logits must be row-major contiguous")
+    if out is None:
+        logp = torch.empty(N, dtype=torch.float32, device=logits.device)
+        lse = torch.empty(N, dtype=torch.float32, device=logits.device)
+    else:
+        logp, lse = out
+    st = L.logits_logp_fwd(_ptr(logits), ld, _code(logits.dtype), _ptr(targets), N, V,
+                           _ptr(logp), _ptr(lse), _stream(stream))
+    _check("logits_logp_fwd", st)
+    return logp, lse
+
+
+def logits_bwd(grad_logp, logits, targets, lse, V=None, *, out=None, stream=None):
+    """grad_logits [N, ld] in the logits dtype (columns [0, V) written)."""
+    torch = _torch()
+    L = load()
+    N, ld = logits.shape
+    V = ld if V is None else V
+    if out is None:
+        out = torch.empty_like(logits)
+    st = L.logits_logp_bwd(_ptr(grad_logp), _ptr(logits), ld, _code(logits.dtype),
+                           _ptr(targets), _ptr(lse), N, V, _ptr(out), _stream(stream))
+    _check("logits_logp_bwd", st)
+    return out
+
+
+def launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(load().ll_launch_count())
+
+
+def profile(enable: bool):
+    """Start (clearing earlier records) or stop per-phase CUDA-event tracing."""
+    load().ll_profile_enable(int(bool(enable)))
+
+
+def profile_summary() -> dict:
+    """{phase: (count, total_ms)} of the recorded phases (synchronises)."""
+    buf = ctypes.create_string_buffer(8192)
+    n = load().ll_profile_summary(buf, len(buf))
+    if n < 0:
+        raise LLError("ll_profile_summary", -n)
+    out = {}
+    for line in buf.value.decode().splitlines():
+        name, cnt, ms = line.split()
+        out[name] = (int(cnt), float(ms))
+    return out
+
+
+def check_status(stream=None) -> int:
+    """Synchronise and return (and clear) the device-side status word."""
+    return int(load().ll_check_status(_stream(stream)))

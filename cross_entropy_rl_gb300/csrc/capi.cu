@@ -1,0 +1,549 @@
+// C ABI of the fused linear log-probability library: argument validation,
+// device guard, workspace layout and the launch sequence of each call.
+// Declarations and the contract of every entry point: ll_linear_logp.h.
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "ll_internal.h"
+
+namespace ll {
+
+__device__ int g_ll_status;  // first device-side error since the last check
+
+static uint64_t g_wait_limit_ns = 2000000000ull;
+uint64_t wait_limit_ns() { return g_wait_limit_ns; }
+
+static std::atomic<long long> g_launches{0};
+void note_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// ------------------------------------------------------------------ tracing
+// When enabled, every phase of a call is bracketed by CUDA events recorded
+// on the call's stream; ll_profile_summary() aggregates them per phase.
+namespace {
+struct ProfRec {
+    const char* label;
+    cudaEvent_t a, b;
+};
+std::atomic<int> g_prof_on{0};
+std::mutex g_prof_mu;
+std::vector<ProfRec> g_prof;
+
+struct Phase {
+    const char* label;
+    cudaStream_t s;
+    cudaEvent_t a = nullptr, b = nullptr;
+    Phase(const char* l, cudaStream_t st) : label(l), s(st) {
+        if (!g_prof_on.load()) return;
+        if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) {
+            a = b = nullptr;
+            return;
+        }
+        cudaEventRecord(a, s);
+    }
+    ~Phase() {
+        if (!a) return;
+        cudaEventRecord(b, s);
+        std::lock_guard<std::mutex> lk(g_prof_mu);
+        g_prof.push_back({label, a, b});
+    }
+};
+}  // namespace
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+size_t esize(int dtype) { return dtype == LL_F32 ? 4 : 2; }
+bool dtype_ok(int dt) { return dt == LL_F32 || dt == LL_F16 || dt == LL_BF16; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+struct DevCache {
+    bool ready = false;
+    int num_sms = 0;
+    int* status = nullptr;
+    int cc_major = 0, cc_minor = 0;
+};
+DevCache g_dev[64];
+std::mutex g_dev_mu;
+
+// Switches to the device owning `ptr` for the lifetime of the guard.
+struct DeviceGuard {
+    int prev = -1;
+    int dev = -1;
+    int err = LL_OK;
+    explicit DeviceGuard(const void* ptr) {
+        cudaPointerAttributes attr;
+        if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
+            cudaGetLastError();
+            err = LL_ERR_INVALID_ARG;
+            return;
+        }
+        if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) {
+            err = LL_ERR_INVALID_ARG;
+            return;
+        }
+        dev = attr.device;
+        if (dev < 0 || dev >= 64) {
+            err = LL_ERR_INVALID_ARG;
+            return;
+        }
+        if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) {
+            err = LL_ERR_CUDA;
+            return;
+        }
+    }
+    ~DeviceGuard() {
+        if (prev >= 0 && prev != dev) cudaSetDevice(prev);
+    }
+};
+
+int device_info(int dev, DevInfo* out) {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DevCache& c = g_dev[dev];
+    if (!c.ready) {
+        if (cudaDeviceGetAttribute(&c.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return LL_ERR_CUDA;
+        cudaDeviceGetAttribute(&c.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&c.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_ll_status) != cudaSuccess) {
+            cudaGetLastError();
+            return LL_ERR_UNSUPPORTED;
+        }
+        c.status = static_cast<int*>(p);
+        c.ready = true;
+    }
+    if (!(c.cc_major == 10 && c.cc_minor == 3)) return LL_ERR_UNSUPPORTED;
+    out->device = dev;
+    out->num_sms = c.num_sms;
+    out->status = c.status;
+    return LL_OK;
+}
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return LL_OK;
+    fprintf(stderr, "ll: CUDA error %s\n", cudaGetErrorString(e));
+    return LL_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- layouts
+struct FwdLayout {
+    int64_t n_segs;
+    size_t part_m, part_s, zy, total;
+};
+FwdLayout fwd_layout(int64_t N, int64_t V) {
+    FwdLayout L;
+    L.n_segs = cdiv(cdiv(V, kBN), kVocabTilesPerSeg);
+    size_t off = 0;
+    L.part_m = off;
+    off = align_up(off + size_t(L.n_segs) * size_t(N) * 4);
+    L.part_s = off;
+    off = align_up(off + size_t(L.n_segs) * size_t(N) * 4);
+    L.zy = off;
+    off = align_up(off + size_t(N) * 4);
+    L.total = N == 0 ? 0 : off;
+    return L;
+}
+
+constexpr size_t kAutoChunkBytes = size_t(2) << 30;  // softmax workspace budget
+
+struct BwdLayout {
+    int64_t chunks, Nc, ldS;
+    size_t S, keys, offs, db, total;
+};
+BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need_db) {
+    BwdLayout L;
+    L.ldS = round_up(V, 8);
+    const size_t row_bytes = size_t(L.ldS) * esize(dtype);
+    const int64_t n1 = N > 0 ? N : 1;
+    int64_t k = token_chunks;
+    if (k <= 0) {
+        k = 1;
+        while (size_t(round_up(cdiv(n1, k), kBM)) * row_bytes > kAutoChunkBytes && k < n1) ++k;
+    }
+    if (k > n1) k = n1;
+    L.Nc = token_chunks > 0 ? cdiv(n1, k) : round_up(cdiv(n1, k), kBM);
+    if (L.Nc > n1) L.Nc = n1;
+    L.chunks = cdiv(n1, L.Nc);
+    size_t off = 0;
+    L.S = off;
+    off = align_up(off + size_t(L.Nc) * row_bytes);
+    L.keys = off;
+    off = align_up(off + token_sort_bytes(n1));
+    L.offs = off;
+    off = align_up(off + size_t(V + 1) * 4);
+    L.db = off;
+    if (need_db) off = align_up(off + db_partial_bytes(L.Nc, V));
+    L.total = off;
+    return L;
+}
+
+int check_sizes(int64_t N, int64_t D, int64_t V) {
+    if (N < 0 || D < 1 || V < 1) return LL_ERR_SHAPE;
+    if (V > kMaxV || N > (int64_t(1) << 31) - 256 || D > (int64_t(1) << 31) - 256)
+        return LL_ERR_SHAPE;
+    return LL_OK;
+}
+
+}  // namespace
+}  // namespace ll
+
+using namespace ll;
+
+extern "C" {
+
+const char* ll_status_string(int status) {
+    switch (status) {
+        case LL_OK: return "ok";
+        case LL_ERR_INVALID_ARG: return "invalid argument";
+        case LL_ERR_DTYPE: return "unsupported dtype";
+        case LL_ERR_SHAPE: return "invalid shape";
+        case LL_ERR_ALIGN: return "misaligned pointer or stride";
+        case LL_ERR_WORKSPACE: return "workspace missing or too small";
+        case LL_ERR_CUDA: return "CUDA error";
+        case LL_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case LL_ERR_UNSUPPORTED: return "unsupported device";
+        default: return "unknown status";
+    }
+}
+
+int ll_version(void) { return 100; }
+
+size_t ll_workspace_size(int64_t N, int64_t D, int64_t V, int dtype, int token_chunks,
+                         int is_backward, int flags) {
+    (void)D;
+    if (N < 0 || V < 1 || !dtype_ok(dtype)) return 0;
+    if (!is_backward) return fwd_layout(N, V).total;
+    return bwd_layout(N, V, dtype, token_chunks, flags & 1).total;
+}
+
+void ll_set_wait_limit_ns(int64_t ns) { g_wait_limit_ns = ns > 0 ? uint64_t(ns) : 2000000000ull; }
+
+int ll_forward(const void* hidden, const void* weight, const void* bias, const int64_t* targets,
+               int64_t N, int64_t D, int64_t V, int dtype, float* logp, float* lse,
+               void* workspace, size_t ws_bytes, void* stream) {
+    int st = check_sizes(N, D, V);
+    if (st) return st;
+    if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
+    if (!weight) return LL_ERR_INVALID_ARG;
+    if (N == 0) return LL_OK;
+    if (!hidden || !targets || !logp || !lse) return LL_ERR_INVALID_ARG;
+    if (D % 8 != 0 || !aligned16(hidden) || !aligned16(weight)) return LL_ERR_ALIGN;
+    const FwdLayout L = fwd_layout(N, V);
+    if (!workspace || ws_bytes < L.total) return LL_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return LL_ERR_WORKSPACE;
+    DeviceGuard guard(hidden);
+    if (guard.err) return guard.err;
+    DevInfo dev;
+    if ((st = device_info(guard.dev, &dev))) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    float* part_m = reinterpret_cast<float*>(ws + L.part_m);
+    float* part_s = reinterpret_cast<float*>(ws + L.part_s);
+    float* zy = reinterpret_cast<float*>(ws + L.zy);
+
+    GemmShape sh;
+    sh.m_blocks = cdiv(N, kBM);
+    sh.n_tiles = cdiv(V, kBN);
+    sh.tiles_per_unit = kVocabTilesPerSeg;
+    sh.n_segs = L.n_segs;
+    sh.k_blocks = cdiv(D, 64);
+    sh.unit_order = 0;
+    EpiArgs ea;
+    memset(&ea, 0, sizeof(ea));
+    ea.M = N;
+    ea.Ncols = V;
+    ea.V = V;
+    ea.targets = targets;
+    ea.bias = bias;
+    ea.part_m = part_m;
+    ea.part_s = part_s;
+    ea.zy = zy;
+    ea.part_ld = N;
+    ea.status = dev.status;
+    ea.wait_ns = wait_limit_ns();
+    cudaError_t e;
+    {
+        Phase ph(dtype == LL_F32 ? "fwd_gemm_f32" : "fwd_gemm", s);
+        e = launch_gemm(EpiKind::Fwd, dtype, hidden, D, 0, weight, D, 0, N, V, D, sh, ea, dev, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    {
+        Phase ph("lse_merge", s);
+        e = launch_lse_merge(part_m, part_s, zy, N, L.n_segs, targets, N, V, logp, lse, s);
+    }
+    return cuda_status(e);
+}
+
+int ll_backward(const float* grad_logp, const void* hidden, const void* weight, const void* bias,
+                const int64_t* targets, const float* lse, int64_t N, int64_t D, int64_t V,
+                int dtype, int need_dh, int need_dw, int need_db, void* grad_hidden,
+                int dh_dtype, void* grad_weight, int dw_dtype, void* grad_bias,
+                int token_chunks, void* workspace, size_t ws_bytes, void* stream) {
+    int st = check_sizes(N, D, V);
+    if (st) return st;
+    if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
+    if ((need_dh | need_dw | need_db) & ~1) return LL_ERR_INVALID_ARG;
+    if (token_chunks < 0) return LL_ERR_INVALID_ARG;
+    if (need_dh && !(dh_dtype == dtype || dh_dtype == LL_F32)) return LL_ERR_DTYPE;
+    if ((need_dw || need_db) && !(dw_dtype == dtype || dw_dtype == LL_F32)) return LL_ERR_DTYPE;
+    if (!weight) return LL_ERR_INVALID_ARG;
+    if (need_dw && !grad_weight) return LL_ERR_INVALID_ARG;
+    if (need_db && !grad_bias) return LL_ERR_INVALID_ARG;
+    if (need_dh && N > 0 && !grad_hidden) return LL_ERR_INVALID_ARG;
+    if (D % 8 != 0 || !aligned16(weight)) return LL_ERR_ALIGN;
+    if (need_dw && !aligned16(grad_weight)) return LL_ERR_ALIGN;
+    if (!need_dh && !need_dw && !need_db) return LL_OK;
+
+    DeviceGuard guard(weight);
+    if (guard.err) return guard.err;
+    DevInfo dev;
+    if ((st = device_info(guard.dev, &dev))) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+
+    if (N == 0) {  // empty batch: requested table gradients are +0
+        if (need_dw) e = launch_fill_zero(grad_weight, V * D, dw_dtype, s);
+        if (e == cudaSuccess && need_db) e = launch_fill_zero(grad_bias, V, dw_dtype, s);
+        return cuda_status(e);
+    }
+    if (!grad_logp || !hidden || !targets || !lse) return LL_ERR_INVALID_ARG;
+    if (!aligned16(hidden) || (need_dh && !aligned16(grad_hidden))) return LL_ERR_ALIGN;
+    const BwdLayout L = bwd_layout(N, V, dtype, token_chunks, need_db);
+    if (!workspace || ws_bytes < L.total) return LL_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return LL_ERR_WORKSPACE;
+
+    char* ws = static_cast<char*>(workspace);
+    void* S = ws + L.S;
+    int64_t* keys = reinterpret_cast<int64_t*>(ws + L.keys);
+    int* offs = reinterpret_cast<int*>(ws + L.offs);
+    float* db_part = reinterpret_cast<float*>(ws + L.db);
+    const int64_t db_groups_v = (L.Nc < 64 ? L.Nc : 64) * V;
+    float* db_acc = db_part + db_groups_v;
+    const size_t es = esize(dtype);
+
+    if (need_dw || need_db) {
+        Phase ph("token_sort", s);
+        e = launch_token_sort(targets, N, V, keys, offs, s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+
+    EpiArgs base;
+    memset(&base, 0, sizeof(base));
+    base.V = V;
+    base.bias = bias;
+    base.status = dev.status;
+    base.wait_ns = wait_limit_ns();
+
+    for (int64_t c = 0; c < L.chunks; ++c) {
+        const int64_t r0 = c * L.Nc;
+        const int64_t rows = (N - r0) < L.Nc ? (N - r0) : L.Nc;
+        const char* h_c = static_cast<const char*>(hidden) + size_t(r0) * size_t(D) * es;
+
+        // (1) recompute z for the chunk, store S = -grad * softmax
+        {
+            GemmShape sh;
+            sh.m_blocks = cdiv(rows, kBM);
+            sh.n_tiles = cdiv(V, kBN);
+            sh.tiles_per_unit = kVocabTilesPerSeg;
+            sh.n_segs = cdiv(sh.n_tiles, sh.tiles_per_unit);
+            sh.k_blocks = cdiv(D, 64);
+            sh.unit_order = 0;
+            EpiArgs ea = base;
+            ea.M = rows;
+            ea.Ncols = V;
+            ea.targets = targets + r0;
+            ea.lse = lse + r0;
+            ea.grad = grad_logp + r0;
+            ea.S = S;
+            ea.ldS = L.ldS;
+            Phase ph(dtype == LL_F32 ? "recompute_gemm_f32" : "recompute_gemm", s);
+            e = launch_gemm(EpiKind::Recomp, dtype, h_c, D, 0, weight, D, 0, rows, V, D, sh, ea,
+                            dev, s);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        // (2) grad_hidden rows of the chunk: S . W + grad * W[y]
+        if (need_dh) {
+            GemmShape sh;
+            sh.m_blocks = cdiv(rows, kBM);
+            sh.n_tiles = cdiv(D, kBN);
+            sh.tiles_per_unit = 1;
+            sh.n_segs = sh.n_tiles;
+            sh.k_blocks = cdiv(V, 64);
+            sh.unit_order = 0;
+            EpiArgs ea = base;
+            ea.M = rows;
+            ea.Ncols = D;
+            ea.targets = targets + r0;
+            ea.grad = grad_logp + r0;
+            ea.W = weight;
+            ea.ldW = D;
+            ea.out = static_cast<char*>(grad_hidden) + size_t(r0) * size_t(D) * esize(dh_dtype);
+            ea.ld_out = D;
+            ea.out_dtype = dh_dtype;
+            Phase ph(dtype == LL_F32 ? "dh_gemm_f32" : "dh_gemm", s);
+            e = launch_gemm(EpiKind::Dh, dtype, S, L.ldS, 0, weight, D, 1, rows, D, V, sh, ea,
+                            dev, s);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        // (3) grad_weight += S^T . h (+ one-hot part on the last chunk)
+        if (need_dw) {
+            GemmShape sh;
+            sh.m_blocks = cdiv(V, kBM);
+            sh.n_tiles = cdiv(D, kBN);
+            sh.tiles_per_unit = 1;
+            sh.n_segs = sh.n_tiles;
+            sh.k_blocks = cdiv(rows, 64);
+            sh.unit_order = 1;
+            EpiArgs ea = base;
+            ea.M = V;
+            ea.Ncols = D;
+            ea.out = grad_weight;
+            ea.ld_out = D;
+            ea.out_dtype = dw_dtype;
+            ea.first_chunk = c == 0;
+            ea.last_chunk = c == L.chunks - 1;
+            ea.offs = offs;
+            ea.keys = keys;
+            ea.grad_all = grad_logp;
+            ea.h_all = hidden;
+            ea.ld_h = D;
+            Phase ph(dtype == LL_F32 ? "dw_gemm_f32" : "dw_gemm", s);
+            e = launch_gemm(EpiKind::Dw, dtype, S, L.ldS, 1, h_c, D, 1, V, D, rows, sh, ea, dev,
+                            s);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        // (4) grad_bias: fixed-order column sums of S (+ one-hot part at the end)
+        if (need_db) {
+            Phase ph("db_sums", s);
+            e = launch_db_chunk(S, L.ldS, dtype, rows, V, db_part, db_acc, c == 0,
+                                c == L.chunks - 1, offs, keys, grad_logp, grad_bias, dw_dtype, s);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+    }
+    return LL_OK;
+}
+
+int logits_logp_fwd(const void* logits, int64_t ld, int dtype, const int64_t* targets, int64_t N,
+                    int64_t V, float* logp, float* lse, void* stream) {
+    if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
+    if (N < 0 || V < 1 || V > kMaxV || ld < V || N > (int64_t(1) << 31) - 1) return LL_ERR_SHAPE;
+    if (N == 0) return LL_OK;
+    if (!logits || !targets || !logp || !lse) return LL_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(logits) % esize(dtype)) return LL_ERR_ALIGN;
+    DeviceGuard guard(logits);
+    if (guard.err) return guard.err;
+    DevInfo dev;
+    int st = device_info(guard.dev, &dev);
+    if (st) return st;
+    Phase ph("logits_fwd", static_cast<cudaStream_t>(stream));
+    return cuda_status(launch_logits_fwd(logits, ld, dtype, targets, N, V, logp, lse,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+int logits_logp_bwd(const float* grad_logp, const void* logits, int64_t ld, int dtype,
+                    const int64_t* targets, const float* lse, int64_t N, int64_t V,
+                    void* grad_logits, void* stream) {
+    if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
+    if (N < 0 || V < 1 || V > kMaxV || ld < V || N > (int64_t(1) << 31) - 1) return LL_ERR_SHAPE;
+    if (N == 0) return LL_OK;
+    if (!grad_logp || !logits || !targets || !lse || !grad_logits) return LL_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(logits) % esize(dtype) ||
+        reinterpret_cast<uintptr_t>(grad_logits) % esize(dtype))
+        return LL_ERR_ALIGN;
+    const char* a = static_cast<const char*>(logits);
+    const char* b = static_cast<const char*>(grad_logits);
+    const size_t span = size_t(N) * size_t(ld) * esize(dtype);
+    if (a < b + span && b < a + span) return LL_ERR_INVALID_ARG;  // no aliasing
+    DeviceGuard guard(logits);
+    if (guard.err) return guard.err;
+    DevInfo dev;
+    int st = device_info(guard.dev, &dev);
+    if (st) return st;
+    Phase ph("logits_bwd", static_cast<cudaStream_t>(stream));
+    return cuda_status(launch_logits_bwd(grad_logp, logits, ld, dtype, targets, lse, N, V,
+                                         grad_logits, static_cast<cudaStream_t>(stream)));
+}
+
+int ll_check_status(void* stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return LL_ERR_CUDA;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return cuda_status(cudaGetLastError());
+    DevInfo info;
+    int st = device_info(dev, &info);
+    if (st) return st;
+    int v = 0;
+    if (cudaMemcpy(&v, info.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return LL_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        cudaMemcpy(info.status, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    }
+    return v;
+}
+
+long long ll_launch_count(void) { return g_launches.load(); }
+
+void ll_profile_enable(int on) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    for (auto& r : g_prof) {
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    g_prof.clear();
+    g_prof_on.store(on ? 1 : 0);
+}
+
+int ll_profile_summary(char* buf, size_t len) {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    std::vector<std::string> labels;
+    std::vector<double> total;
+    std::vector<long> count;
+    for (auto& r : g_prof) {
+        if (cudaEventSynchronize(r.b) != cudaSuccess) return -LL_ERR_CUDA;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) return -LL_ERR_CUDA;
+        size_t i = 0;
+        while (i < labels.size() && labels[i] != r.label) ++i;
+        if (i == labels.size()) {
+            labels.push_back(r.label);
+            total.push_back(0.0);
+            count.push_back(0);
+        }
+        total[i] += ms;
+        count[i] += 1;
+    }
+    std::string out;
+    char line[160];
+    for (size_t i = 0; i < labels.size(); ++i) {
+        snprintf(line, sizeof(line), "%s %ld %.6f\n", labels[i].c_str(), count[i], total[i]);
+        out += line;
+    }
+    if (buf && len) {
+        strncpy(buf, out.c_str(), len - 1);
+        buf[len - 1] = 0;
+    }
+    return static_cast<int>(labels.size());
+}
+
+int ll_debug_unsatisfied_wait(int* device_flag, void* stream) {
+    if (!device_flag) return LL_ERR_INVALID_ARG;
+    DeviceGuard guard(device_flag);
+    if (guard.err) return guard.err;
+    DevInfo dev;
+    int st = device_info(guard.dev, &dev);
+    if (st) return st;
+    return cuda_status(launch_unsatisfied_wait(device_flag, dev.status, wait_limit_ns(),
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

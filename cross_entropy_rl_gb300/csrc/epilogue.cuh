@@ -1,0 +1,199 @@
+// Fused GEMM epilogues of the linear log-probability path.
+//
+// Each epilogue thread owns one row of the output tile (one TMEM lane on the
+// tensor-core path) and sees that row in chunks of 32 consecutive columns.
+// The four kinds:
+//
+//   Fwd     z = h W^T (+b) tile -> running max / rescaled sum-exp of the row
+//           over the vocab tiles of one segment (online softmax), target
+//           logit picked up when it falls in the tile.  Per-segment partials
+//           are merged afterwards in ascending segment order.
+//   Recomp  the same z tile recomputed -> p = exp(z - lse), stores the
+//           softmax part of g, S = -grad_logp * p, to the chunk workspace.
+//   Dh      acc = S . W tile -> adds the one-hot part grad_logp * W[y] in
+//           FP32 and stores grad_hidden.
+//   Dw      acc = S^T . h tile -> adds the running grad_weight (FP32 +0
+//           start on the first token chunk) and, on the last chunk, the
+//           one-hot part sum over tokens with target v of grad_logp * h, in
+//           ascending token order.
+//
+// The split of g = grad_logp * (onehot - p) into the exact FP32 one-hot part
+// and the small softmax part S keeps the 16-bit rounding of S far below the
+// gradient tolerances.  Zero rules (issue #261, "Correctness boundary"):
+// rows with an invalid target or a zero upstream gradient store exact +0;
+// sums start from +0.
+#pragma once
+#include "ll_device.cuh"
+
+namespace ll {
+
+// Storage tag that selects T in the run-time-typed loads and stores below.
+template <typename T>
+constexpr int own_tag() { return sizeof(T) == 4 ? LL_F32 : LL_BF16; }
+
+template <typename T>
+__device__ __forceinline__ float ld_elem(const void* p, int64_t i) {
+    return Elem<T>::to_f(static_cast<const T*>(p)[i]);
+}
+
+// Store 32 values to p[0..31] (16-byte aligned), dtype chosen at run time
+// (LL_F32 or the 16-bit type T); only 8-element groups below `limit`.
+template <typename T>
+__device__ __forceinline__ void store_row32(void* base, int64_t idx, const float (&v)[32],
+                                            int64_t col0, int64_t limit, int out_dtype) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if (col0 + 8 * g >= limit) break;
+        float f[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = v[8 * g + j];
+        if (out_dtype == LL_F32)
+            store8(static_cast<float*>(base) + idx + 8 * g, f);
+        else
+            store8(static_cast<T*>(base) + idx + 8 * g, f);
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void load_row32(const void* base, int64_t idx, float (&v)[32],
+                                           int64_t col0, int64_t limit, int in_dtype) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (col0 + 8 * g < limit) {
+            if (in_dtype == LL_F32)
+                load8(static_cast<const float*>(base) + idx + 8 * g, f);
+            else
+                load8(static_cast<const T*>(base) + idx + 8 * g, f);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[8 * g + j] = f[j];
+    }
+}
+
+template <EpiKind E, typename T>
+struct RowEpilogue {
+    int64_t row;   // row in the M dimension of the launch
+    bool rvalid;
+    int64_t y;
+    float coef;    // Recomp: -grad (0 for dead rows); Dh: grad (0 for dead rows)
+    float lse2;    // Recomp: lse * log2(e)
+    float m2, s;   // Fwd: running max (log2 units) and sum
+    float zyv;
+    bool found;
+    int oh_beg, oh_end;  // Dw: one-hot token range in the sorted key list
+
+    __device__ __forceinline__ void begin_unit(const EpiArgs& ea, int64_t row_) {
+        row = row_;
+        rvalid = row < ea.M;
+        if constexpr (E == EpiKind::Fwd) {
+            m2 = -INFINITY;
+            s = 0.f;
+            found = false;
+            zyv = 0.f;
+            y = rvalid ? ea.targets[row] : -1;
+        } else if constexpr (E == EpiKind::Recomp || E == EpiKind::Dh) {
+            y = rvalid ? ea.targets[row] : -1;
+            const float g = rvalid ? ea.grad[row] : 0.f;
+            const bool live = rvalid && y >= 0 && y < ea.V && g != 0.f;
+            coef = live ? (E == EpiKind::Recomp ? -g : g) : 0.f;
+            if constexpr (E == EpiKind::Recomp) lse2 = rvalid ? ea.lse[row] * kLog2e : 0.f;
+        } else {  // Dw: row is a vocab index
+            oh_beg = oh_end = 0;
+            if (ea.last_chunk && rvalid) {
+                oh_beg = ea.offs[row];
+                oh_end = ea.offs[row + 1];
+            }
+        }
+    }
+
+    __device__ __forceinline__ void chunk(const EpiArgs& ea, float (&v)[32], int64_t col0) {
+        if constexpr (E == EpiKind::Fwd || E == EpiKind::Recomp) {
+            const int64_t V = ea.Ncols;
+            if (ea.bias) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (col0 + j < V) v[j] += ld_elem<T>(ea.bias, col0 + j);
+            }
+            if constexpr (E == EpiKind::Fwd) {
+                if (col0 + 32 > V) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (col0 + j >= V) v[j] = -INFINITY;
+                }
+                const int64_t off = y - col0;
+                if (off >= 0 && off < 32) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j == off) zyv = v[j];
+                    found = true;
+                }
+                float cmax = v[0];
+#pragma unroll
+                for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, v[j]);
+                const float mu = cmax * kLog2e;
+                if (mu > m2) {
+                    s = s * ex2(m2 - mu);
+                    m2 = mu;
+                }
+                if (m2 != -INFINITY) {
+                    float acc = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) acc += ex2(fmaf(v[j], kLog2e, -m2));
+                    s += acc;
+                }
+            } else {  // Recomp: S = -grad * exp(z - lse)
+                if (!rvalid) return;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = coef * ex2(fmaf(v[j], kLog2e, -lse2));
+                store_row32<T>(ea.S, row * ea.ldS + col0, v, col0, V, own_tag<T>());
+            }
+        } else if constexpr (E == EpiKind::Dh) {
+            if (!rvalid) return;
+            const int64_t D = ea.Ncols;
+            if (coef != 0.f) {
+                float w[32];
+                load_row32<T>(ea.W, y * ea.ldW + col0, w, col0, D, own_tag<T>());
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = fmaf(coef, w[j], v[j]) + 0.f;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+            store_row32<T>(ea.out, row * ea.ld_out + col0, v, col0, D, ea.out_dtype);
+        } else {  // Dw
+            if (!rvalid) return;
+            const int64_t D = ea.Ncols;
+            if (ea.first_chunk) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f + v[j];
+            } else {
+                float prev[32];
+                load_row32<T>(ea.out, row * ea.ld_out + col0, prev, col0, D, ea.out_dtype);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = prev[j] + v[j];
+            }
+            for (int i = oh_beg; i < oh_end; ++i) {
+                const int64_t n = static_cast<int64_t>(ea.keys[i] & 0xffffffffll);
+                const float g = ea.grad_all[n];
+                if (g == 0.f) continue;
+                float hv[32];
+                load_row32<T>(ea.h_all, n * ea.ld_h + col0, hv, col0, D, own_tag<T>());
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = fmaf(g, hv[j], v[j]);
+            }
+            store_row32<T>(ea.out, row * ea.ld_out + col0, v, col0, D, ea.out_dtype);
+        }
+    }
+
+    __device__ __forceinline__ void end_unit(const EpiArgs& ea, int64_t seg) {
+        if constexpr (E == EpiKind::Fwd) {
+            if (!rvalid) return;
+            ea.part_m[seg * ea.part_ld + row] = m2;
+            ea.part_s[seg * ea.part_ld + row] = s;
+            if (found) ea.zy[row] = zyv;
+        }
+    }
+};
+
+}  // namespace ll

@@ -1,0 +1,115 @@
+// Internal host-side interface between the C ABI (capi.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/ll_linear_logp.h"
+
+namespace ll {
+
+// Tile shape of the tensor-core GEMMs (M rows x N columns per output tile,
+// K elements per pipeline stage for 16-bit operands).
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kVocabTilesPerSeg = 4;  // vocab tiles per LSE segment (1024 vocab)
+
+// Maximum vocab size: inner indices within a row stay below 2^31.
+constexpr int64_t kMaxV = (int64_t(1) << 31) - 1 - 256;
+
+struct DevInfo {
+    int device;
+    int num_sms;
+    int* status;  // device status word (static device storage)
+};
+
+// Wait limit for bounded device-side waits, nanoseconds.
+uint64_t wait_limit_ns();
+
+// Count of kernels this library has launched (for launch accounting).
+void note_launches(int n);
+
+// --- logits-input kernels (logits_kernels.cu) --------------------------------
+cudaError_t launch_logits_fwd(const void* logits, int64_t ld, int dtype, const int64_t* targets,
+                              int64_t N, int64_t V, float* logp, float* lse, cudaStream_t s);
+cudaError_t launch_logits_bwd(const float* grad, const void* logits, int64_t ld, int dtype,
+                              const int64_t* targets, const float* lse, int64_t N, int64_t V,
+                              void* grad_logits, cudaStream_t s);
+
+// --- GEMM-based linear path -------------------------------------------------
+enum class EpiKind : int { Fwd = 0, Recomp = 1, Dh = 2, Dw = 3 };
+
+// Everything an epilogue may need; unused fields are ignored by a given kind.
+struct EpiArgs {
+    int64_t M;            // valid rows of the output tile grid (M dimension)
+    int64_t Ncols;        // valid columns (N dimension)
+    int64_t V;            // vocab size
+    // forward / recompute (M = tokens of the launch, N = vocab)
+    const int64_t* targets;  // [M]
+    const void* bias;        // [V] or nullptr
+    float* part_m;           // [n_segs, part_ld] running max (log2 units)
+    float* part_s;           // [n_segs, part_ld] running sum
+    float* zy;               // [M] target logit
+    int64_t part_ld;
+    const float* lse;        // [M]
+    const float* grad;       // [M] grad_logp
+    void* S;                 // [M, ldS] softmax part of g
+    int64_t ldS;
+    // dh (M = tokens, N = D): adds gl * W[y] and stores
+    const void* W;
+    int64_t ldW;
+    void* out;               // dh [M, ld_out] or dW [V, ld_out]
+    int64_t ld_out;
+    int out_dtype;
+    // dW (M = vocab, N = D)
+    int first_chunk, last_chunk;
+    const int* offs;         // [V + 1] token list offsets per vocab row
+    const int64_t* keys;     // sorted (target << 32 | token)
+    const float* grad_all;   // [N] grad_logp of every token
+    const void* h_all;       // [N, D] hidden of every token
+    int64_t ld_h;
+    int* status;
+    uint64_t wait_ns;
+};
+
+struct GemmShape {
+    int64_t m_blocks;        // M / 128, rounded up
+    int64_t n_tiles;         // N / 256, rounded up
+    int64_t tiles_per_unit;  // N tiles per work unit (forward segments), else 1
+    int64_t n_segs;          // ceil(n_tiles / tiles_per_unit)
+    int64_t k_blocks;        // K / BK, rounded up
+    int unit_order;          // 0: segment-major, 1: m-major
+};
+
+// One tensor-core GEMM with a fused epilogue.  dtype: LL_BF16 / LL_F16 /
+// LL_F32 (FP32 runs on the CUDA-core path).  Operand maps are built inside.
+//   A: [M, K] (a_mn = 0, row stride lda) or [K, M] (a_mn = 1)
+//   B: [N, K] (b_mn = 0) or [K, N] (b_mn = 1)
+cudaError_t launch_gemm(EpiKind kind, int dtype, const void* A, int64_t lda, int a_mn,
+                        const void* B, int64_t ldb, int b_mn, int64_t M, int64_t N, int64_t K,
+                        const GemmShape& shape, const EpiArgs& ea, const DevInfo& dev,
+                        cudaStream_t s);
+
+// --- small kernels (aux_kernels.cu) ------------------------------------------
+cudaError_t launch_lse_merge(const float* part_m, const float* part_s, const float* zy,
+                             int64_t part_ld, int64_t n_segs, const int64_t* targets, int64_t N,
+                             int64_t V, float* logp, float* lse, cudaStream_t s);
+// keys[i] = (y << 32 | i) for valid targets, all-ones otherwise; sorted
+// ascending; offs[v] = first index whose target is >= v (v in [0, V]).
+size_t token_sort_bytes(int64_t N);
+cudaError_t launch_token_sort(const int64_t* targets, int64_t N, int64_t V, int64_t* keys,
+                              int* offs, cudaStream_t s);
+// db: column sums of S over the chunk's rows added into db_acc (FP32),
+// first chunk starts from +0; with `last`, adds the one-hot term and writes
+// grad_bias in out_dtype.
+size_t db_partial_bytes(int64_t Nc, int64_t V);
+cudaError_t launch_db_chunk(const void* S, int64_t ldS, int s_dtype, int64_t rows, int64_t V,
+                            float* partial, float* db_acc, int first, int last, const int* offs,
+                            const int64_t* keys, const float* grad_all, void* grad_bias,
+                            int out_dtype, cudaStream_t s);
+cudaError_t launch_fill_zero(void* p, int64_t n_elems, int dtype, cudaStream_t s);
+cudaError_t launch_unsatisfied_wait(int* flag, int* status, uint64_t wait_ns, cudaStream_t s);
+
+}  // namespace ll

@@ -1,0 +1,198 @@
+/*
+ * ll_linear_logp.h -- C ABI of the GB300-native fused linear log-probability.
+ *
+ * The operation (RL-Kernel issue #261, "Current production path" and
+ * "Current accumulation"; RL-Kernel PR #495, "Summary" and "Behavior changes";
+ * Liger-Kernel PR #1324, "Details"):
+ *
+ *   forward   z = h . W^T (+ b)                              [N, V], never stored
+ *             lse[n]  = log sum_v exp z[n, v]
+ *             logp[n] = z[n, y_n] - lse[n]   if 0 <= y_n < V, else 0
+ *   backward  g = grad_logp[n] * (onehot(y_n) - softmax(z[n, :]))   (never stored)
+ *             grad_hidden = g . W          [N, D]
+ *             grad_weight = g^T . h        [V, D]  (FP32 by default)
+ *             grad_bias   = sum_n g[n, :]  [V]
+ *   logits-input variant: the same with the logits [N, V] given.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named as device pointers must be CUDA device (or managed)
+ *   memory on one device; the call switches to that device for its duration
+ *   and restores the caller's current device before returning.
+ * - Every call is asynchronous on `stream` (a cudaStream_t; NULL means the
+ *   legacy default stream).  Outputs are valid once the stream reaches the
+ *   call.  Arguments are validated on the host before anything is launched;
+ *   on an error nothing is launched and no output is touched.
+ * - The library never allocates device memory.  The caller owns every buffer,
+ *   including the scratch `workspace`, whose size ll_workspace_size() gives.
+ *   A workspace must not be shared by calls that may overlap on the GPU.
+ * - Row-major, contiguous layouts.  Element types are given by ll_dtype:
+ *   hidden, weight and bias share one dtype.  logp, lse and grad_logp are
+ *   FP32.  targets are int64.
+ * - Targets outside [0, V) (for instance the ignore index -100) give logp = 0
+ *   and an exactly +0 gradient row (PR #495, "Behavior changes").
+ * - Gradient entries that receive no non-zero contribution are +0, as with a
+ *   +0-initialised gradient table (issue #261, "Correctness boundary"); a
+ *   row whose grad_logp is +-0 is exactly +0.
+ * - Results are deterministic: the same inputs give the same bits.  logp,
+ *   lse, grad_hidden and grad_logits of a row do not depend on the other rows
+ *   of the batch, on the batch size or on the row's position (batch
+ *   invariance, PR #495, "Prior art & reuse decision").
+ * - Indexing is 64-bit; N * V and V * D may exceed 2^31.  V must be below
+ *   2^31 - 256.
+ * - Device-side waits are bounded.  A wait that runs out records
+ *   LL_ERR_DEVICE_TIMEOUT in a per-device status word that ll_check_status()
+ *   returns; the kernel then returns without hanging the device.
+ */
+#ifndef LL_LINEAR_LOGP_H
+#define LL_LINEAR_LOGP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LL_OK = 0,
+    LL_ERR_INVALID_ARG = 1,     /* null pointer where one is required, bad flag  */
+    LL_ERR_DTYPE = 2,           /* unsupported dtype or dtype combination        */
+    LL_ERR_SHAPE = 3,           /* negative or too large N, D, V, ld             */
+    LL_ERR_ALIGN = 4,           /* pointer or row stride not 16-byte aligned     */
+    LL_ERR_WORKSPACE = 5,       /* workspace missing, too small or misaligned    */
+    LL_ERR_CUDA = 6,            /* a CUDA runtime/driver call failed             */
+    LL_ERR_DEVICE_TIMEOUT = 7,  /* a bounded device-side wait ran out            */
+    LL_ERR_UNSUPPORTED = 8      /* device is not sm_103 / feature not built      */
+} ll_status;
+
+typedef enum { LL_F32 = 0, LL_F16 = 1, LL_BF16 = 2 } ll_dtype;
+
+/* Human-readable name of a status code (static storage). */
+const char* ll_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int ll_version(void);
+
+/*
+ * Workspace bytes needed by ll_forward (is_backward = 0) or ll_backward
+ * (is_backward = 1) for these sizes; `flags` is the need_db flag for the
+ * backward (bias gradient partials) and ignored for the forward.
+ * token_chunks: number of token chunks the backward splits N into (0 =
+ * automatic, see ll_backward).  Returns 0 only for N == 0 in the forward.
+ * The workspace pointer must be 256-byte aligned.
+ */
+size_t ll_workspace_size(int64_t N, int64_t D, int64_t V, int dtype,
+                         int token_chunks, int is_backward, int flags);
+
+/*
+ * Forward.  Issue #261 "Current production path" (the linear_logp op) and
+ * PR #495 "Summary" (logp of the selected token; lse is saved for backward).
+ *   hidden  [N, D] dtype, device, 16-byte aligned, D * elemsize % 16 == 0
+ *   weight  [V, D] dtype, device, 16-byte aligned
+ *   bias    [V]    dtype, device, or NULL
+ *   targets [N]    int64, device
+ *   logp    [N]    float, device (written)
+ *   lse     [N]    float, device (written; pass it to ll_backward)
+ * N == 0 launches nothing.  D >= 1, V >= 1.
+ */
+int ll_forward(const void* hidden, const void* weight, const void* bias,
+               const int64_t* targets, int64_t N, int64_t D, int64_t V, int dtype,
+               float* logp, float* lse, void* workspace, size_t ws_bytes,
+               void* stream);
+
+/*
+ * Backward.  Issue #261 "Current accumulation" (FP32 grad_w table, per-chunk
+ * accumulation) and "Static traffic model" (C = floor(2^24 / V) rows per
+ * chunk); Liger-Kernel PR #1324 "Details" (accumulate each chunk's
+ * contribution into grad_weight with no [V, D] temporary).
+ *   grad_logp [N] float, device.  hidden/weight/bias/targets as in ll_forward.
+ *   lse       [N] float, device: the forward's lse for the same inputs.
+ *   need_dh / need_dw / need_db: which gradients to produce (0 or 1).
+ *   grad_hidden [N, D] of dh_dtype (written when need_dh).
+ *   grad_weight [V, D] of dw_dtype (written, i.e. overwritten, when need_dw).
+ *     LL_F32 accumulates and stores FP32.  A 16-bit dw_dtype equal to dtype
+ *     accumulates each token chunk in FP32 and rounds the running table once
+ *     per chunk (once in total when token_chunks == 1).
+ *   grad_bias [V] of dw_dtype (written when need_db; requires a bias).
+ *   token_chunks: 0 = automatic (one chunk when its softmax workspace is at
+ *     most 2 GiB, otherwise the fewest chunks that fit), else the number of
+ *     chunks N is split into, in order.  logp-independent outputs (dh) are
+ *     bitwise independent of token_chunks; dW/db differ by FP32 rounding.
+ * N == 0: grad_weight / grad_bias (if requested) are filled with +0.
+ */
+int ll_backward(const float* grad_logp, const void* hidden, const void* weight,
+                const void* bias, const int64_t* targets, const float* lse,
+                int64_t N, int64_t D, int64_t V, int dtype,
+                int need_dh, int need_dw, int need_db,
+                void* grad_hidden, int dh_dtype,
+                void* grad_weight, int dw_dtype,
+                void* grad_bias, int token_chunks,
+                void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Logits-input forward.  PR #495 "Summary" (fused logp forward: one row per
+ * block, logp of the target, constant 0 for targets outside [0, V)).
+ *   logits [N, ld] dtype, device; row n starts at logits + n * ld; columns
+ *          [V, ld) are ignored.  ld >= V.
+ *   logp, lse [N] float, device (written).
+ * N == 0 launches nothing.  No workspace.
+ */
+int logits_logp_fwd(const void* logits, int64_t ld, int dtype, const int64_t* targets,
+                    int64_t N, int64_t V, float* logp, float* lse, void* stream);
+
+/*
+ * Logits-input backward.  PR #495 "Summary" (dlogits = grad * (one_hot -
+ * softmax) written in the logits dtype, no workspace) using the saved lse:
+ * one read and one write of the logits.
+ *   grad_logits [N, ld] dtype, device (columns [0, V) written; [V, ld)
+ *               untouched).  It may not overlap logits.
+ * N == 0 launches nothing.
+ */
+int logits_logp_bwd(const float* grad_logp, const void* logits, int64_t ld, int dtype,
+                    const int64_t* targets, const float* lse, int64_t N, int64_t V,
+                    void* grad_logits, void* stream);
+
+/*
+ * Device status word of the current device: synchronises `stream`, returns
+ * LL_OK or the first device-side error recorded since the last call
+ * (LL_ERR_DEVICE_TIMEOUT), and clears it.
+ */
+int ll_check_status(void* stream);
+
+/*
+ * Tracing.  ll_launch_count(): number of kernels this library has launched
+ * in the process.  ll_profile_enable(1) clears earlier records and brackets
+ * every phase of later calls (fwd_gemm, lse_merge, token_sort,
+ * recompute_gemm, dh_gemm, dw_gemm, db_sums, logits_fwd, logits_bwd; an
+ * _f32 suffix for the CUDA-core FP32 GEMMs) with CUDA events on the call's
+ * stream; ll_profile_enable(0) stops recording.  ll_profile_summary()
+ * synchronises on the recorded events and writes one line per phase,
+ * "label count total_ms", into buf (NUL-terminated, truncated to len);
+ * it returns the number of phases, or -LL_ERR_CUDA.
+ */
+long long ll_launch_count(void);
+void ll_profile_enable(int on);
+int ll_profile_summary(char* buf, size_t len);
+
+/*
+ * Test hook for the bounded waits: when `ns` > 0 every device-side wait of
+ * later launches gives up after `ns` nanoseconds (default 2e9).  Used by the
+ * tests to show that a wait that can never complete returns an error status
+ * instead of hanging.  Host-side setting, not thread-safe.
+ */
+void ll_set_wait_limit_ns(int64_t ns);
+
+/*
+ * Test hook: a kernel that waits on a device barrier nothing will ever
+ * complete, bounded by the wait limit.  It must end with
+ * LL_ERR_DEVICE_TIMEOUT in the status word.  `device_flag` is one int of
+ * device memory the kernel writes its exit path into (1 = timed out).
+ */
+int ll_debug_unsatisfied_wait(int* device_flag, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LL_LINEAR_LOGP_H */

@@ -1,0 +1,83 @@
+"""Helpers for the GPU parity tests: moving the synthetic storage arrays to
+the device and comparing against the FP64 oracle with the stated
+tolerances.
+
+Tolerances (|got - ref| <= atol + rtol * |ref| (+ one output ulp)):
+  FP32 operands:            atol 1e-5, rtol 5e-4 on every output
+  16-bit operands, logp/lse: atol 5e-3
+  16-bit operands, grads:    atol 5e-4, plus one ulp of the output dtype at
+                             |ref| when the output itself is 16-bit (its own
+                             rounding is up to half an ulp)
+"""
+import math
+
+import numpy as np
+import torch
+
+TOL = {
+    "f32": dict(logp=(1e-5, 5e-4), grad=(1e-5, 5e-4)),
+    "f16": dict(logp=(5e-3, 0.0), grad=(5e-4, 0.0)),
+    "bf16": dict(logp=(5e-3, 0.0), grad=(5e-4, 0.0)),
+}
+TORCH = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+MANT = {torch.bfloat16: 7, torch.float16: 10}
+
+
+def dev(a, dtype=None, device="cuda"):
+    """numpy storage array -> device tensor (bf16 arrives as uint16 bits)."""
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a)
+    if dtype == "bf16":
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(a).to(device)
+
+
+def host64(t):
+    return t.detach().float().cpu().numpy().astype(np.float64) if t.dtype != torch.float64 else \
+        t.detach().cpu().numpy()
+
+
+def ulp(ref, tdtype):
+    """One ulp of the 16-bit output dtype at |ref| (0 for FP32 outputs)."""
+    if tdtype not in MANT:
+        return np.zeros_like(ref)
+    m = MANT[tdtype]
+    a = np.abs(ref)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    sub = -14 if tdtype == torch.float16 else -126
+    e = np.maximum(e, sub)
+    return np.exp2(e - m)
+
+
+def check(name, got, ref, atol, rtol, out_dtype=None, report=None):
+    g = host64(got) if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert g.shape == ref.shape, (name, g.shape, ref.shape)
+    if g.size == 0:
+        return 0.0
+    err = np.abs(g - ref)
+    bound = atol + rtol * np.abs(ref)
+    if out_dtype is not None:
+        bound = bound + ulp(ref, out_dtype)
+    bad = ~(err <= bound)
+    worst = float(np.nanmax(err)) if np.isfinite(err).any() else math.inf
+    if report is not None:
+        report[name] = worst
+    if bad.any():
+        i = np.unravel_index(np.argmax(np.where(bad, err - bound, -np.inf)), err.shape)
+        raise AssertionError(
+            f"{name}: {int(bad.sum())}/{bad.size} outside tolerance; worst at {i}: got "
+            f"{g[i]!r} ref {ref[i]!r} (bound {bound[i]:.3g}); max err {worst:.3g}")
+    return worst
+
+
+def assert_pos_zero(name, t):
+    x = t.detach().float().cpu()
+    assert bool((x == 0).all()), f"{name}: not all zero"
+    assert not bool(torch.signbit(x).any()), f"{name}: negative zero present"
+
+
+def bits_equal(a, b):
+    return torch.equal(a.view(torch.int8) if a.dtype != torch.int8 else a,
+                       b.view(torch.int8) if b.dtype != torch.int8 else b)

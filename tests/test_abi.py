@@ -1,0 +1,155 @@
+"""The C-ABI library loads, exports every declared symbol, and validates its
+arguments on the host (no GPU needed: every case here returns before the
+first CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import cross_entropy_rl_gb300 as ll
+from cross_entropy_rl_gb300 import build as B
+
+HEADER = os.path.join(B.ROOT, "include", "ll_linear_logp.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return ll.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for must in ("ll_forward", "ll_backward", "logits_logp_fwd", "logits_logp_bwd",
+                 "ll_workspace_size", "ll_check_status", "ll_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert name in ll.EXPORTS, f"binding does not marshal {name}"
+
+
+def test_version_and_status_strings(L):
+    assert L.ll_version() >= 100
+    assert L.ll_status_string(0) == b"ok"
+    assert L.ll_status_string(4).startswith(b"misaligned")
+    assert L.ll_status_string(999) == b"unknown status"
+
+
+def test_workspace_size_rules(L):
+    # forward: two FP32 partials per (segment, row) + target logit per row
+    N, V = 4096, 32768
+    n_segs = -(-(-(-V // 256)) // 4)
+    fwd = L.ll_workspace_size(N, 2048, V, ll.LL_BF16, 0, 0, 0)
+    assert fwd >= (2 * n_segs + 1) * N * 4
+    assert L.ll_workspace_size(0, 2048, V, ll.LL_BF16, 0, 0, 0) == 0
+    # backward, one chunk: [N, round_up(V, 8)] 16-bit softmax part
+    bwd1 = L.ll_workspace_size(N, 2048, V, ll.LL_BF16, 1, 1, 0)
+    assert bwd1 >= N * V * 2
+    bwd8 = L.ll_workspace_size(N, 2048, V, ll.LL_BF16, 8, 1, 0)
+    assert bwd8 < bwd1 and bwd8 >= (N // 8) * V * 2
+    # automatic chunking keeps the softmax part within 2 GiB
+    big = L.ll_workspace_size(32768, 4096, 151936, ll.LL_BF16, 0, 1, 0)
+    assert big <= (2 << 30) + (64 << 20)
+    assert L.ll_workspace_size(N, 2048, V, ll.LL_F32, 1, 1, 0) >= N * V * 4
+    # grad_bias partials only when requested
+    assert L.ll_workspace_size(N, 2048, V, ll.LL_BF16, 1, 1, 1) > bwd1
+
+
+NULL = None
+
+
+def fwd(L, **kw):
+    a = dict(hidden=16, weight=32, bias=NULL, targets=48, N=4, D=8, V=10, dtype=ll.LL_BF16,
+             logp=64, lse=80, ws=256, ws_bytes=1 << 20)
+    a.update(kw)
+    p = lambda x: None if x is None else ctypes.c_void_p(x)
+    return L.ll_forward(p(a["hidden"]), p(a["weight"]), p(a["bias"]), p(a["targets"]), a["N"],
+                        a["D"], a["V"], a["dtype"], p(a["logp"]), p(a["lse"]), p(a["ws"]),
+                        a["ws_bytes"], None)
+
+
+def test_forward_validation_before_launch(L):
+    assert fwd(L, N=-1) == 3
+    assert fwd(L, V=0) == 3
+    assert fwd(L, D=0) == 3
+    assert fwd(L, V=(1 << 31)) == 3
+    assert fwd(L, dtype=7) == 2
+    assert fwd(L, weight=None) == 1
+    assert fwd(L, N=0) == 0              # empty batch: nothing to do
+    assert fwd(L, hidden=None) == 1
+    assert fwd(L, D=12) == 4             # rows not 16-byte multiples
+    assert fwd(L, hidden=24) == 4        # misaligned pointer
+    assert fwd(L, ws=None) == 5
+    assert fwd(L, ws_bytes=8) == 5
+    assert fwd(L, ws=264) == 5           # workspace not 256-byte aligned
+
+
+def bwd(L, **kw):
+    a = dict(grad=8, hidden=16, weight=32, bias=NULL, targets=48, lse=64, N=4, D=8, V=10,
+             dtype=ll.LL_BF16, dh=1, dw=1, db=0, dh_ptr=256, dh_dt=ll.LL_BF16, dw_ptr=512,
+             dw_dt=ll.LL_F32, db_ptr=None, chunks=0, ws=1024, ws_bytes=1 << 20)
+    a.update(kw)
+    p = lambda x: None if x is None else ctypes.c_void_p(x)
+    return L.ll_backward(p(a["grad"]), p(a["hidden"]), p(a["weight"]), p(a["bias"]),
+                         p(a["targets"]), p(a["lse"]), a["N"], a["D"], a["V"], a["dtype"],
+                         a["dh"], a["dw"], a["db"], p(a["dh_ptr"]), a["dh_dt"], p(a["dw_ptr"]),
+                         a["dw_dt"], p(a["db_ptr"]), a["chunks"], p(a["ws"]), a["ws_bytes"], None)
+
+
+def test_backward_validation_before_launch(L):
+    assert bwd(L, N=-3) == 3
+    assert bwd(L, dtype=5) == 2
+    assert bwd(L, dh=2) == 1
+    assert bwd(L, chunks=-1) == 1
+    assert bwd(L, dh_dt=ll.LL_F16) == 2           # dh must be the operand dtype or FP32
+    assert bwd(L, dw_dt=ll.LL_F16) == 2           # dW must be FP32 or the operand dtype
+    assert bwd(L, dw_ptr=None) == 1
+    assert bwd(L, db=1, db_ptr=None) == 1
+    assert bwd(L, D=20) == 4
+    assert bwd(L, dw_ptr=520) == 4
+    assert bwd(L, dh=0, dw=0, db=0) == 0          # nothing requested: nothing to do
+
+
+def logits(L, fn, **kw):
+    a = dict(grad=8, logits=16, ld=10, dtype=ll.LL_BF16, targets=32, lse=48, N=4, V=10,
+             logp=64, out=4096)
+    a.update(kw)
+    p = lambda x: None if x is None else ctypes.c_void_p(x)
+    if fn == "fwd":
+        return L.logits_logp_fwd(p(a["logits"]), a["ld"], a["dtype"], p(a["targets"]), a["N"],
+                                 a["V"], p(a["logp"]), p(a["lse"]), None)
+    return L.logits_logp_bwd(p(a["grad"]), p(a["logits"]), a["ld"], a["dtype"], p(a["targets"]),
+                             p(a["lse"]), a["N"], a["V"], p(a["out"]), None)
+
+
+def test_logits_validation_before_launch(L):
+    assert logits(L, "fwd", ld=5) == 3            # ld < V
+    assert logits(L, "fwd", dtype=9) == 2
+    assert logits(L, "fwd", N=0) == 0
+    assert logits(L, "fwd", targets=None) == 1
+    assert logits(L, "fwd", logits=17) == 4       # not element aligned
+    assert logits(L, "bwd", out=20) == 1          # output overlaps the logits
+    assert logits(L, "bwd", grad=None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    import importlib
+
+    mod = importlib.reload(ll)
+    try:
+        mod._LIB = None
+        with pytest.raises(RuntimeError, match="not built"):
+            mod.load(str(tmp_path / "missing.so"))
+    finally:
+        importlib.reload(ll)

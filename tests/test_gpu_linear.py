@@ -1,0 +1,244 @@
+"""GPU parity of the fused linear logp path (C ABI through the binding)
+against the FP64 oracle, plus the GPU-side invariants: determinism, batch
+invariance, token-chunk independence of grad_hidden, zero rules."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from cross_entropy_rl_gb300 import synth
+from gpu_util import TOL, TORCH, assert_pos_zero, bits_equal, check, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run(ll, p, *, token_chunks=0, dh_dtype=None, dw_dtype=None, gl=None, need=(1, 1, None)):
+    dt = p["dtype"]
+    h, W, b = dev(p["h"], dt), dev(p["W"], dt), dev(p["b"], dt)
+    y = dev(p["y"])
+    g = dev(p["gl"] if gl is None else gl)
+    logp, lse = ll.forward(h, W, b, y)
+    need_db = (b is not None) if need[2] is None else need[2]
+    dh, dW, db = ll.backward(g, h, W, b, y, lse, need_dh=need[0], need_dw=need[1],
+                             need_db=need_db, token_chunks=token_chunks,
+                             dh_dtype=dh_dtype, dw_dtype=dw_dtype)
+    torch.cuda.synchronize()
+    assert ll.check_status() == 0
+    return dict(logp=logp, lse=lse, dh=dh, dW=dW, db=db)
+
+
+def compare(p, got, ref, report=None):
+    dt = p["dtype"]
+    la, lr = TOL[dt]["logp"]
+    ga, gr = TOL[dt]["grad"]
+    check("logp", got["logp"], ref["logp"], la, lr, report=report)
+    check("lse", got["lse"], ref["lse"], la, lr, report=report)
+    if got["dh"] is not None:
+        check("dh", got["dh"], ref["dh"], ga, gr, out_dtype=got["dh"].dtype, report=report)
+    if got["dW"] is not None:
+        check("dW", got["dW"], ref["dW"], ga, gr, out_dtype=got["dW"].dtype, report=report)
+    if got["db"] is not None:
+        check("db", got["db"], ref["db"], ga, gr, out_dtype=got["db"].dtype, report=report)
+
+
+def full_ref(p, gl=None):
+    return O.linear_forward_backward(p["gl"] if gl is None else gl, p["h"], p["W"], p["b"],
+                                     p["y"], p["dtype"])
+
+
+# ------------------------------------------------------------ small, full --
+
+def test_fp32_small_full_parity(lib):
+    """The FP32 small problem (128 x 256 x 4096, bias), compared in full."""
+    p = synth.linear_inputs(**synth.WORKLOADS["fp32_small"], seed=0)
+    got = run(lib, p)
+    compare(p, got, full_ref(p))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("N,D,V,bias,chunks", [
+    (300, 136, 1031, True, 0),     # ragged M, K (136 = 2*64 + 8) and vocab tiles
+    (129, 64, 255, False, 0),      # one row past a tile, vocab below one tile
+    (513, 264, 4099, True, 3),     # several tiles, three token chunks
+    (1, 8, 1, True, 0),            # single row, single class
+    (256, 512, 2304, False, 2),    # exact tiles, two chunks
+])
+def test_16bit_full_parity(lib, dt, N, D, V, bias, chunks):
+    p = synth.linear_inputs(N, D, V, dtype=dt, bias=bias, seed=N + V)
+    got = run(lib, p, token_chunks=chunks)
+    compare(p, got, full_ref(p))
+
+
+@pytest.mark.parametrize("N,D,V,bias", [(200, 72, 1031, True), (64, 8, 7, False)])
+def test_fp32_ragged_full_parity(lib, N, D, V, bias):
+    p = synth.linear_inputs(N, D, V, dtype="f32", bias=bias, seed=7)
+    got = run(lib, p, token_chunks=2)
+    compare(p, got, full_ref(p))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_16bit_grad_weight_output(lib, dt):
+    """grad_weight / grad_bias in the operand dtype: FP32 accumulation, one
+    rounding per token chunk; grad_hidden in FP32 on request."""
+    p = synth.linear_inputs(384, 128, 1500, dtype=dt, bias=True, seed=3, grad="mean")
+    got = run(lib, p, token_chunks=1, dw_dtype=TORCH[dt], dh_dtype=torch.float32)
+    assert got["dW"].dtype == TORCH[dt] and got["dh"].dtype == torch.float32
+    compare(p, got, full_ref(p))
+
+
+def test_repeated_targets(lib):
+    """Many tokens share a few targets: the one-hot part of grad_weight sums
+    each target's tokens in a fixed order."""
+    p = synth.linear_inputs(1000, 64, 300, dtype="bf16", bias=True, seed=11)
+    p["y"] = (p["y"] % 5).astype(np.int64)
+    got = run(lib, p, token_chunks=3)
+    compare(p, got, full_ref(p))
+    again = run(lib, p, token_chunks=3)
+    assert bits_equal(got["dW"], again["dW"]) and bits_equal(got["db"], again["db"])
+
+
+# ------------------------------------------------------------- invariants --
+
+def test_bitwise_determinism(lib):
+    p = synth.linear_inputs(700, 256, 5000, dtype="bf16", bias=True, seed=5)
+    a, b = run(lib, p), run(lib, p)
+    for k in ("logp", "lse", "dh", "dW", "db"):
+        assert bits_equal(a[k], b[k]), k
+
+
+def test_batch_invariance(lib):
+    """logp, lse and grad_hidden of a row do not depend on the batch it is in."""
+    p = synth.linear_inputs(700, 192, 3000, dtype="bf16", bias=True, seed=9)
+    full = run(lib, p)
+    for rows in ([0], [699], [350, 5, 1], list(range(128, 300))):
+        q = dict(p)
+        q["h"], q["y"], q["gl"] = p["h"][rows], p["y"][rows], p["gl"][rows]
+        q["N"] = len(rows)
+        part = run(lib, q)
+        idx = torch.tensor(rows, device="cuda")
+        for k in ("logp", "lse", "dh"):
+            assert bits_equal(part[k], full[k][idx]), (k, rows[:4])
+
+
+def test_token_chunks(lib):
+    """grad_hidden is bitwise independent of the token chunking; grad_weight
+    differs only by FP32 rounding."""
+    p = synth.linear_inputs(1000, 128, 2048, dtype="bf16", bias=True, seed=13)
+    ref = full_ref(p)
+    outs = {k: run(lib, p, token_chunks=k) for k in (1, 2, 4, 7)}
+    for k, o in outs.items():
+        assert bits_equal(o["dh"], outs[1]["dh"]), k
+        compare(p, o, ref)
+
+
+def test_invalid_targets_and_zero_rows(lib):
+    N, D, V = 260, 64, 700
+    p = synth.linear_inputs(N, D, V, dtype="bf16", bias=True, seed=17)
+    p["y"][[0, 5, 130, 259]] = [-100, V, V + 5, -1]
+    p["gl"][[7, 140]] = [0.0, -0.0]
+    got = run(lib, p, token_chunks=2)
+    compare(p, got, full_ref(p))
+    for r in (0, 5, 130, 259):
+        assert float(got["logp"][r]) == 0.0
+        assert_pos_zero(f"dh[{r}]", got["dh"][r])
+    for r in (7, 140):
+        assert_pos_zero(f"dh[{r}]", got["dh"][r])
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_zero_upstream_gives_positive_zeros(lib, dt):
+    p = synth.linear_inputs(300, 64, 1000, dtype=dt, bias=True, seed=19)
+    got = run(lib, p, gl=np.zeros(300, np.float32), token_chunks=2)
+    for k in ("dh", "dW", "db"):
+        assert_pos_zero(k, got[k])
+
+
+def test_empty_batch(lib):
+    D, V = 64, 300
+    W = dev(synth.normal(0, "weight", (V, D), 0.1, "bf16"), "bf16")
+    b = dev(synth.normal(0, "bias", (V,), 0.1, "bf16"), "bf16")
+    h = torch.empty(0, D, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(0, dtype=torch.int64, device="cuda")
+    g = torch.empty(0, dtype=torch.float32, device="cuda")
+    logp, lse = lib.forward(h, W, b, y)
+    assert logp.numel() == 0
+    dW = torch.full((V, D), 7.0, device="cuda")
+    db = torch.full((V,), 7.0, device="cuda")
+    dh = torch.empty(0, D, dtype=torch.bfloat16, device="cuda")
+    lib.backward(g, h, W, b, y, lse, out=(dh, dW, db), need_db=True)
+    torch.cuda.synchronize()
+    assert_pos_zero("dW", dW)
+    assert_pos_zero("db", db)
+
+
+def test_linearity_in_upstream(lib):
+    """Scaling grad_logp by 2 scales every gradient by exactly 2."""
+    p = synth.linear_inputs(300, 128, 1500, dtype="bf16", bias=True, seed=23)
+    a = run(lib, p, dh_dtype=torch.float32)
+    b = run(lib, p, gl=p["gl"] * np.float32(2.0), dh_dtype=torch.float32)
+    for k in ("dh", "dW", "db"):
+        assert torch.equal(b[k], 2 * a[k]), k
+
+
+# --------------------------------------------------------- full-size cases --
+
+def sampled(lib, p, rows, dw_rows=None, token_chunks=0, dw_dtype=None, report=None):
+    """Compare sampled rows (logp, lse, dh) of the full run, then grad_weight /
+    grad_bias of a run whose grad_logp is zero outside the sample."""
+    got = run(lib, p, token_chunks=token_chunks, dw_dtype=dw_dtype, need=(1, 0, 0))
+    ref = O.linear_rows(p["gl"], p["h"], p["W"], p["b"], p["y"], p["dtype"], rows,
+                        dw_rows=dw_rows)
+    idx = torch.tensor(rows, device="cuda")
+    dt = p["dtype"]
+    la, lr = TOL[dt]["logp"]
+    ga, gr = TOL[dt]["grad"]
+    check("logp", got["logp"][idx], ref["logp"], la, lr, report=report)
+    check("lse", got["lse"][idx], ref["lse"], la, lr, report=report)
+    check("dh", got["dh"][idx], ref["dh"], ga, gr, out_dtype=got["dh"].dtype, report=report)
+    del got
+    glm = np.zeros_like(p["gl"])
+    glm[rows] = p["gl"][rows]
+    got = run(lib, p, token_chunks=token_chunks, dw_dtype=dw_dtype, gl=glm, need=(0, 1, None))
+    dW = got["dW"] if dw_rows is None else got["dW"][torch.tensor(dw_rows, device="cuda")]
+    check("dW", dW, ref["dW"], ga, gr, out_dtype=got["dW"].dtype, report=report)
+    if got["db"] is not None:
+        check("db", got["db"], ref["db"], ga, gr, out_dtype=got["db"].dtype, report=report)
+
+
+@pytest.mark.slow
+def test_bf16_4k_2k_32k_sampled(lib):
+    """The benchmark workload (4096 x 2048 x 32768, bf16, FP32 grad_weight) in
+    the benchmark's launch configuration (automatic token chunks)."""
+    p = synth.linear_inputs(**synth.WORKLOADS["bf16_4k_2k_32k"], seed=0)
+    rows = synth.sample_rows(0, p["N"])
+    sampled(lib, p, rows)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("chunks", [2, 4, 8])
+def test_bf16_4k_2k_32k_token_chunks(lib, chunks):
+    p = synth.linear_inputs(**synth.WORKLOADS["bf16_4k_2k_32k"], seed=0)
+    rows = synth.sample_rows(1, p["N"])
+    sampled(lib, p, rows, token_chunks=chunks)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("bias", [False, True])
+def test_sweep_16k_4k_32000_sampled(lib, dt, bias):
+    """Operands and grad_weight in one dtype, mean-loss upstream 1/N."""
+    p = synth.linear_inputs(**synth.WORKLOADS["sweep_16k_4k_32000"], dtype=dt, bias=bias, seed=2)
+    rows = synth.sample_rows(2, p["N"])
+    sampled(lib, p, rows, dw_dtype=TORCH[dt])
+
+
+@pytest.mark.slow
+def test_bf16_32k_4k_151936_sampled(lib):
+    """Large vocab, N*V > 2^31 (64-bit indexing), 10 % zero upstream rows."""
+    p = synth.linear_inputs(**synth.WORKLOADS["bf16_32k_4k_151936"], seed=4)
+    rows = synth.sample_rows(4, p["N"])
+    zero = synth.zero_rows(4, p["N"], 0.1)
+    assert (p["gl"][zero] == 0).all()
+    dw_rows = np.unique(np.concatenate([p["y"][rows], np.arange(0, 151936, 593),
+                                        [151935]])).astype(np.int64)
+    sampled(lib, p, rows, dw_rows=dw_rows)

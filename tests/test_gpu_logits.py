@@ -1,0 +1,148 @@
+"""GPU parity of the logits-input logp forward/backward against the FP64
+oracle; batch-size / row-position invariance sweep (bitwise); masked tails,
+invalid targets, unaligned row strides."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from cross_entropy_rl_gb300 import synth
+from gpu_util import TOL, assert_pos_zero, bits_equal, check, dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run(ll, x, y, gl, V=None):
+    logp, lse = ll.logits_fwd(x, y, V)
+    g = ll.logits_bwd(gl, x, y, lse, V)
+    torch.cuda.synchronize()
+    return logp, lse, g
+
+
+def compare(p, got, rows=None, V=None):
+    dt = p["dtype"]
+    x = p["logits"] if rows is None else p["logits"][rows]
+    y = p["y"] if rows is None else p["y"][rows]
+    gl = p["gl"] if rows is None else p["gl"][rows]
+    Vv = p["V"] if V is None else V
+    lr_logp, lr_lse = O.logits_forward(x, y, dt, V=Vv)
+    g_ref = O.logits_backward(gl, x, y, dt, V=Vv)
+    logp, lse, g = got
+    if rows is not None:
+        idx = torch.tensor(rows, device="cuda")
+        logp, lse, g = logp[idx], lse[idx], g[idx]
+    la, lr = TOL[dt]["logp"]
+    ga, gr = TOL[dt]["grad"]
+    check("logp", logp, lr_logp, la, lr)
+    check("lse", lse, lr_lse, la, lr)
+    check("dlogits", g[:, :Vv], g_ref, ga, gr, out_dtype=g.dtype)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("V", [1, 255, 1031, 151936])
+def test_full_parity(lib, dt, V):
+    N = 64 if V > 10000 else 200
+    p = synth.logits_inputs(N, V, seed=V, dtype=dt)
+    x, y, gl = dev(p["logits"], dt), dev(p["y"]), dev(p["gl"])
+    compare(p, run(lib, x, y, gl))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_padded_and_unaligned_rows(lib, dt):
+    """Row stride ld > V: aligned (vector path) and not 16-byte aligned."""
+    for ld in (1040, 1033):
+        p = synth.logits_inputs(96, 1031, seed=ld, dtype=dt, ld=ld)
+        x, y, gl = dev(p["logits"], dt), dev(p["y"]), dev(p["gl"])
+        got = run(lib, x, y, gl, V=1031)
+        compare(p, got, V=1031)
+        # columns [V, ld) of the gradient are not written
+        out = torch.full_like(x, 3.0)
+        lib.logits_bwd(gl, x, y, got[1], V=1031, out=out)
+        torch.cuda.synchronize()
+        assert bool((out[:, 1031:] == 3.0).all())
+
+
+def test_invalid_targets_masked_tail(lib):
+    """-inf tail (targets kept below it), invalid targets -100 / V / V+5,
+    an all -inf row with an invalid target, zero upstream rows."""
+    N, V = 40, 4096
+    p = synth.logits_inputs(N, V, seed=3)
+    x = dev(p["logits"], "bf16")
+    x[:, 3000:] = -float("inf")
+    x[11, :] = -float("inf")
+    y = p["y"] % 1000
+    y[[2, 9, 11, 30]] = [-100, V, -100, V + 5]
+    gl = p["gl"].copy()
+    gl[[4, 20]] = [0.0, -0.0]
+    q = dict(p, y=y, gl=gl, logits=x.view(torch.int16).cpu().numpy().view(np.uint16))
+    got = run(lib, x, dev(y), dev(gl))
+    compare(q, got)
+    logp, lse, g = got
+    assert torch.isfinite(g.float()).all()
+    for r in (2, 9, 11, 30, 4, 20):
+        assert_pos_zero(f"g[{r}]", g[r])
+    assert float(logp[11]) == 0.0 and float(lse[11]) == -float("inf")
+    assert_pos_zero("tail", g[:, 3000:])
+
+
+def test_empty(lib):
+    x = torch.empty(0, 100, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(0, dtype=torch.int64, device="cuda")
+    logp, lse = lib.logits_fwd(x, y)
+    assert logp.numel() == 0
+
+
+def _sweep_sizes(full):
+    s = list(range(1, 10))
+    k = 2
+    while 2 ** k <= 2048:
+        s += [2 ** k - 1, 2 ** k, 2 ** k + 1]
+        k += 1
+    s = sorted(set(s))
+    if full:
+        s += [4096, 32768]
+    return s
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_batch_invariance_sweep(lib, seed):
+    """Eight probe rows alone vs at the front, middle and back of batches of
+    sizes 1-9 and 2^k-1 / 2^k / 2^k+1 up to 2048: logp, lse and dlogits
+    bitwise identical."""
+    V = 151936
+    probes = synth.logits_inputs(8, V, seed=100 + seed)
+    px, py, pg = dev(probes["logits"], "bf16"), dev(probes["y"]), dev(probes["gl"])
+    alone = [run(lib, px[i:i + 1], py[i:i + 1], pg[i:i + 1]) for i in range(8)]
+    filler = synth.logits_inputs(2048 + 8, V, seed=200 + seed)
+    fx, fy, fg = dev(filler["logits"], "bf16"), dev(filler["y"]), dev(filler["gl"])
+    differ = 0
+    total = 0
+    for n in _sweep_sizes(False):
+        for where in ("front", "middle", "back"):
+            m = min(8, n)
+            x, y, g = fx[:n].clone(), fy[:n].clone(), fg[:n].clone()
+            pos = {"front": 0, "middle": (n - m) // 2, "back": n - m}[where]
+            x[pos:pos + m], y[pos:pos + m], g[pos:pos + m] = px[:m], py[:m], pg[:m]
+            logp, lse, dl = run(lib, x, y, g)
+            for i in range(m):
+                total += 1
+                a = alone[i]
+                same = (bits_equal(logp[pos + i:pos + i + 1], a[0]) and
+                        bits_equal(lse[pos + i:pos + i + 1], a[1]) and
+                        bits_equal(dl[pos + i:pos + i + 1], a[2]))
+                differ += 0 if same else 1
+    assert differ == 0, f"{differ} of {total} probe rows differ"
+
+
+@pytest.mark.slow
+def test_logits_32k_151936_sampled(lib):
+    """The full logits workload (32768 x 151936 bf16; N*V > 2^31) on 256
+    sampled rows, plus rows 0, N/2, N-1."""
+    p = synth.logits_inputs(**synth.WORKLOADS["logits_32k_151936"], seed=0)
+    x, y, gl = dev(p["logits"], "bf16"), dev(p["y"]), dev(p["gl"])
+    got = run(lib, x, y, gl)
+    rows = synth.sample_rows(0, p["N"])
+    compare(p, got, rows=rows)
+    # the probe rows of the sweep are position independent at full size too
+    alone = run(lib, x[-1:], y[-1:], gl[-1:])
+    assert bits_equal(alone[2], got[2][-1:]) and bits_equal(alone[1], got[1][-1:])

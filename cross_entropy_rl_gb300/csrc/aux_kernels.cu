@@ -128,15 +128,14 @@ __global__ void db_finish_kernel(const float* __restrict__ partial, int64_t grou
                                  float* __restrict__ db_acc, int first, int last,
                                  const int* __restrict__ offs,
                                  const unsigned long long* __restrict__ keys,
-                                 const float* __restrict__ grad_all, TO* __restrict__ out) {
+                                 const float* __restrict__ tc_all, TO* __restrict__ out) {
     const int64_t v = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
     if (v >= V) return;
     float acc = first ? 0.f : db_acc[v];
     for (int64_t g = 0; g < groups; ++g) acc = acc + partial[g * V + v];
     if (last) {
         for (int i = offs[v]; i < offs[v + 1]; ++i) {
-            const float gl = grad_all[keys[i] & 0xffffffffull];
-            acc = acc + gl;
+            acc = acc + tc_all[keys[i] & 0xffffffffull];
         }
         out[v] = Elem<TO>::from_f(acc + 0.f);
     } else {
@@ -219,7 +218,7 @@ size_t db_partial_bytes(int64_t Nc, int64_t V) {
 
 cudaError_t launch_db_chunk(const void* S, int64_t ldS, int s_dtype, int64_t rows, int64_t V,
                             float* partial, float* db_acc, int first, int last, const int* offs,
-                            const int64_t* keys, const float* grad_all, void* grad_bias,
+                            const int64_t* keys, const float* tc_all, void* grad_bias,
                             int out_dtype, cudaStream_t s) {
     const int64_t groups = rows < 64 ? (rows > 0 ? rows : 1) : 64;
     const int64_t rpg = (rows + groups - 1) / groups;
@@ -238,13 +237,13 @@ cudaError_t launch_db_chunk(const void* S, int64_t ldS, int s_dtype, int64_t row
     const unsigned long long* k = reinterpret_cast<const unsigned long long*>(keys);
     if (out_dtype == LL_F32)
         db_finish_kernel<float><<<fb, 256, 0, s>>>(partial, groups, V, db_acc, first, last, offs,
-                                                   k, grad_all, static_cast<float*>(grad_bias));
+                                                   k, tc_all, static_cast<float*>(grad_bias));
     else if (out_dtype == LL_F16)
         db_finish_kernel<__half><<<fb, 256, 0, s>>>(partial, groups, V, db_acc, first, last, offs,
-                                                    k, grad_all, static_cast<__half*>(grad_bias));
+                                                    k, tc_all, static_cast<__half*>(grad_bias));
     else
         db_finish_kernel<__nv_bfloat16><<<fb, 256, 0, s>>>(
-            partial, groups, V, db_acc, first, last, offs, k, grad_all,
+            partial, groups, V, db_acc, first, last, offs, k, tc_all,
             static_cast<__nv_bfloat16*>(grad_bias));
     return cudaGetLastError();
 }

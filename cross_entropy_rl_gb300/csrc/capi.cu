@@ -157,7 +157,7 @@ constexpr size_t kAutoChunkBytes = size_t(2) << 30;  // softmax workspace budget
 
 struct BwdLayout {
     int64_t chunks, Nc, ldS;
-    size_t S, keys, offs, db, total;
+    size_t S, tc, keys, offs, db, total;
 };
 BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need_db) {
     BwdLayout L;
@@ -176,6 +176,8 @@ BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need
     size_t off = 0;
     L.S = off;
     off = align_up(off + size_t(L.Nc) * row_bytes);
+    L.tc = off;
+    off = align_up(off + size_t(n1) * 4);
     L.keys = off;
     off = align_up(off + token_sort_bytes(n1));
     L.offs = off;
@@ -323,6 +325,7 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight, 
 
     char* ws = static_cast<char*>(workspace);
     void* S = ws + L.S;
+    float* tc = reinterpret_cast<float*>(ws + L.tc);
     int64_t* keys = reinterpret_cast<int64_t*>(ws + L.keys);
     int* offs = reinterpret_cast<int*>(ws + L.offs);
     float* db_part = reinterpret_cast<float*>(ws + L.db);
@@ -365,6 +368,7 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight, 
             ea.grad = grad_logp + r0;
             ea.S = S;
             ea.ldS = L.ldS;
+            ea.tc = tc + r0;
             Phase ph(dtype == LL_F32 ? "recompute_gemm_f32" : "recompute_gemm", s);
             e = launch_gemm(EpiKind::Recomp, dtype, h_c, D, 0, weight, D, 0, rows, V, D, sh, ea,
                             dev, s);
@@ -384,6 +388,7 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight, 
             ea.Ncols = D;
             ea.targets = targets + r0;
             ea.grad = grad_logp + r0;
+            ea.tc = tc + r0;
             ea.W = weight;
             ea.ldW = D;
             ea.out = static_cast<char*>(grad_hidden) + size_t(r0) * size_t(D) * esize(dh_dtype);
@@ -413,7 +418,7 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight, 
             ea.last_chunk = c == L.chunks - 1;
             ea.offs = offs;
             ea.keys = keys;
-            ea.grad_all = grad_logp;
+            ea.tc_all = tc;
             ea.h_all = hidden;
             ea.ld_h = D;
             Phase ph(dtype == LL_F32 ? "dw_gemm_f32" : "dw_gemm", s);
@@ -425,7 +430,7 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight, 
         if (need_db) {
             Phase ph("db_sums", s);
             e = launch_db_chunk(S, L.ldS, dtype, rows, V, db_part, db_acc, c == 0,
-                                c == L.chunks - 1, offs, keys, grad_logp, grad_bias, dw_dtype, s);
+                                c == L.chunks - 1, offs, keys, tc, grad_bias, dw_dtype, s);
             if (e != cudaSuccess) return cuda_status(e);
         }
     }

@@ -8,18 +8,21 @@
 //           over the vocab tiles of one segment (online softmax), target
 //           logit picked up when it falls in the tile.  Per-segment partials
 //           are merged afterwards in ascending segment order.
-//   Recomp  the same z tile recomputed -> p = exp(z - lse), stores the
-//           softmax part of g, S = -grad_logp * p, to the chunk workspace.
-//   Dh      acc = S . W tile -> adds the one-hot part grad_logp * W[y] in
-//           FP32 and stores grad_hidden.
+//   Recomp  the same z tile recomputed -> p = exp(z - lse); stores the
+//           off-target part of g, S[n, v] = -grad_logp * p (S = 0 at the
+//           target), to the chunk workspace, and the FP32 target entry
+//           c[n] = grad_logp * (1 - p[n, y]) to a per-token array.
+//   Dh      acc = S . W tile -> adds c[n] * W[y] in FP32, stores grad_hidden.
 //   Dw      acc = S^T . h tile -> adds the running grad_weight (FP32 +0
 //           start on the first token chunk) and, on the last chunk, the
-//           one-hot part sum over tokens with target v of grad_logp * h, in
+//           target part sum over tokens with target v of c[n] * h[n], in
 //           ascending token order.
 //
-// The split of g = grad_logp * (onehot - p) into the exact FP32 one-hot part
-// and the small softmax part S keeps the 16-bit rounding of S far below the
-// gradient tolerances.  Zero rules (issue #261, "Correctness boundary"):
+// g = grad_logp * (onehot - p) is split into its target column, kept exact
+// in FP32 (c), and the off-target entries S, stored in 16 bits.  The 16-bit
+// rounding then only touches the entries -grad * p[n, v], v != y, whose sum
+// over v is grad * (1 - p[n, y]); a sharp distribution (p[n, y] -> 1) makes
+// that error vanish instead of leaving a 2^-9 * |grad| error at the target.  Zero rules (issue #261, "Correctness boundary"):
 // rows with an invalid target or a zero upstream gradient store exact +0;
 // sums start from +0.
 #pragma once
@@ -76,7 +79,8 @@ struct RowEpilogue {
     int64_t row;   // row in the M dimension of the launch
     bool rvalid;
     int64_t y;
-    float coef;    // Recomp: -grad (0 for dead rows); Dh: grad (0 for dead rows)
+    float coef;    // Recomp: -grad (0 for dead rows); Dh: c[row] (0 for dead rows)
+    bool live;     // Recomp / Dh: valid target and non-zero upstream gradient
     float lse2;    // Recomp: lse * log2(e)
     float m2, s;   // Fwd: running max (log2 units) and sum
     float zyv;
@@ -95,8 +99,11 @@ struct RowEpilogue {
         } else if constexpr (E == EpiKind::Recomp || E == EpiKind::Dh) {
             y = rvalid ? ea.targets[row] : -1;
             const float g = rvalid ? ea.grad[row] : 0.f;
-            const bool live = rvalid && y >= 0 && y < ea.V && g != 0.f;
-            coef = live ? (E == EpiKind::Recomp ? -g : g) : 0.f;
+            live = rvalid && y >= 0 && y < ea.V && g != 0.f;
+            if constexpr (E == EpiKind::Recomp)
+                coef = live ? -g : 0.f;
+            else
+                coef = live ? ea.tc[row] : 0.f;
             if constexpr (E == EpiKind::Recomp) lse2 = rvalid ? ea.lse[row] * kLog2e : 0.f;
         } else {  // Dw: row is a vocab index
             oh_beg = oh_end = 0;
@@ -142,16 +149,30 @@ struct RowEpilogue {
                     for (int j = 0; j < 32; ++j) acc += ex2(fmaf(v[j], kLog2e, -m2));
                     s += acc;
                 }
-            } else {  // Recomp: S = -grad * exp(z - lse)
+            } else {  // Recomp: S = -grad * exp(z - lse), target entry apart
                 if (!rvalid) return;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = coef * ex2(fmaf(v[j], kLog2e, -lse2));
+                for (int j = 0; j < 32; ++j) v[j] = ex2(fmaf(v[j], kLog2e, -lse2));
+                const int64_t off = y - col0;
+                if (off >= 0 && off < 32) {
+                    float py = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j == off) py = v[j];
+                    // -coef = grad for live rows, 0 otherwise
+                    ea.tc[row] = coef != 0.f ? -coef * (1.f - py) : 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j == off) v[j] = 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = coef * v[j];
                 store_row32<T>(ea.S, row * ea.ldS + col0, v, col0, V, own_tag<T>());
             }
         } else if constexpr (E == EpiKind::Dh) {
             if (!rvalid) return;
             const int64_t D = ea.Ncols;
-            if (coef != 0.f) {
+            if (live) {
                 float w[32];
                 load_row32<T>(ea.W, y * ea.ldW + col0, w, col0, D, own_tag<T>());
 #pragma unroll
@@ -175,7 +196,7 @@ struct RowEpilogue {
             }
             for (int i = oh_beg; i < oh_end; ++i) {
                 const int64_t n = static_cast<int64_t>(ea.keys[i] & 0xffffffffll);
-                const float g = ea.grad_all[n];
+                const float g = ea.tc_all[n];
                 if (g == 0.f) continue;
                 float hv[32];
                 load_row32<T>(ea.h_all, n * ea.ld_h + col0, hv, col0, D, own_tag<T>());

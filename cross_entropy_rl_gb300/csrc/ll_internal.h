@@ -55,8 +55,10 @@ struct EpiArgs {
     int64_t part_ld;
     const float* lse;        // [M]
     const float* grad;       // [M] grad_logp
-    void* S;                 // [M, ldS] softmax part of g
+    void* S;                 // [M, ldS] off-target part of g (0 at the target)
     int64_t ldS;
+    float* tc;               // [M] target entry of g: grad * (1 - p[y]) (Recomp writes,
+                             //     Dh reads; offset to the launch's rows)
     // dh (M = tokens, N = D): adds gl * W[y] and stores
     const void* W;
     int64_t ldW;
@@ -67,7 +69,7 @@ struct EpiArgs {
     int first_chunk, last_chunk;
     const int* offs;         // [V + 1] token list offsets per vocab row
     const int64_t* keys;     // sorted (target << 32 | token)
-    const float* grad_all;   // [N] grad_logp of every token
+    const float* tc_all;     // [N] target entry of g of every token
     const void* h_all;       // [N, D] hidden of every token
     int64_t ld_h;
     int* status;
@@ -102,12 +104,12 @@ size_t token_sort_bytes(int64_t N);
 cudaError_t launch_token_sort(const int64_t* targets, int64_t N, int64_t V, int64_t* keys,
                               int* offs, cudaStream_t s);
 // db: column sums of S over the chunk's rows added into db_acc (FP32),
-// first chunk starts from +0; with `last`, adds the one-hot term and writes
-// grad_bias in out_dtype.
+// first chunk starts from +0; with `last`, adds the target entries c[n] of
+// the tokens of each vocab row and writes grad_bias in out_dtype.
 size_t db_partial_bytes(int64_t Nc, int64_t V);
 cudaError_t launch_db_chunk(const void* S, int64_t ldS, int s_dtype, int64_t rows, int64_t V,
                             float* partial, float* db_acc, int first, int last, const int* offs,
-                            const int64_t* keys, const float* grad_all, void* grad_bias,
+                            const int64_t* keys, const float* tc_all, void* grad_bias,
                             int out_dtype, cudaStream_t s);
 cudaError_t launch_fill_zero(void* p, int64_t n_elems, int dtype, cudaStream_t s);
 cudaError_t launch_unsatisfied_wait(int* flag, int* status, uint64_t wait_ns, cudaStream_t s);

@@ -8,6 +8,15 @@ Tolerances (|got - ref| <= atol + rtol * |ref| (+ one output ulp)):
   16-bit operands, grads:    atol 5e-4, plus one ulp of the output dtype at
                              |ref| when the output itself is 16-bit (its own
                              rounding is up to half an ulp)
+
+For 16-bit operands the off-target entries S = -grad * p of g are stored in
+the operand dtype before the two gradient contractions.  Outside the
+benchmark shapes (small vocabularies, where p is large) that rounding alone
+can exceed 5e-4, so the small full-parity cases add its worst-case bound,
+u * (|S| . |W|) for grad_hidden, u * (|S|^T . |h|) for grad_weight and
+u * sum_n |S| for grad_bias (u = 2^-8 for bf16, 2^-11 for fp16), computed
+in float64 from the exact S.  At the benchmark shapes the term is below
+1e-5 and the bar is the plain 5e-4.
 """
 import math
 
@@ -50,16 +59,41 @@ def ulp(ref, tdtype):
     return np.exp2(e - m)
 
 
-def check(name, got, ref, atol, rtol, out_dtype=None, report=None):
+def s_rounding_bounds(p):
+    """Worst-case effect of storing S = -grad * p (off-target) in 16 bits."""
+    import oracle as O
+
+    dt = p["dtype"]
+    if dt == "f32":
+        return {}
+    u = 2.0 ** -8 if dt == "bf16" else 2.0 ** -11
+    h, W, b = O.decode(p["h"], dt), O.decode(p["W"], dt), O.decode(p["b"], dt)
+    z = O.linear_logits(h, W, b)
+    lse = O.logsumexp_rows(z)
+    S = np.abs(np.asarray(p["gl"], np.float64))[:, None] * np.exp(z - lse[:, None])
+    y = np.asarray(p["y"])
+    V = W.shape[0]
+    ok = (y >= 0) & (y < V) & (np.asarray(p["gl"]) != 0)
+    S[~ok] = 0.0
+    idx = np.nonzero(ok)[0]
+    S[idx, y[idx]] = 0.0
+    return {"dh": u * S @ np.abs(W), "dW": u * S.T @ np.abs(h), "db": u * S.sum(axis=0)}
+
+
+def check(name, got, ref, atol, rtol, out_dtype=None, report=None, extra=None):
     g = host64(got) if isinstance(got, torch.Tensor) else np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert g.shape == ref.shape, (name, g.shape, ref.shape)
     if g.size == 0:
         return 0.0
-    err = np.abs(g - ref)
-    bound = atol + rtol * np.abs(ref)
+    with np.errstate(invalid="ignore"):
+        err = np.abs(g - ref)
+    err = np.where(g == ref, 0.0, err)  # equal infinities match
+    bound = atol + rtol * np.abs(np.where(np.isfinite(ref), ref, 0.0))
     if out_dtype is not None:
-        bound = bound + ulp(ref, out_dtype)
+        bound = bound + ulp(np.where(np.isfinite(ref), ref, 0.0), out_dtype)
+    if extra is not None:
+        bound = bound + extra
     bad = ~(err <= bound)
     worst = float(np.nanmax(err)) if np.isfinite(err).any() else math.inf
     if report is not None:

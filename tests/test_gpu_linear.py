@@ -7,7 +7,7 @@ import torch
 
 import oracle as O
 from cross_entropy_rl_gb300 import synth
-from gpu_util import TOL, TORCH, assert_pos_zero, bits_equal, check, dev
+from gpu_util import TOL, TORCH, assert_pos_zero, bits_equal, check, dev, s_rounding_bounds
 
 pytestmark = pytest.mark.gpu
 
@@ -27,18 +27,18 @@ def run(ll, p, *, token_chunks=0, dh_dtype=None, dw_dtype=None, gl=None, need=(1
     return dict(logp=logp, lse=lse, dh=dh, dW=dW, db=db)
 
 
-def compare(p, got, ref, report=None):
+def compare(p, got, ref, report=None, gl=None):
+    """Full comparison; small 16-bit cases add the S-storage bound."""
     dt = p["dtype"]
     la, lr = TOL[dt]["logp"]
     ga, gr = TOL[dt]["grad"]
+    sb = s_rounding_bounds(dict(p, gl=p["gl"] if gl is None else gl))
     check("logp", got["logp"], ref["logp"], la, lr, report=report)
     check("lse", got["lse"], ref["lse"], la, lr, report=report)
-    if got["dh"] is not None:
-        check("dh", got["dh"], ref["dh"], ga, gr, out_dtype=got["dh"].dtype, report=report)
-    if got["dW"] is not None:
-        check("dW", got["dW"], ref["dW"], ga, gr, out_dtype=got["dW"].dtype, report=report)
-    if got["db"] is not None:
-        check("db", got["db"], ref["db"], ga, gr, out_dtype=got["db"].dtype, report=report)
+    for k in ("dh", "dW", "db"):
+        if got[k] is not None:
+            check(k, got[k], ref[k], ga, gr, out_dtype=got[k].dtype, report=report,
+                  extra=sb.get(k))
 
 
 def full_ref(p, gl=None):

@@ -69,10 +69,11 @@ __global__ void __launch_bounds__(kSortThreads) bitonic_local_kernel(unsigned lo
     const int64_t k_lo = full ? 2 : k_fixed;
     const int64_t k_hi = full ? kSortSeg : k_fixed;
     for (int64_t k = k_lo; k <= k_hi; k <<= 1) {
-        const int64_t j0 = full ? (k >> 1) : (kSortSeg >> 1);
-        for (int64_t j = j0; j > 0; j >>= 1) {
+        const int j0 = full ? static_cast<int>(k >> 1) : (kSortSeg >> 1);
+        for (int j = j0; j > 0; j >>= 1) {
             for (int p = threadIdx.x; p < kSortSeg / 2; p += kSortThreads) {
-                const int i = static_cast<int>(2 * j * (p / j) + (p % j));
+                // pair index p -> lower element i of the pair (j is a power of two)
+                const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
                 const bool up = ((base + i) & k) == 0;
                 cmp_swap(s[i], s[i + j], up);
             }
@@ -85,7 +86,7 @@ __global__ void __launch_bounds__(kSortThreads) bitonic_local_kernel(unsigned lo
 __global__ void bitonic_global_kernel(unsigned long long* keys, int64_t n, int64_t k, int64_t j) {
     const int64_t p = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
     if (p >= n / 2) return;
-    const int64_t i = 2 * j * (p / j) + (p % j);
+    const int64_t i = ((p & ~(j - 1)) << 1) | (p & (j - 1));  // j is a power of two
     const bool up = (i & k) == 0;
     unsigned long long a = keys[i], b = keys[i + j];
     cmp_swap(a, b, up);

@@ -310,7 +310,7 @@ def run_ours(args, rank, world, local_rank):
         return
     pk, pk_kind = peaks()
     flops = {"fwd_gemm": 2.0 * N * D * V, "recompute_gemm": 2.0 * N * D * V,
-             "dh_gemm": 2.0 * N * D * V, "dw_gemm": 2.0 * N * D * V}
+             "grad_gemm": 4.0 * N * D * V}  # grad_hidden + grad_weight tiles
     gemms = {k: v for k, v in prof.items() if k in flops}
     dom = max(gemms, key=lambda k: gemms[k][1])
     cnt, tot = gemms[dom]

@@ -57,6 +57,7 @@ struct Phase {
 namespace {
 
 constexpr size_t kAlign = 256;
+constexpr int kSideSms = 2;  // SMs left to the side stream during an overlapped GEMM
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -70,6 +71,7 @@ struct DevCache {
     int num_sms = 0;
     int* status = nullptr;
     int cc_major = 0, cc_minor = 0;
+    cudaStream_t side = nullptr;  // side stream for work that overlaps a GEMM
 };
 DevCache g_dev[64];
 std::mutex g_dev_mu;
@@ -119,12 +121,17 @@ int device_info(int dev, DevInfo* out) {
             return LL_ERR_UNSUPPORTED;
         }
         c.status = static_cast<int*>(p);
+        if (cudaStreamCreateWithFlags(&c.side, cudaStreamNonBlocking) != cudaSuccess) {
+            cudaGetLastError();
+            c.side = nullptr;
+        }
         c.ready = true;
     }
     if (!(c.cc_major == 10 && c.cc_minor == 3)) return LL_ERR_UNSUPPORTED;
     out->device = dev;
     out->num_sms = c.num_sms;
     out->status = c.status;
+    out->side = c.side;
     return LL_OK;
 }
 
@@ -157,7 +164,7 @@ constexpr size_t kAutoChunkBytes = size_t(2) << 30;  // softmax workspace budget
 
 struct BwdLayout {
     int64_t chunks, Nc, ldS;
-    size_t S, tc, keys, offs, db, total;
+    size_t S, tc, keys, offs, ctr, db, total;
 };
 BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need_db) {
     BwdLayout L;
@@ -182,6 +189,8 @@ BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need
     off = align_up(off + token_sort_bytes(n1));
     L.offs = off;
     off = align_up(off + size_t(V + 1) * 4);
+    L.ctr = off;
+    off = align_up(off + 64);
     L.db = off;
     if (need_db) off = align_up(off + db_partial_bytes(L.Nc, V));
     L.total = off;
@@ -272,10 +281,18 @@ int ll_forward(const void* hidden, const void* weight, const void* bias, const i
     ea.part_ld = N;
     ea.status = dev.status;
     ea.wait_ns = wait_limit_ns();
+    GemmLaunch G;
+    memset(&G, 0, sizeof(G));
+    G.dtype = dtype;
+    G.nkinds = 1;
+    G.kind[0] = EpiKind::Fwd;
+    G.op[0] = GemmOperands{hidden, D, 0, weight, D, 0, N, V, D};
+    G.shape[0] = sh;
+    G.ea[0] = ea;
     cudaError_t e;
     {
         Phase ph(dtype == LL_F32 ? "fwd_gemm_f32" : "fwd_gemm", s);
-        e = launch_gemm(EpiKind::Fwd, dtype, hidden, D, 0, weight, D, 0, N, V, D, sh, ea, dev, s);
+        e = launch_gemm(G, dev, s);
     }
     if (e != cudaSuccess) return cuda_status(e);
     {
@@ -328,14 +345,37 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight, 
     float* tc = reinterpret_cast<float*>(ws + L.tc);
     int64_t* keys = reinterpret_cast<int64_t*>(ws + L.keys);
     int* offs = reinterpret_cast<int*>(ws + L.offs);
+    int* counter = reinterpret_cast<int*>(ws + L.ctr);
     float* db_part = reinterpret_cast<float*>(ws + L.db);
     const int64_t db_groups_v = (L.Nc < 64 ? L.Nc : 64) * V;
     float* db_acc = db_part + db_groups_v;
     const size_t es = esize(dtype);
 
-    if (need_dw || need_db) {
-        Phase ph("token_sort", s);
-        e = launch_token_sort(targets, N, V, keys, offs, s);
+    // The token sort (only the last chunk's grad_weight / grad_bias epilogue
+    // reads it) runs on a side stream, overlapping the first recompute GEMM,
+    // which leaves kSideSms SMs free for it.
+    cudaEvent_t sort_done = nullptr;
+    const bool need_sort = need_dw || need_db;
+    bool overlap = false;
+    if (need_sort) {
+        cudaEvent_t fork = nullptr;
+        overlap = dev.side != nullptr &&
+                  cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&sort_done, cudaEventDisableTiming) == cudaSuccess;
+        cudaStream_t ss = s;
+        if (overlap) {
+            cudaEventRecord(fork, s);
+            cudaStreamWaitEvent(dev.side, fork, 0);
+            ss = dev.side;
+        }
+        {
+            Phase ph("token_sort", ss);
+            e = launch_token_sort(targets, N, V, keys, offs, ss);
+        }
+        if (overlap) {
+            cudaEventRecord(sort_done, ss);
+            cudaEventDestroy(fork);
+        }
         if (e != cudaSuccess) return cuda_status(e);
     }
 
@@ -351,16 +391,23 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight, 
         const int64_t rows = (N - r0) < L.Nc ? (N - r0) : L.Nc;
         const char* h_c = static_cast<const char*>(hidden) + size_t(r0) * size_t(D) * es;
 
-        // (1) recompute z for the chunk, store S = -grad * softmax
+        // (1) recompute z for the chunk, store S = -grad * p off target and c
         {
-            GemmShape sh;
+            GemmLaunch G;
+            memset(&G, 0, sizeof(G));
+            G.dtype = dtype;
+            G.nkinds = 1;
+            G.kind[0] = EpiKind::Recomp;
+            G.op[0] = GemmOperands{h_c, D, 0, weight, D, 0, rows, V, D};
+            GemmShape& sh = G.shape[0];
             sh.m_blocks = cdiv(rows, kBM);
             sh.n_tiles = cdiv(V, kBN);
             sh.tiles_per_unit = kVocabTilesPerSeg;
             sh.n_segs = cdiv(sh.n_tiles, sh.tiles_per_unit);
             sh.k_blocks = cdiv(D, 64);
             sh.unit_order = 0;
-            EpiArgs ea = base;
+            EpiArgs& ea = G.ea[0];
+            ea = base;
             ea.M = rows;
             ea.Ncols = V;
             ea.targets = targets + r0;
@@ -369,61 +416,83 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight, 
             ea.S = S;
             ea.ldS = L.ldS;
             ea.tc = tc + r0;
+            G.out[0] = OutDesc{S, dtype, rows, V, L.ldS};
+            G.zero_counter = counter;  // for the gradient launch that follows
+            if (overlap && c == 0) G.max_ctas = dev.num_sms - kSideSms;
             Phase ph(dtype == LL_F32 ? "recompute_gemm_f32" : "recompute_gemm", s);
-            e = launch_gemm(EpiKind::Recomp, dtype, h_c, D, 0, weight, D, 0, rows, V, D, sh, ea,
-                            dev, s);
+            e = launch_gemm(G, dev, s);
             if (e != cudaSuccess) return cuda_status(e);
         }
-        // (2) grad_hidden rows of the chunk: S . W + grad * W[y]
-        if (need_dh) {
-            GemmShape sh;
-            sh.m_blocks = cdiv(rows, kBM);
-            sh.n_tiles = cdiv(D, kBN);
-            sh.tiles_per_unit = 1;
-            sh.n_segs = sh.n_tiles;
-            sh.k_blocks = cdiv(V, 64);
-            sh.unit_order = 0;
-            EpiArgs ea = base;
-            ea.M = rows;
-            ea.Ncols = D;
-            ea.targets = targets + r0;
-            ea.grad = grad_logp + r0;
-            ea.tc = tc + r0;
-            ea.W = weight;
-            ea.ldW = D;
-            ea.out = static_cast<char*>(grad_hidden) + size_t(r0) * size_t(D) * esize(dh_dtype);
-            ea.ld_out = D;
-            ea.out_dtype = dh_dtype;
-            Phase ph(dtype == LL_F32 ? "dh_gemm_f32" : "dh_gemm", s);
-            e = launch_gemm(EpiKind::Dh, dtype, S, L.ldS, 0, weight, D, 1, rows, D, V, sh, ea,
-                            dev, s);
-            if (e != cudaSuccess) return cuda_status(e);
+        if (overlap && c == L.chunks - 1) {  // the last chunk's epilogues read the sort
+            cudaStreamWaitEvent(s, sort_done, 0);
+            cudaEventDestroy(sort_done);
+            overlap = false;
         }
-        // (3) grad_weight += S^T . h (+ one-hot part on the last chunk)
-        if (need_dw) {
-            GemmShape sh;
-            sh.m_blocks = cdiv(V, kBM);
-            sh.n_tiles = cdiv(D, kBN);
-            sh.tiles_per_unit = 1;
-            sh.n_segs = sh.n_tiles;
-            sh.k_blocks = cdiv(rows, 64);
-            sh.unit_order = 1;
-            EpiArgs ea = base;
-            ea.M = V;
-            ea.Ncols = D;
-            ea.out = grad_weight;
-            ea.ld_out = D;
-            ea.out_dtype = dw_dtype;
-            ea.first_chunk = c == 0;
-            ea.last_chunk = c == L.chunks - 1;
-            ea.offs = offs;
-            ea.keys = keys;
-            ea.tc_all = tc;
-            ea.h_all = hidden;
-            ea.ld_h = D;
-            Phase ph(dtype == LL_F32 ? "dw_gemm_f32" : "dw_gemm", s);
-            e = launch_gemm(EpiKind::Dw, dtype, S, L.ldS, 1, h_c, D, 1, V, D, rows, sh, ea, dev,
-                            s);
+        // (2)+(3) grad_hidden rows of the chunk (S . W + c * W[y]) and
+        // grad_weight += S^T . h (+ the target part on the last chunk), in
+        // one launch: grad_hidden tiles (K = V) first, grad_weight tiles after
+        if (need_dh || need_dw) {
+            GemmLaunch G;
+            memset(&G, 0, sizeof(G));
+            G.dtype = dtype;
+            int k = 0;
+            if (need_dh) {
+                G.kind[k] = EpiKind::Dh;
+                G.op[k] = GemmOperands{S, L.ldS, 0, weight, D, 1, rows, D, V};
+                GemmShape& sh = G.shape[k];
+                sh.m_blocks = cdiv(rows, kBM);
+                sh.n_tiles = cdiv(D, kBN);
+                sh.tiles_per_unit = 1;
+                sh.n_segs = sh.n_tiles;
+                sh.k_blocks = cdiv(V, 64);
+                sh.unit_order = 0;
+                EpiArgs& ea = G.ea[k];
+                ea = base;
+                ea.M = rows;
+                ea.Ncols = D;
+                ea.targets = targets + r0;
+                ea.grad = grad_logp + r0;
+                ea.tc = tc + r0;
+                ea.W = weight;
+                ea.ldW = D;
+                ea.out = static_cast<char*>(grad_hidden) + size_t(r0) * size_t(D) * esize(dh_dtype);
+                ea.ld_out = D;
+                ea.out_dtype = dh_dtype;
+                G.out[k] = OutDesc{ea.out, dh_dtype, rows, D, D};
+                ++k;
+            }
+            if (need_dw) {
+                G.kind[k] = EpiKind::Dw;
+                G.op[k] = GemmOperands{S, L.ldS, 1, h_c, D, 1, V, D, rows};
+                GemmShape& sh = G.shape[k];
+                sh.m_blocks = cdiv(V, kBM);
+                sh.n_tiles = cdiv(D, kBN);
+                sh.tiles_per_unit = 1;
+                sh.n_segs = sh.n_tiles;
+                sh.k_blocks = cdiv(rows, 64);
+                sh.unit_order = 1;
+                EpiArgs& ea = G.ea[k];
+                ea = base;
+                ea.M = V;
+                ea.Ncols = D;
+                ea.out = grad_weight;
+                ea.ld_out = D;
+                ea.out_dtype = dw_dtype;
+                ea.first_chunk = c == 0;
+                ea.last_chunk = c == L.chunks - 1;
+                ea.offs = offs;
+                ea.keys = keys;
+                ea.tc_all = tc;
+                ea.h_all = hidden;
+                ea.ld_h = D;
+                G.out[k] = OutDesc{grad_weight, dw_dtype, V, D, D};
+                ++k;
+            }
+            G.nkinds = k;
+            G.counter = k == 2 ? counter : nullptr;
+            const char* label = dtype == LL_F32 ? "grad_gemm_f32" : "grad_gemm";
+            Phase ph(label, s);
+            e = launch_gemm(G, dev, s);
             if (e != cudaSuccess) return cuda_status(e);
         }
         // (4) grad_bias: fixed-order column sums of S (+ one-hot part at the end)

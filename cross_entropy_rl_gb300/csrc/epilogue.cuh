@@ -13,10 +13,11 @@
 //           target), to the chunk workspace, and the FP32 target entry
 //           c[n] = grad_logp * (1 - p[n, y]) to a per-token array.
 //   Dh      acc = S . W tile -> adds c[n] * W[y] in FP32, stores grad_hidden.
-//   Dw      acc = S^T . h tile -> adds the running grad_weight (FP32 +0
-//           start on the first token chunk) and, on the last chunk, the
-//           target part sum over tokens with target v of c[n] * h[n], in
-//           ascending token order.
+//   Dw      acc = S^T . h tile -> on the first token chunk 0 + acc (a +0
+//           start), on later chunks the running grad_weight is added (here,
+//           or by the TMA reduce-add of the store); on the last chunk the
+//           target part sum over tokens with target v of c[n] * h[n] is
+//           added in ascending token order.
 //
 // g = grad_logp * (onehot - p) is split into its target column, kept exact
 // in FP32 (c), and the off-target entries S, stored in 16 bits.  The 16-bit
@@ -167,7 +168,6 @@ struct RowEpilogue {
                 }
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = coef * v[j];
-                store_row32<T>(ea.S, row * ea.ldS + col0, v, col0, V, own_tag<T>());
             }
         } else if constexpr (E == EpiKind::Dh) {
             if (!rvalid) return;
@@ -181,14 +181,13 @@ struct RowEpilogue {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.f;
             }
-            store_row32<T>(ea.out, row * ea.ld_out + col0, v, col0, D, ea.out_dtype);
         } else {  // Dw
             if (!rvalid) return;
             const int64_t D = ea.Ncols;
             if (ea.first_chunk) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.f + v[j];
-            } else {
+            } else if (ea.dw_add_prev) {
                 float prev[32];
                 load_row32<T>(ea.out, row * ea.ld_out + col0, prev, col0, D, ea.out_dtype);
 #pragma unroll
@@ -203,7 +202,17 @@ struct RowEpilogue {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = fmaf(g, hv[j], v[j]);
             }
-            store_row32<T>(ea.out, row * ea.ld_out + col0, v, col0, D, ea.out_dtype);
+        }
+    }
+
+    // Direct row stores (CUDA-core path); the tensor-core path stages the
+    // values in shared memory and writes them with TMA instead.
+    __device__ __forceinline__ void store_direct(const EpiArgs& ea, const float (&v)[32],
+                                                 int64_t col0) {
+        if constexpr (E == EpiKind::Recomp) {
+            if (rvalid) store_row32<T>(ea.S, row * ea.ldS + col0, v, col0, ea.Ncols, own_tag<T>());
+        } else if constexpr (E == EpiKind::Dh || E == EpiKind::Dw) {
+            if (rvalid) store_row32<T>(ea.out, row * ea.ld_out + col0, v, col0, ea.Ncols, ea.out_dtype);
         }
     }
 

@@ -1,10 +1,9 @@
-// Tensor-core GEMM with fused epilogues for the 16-bit operand paths
+// Tensor-core GEMMs with fused epilogues for the 16-bit operand paths
 // (bf16 / fp16 operands, FP32 accumulation in TMEM).
 //
 // The three contractions of the fused linear logp (RL-Kernel issue #261,
-// "Current accumulation": the chunked matmul and its accumulation into an
-// FP32 gradient table; Liger-Kernel PR #1324, "Details": no [V, H]
-// temporary) run here:
+// "Current accumulation": the chunked matmul accumulated into an FP32
+// gradient table; Liger-Kernel PR #1324, "Details": no [V, H] temporary):
 //   forward / recompute   z  = h . W^T        A = h [rows, D]  (K-major)
 //                                              B = W [V, D]     (K-major)
 //   grad_hidden           dh = S . W          A = S [rows, V]  (K-major)
@@ -13,12 +12,22 @@
 //                                              B = h [rows, D]  (MN-major)
 //
 // Design (sm_103a): one persistent CTA per SM, 6 warps.
-//   warp 0      TMA producer: 128-byte-swizzled tiles into a 4-stage ring
+//   warp 0      scheduler + TMA producer: picks work units (static
+//               round-robin, or an atomic counter), publishes them in a
+//               shared-memory ring, loads 128-byte-swizzled tiles into a
+//               4-stage ring
 //   warp 1      allocates 512 TMEM columns, issues tcgen05.mma (128x256x16)
-//   warps 2..5  epilogue: tcgen05.ld of its 32 TMEM lanes, fused epilogue
-// Two 256-column accumulators in TMEM let the epilogue of one tile overlap
-// the MMAs of the next.  Work units are walked in a static round-robin order
-// so that the result never depends on scheduling.
+//   warps 2..5  epilogue: tcgen05.ld of its 32 TMEM lanes, fused epilogue,
+//               output rows staged in swizzled shared memory and written by
+//               TMA bulk-tensor stores (or reduce-adds)
+// One launch may carry two tile kinds (grad_hidden and grad_weight tiles of
+// the same chunk), the long kind first, so that the dynamic scheduler evens
+// out the SMs' work.  Two 256-column accumulators in TMEM let the epilogue
+// of one tile overlap the MMAs of the next.  Which SM computes a tile never
+// changes any result: every output element is one MMA accumulation over K
+// in a fixed order.
+#include <string.h>
+
 #include <mutex>
 #include <type_traits>
 
@@ -35,41 +44,174 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kMnBoxBytes = 64 * kBK * 2;  // one 64(MN) x 64(K) box, 8 KB
 constexpr int kThreads = 192;
 constexpr int kTmemCols = 512;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kSchedDepth = 4;
+constexpr int kOutBufBytes = 32 * 128;  // one warp's 32 rows x 128 bytes
+constexpr int kOutBytes = 4 * 2 * kOutBufBytes;
+constexpr int kSmemBytes = kStages * kStageBytes + kOutBytes + 1024 /*align*/ + 512 /*bars*/;
 
 struct Bars {
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
+    uint64_t sfull[kSchedDepth];
+    uint64_t sempty[kSchedDepth];
     uint64_t drain;
+    int sched[kSchedDepth];
     uint32_t tmem_base;
     int abort;
 };
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
-__device__ __forceinline__ void decode_unit(const GemmShape& sh, int64_t u, int64_t& mb,
-                                            int64_t& seg) {
+// Launch-wide parameters (by value).
+struct KParams {
+    GemmShape sh[2];
+    int64_t n_units[2];  // units of kind 0, then kind 1
+    int dynamic;         // 1: units handed out by an atomic counter
+    int* counter;        // zero before the launch when dynamic
+    int* zero_counter;   // if set, CTA 0 zeroes it (for the next launch)
+    int out16[2];        // output element of the kind is 16-bit
+    int reduce[2];       // TMA reduce-add instead of store
+    int64_t out_rows[2], out_cols[2];
+};
+
+// ----------------------------------------------------------- bulk stores
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x,
+                                             int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src,
+                                                  int32_t x, int32_t y) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group"
+        " [%0, {%2, %3}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+struct Unit {
+    int kind;
+    int64_t mb, seg, t0, t1, k_blocks;
+};
+
+__device__ __forceinline__ Unit decode_unit(const KParams& P, int64_t u) {
+    Unit r;
+    r.kind = u < P.n_units[0] ? 0 : 1;
+    const GemmShape& sh = P.sh[r.kind];
+    const int64_t v = r.kind ? u - P.n_units[0] : u;
     if (sh.unit_order == 0) {
-        seg = u / sh.m_blocks;
-        mb = u % sh.m_blocks;
+        r.seg = v / sh.m_blocks;
+        r.mb = v % sh.m_blocks;
     } else {
-        mb = u / sh.n_segs;
-        seg = u % sh.n_segs;
+        r.mb = v / sh.n_segs;
+        r.seg = v % sh.n_segs;
+    }
+    r.t0 = r.seg * sh.tiles_per_unit;
+    r.t1 = min(r.t0 + sh.tiles_per_unit, sh.n_tiles);
+    r.k_blocks = sh.k_blocks;
+    return r;
+}
+
+template <typename T, EpiKind E, bool A_MN, bool B_MN>
+struct Kind {
+    using Epi = RowEpilogue<E, T>;
+    static constexpr EpiKind kEpi = E;
+    static constexpr bool kAmn = A_MN, kBmn = B_MN;
+    static constexpr int kFmt = std::is_same<T, __half>::value ? 0 : 1;
+    static constexpr uint32_t kIdesc = instr_desc(kFmt, A_MN, B_MN, kBM, kBN);
+};
+
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void load_stage(uint8_t* sa, const CUtensorMap* tmA,
+                                           const CUtensorMap* tmB, uint64_t* fb, int32_t k0,
+                                           int32_t m0, int32_t n0) {
+    uint8_t* sb = sa + kABytes;
+    mbar_arrive_expect_tx(fb, kStageBytes);
+    if constexpr (!A_MN) {
+        tma_load_2d(sa, tmA, fb, k0, m0);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sa + j * kMnBoxBytes, tmA, fb, m0 + 64 * j, k0);
+    }
+    if constexpr (!B_MN) {
+        tma_load_2d(sb, tmB, fb, k0, n0);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sb + j * kMnBoxBytes, tmB, fb, n0 + 64 * j, k0);
     }
 }
 
-template <EpiKind E, typename T, bool A_MN, bool B_MN>
+template <bool A_MN, bool B_MN, uint32_t IDESC>
+__device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t sa, bool first) {
+    const uint32_t sb = sa + kABytes;
+#pragma unroll
+    for (int kk = 0; kk < kBK / 16; ++kk) {
+        const uint64_t ad = A_MN ? smem_desc_sw128(sa + kk * 2048, kMnBoxBytes, 1024)
+                                 : smem_desc_sw128(sa + kk * 32, 16, 1024);
+        const uint64_t bd = B_MN ? smem_desc_sw128(sb + kk * 2048, kMnBoxBytes, 1024)
+                                 : smem_desc_sw128(sb + kk * 32, 16, 1024);
+        tc_mma<0>(d_tmem, ad, bd, IDESC, (!first || kk > 0) ? 1u : 0u);
+    }
+}
+
+// Stage 32 values of this thread's row into the warp's swizzled buffer
+// (32 rows x 128 bytes, 16-byte chunk c of row r at chunk c ^ (r & 7), the
+// layout of a 128-byte-swizzled TMA box): fp32 fills the whole row; 16-bit
+// fills half `h` of it.
+template <typename T>
+__device__ __forceinline__ void stage_row(uint8_t* buf, int lane, const float (&v)[32], bool out16,
+                                          int h) {
+    uint8_t* rowp = buf + lane * 128;
+    const int sw = lane & 7;
+    if (!out16) {
+#pragma unroll
+        for (int sl = 0; sl < 8; ++sl)
+            *reinterpret_cast<float4*>(rowp + ((sl ^ sw) << 4)) =
+                make_float4(v[4 * sl], v[4 * sl + 1], v[4 * sl + 2], v[4 * sl + 3]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint4 u;
+            T* e = reinterpret_cast<T*>(&u);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) e[j] = Elem<T>::from_f(v[8 * k + j]);
+            *reinterpret_cast<uint4*>(rowp + (((4 * h + k) ^ sw) << 4)) = u;
+        }
+    }
+}
+
+template <typename T, class K0, class K1, int NK>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const GemmShape sh,
-                   const EpiArgs ea) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
+                   const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmA1,
+                   const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO1,
+                   const KParams P, const EpiArgs ea0, const EpiArgs ea1) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Bars* bars = reinterpret_cast<Bars*>(smem + kStages * kStageBytes);
+    uint8_t* outbuf = smem + kStages * kStageBytes;
+    Bars* bars = reinterpret_cast<Bars*>(outbuf + kOutBytes);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t n_units = sh.m_blocks * sh.n_segs;
+    const int64_t total = P.n_units[0] + (NK > 1 ? P.n_units[1] : 0);
+    const uint64_t wait_ns = ea0.wait_ns;
+    int* status = ea0.status;
     volatile int* abort = &bars->abort;
 
     if (threadIdx.x == 0) {
@@ -81,11 +223,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->tfull[b], 1);
             mbar_init(&bars->tempty[b], 4);
         }
+        for (int s = 0; s < kSchedDepth; ++s) {
+            mbar_init(&bars->sfull[s], 1);
+            mbar_init(&bars->sempty[s], 5);  // MMA warp + 4 epilogue warps
+        }
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmA0);
+        tma_prefetch_desc(&tmB0);
+        if (NK > 1) {
+            tma_prefetch_desc(&tmA1);
+            tma_prefetch_desc(&tmB1);
+        }
+        if (P.zero_counter && blockIdx.x == 0) *P.zero_counter = 0;
     }
     if (warp == 1) {
         tmem_alloc(&bars->tmem_base, kTmemCols);
@@ -97,46 +248,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        int stage = 0;
-        uint32_t phase = 0;
+        // ------------------------------------------- scheduler + TMA producer
+        int stage = 0, sslot = 0;
+        uint32_t phase = 0, sphase = 0;
         uint32_t issued_phase[kStages];
         bool issued[kStages];
         for (int s = 0; s < kStages; ++s) issued[s] = false;
         bool ok = true;
-        for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            int64_t mb, seg;
-            decode_unit(sh, u, mb, seg);
-            const int64_t t0 = seg * sh.tiles_per_unit;
-            const int64_t t1 = min(t0 + sh.tiles_per_unit, sh.n_tiles);
-            for (int64_t t = t0; t < t1 && ok; ++t) {
-                for (int64_t kb = 0; kb < sh.k_blocks; ++kb) {
-                    if (!__all_sync(0xffffffffu, mbar_wait(&bars->empty[stage], phase ^ 1, ea.wait_ns, abort))) {
+        int64_t next_static = blockIdx.x;
+        while (ok) {
+            int64_t u;
+            if (P.dynamic) {
+                int got = 0;
+                if (lane == 0) got = atomicAdd(P.counter, 1);
+                u = __shfl_sync(0xffffffffu, got, 0);
+            } else {
+                u = next_static;
+                next_static += gridDim.x;
+            }
+            if (u >= total) u = -1;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(&bars->sempty[sslot], sphase ^ 1, wait_ns, abort))) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                bars->sched[sslot] = static_cast<int>(u);
+                mbar_arrive(&bars->sfull[sslot]);
+            }
+            __syncwarp();
+            if (++sslot == kSchedDepth) {
+                sslot = 0;
+                sphase ^= 1;
+            }
+            if (u < 0) break;
+            const Unit un = decode_unit(P, u);
+            for (int64_t t = un.t0; t < un.t1 && ok; ++t) {
+                for (int64_t kb = 0; kb < un.k_blocks; ++kb) {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(&bars->empty[stage], phase ^ 1, wait_ns, abort))) {
                         ok = false;
                         break;
                     }
                     if (lane == 0) {
-                        uint64_t* fb = &bars->full[stage];
                         uint8_t* sa = smem + stage * kStageBytes;
-                        uint8_t* sb = sa + kABytes;
-                        mbar_arrive_expect_tx(fb, kStageBytes);
                         const int32_t k0 = static_cast<int32_t>(kb * kBK);
-                        const int32_t m0 = static_cast<int32_t>(mb * kBM);
+                        const int32_t m0 = static_cast<int32_t>(un.mb * kBM);
                         const int32_t n0 = static_cast<int32_t>(t * kBN);
-                        if constexpr (!A_MN) {
-                            tma_load_2d(sa, &tmA, fb, k0, m0);
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < kBM / 64; ++j)
-                                tma_load_2d(sa + j * kMnBoxBytes, &tmA, fb, m0 + 64 * j, k0);
-                        }
-                        if constexpr (!B_MN) {
-                            tma_load_2d(sb, &tmB, fb, k0, n0);
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < kBN / 64; ++j)
-                                tma_load_2d(sb + j * kMnBoxBytes, &tmB, fb, n0 + 64 * j, k0);
-                        }
+                        if (NK == 1 || un.kind == 0)
+                            load_stage<K0::kAmn, K0::kBmn>(sa, &tmA0, &tmB0, &bars->full[stage],
+                                                           k0, m0, n0);
+                        else
+                            load_stage<K1::kAmn, K1::kBmn>(sa, &tmA1, &tmB1, &bars->full[stage],
+                                                           k0, m0, n0);
                     }
                     __syncwarp();
                     issued[stage] = true;
@@ -149,53 +313,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (!ok) {
-            if (lane == 0) set_status(ea.status, LL_ERR_DEVICE_TIMEOUT);
+            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
             bars->abort = 1;
-            // let every issued copy land before the CTA may exit
             for (int s = 0; s < kStages; ++s)
-                if (issued[s]) mbar_wait(&bars->full[s], issued_phase[s], ea.wait_ns, nullptr);
+                if (issued[s]) mbar_wait(&bars->full[s], issued_phase[s], wait_ns, nullptr);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        constexpr int fmt = std::is_same<T, __half>::value ? 0 : 1;
-        constexpr uint32_t idesc = instr_desc(fmt, A_MN, B_MN, kBM, kBN);
-        int stage = 0;
-        uint32_t phase = 0;
-        int buf = 0;
-        uint32_t bphase = 0;
+        int stage = 0, sslot = 0, buf = 0;
+        uint32_t phase = 0, sphase = 0, bphase = 0;
         bool ok = true;
         const uint32_t sbase = smem_u32(smem);
-        for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            int64_t mb, seg;
-            decode_unit(sh, u, mb, seg);
-            const int64_t t0 = seg * sh.tiles_per_unit;
-            const int64_t t1 = min(t0 + sh.tiles_per_unit, sh.n_tiles);
-            for (int64_t t = t0; t < t1 && ok; ++t) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&bars->tempty[buf], bphase ^ 1, ea.wait_ns, abort))) {
+        while (ok) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->sfull[sslot], sphase, wait_ns, abort))) {
+                ok = false;
+                break;
+            }
+            const int u = *reinterpret_cast<volatile int*>(&bars->sched[sslot]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->sempty[sslot]);
+            if (++sslot == kSchedDepth) {
+                sslot = 0;
+                sphase ^= 1;
+            }
+            if (u < 0) break;
+            const Unit un = decode_unit(P, u);
+            for (int64_t t = un.t0; t < un.t1 && ok; ++t) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&bars->tempty[buf], bphase ^ 1, wait_ns, abort))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + buf * kBN;
-                for (int64_t kb = 0; kb < sh.k_blocks; ++kb) {
-                    if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[stage], phase, ea.wait_ns, abort))) {
+                for (int64_t kb = 0; kb < un.k_blocks; ++kb) {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(&bars->full[stage], phase, wait_ns, abort))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     if (lane == 0) {
                         const uint32_t sa = sbase + stage * kStageBytes;
-                        const uint32_t sb = sa + kABytes;
-#pragma unroll
-                        for (int kk = 0; kk < kBK / 16; ++kk) {
-                            const uint64_t ad =
-                                A_MN ? smem_desc_sw128(sa + kk * 2048, kMnBoxBytes, 1024)
-                                     : smem_desc_sw128(sa + kk * 32, 16, 1024);
-                            const uint64_t bd =
-                                B_MN ? smem_desc_sw128(sb + kk * 2048, kMnBoxBytes, 1024)
-                                     : smem_desc_sw128(sb + kk * 32, 16, 1024);
-                            tc_mma<0>(d_tmem, ad, bd, idesc, (kb > 0 || kk > 0) ? 1u : 0u);
-                        }
+                        if (NK == 1 || un.kind == 0)
+                            mma_stage<K0::kAmn, K0::kBmn, K0::kIdesc>(d_tmem, sa, kb == 0);
+                        else
+                            mma_stage<K1::kAmn, K1::kBmn, K1::kIdesc>(d_tmem, sa, kb == 0);
                         tc_commit(&bars->empty[stage]);
                     }
                     __syncwarp();
@@ -214,29 +377,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (!ok) {
-            if (lane == 0) set_status(ea.status, LL_ERR_DEVICE_TIMEOUT);
+            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
             bars->abort = 1;
         }
-        // every MMA issued by this warp completes before TMEM is released
         if (lane == 0) tc_commit(&bars->drain);
         __syncwarp();
-        mbar_wait(&bars->drain, 0, ea.wait_ns, nullptr);
+        mbar_wait(&bars->drain, 0, wait_ns, nullptr);
     } else {
         // ------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lanes [32q, 32q + 32)
         const int r_in_tile = q * 32 + lane;
-        int buf = 0;
-        uint32_t bphase = 0;
+        uint8_t* wbuf = outbuf + q * 2 * kOutBufBytes;
+        int sslot = 0, buf = 0, sidx = 0;
+        uint32_t sphase = 0, bphase = 0;
         bool ok = true;
-        RowEpilogue<E, T> epi;
-        for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            int64_t mb, seg;
-            decode_unit(sh, u, mb, seg);
-            const int64_t t0 = seg * sh.tiles_per_unit;
-            const int64_t t1 = min(t0 + sh.tiles_per_unit, sh.n_tiles);
-            epi.begin_unit(ea, mb * kBM + r_in_tile);
-            for (int64_t t = t0; t < t1; ++t) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&bars->tfull[buf], bphase, ea.wait_ns, abort))) {
+        typename K0::Epi epi0;
+        typename K1::Epi epi1;
+        while (ok) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&bars->sfull[sslot], sphase, wait_ns, abort))) {
+                ok = false;
+                break;
+            }
+            const int u = *reinterpret_cast<volatile int*>(&bars->sched[sslot]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->sempty[sslot]);
+            if (++sslot == kSchedDepth) {
+                sslot = 0;
+                sphase ^= 1;
+            }
+            if (u < 0) break;
+            const Unit un = decode_unit(P, u);
+            const int kind = (NK == 1) ? 0 : un.kind;
+            const EpiArgs& ea = kind == 0 ? ea0 : ea1;
+            const CUtensorMap* tmO = kind == 0 ? &tmO0 : &tmO1;
+            const bool out16 = P.out16[kind] != 0;
+            const bool reduce = P.reduce[kind] != 0;
+            const bool stores = (kind == 0 ? K0::kEpi : K1::kEpi) != EpiKind::Fwd;
+            const int64_t row0 = un.mb * kBM + q * 32;  // first output row of this warp
+            if (kind == 0)
+                epi0.begin_unit(ea, un.mb * kBM + r_in_tile);
+            else
+                epi1.begin_unit(ea, un.mb * kBM + r_in_tile);
+            for (int64_t t = un.t0; t < un.t1; ++t) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&bars->tfull[buf], bphase, wait_ns, abort))) {
                     ok = false;
                     break;
                 }
@@ -251,7 +435,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    epi.chunk(ea, v, t * kBN + c * 32);
+                    const int64_t col0 = t * kBN + c * 32;
+                    if (kind == 0)
+                        epi0.chunk(ea, v, col0);
+                    else
+                        epi1.chunk(ea, v, col0);
+                    if (!stores) continue;
+                    const int h = out16 ? (c & 1) : 0;
+                    uint8_t* sb = wbuf + (sidx & 1) * kOutBufBytes;
+                    if (h == 0) {  // the store that last used this buffer has read it
+                        if (lane == 0) bulk_wait_read_1();
+                        __syncwarp();
+                    }
+                    stage_row<T>(sb, lane, v, out16, h);
+                    if (!out16 || h == 1) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        const int64_t x0 = out16 ? col0 - 32 : col0;
+                        if (lane == 0 && row0 < P.out_rows[kind] && x0 < P.out_cols[kind]) {
+                            if (reduce)
+                                tma_reduce_add_2d(tmO, sb, static_cast<int32_t>(x0),
+                                                  static_cast<int32_t>(row0));
+                            else
+                                tma_store_2d(tmO, sb, static_cast<int32_t>(x0),
+                                             static_cast<int32_t>(row0));
+                            bulk_commit();
+                        }
+                        ++sidx;
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -262,10 +473,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) break;
-            epi.end_unit(ea, seg);
+            if (kind == 0)
+                epi0.end_unit(ea, un.seg);
+            else
+                epi1.end_unit(ea, un.seg);
         }
+        if (lane == 0) bulk_wait_all();
         if (!ok) {
-            if (lane == 0) set_status(ea.status, LL_ERR_DEVICE_TIMEOUT);
+            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
             bars->abort = 1;
         }
     }
@@ -296,27 +511,54 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+CUtensorMapDataType map_type(int dtype) {
+    return dtype == LL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                            : dtype == LL_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+}
+
 // 2-D map over a row-major [rows, cols] matrix with row stride `ld`
 // elements; box = box_cols x box_rows, 128-byte swizzle, zero fill.
-bool make_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int esize,
-              int64_t cols, int64_t rows, int64_t ld, int box_cols, int box_rows) {
+bool make_map(CUtensorMap* map, const void* base, int dtype, int64_t cols, int64_t rows,
+              int64_t ld, int box_cols, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
+    const int es = dtype == LL_F32 ? 4 : 2;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esize};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * es};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols),
                                static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+    return fn(map, map_type(dtype), 2, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <EpiKind E, typename T, bool A_MN, bool B_MN>
-cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const GemmShape& sh,
-                       const EpiArgs& ea, const DevInfo& dev, cudaStream_t s) {
-    auto kern = gemm_tc_kernel<E, T, A_MN, B_MN>;
+bool operand_maps(const GemmOperands& g, int dtype, CUtensorMap* ma, CUtensorMap* mb) {
+    // K-major operand: [rows, K], box 64(K) x rows; MN-major: [K, MN], box 64 x 64.
+    const bool oka = g.a_mn ? make_map(ma, g.A, dtype, g.M, g.K, g.lda, 64, kBK)
+                            : make_map(ma, g.A, dtype, g.K, g.M, g.lda, kBK, kBM);
+    const bool okb = g.b_mn ? make_map(mb, g.B, dtype, g.N, g.K, g.ldb, 64, kBK)
+                            : make_map(mb, g.B, dtype, g.K, g.N, g.ldb, kBK, kBN);
+    return oka && okb;
+}
+
+// Store map of an epilogue output ([rows, cols], row stride ld): boxes of
+// 32 rows x 128 bytes.  TMA clips the parts of a box outside [rows, cols].
+bool out_map(CUtensorMap* m, const OutDesc& o) {
+    if (!o.ptr) {
+        memset(m, 0, sizeof(*m));
+        return true;
+    }
+    const int box_cols = o.dtype == LL_F32 ? 32 : 64;
+    return make_map(m, o.ptr, o.dtype, o.cols, o.rows, o.ld, box_cols, 32);
+}
+
+template <typename T, class K0, class K1, int NK>
+cudaError_t launch_k(const CUtensorMap* m, const KParams& P, const EpiArgs& ea0,
+                     const EpiArgs& ea1, const DevInfo& dev, int max_ctas, cudaStream_t s) {
+    auto kern = gemm_tc_kernel<T, K0, K1, NK>;
     static int configured[64] = {0};
     if (dev.device < 64 && !configured[dev.device]) {
         cudaError_t e =
@@ -324,23 +566,31 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const GemmSha
         if (e != cudaSuccess) return e;
         configured[dev.device] = 1;
     }
-    const int64_t units = sh.m_blocks * sh.n_segs;
-    const int grid = static_cast<int>(units < dev.num_sms ? units : dev.num_sms);
+    const int64_t units = P.n_units[0] + (NK > 1 ? P.n_units[1] : 0);
+    const int cap = (max_ctas > 0 && max_ctas < dev.num_sms) ? max_ctas : dev.num_sms;
+    int grid = static_cast<int>(units < cap ? units : cap);
+    if (grid < 1) grid = 1;
     note_launches(1);
-    kern<<<grid, kThreads, kSmemBytes, s>>>(a, b, sh, ea);
+    kern<<<grid, kThreads, kSmemBytes, s>>>(m[0], m[1], m[2], m[3], m[4], m[5], P, ea0, ea1);
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t dispatch(EpiKind kind, const CUtensorMap& a, const CUtensorMap& b,
-                     const GemmShape& sh, const EpiArgs& ea, const DevInfo& dev,
-                     cudaStream_t s) {
-    switch (kind) {
-        case EpiKind::Fwd: return launch_one<EpiKind::Fwd, T, false, false>(a, b, sh, ea, dev, s);
-        case EpiKind::Recomp:
-            return launch_one<EpiKind::Recomp, T, false, false>(a, b, sh, ea, dev, s);
-        case EpiKind::Dh: return launch_one<EpiKind::Dh, T, false, true>(a, b, sh, ea, dev, s);
-        case EpiKind::Dw: return launch_one<EpiKind::Dw, T, true, true>(a, b, sh, ea, dev, s);
+cudaError_t dispatch(const GemmLaunch& L, const CUtensorMap* m, const KParams& P,
+                     const DevInfo& dev, cudaStream_t s) {
+    using Fwd = Kind<T, EpiKind::Fwd, false, false>;
+    using Rec = Kind<T, EpiKind::Recomp, false, false>;
+    using Dh = Kind<T, EpiKind::Dh, false, true>;
+    using Dw = Kind<T, EpiKind::Dw, true, true>;
+    if (L.nkinds == 1) {
+        switch (L.kind[0]) {
+            case EpiKind::Fwd: return launch_k<T, Fwd, Fwd, 1>(m, P, L.ea[0], L.ea[0], dev, L.max_ctas, s);
+            case EpiKind::Recomp: return launch_k<T, Rec, Rec, 1>(m, P, L.ea[0], L.ea[0], dev, L.max_ctas, s);
+            case EpiKind::Dh: return launch_k<T, Dh, Dh, 1>(m, P, L.ea[0], L.ea[0], dev, L.max_ctas, s);
+            case EpiKind::Dw: return launch_k<T, Dw, Dw, 1>(m, P, L.ea[0], L.ea[0], dev, L.max_ctas, s);
+        }
+    } else if (L.kind[0] == EpiKind::Dh && L.kind[1] == EpiKind::Dw) {
+        return launch_k<T, Dh, Dw, 2>(m, P, L.ea[0], L.ea[1], dev, L.max_ctas, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -353,23 +603,48 @@ cudaError_t launch_gemm_f32(EpiKind kind, const void* A, int64_t lda, int a_mn, 
                             const GemmShape& shape, const EpiArgs& ea, const DevInfo& dev,
                             cudaStream_t s);
 
-cudaError_t launch_gemm(EpiKind kind, int dtype, const void* A, int64_t lda, int a_mn,
-                        const void* B, int64_t ldb, int b_mn, int64_t M, int64_t N, int64_t K,
-                        const GemmShape& shape, const EpiArgs& ea, const DevInfo& dev,
-                        cudaStream_t s) {
-    if (dtype == LL_F32)
-        return launch_gemm_f32(kind, A, lda, a_mn, B, ldb, b_mn, M, N, K, shape, ea, dev, s);
-    const CUtensorMapDataType dt =
-        dtype == LL_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    CUtensorMap ma, mb;
-    // K-major operand: [rows, K] box K=64 x rows; MN-major: [K, MN] box 64 x 64.
-    const bool oka = a_mn ? make_map(&ma, A, dt, 2, M, K, lda, 64, kBK)
-                          : make_map(&ma, A, dt, 2, K, M, lda, kBK, kBM);
-    const bool okb = b_mn ? make_map(&mb, B, dt, 2, N, K, ldb, 64, kBK)
-                          : make_map(&mb, B, dt, 2, K, N, ldb, kBK, kBN);
-    if (!oka || !okb) return cudaErrorInvalidValue;
-    if (dtype == LL_BF16) return dispatch<__nv_bfloat16>(kind, ma, mb, shape, ea, dev, s);
-    return dispatch<__half>(kind, ma, mb, shape, ea, dev, s);
+cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s) {
+    if (L.dtype == LL_F32) {
+        for (int k = 0; k < L.nkinds; ++k) {
+            const GemmOperands& g = L.op[k];
+            EpiArgs ea = L.ea[k];
+            ea.dw_add_prev = !ea.first_chunk;
+            cudaError_t e = launch_gemm_f32(L.kind[k], g.A, g.lda, g.a_mn, g.B, g.ldb, g.b_mn,
+                                            g.M, g.N, g.K, L.shape[k], ea, dev, s);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    CUtensorMap m[6];
+    memset(m, 0, sizeof(m));
+    KParams P;
+    memset(&P, 0, sizeof(P));
+    GemmLaunch G = L;
+    for (int k = 0; k < G.nkinds; ++k) {
+        if (!operand_maps(G.op[k], G.dtype, &m[3 * k], &m[3 * k + 1])) return cudaErrorInvalidValue;
+        if (!out_map(&m[3 * k + 2], G.out[k])) return cudaErrorInvalidValue;
+        P.sh[k] = G.shape[k];
+        P.n_units[k] = G.shape[k].m_blocks * G.shape[k].n_segs;
+        P.out16[k] = G.out[k].dtype != LL_F32;
+        P.out_rows[k] = G.out[k].rows;
+        P.out_cols[k] = G.out[k].cols;
+        if (G.kind[k] == EpiKind::Dw && !G.ea[k].first_chunk) {
+            // later token chunks: an FP32 table is updated by the store's
+            // reduce-add; a 16-bit table is read, added in FP32 and rounded
+            P.reduce[k] = !P.out16[k];
+            G.ea[k].dw_add_prev = P.out16[k];
+        }
+    }
+    if (G.nkinds == 1) {
+        m[3] = m[0];
+        m[4] = m[1];
+        m[5] = m[2];
+    }
+    P.dynamic = G.counter != nullptr;
+    P.counter = G.counter;
+    P.zero_counter = G.zero_counter;
+    if (G.dtype == LL_BF16) return dispatch<__nv_bfloat16>(G, m, P, dev, s);
+    return dispatch<__half>(G, m, P, dev, s);
 }
 
 }  // namespace ll

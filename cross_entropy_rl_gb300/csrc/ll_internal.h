@@ -22,7 +22,8 @@ constexpr int64_t kMaxV = (int64_t(1) << 31) - 1 - 256;
 struct DevInfo {
     int device;
     int num_sms;
-    int* status;  // device status word (static device storage)
+    int* status;         // device status word (static device storage)
+    cudaStream_t side;   // library side stream of the device (may be null)
 };
 
 // Wait limit for bounded device-side waits, nanoseconds.
@@ -67,6 +68,7 @@ struct EpiArgs {
     int out_dtype;
     // dW (M = vocab, N = D)
     int first_chunk, last_chunk;
+    int dw_add_prev;         // epilogue adds the stored grad_weight (else the store reduces)
     const int* offs;         // [V + 1] token list offsets per vocab row
     const int64_t* keys;     // sorted (target << 32 | token)
     const float* tc_all;     // [N] target entry of g of every token
@@ -85,14 +87,42 @@ struct GemmShape {
     int unit_order;          // 0: segment-major, 1: m-major
 };
 
-// One tensor-core GEMM with a fused epilogue.  dtype: LL_BF16 / LL_F16 /
-// LL_F32 (FP32 runs on the CUDA-core path).  Operand maps are built inside.
+// Operands of one GEMM kind:
 //   A: [M, K] (a_mn = 0, row stride lda) or [K, M] (a_mn = 1)
 //   B: [N, K] (b_mn = 0) or [K, N] (b_mn = 1)
-cudaError_t launch_gemm(EpiKind kind, int dtype, const void* A, int64_t lda, int a_mn,
-                        const void* B, int64_t ldb, int b_mn, int64_t M, int64_t N, int64_t K,
-                        const GemmShape& shape, const EpiArgs& ea, const DevInfo& dev,
-                        cudaStream_t s);
+struct GemmOperands {
+    const void* A;
+    int64_t lda;
+    int a_mn;
+    const void* B;
+    int64_t ldb;
+    int b_mn;
+    int64_t M, N, K;
+};
+
+// Tile output written by the epilogue ([rows, cols], row stride ld).
+struct OutDesc {
+    void* ptr;  // nullptr: the kind stores nothing (forward)
+    int dtype;
+    int64_t rows, cols, ld;
+};
+
+// One launch of the tensor-core GEMM kernel: one or two tile kinds (the
+// first kind's units are handed out first).  FP32 operands run each kind on
+// the CUDA-core path instead.
+struct GemmLaunch {
+    int dtype;  // LL_BF16 / LL_F16 / LL_F32
+    int nkinds;
+    EpiKind kind[2];
+    GemmOperands op[2];
+    GemmShape shape[2];
+    EpiArgs ea[2];
+    OutDesc out[2];
+    int* counter;       // dynamic scheduling counter (must be 0), or nullptr
+    int* zero_counter;  // counter of a later launch to zero, or nullptr
+    int max_ctas;       // grid cap (0 = one CTA per SM), leaves SMs to a side stream
+};
+cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s);
 
 // --- small kernels (aux_kernels.cu) ------------------------------------------
 cudaError_t launch_lse_merge(const float* part_m, const float* part_s, const float* zy,

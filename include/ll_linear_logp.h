@@ -164,8 +164,8 @@ int ll_check_status(void* stream);
  * Tracing.  ll_launch_count(): number of kernels this library has launched
  * in the process.  ll_profile_enable(1) clears earlier records and brackets
  * every phase of later calls (fwd_gemm, lse_merge, token_sort,
- * recompute_gemm, dh_gemm, dw_gemm, db_sums, logits_fwd, logits_bwd; an
- * _f32 suffix for the CUDA-core FP32 GEMMs) with CUDA events on the call's
+ * recompute_gemm, grad_gemm (grad_hidden and grad_weight tiles), db_sums,
+ * logits_fwd, logits_bwd; an _f32 suffix for the CUDA-core FP32 GEMMs) with CUDA events on the call's
  * stream; ll_profile_enable(0) stops recording.  ll_profile_summary()
  * synchronises on the recorded events and writes one line per phase,
  * "label count total_ms", into buf (NUL-terminated, truncated to len);

@@ -242,3 +242,14 @@ def test_bf16_32k_4k_151936_sampled(lib):
     dw_rows = np.unique(np.concatenate([p["y"][rows], np.arange(0, 151936, 593),
                                         [151935]])).astype(np.int64)
     sampled(lib, p, rows, dw_rows=dw_rows)
+
+
+@pytest.mark.parametrize("need", [(1, 0, 0), (0, 1, 1), (0, 0, 1), (1, 1, 0)])
+def test_requested_gradients_only(lib, need):
+    """Each subset of (grad_hidden, grad_weight, grad_bias) matches the oracle;
+    the others are not produced."""
+    p = synth.linear_inputs(400, 128, 2100, dtype="bf16", bias=True, seed=29)
+    got = run(lib, p, token_chunks=2, need=need)
+    for k, want in zip(("dh", "dW", "db"), need):
+        assert (got[k] is not None) == bool(want), k
+    compare(p, got, full_ref(p))

@@ -48,6 +48,8 @@ EXPORTS = {
     "ll_check_status": (_c_int, [_c_p]),
     "ll_set_wait_limit_ns": (None, [_c_i64]),
     "ll_debug_unsatisfied_wait": (_c_int, [_c_p, _c_p]),
+    "ll_forward_noalloc": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_int,
+                                    _c_p, _c_p, _c_p]),
     "ll_launch_count": (ctypes.c_longlong, []),
     "ll_profile_enable": (None, [_c_int]),
     "ll_profile_summary": (_c_int, [ctypes.c_char_p, _c_size]),

@@ -131,6 +131,26 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight,
                 void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Forward without a caller workspace.  No counterpart on the source pages:
+ * it exists for callers that cannot allocate device memory (a framework
+ * that forbids allocation during a step, plugin code without access to the
+ * application's allocator).  Same arguments, results and errors as
+ * ll_forward, minus the workspace: the scratch lives in a static 8 MiB
+ * (8388608-byte) device array of the library, held on every GPU that loads
+ * the library until the process exits.  Problems needing more scratch than
+ * that, (2 * ceil(V / 1024) + 1) * N * 4 bytes with 256-byte padding (the
+ * forward's ll_workspace_size), are rejected with LL_ERR_WORKSPACE before
+ * anything runs.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress with that device current); make that first
+ * call before any stream capture.  It allocates nothing.  All calls on a
+ * device share the one array, which keeps the last call's contents: calls
+ * that may overlap on the GPU (other streams, other host threads) race.
+ */
+int ll_forward_noalloc(const void* hidden, const void* weight, const void* bias,
+                       const int64_t* targets, int64_t N, int64_t D, int64_t V, int dtype,
+                       float* logp, float* lse, void* stream);
+
+/*
  * Logits-input forward.  PR #495 "Summary" (fused logp forward: one row per
  * block, logp of the target, constant 0 for targets outside [0, V)).
  *   logits [N, ld] dtype, device; row n starts at logits + n * ld; columns

@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--token-chunks", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-logits", action="store_true",
+                    help="skip the logits-input path measurement")
     return ap.parse_args()
 
 
@@ -344,9 +346,69 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": logp.numel() * 4, "ms_per_step": ms_e2e},
         "clocks": clk,
     }
+    if not args.no_logits:
+        del ws_b, flush_buf
+        torch.cuda.empty_cache()
+        out["logits_path"] = logits_path(args, device, pk)
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(p)
     print(json.dumps(out), flush=True)
+
+
+def logits_path(args, device, pk):
+    """logits_logp_fwd + logits_logp_bwd on bf16 logits [32768, 151936]
+    (9.27 GiB, larger than L2): tokens/s and HBM roofline of each kernel."""
+    import torch
+
+    import cross_entropy_rl_gb300 as ll
+
+    N, V = 32768, 151936
+    g = torch.Generator(device=device)
+    g.manual_seed(0)
+    x = (torch.randn(N, V, generator=g, device=device) * (2.0 ** 0.5)).to(torch.bfloat16)
+    y = torch.randint(0, V, (N,), generator=g, device=device)
+    gl = torch.randn(N, generator=g, device=device)
+    logp = torch.empty(N, device=device)
+    lse = torch.empty(N, device=device)
+    dx = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 20))
+
+    def step():
+        ll.logits_fwd(x, y, out=(logp, lse))
+        ll.logits_bwd(gl, x, y, lse, out=dx)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    ll.profile(True)
+    for _ in range(steps):
+        step()
+    prof = ll.profile_summary()
+    ll.profile(False)
+    assert ll.check_status() == 0
+    fwd_ms = prof["logits_fwd"][1] / prof["logits_fwd"][0]
+    bwd_ms = prof["logits_bwd"][1] / prof["logits_bwd"][0]
+    fwd_b, bwd_b = 2.0 * N * V, 4.0 * N * V
+    peak = pk["hbm_gbs"]
+    return {"workload": "logits_32k_151936", "N": N, "V": V, "dtype": "bf16",
+            "value": N / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "steps": steps, "l2": "inputs (9.27 GiB) larger than L2, no flush",
+            "bytes_per_token": 6 * V, "step_gbs": 6.0 * N * V / (ms * 1e-3) / 1e9,
+            "step_frac_of_hbm": 6.0 * N * V / (ms * 1e-3) / 1e9 / peak,
+            "roofline": {"bound": "hbm", "kernel": "logits_bwd",
+                         "achieved": bwd_b / (bwd_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": bwd_b / (bwd_ms * 1e-3) / 1e9 / peak,
+                         "traffic": ncu_traffic("logits_bwd"), "avg_launch_ms": bwd_ms},
+            "logits_fwd": {"ms": fwd_ms, "gbs": fwd_b / (fwd_ms * 1e-3) / 1e9,
+                           "frac": fwd_b / (fwd_ms * 1e-3) / 1e9 / peak}}
 
 
 def main():

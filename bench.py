@@ -44,6 +44,15 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-logits", action="store_true",
                     help="skip the logits-input path measurement")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=["fp32_small", "bf16_4k_2k_32k", "sweep_16k_4k_32000",
+                             "bf16_32k_4k_151936"],
+                    help="linear workload to time (default: the benchmark workload)")
+    ap.add_argument("--dtype", default=None, choices=["bf16", "f16", "f32"],
+                    help="operand dtype of the dtype sweep workload")
+    ap.add_argument("--bias", action="store_true", help="dtype sweep workload with a bias")
+    ap.add_argument("--logits-rows", type=int, default=32768,
+                    help="rows of the logits-input measurement (vocab 151936)")
     return ap.parse_args()
 
 
@@ -216,32 +225,42 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
     ll.load()
-    p = synth.linear_inputs(**synth.WORKLOADS[WORKLOAD], seed=rank)
-    N, D, V = p["N"], p["D"], p["V"]
+    wl = dict(synth.WORKLOADS[args.workload])
+    if args.workload == "sweep_16k_4k_32000":
+        wl.update(dtype=args.dtype or "bf16", bias=args.bias)
+    p = synth.linear_inputs(**wl, seed=rank)
+    N, D, V, dt = p["N"], p["D"], p["V"], p["dtype"]
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[dt]
+    # grad_weight: FP32, except the dtype sweep (operands and grad_weight in one dtype)
+    dw_dt = tdt if args.workload == "sweep_16k_4k_32000" else torch.float32
+    has_bias = p["b"] is not None
 
     def to_dev(a, bf16=False):
         a = np.ascontiguousarray(a)
         t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if bf16 else torch.from_numpy(a)
         return t.to(device)
 
-    h, W = to_dev(p["h"], True), to_dev(p["W"], True)
+    isbf = dt == "bf16"
+    h, W = to_dev(p["h"], isbf), to_dev(p["W"], isbf)
+    b = to_dev(p["b"], isbf) if has_bias else None
     y, gl = to_dev(p["y"]), to_dev(p["gl"])
     logp = torch.empty(N, dtype=torch.float32, device=device)
     lse = torch.empty_like(logp)
-    dh = torch.empty(N, D, dtype=torch.bfloat16, device=device)
-    dW = torch.empty(V, D, dtype=torch.float32, device=device)
-    ws_f = torch.empty(max(256, ll.workspace_size(N, D, V, torch.bfloat16)),
-                       dtype=torch.uint8, device=device)
-    ws_b = torch.empty(max(256, ll.workspace_size(N, D, V, torch.bfloat16, args.token_chunks,
-                                                  backward=True)),
+    dh = torch.empty(N, D, dtype=tdt, device=device)
+    dW = torch.empty(V, D, dtype=dw_dt, device=device)
+    db = torch.empty(V, dtype=dw_dt, device=device) if has_bias else None
+    ws_f = torch.empty(max(256, ll.workspace_size(N, D, V, tdt)), dtype=torch.uint8,
+                       device=device)
+    ws_b = torch.empty(max(256, ll.workspace_size(N, D, V, tdt, args.token_chunks,
+                                                  backward=True, need_db=has_bias)),
                        dtype=torch.uint8, device=device)
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
 
     def step(hh, yy, gg):
-        ll.forward(hh, W, None, yy, workspace=ws_f, out=(logp, lse))
-        ll.backward(gg, hh, W, None, yy, lse, need_dh=True, need_dw=True, need_db=False,
-                    token_chunks=args.token_chunks, workspace=ws_b, out=(dh, dW, None))
+        ll.forward(hh, W, b, yy, workspace=ws_f, out=(logp, lse))
+        ll.backward(gg, hh, W, b, yy, lse, need_dh=True, need_dw=True, need_db=has_bias,
+                    token_chunks=args.token_chunks, workspace=ws_b, out=(dh, dW, db))
 
     def barrier():
         if dist is not None:
@@ -286,7 +305,7 @@ def run_ours(args, rank, world, local_rank):
     ll.profile(False)
 
     # end to end: per-step inputs from pinned host memory, logp read back
-    h_host = torch.empty(N, D, dtype=torch.bfloat16).pin_memory()
+    h_host = torch.empty(N, D, dtype=tdt).pin_memory()
     h_host.copy_(h.cpu())
     y_host = y.cpu().pin_memory()
     g_host = gl.cpu().pin_memory()
@@ -311,30 +330,39 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return
     pk, pk_kind = peaks()
-    flops = {"fwd_gemm": 2.0 * N * D * V, "recompute_gemm": 2.0 * N * D * V,
-             "grad_gemm": 4.0 * N * D * V}  # grad_hidden + grad_weight tiles
+    sfx = "_f32" if dt == "f32" else ""
+    flops = {"fwd_gemm" + sfx: 2.0 * N * D * V, "recompute_gemm" + sfx: 2.0 * N * D * V,
+             "grad_gemm" + sfx: 4.0 * N * D * V}  # grad_hidden + grad_weight tiles
     gemms = {k: v for k, v in prof.items() if k in flops}
     dom = max(gemms, key=lambda k: gemms[k][1])
     cnt, tot = gemms[dom]
     avg_ms = tot / cnt
     achieved = flops[dom] / (avg_ms * 1e-3) / 1e12
-    peak = pk["bf16_tflops"]
+    if dt == "f32":
+        # FP32 FFMA on the CUDA cores: 152 SMs x 128 lanes x 2 flops x max SM clock
+        peak, bound = 152 * 128 * 2 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12, "alu"
+        pk_kind = "derived (152 SMs x 128 FP32 lanes x 2 x max clock)"
+    else:
+        # fp16 has the same dense tensor rate as bf16
+        peak, bound = pk["bf16_tflops"], "tensor"
     useful = 6.0 * N * D * V / (ms * 1e-3) / 1e12
     executed = 8.0 * N * D * V / (ms * 1e-3) / 1e12
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dt,
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "N": N, "D": D, "V": V, "bias": False,
-                   "grad_weight": "fp32", "grad_hidden": "bf16",
+        "config": {"workload": args.workload, "N": N, "D": D, "V": V, "bias": has_bias,
+                   "grad_weight": str(dw_dt).replace("torch.", ""),
+                   "grad_hidden": str(tdt).replace("torch.", ""),
                    "token_chunks": args.token_chunks or "auto",
                    "l2": "flushed between steps (512 MiB write outside the timed events)",
                    "parallelism": f"dp{world}"},
-        "useful_tflops": useful, "useful_frac_of_bf16_peak": useful / peak,
+        "useful_tflops": useful, "useful_frac_of_bf16_peak": useful / pk["bf16_tflops"],
+        "useful_frac_of_peak": useful / peak, "peak_tflops": peak,
         "executed_tflops_incl_recompute": executed,
         "peak_source": pk_kind,
-        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+        "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
                      "frac_of_sustained": achieved / pk.get("bf16_tflops_sustained", peak),
                      "traffic": ncu_traffic(dom), "avg_launch_ms": avg_ms,
@@ -342,11 +370,11 @@ def run_ours(args, rank, world, local_rank):
         "kernels_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},
         "gpu_launches": launches,
         "e2e": {"value": world * N / (ms_e2e * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h.numel() * 2 + y.numel() * 8 + gl.numel() * 4,
+                "h2d_bytes_per_step": h.numel() * h.element_size() + y.numel() * 8 + gl.numel() * 4,
                 "d2h_bytes_per_step": logp.numel() * 4, "ms_per_step": ms_e2e},
         "clocks": clk,
     }
-    if not args.no_logits:
+    if not args.no_logits and args.workload == WORKLOAD:
         del ws_b, flush_buf
         torch.cuda.empty_cache()
         out["logits_path"] = logits_path(args, device, pk)
@@ -362,7 +390,7 @@ def logits_path(args, device, pk):
 
     import cross_entropy_rl_gb300 as ll
 
-    N, V = 32768, 151936
+    N, V = args.logits_rows, 151936
     g = torch.Generator(device=device)
     g.manual_seed(0)
     x = (torch.randn(N, V, generator=g, device=device) * (2.0 ** 0.5)).to(torch.bfloat16)
@@ -398,7 +426,8 @@ def logits_path(args, device, pk):
     bwd_ms = prof["logits_bwd"][1] / prof["logits_bwd"][0]
     fwd_b, bwd_b = 2.0 * N * V, 4.0 * N * V
     peak = pk["hbm_gbs"]
-    return {"workload": "logits_32k_151936", "N": N, "V": V, "dtype": "bf16",
+    return {"workload": "logits_32k_151936" if N == 32768 else f"logits_{N}_151936",
+            "N": N, "V": V, "dtype": "bf16",
             "value": N / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "steps": steps, "l2": "inputs (9.27 GiB) larger than L2, no flush",
             "bytes_per_token": 6 * V, "step_gbs": 6.0 * N * V / (ms * 1e-3) / 1e9,

@@ -260,7 +260,8 @@ def run_ours(args, rank, world, local_rank):
     def step(hh, yy, gg):
         ll.forward(hh, W, b, yy, workspace=ws_f, out=(logp, lse))
         ll.backward(gg, hh, W, b, yy, lse, need_dh=True, need_dw=True, need_db=has_bias,
-                    token_chunks=args.token_chunks, workspace=ws_b, out=(dh, dW, db))
+                    dh_dtype=tdt, dw_dtype=dw_dt, token_chunks=args.token_chunks,
+                    workspace=ws_b, out=(dh, dW, db))
 
     def barrier():
         if dist is not None:

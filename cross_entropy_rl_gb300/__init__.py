@@ -17,7 +17,8 @@ import ctypes
 import os
 
 __all__ = [
-    "LLError", "load", "lib", "forward", "backward", "logits_fwd", "logits_bwd",
+    "LLError", "load", "lib", "forward", "backward", "forward_backward", "logits_fwd",
+    "logits_bwd",
     "workspace_size", "check_status", "DTYPE_CODES", "EXPORTS",
 ]
 
@@ -42,6 +43,9 @@ EXPORTS = {
     "ll_backward": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64,
                              _c_int, _c_int, _c_int, _c_int, _c_p, _c_int, _c_p, _c_int,
                              _c_p, _c_int, _c_p, _c_size, _c_p]),
+    "ll_forward_backward": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64,
+                                     _c_int, _c_p, _c_p, _c_int, _c_int, _c_int, _c_p, _c_int,
+                                     _c_p, _c_int, _c_p, _c_int, _c_p, _c_size, _c_p]),
     "logits_logp_fwd": (_c_int, [_c_p, _c_i64, _c_int, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_p]),
     "logits_logp_bwd": (_c_int, [_c_p, _c_p, _c_i64, _c_int, _c_p, _c_p, _c_i64, _c_i64,
                                  _c_p, _c_p]),
@@ -112,6 +116,8 @@ def _ptr(t):
 
 def _stream(stream=None):
     torch = _torch()
+    if stream is None and not torch.cuda.is_available():
+        return ctypes.c_void_p(None)  # the call itself then fails: no device memory
     s = torch.cuda.current_stream() if stream is None else stream
     return ctypes.c_void_p(s.cuda_stream)
 
@@ -127,26 +133,94 @@ def workspace_size(N, D, V, dtype, token_chunks=0, backward=False, need_db=False
                                         int(bool(need_db))))
 
 
+def _need(t, name, shape, dtype=None, device=None, dtypes=None):
+    """Raise unless tensor t is contiguous, on `device`, of `shape` and dtype.
+
+    The C ABI receives bare pointers, so every buffer it reads or writes is
+    checked here, where the sizes are still known."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected one of {dtypes}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if t.numel() and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _check_linear(hidden, weight, bias, targets):
+    torch = _torch()
+    if hidden.dim() != 2 or weight.dim() != 2:
+        raise ValueError("hidden and weight must be 2-D")
+    N, D = hidden.shape
+    V = weight.shape[0]
+    dev = hidden.device
+    _need(hidden, "hidden", (N, D), device=dev,
+          dtypes=(torch.float32, torch.float16, torch.bfloat16))
+    _need(weight, "weight", (V, D), hidden.dtype, dev)
+    if bias is not None:
+        _need(bias, "bias", (V,), hidden.dtype, dev)
+    _need(targets, "targets", (N,), torch.int64, dev)
+    return N, D, V, dev
+
+
 def _workspace(nbytes, device):
     torch = _torch()
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def _grad_outputs(out, need_dh, need_dw, need_db, N, D, V, op_dtype, dh_dtype, dw_dtype, dev):
+    """Gradient buffers (given or allocated) and their dtypes.  A given
+    buffer's dtype decides; an explicit dtype that disagrees with it raises."""
+    torch = _torch()
+    if out is not None:
+        dh, dW, db = out
+        if dh is not None:
+            if dh_dtype is not None and dh_dtype != dh.dtype:
+                raise TypeError("dh_dtype disagrees with the given grad_hidden")
+            dh_dtype = dh.dtype
+        if dW is not None or db is not None:
+            given = (dW if dW is not None else db).dtype
+            if dw_dtype is not None and dw_dtype != given:
+                raise TypeError("dw_dtype disagrees with the given grad_weight / grad_bias")
+            dw_dtype = given
+    dh_dtype = op_dtype if dh_dtype is None else dh_dtype
+    dw_dtype = torch.float32 if dw_dtype is None else dw_dtype
+    if out is None:
+        dh = torch.empty(N, D, dtype=dh_dtype, device=dev) if need_dh else None
+        dW = torch.empty(V, D, dtype=dw_dtype, device=dev) if need_dw else None
+        db = torch.empty(V, dtype=dw_dtype, device=dev) if need_db else None
+    if need_dh:
+        _need(dh, "grad_hidden", (N, D), dh_dtype, dev)
+    if need_dw:
+        _need(dW, "grad_weight", (V, D), dw_dtype, dev)
+    if need_db:
+        _need(db, "grad_bias", (V,), dw_dtype, dev)
+    return dh, dW, db, dh_dtype, dw_dtype
 
 
 def forward(hidden, weight, bias, targets, *, workspace=None, out=None, stream=None):
     """(logp [N] fp32, lse [N] fp32) of z = hidden . weight^T (+ bias)."""
     torch = _torch()
     L = load()
-    N, D = hidden.shape
-    V = weight.shape[0]
+    N, D, V, dev = _check_linear(hidden, weight, bias, targets)
     code = _code(hidden.dtype)
     if out is None:
-        logp = torch.empty(N, dtype=torch.float32, device=hidden.device)
-        lse = torch.empty(N, dtype=torch.float32, device=hidden.device)
+        logp = torch.empty(N, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
     else:
         logp, lse = out
+    _need(logp, "logp", (N,), torch.float32, dev)
+    _need(lse, "lse", (N,), torch.float32, dev)
     ws_need = L.ll_workspace_size(N, D, V, code, 0, 0, 0)
     if workspace is None:
-        workspace = _workspace(ws_need, hidden.device)
+        workspace = _workspace(ws_need, dev)
+    _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
     st = L.ll_forward(_ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets), N, D, V, code,
                       _ptr(logp), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream))
     _check("ll_forward", st)
@@ -162,23 +236,18 @@ def backward(grad_logp, hidden, weight, bias, targets, lse, *, need_dh=True, nee
     """
     torch = _torch()
     L = load()
-    N, D = hidden.shape
-    V = weight.shape[0]
+    N, D, V, dev = _check_linear(hidden, weight, bias, targets)
     code = _code(hidden.dtype)
     if need_db is None:
         need_db = bias is not None
-    dh_dtype = hidden.dtype if dh_dtype is None else dh_dtype
-    dw_dtype = torch.float32 if dw_dtype is None else dw_dtype
-    dev = hidden.device
-    if out is not None:
-        dh, dW, db = out
-    else:
-        dh = torch.empty(N, D, dtype=dh_dtype, device=dev) if need_dh else None
-        dW = torch.empty(V, D, dtype=dw_dtype, device=dev) if need_dw else None
-        db = torch.empty(V, dtype=dw_dtype, device=dev) if need_db else None
+    _need(grad_logp, "grad_logp", (N,), torch.float32, dev)
+    _need(lse, "lse", (N,), torch.float32, dev)
+    dh, dW, db, dh_dtype, dw_dtype = _grad_outputs(out, need_dh, need_dw, need_db, N, D, V,
+                                                   hidden.dtype, dh_dtype, dw_dtype, dev)
     ws_need = L.ll_workspace_size(N, D, V, code, token_chunks, 1, int(bool(need_db)))
     if workspace is None:
         workspace = _workspace(ws_need, dev)
+    _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
     st = L.ll_backward(_ptr(grad_logp), _ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets),
                        _ptr(lse), N, D, V, code, int(bool(need_dh)), int(bool(need_dw)),
                        int(bool(need_db)), _ptr(dh), _code(dh_dtype), _ptr(dW), _code(dw_dtype),
@@ -188,19 +257,60 @@ def backward(grad_logp, hidden, weight, bias, targets, lse, *, need_dh=True, nee
     return dh, dW, db
 
 
+def forward_backward(grad_logp, hidden, weight, bias, targets, *, need_dh=True, need_dw=True,
+                     need_db=None, dh_dtype=None, dw_dtype=None, token_chunks=0,
+                     workspace=None, out=None, stream=None):
+    """(logp, lse, grad_hidden, grad_weight, grad_bias) in one call, for a
+    grad_logp known before the forward; bitwise equal to forward + backward."""
+    torch = _torch()
+    L = load()
+    N, D, V, dev = _check_linear(hidden, weight, bias, targets)
+    code = _code(hidden.dtype)
+    if need_db is None:
+        need_db = bias is not None
+    _need(grad_logp, "grad_logp", (N,), torch.float32, dev)
+    if out is not None:
+        logp, lse, dh, dW, db = out
+        grads = (dh, dW, db)
+    else:
+        logp = torch.empty(N, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+        grads = None
+    _need(logp, "logp", (N,), torch.float32, dev)
+    _need(lse, "lse", (N,), torch.float32, dev)
+    dh, dW, db, dh_dtype, dw_dtype = _grad_outputs(grads, need_dh, need_dw, need_db, N, D, V,
+                                                   hidden.dtype, dh_dtype, dw_dtype, dev)
+    ws_need = L.ll_workspace_size(N, D, V, code, token_chunks, 2, int(bool(need_db)))
+    if workspace is None:
+        workspace = _workspace(ws_need, dev)
+    _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
+    st = L.ll_forward_backward(_ptr(grad_logp), _ptr(hidden), _ptr(weight), _ptr(bias),
+                               _ptr(targets), N, D, V, code, _ptr(logp), _ptr(lse),
+                               int(bool(need_dh)), int(bool(need_dw)), int(bool(need_db)),
+                               _ptr(dh), _code(dh_dtype), _ptr(dW), _code(dw_dtype), _ptr(db),
+                               int(token_chunks), _ptr(workspace), workspace.numel(),
+                               _stream(stream))
+    _check("ll_forward_backward", st)
+    return logp, lse, dh, dW, db
+
+
 def logits_fwd(logits, targets, V=None, *, out=None, stream=None):
     """(logp, lse) from logits [N, ld]; columns >= V (default ld) ignored."""
     torch = _torch()
     L = load()
     N, ld = logits.shape
     V = ld if V is None else V
-    if logits.stride(1) != 1 or (N > 1 and logits.stride(0) != ld):
-        raise ValueError("logits must be row-major contiguous")
+    dev = logits.device
+    _need(logits, "logits", (N, ld), device=dev,
+          dtypes=(torch.float32, torch.float16, torch.bfloat16))
+    _need(targets, "targets", (N,), torch.int64, dev)
     if out is None:
-        logp = torch.empty(N, dtype=torch.float32, device=logits.device)
-        lse = torch.empty(N, dtype=torch.float32, device=logits.device)
+        logp = torch.empty(N, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
     else:
         logp, lse = out
+    _need(logp, "logp", (N,), torch.float32, dev)
+    _need(lse, "lse", (N,), torch.float32, dev)
     st = L.logits_logp_fwd(_ptr(logits), ld, _code(logits.dtype), _ptr(targets), N, V,
                            _ptr(logp), _ptr(lse), _stream(stream))
     _check("logits_logp_fwd", st)
@@ -213,8 +323,15 @@ def logits_bwd(grad_logp, logits, targets, lse, V=None, *, out=None, stream=None
     L = load()
     N, ld = logits.shape
     V = ld if V is None else V
+    dev = logits.device
+    _need(logits, "logits", (N, ld), device=dev,
+          dtypes=(torch.float32, torch.float16, torch.bfloat16))
+    _need(targets, "targets", (N,), torch.int64, dev)
+    _need(grad_logp, "grad_logp", (N,), torch.float32, dev)
+    _need(lse, "lse", (N,), torch.float32, dev)
     if out is None:
         out = torch.empty_like(logits)
+    _need(out, "grad_logits", (N, ld), logits.dtype, dev)
     st = L.logits_logp_bwd(_ptr(grad_logp), _ptr(logits), ld, _code(logits.dtype),
                            _ptr(targets), _ptr(lse), N, V, _ptr(out), _stream(stream))
     _check("logits_logp_bwd", st)

@@ -144,6 +144,51 @@ __global__ void db_finish_kernel(const float* __restrict__ partial, int64_t grou
     }
 }
 
+// One CTA per row: p = 2^(z * log2e - lse * log2e) exactly as the recompute
+// epilogue forms it, S = -grad * p off target, S = 0 / tc = grad * (1 - p)
+// at the target.
+template <typename T>
+__global__ void __launch_bounds__(256) softmax_part_kernel(
+    const float* __restrict__ Z, int64_t ldZ, int64_t V, const int64_t* __restrict__ targets,
+    const float* __restrict__ grad, const float* __restrict__ lse, T* __restrict__ S,
+    int64_t ldS, float* __restrict__ tc) {
+    const int64_t row = blockIdx.x;
+    const int64_t y = targets[row];
+    const float g = grad[row];
+    const bool live = y >= 0 && y < V && g != 0.f;
+    const float coef = live ? -g : 0.f;
+    const float lse2 = lse[row] * kLog2e;
+    const float* z = Z + row * ldZ;
+    T* out = S + row * ldS;
+    for (int64_t c = int64_t(threadIdx.x) * 8; c < V; c += int64_t(blockDim.x) * 8) {
+        float f[8];
+        if (c + 8 <= V) {
+            load8(z + c, f);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = (c + j < V) ? z[c + j] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = ex2(fmaf(f[j], kLog2e, -lse2));
+        if (y >= c && y < c + 8) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (c + j == y) {
+                    tc[row] = coef != 0.f ? -coef * (1.f - f[j]) : 0.f;
+                    f[j] = 0.f;
+                }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = coef * f[j];
+        if (c + 8 <= V) {
+            store8(out + c, f);
+        } else {
+            for (int j = 0; j < 8 && c + j < V; ++j) out[c + j] = Elem<T>::from_f(f[j]);
+        }
+    }
+    if (!(y >= 0 && y < V) && threadIdx.x == 0) tc[row] = 0.f;
+}
+
 __global__ void fill_zero_kernel(uint32_t* p, int64_t n_words) {
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n_words;
          i += int64_t(gridDim.x) * blockDim.x)
@@ -246,6 +291,24 @@ cudaError_t launch_db_chunk(const void* S, int64_t ldS, int s_dtype, int64_t row
         db_finish_kernel<__nv_bfloat16><<<fb, 256, 0, s>>>(
             partial, groups, V, db_acc, first, last, offs, k, tc_all,
             static_cast<__nv_bfloat16*>(grad_bias));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_softmax_part(const float* Z, int64_t ldZ, int64_t rows, int64_t V,
+                                const int64_t* targets, const float* grad, const float* lse,
+                                void* S, int64_t ldS, int s_dtype, float* tc, cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    note_launches(1);
+    const unsigned grid = static_cast<unsigned>(rows);
+    if (s_dtype == LL_BF16)
+        softmax_part_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            Z, ldZ, V, targets, grad, lse, static_cast<__nv_bfloat16*>(S), ldS, tc);
+    else if (s_dtype == LL_F16)
+        softmax_part_kernel<__half><<<grid, 256, 0, s>>>(Z, ldZ, V, targets, grad, lse,
+                                                         static_cast<__half*>(S), ldS, tc);
+    else
+        softmax_part_kernel<float><<<grid, 256, 0, s>>>(Z, ldZ, V, targets, grad, lse,
+                                                        static_cast<float*>(S), ldS, tc);
     return cudaGetLastError();
 }
 

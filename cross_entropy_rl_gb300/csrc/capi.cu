@@ -163,13 +163,19 @@ FwdLayout fwd_layout(int64_t N, int64_t V) {
 constexpr size_t kAutoChunkBytes = size_t(2) << 30;  // softmax workspace budget
 
 struct BwdLayout {
-    int64_t chunks, Nc, ldS;
-    size_t S, tc, keys, offs, ctr, db, total;
+    int64_t chunks, Nc, ldS, ldZ, n_segs;
+    size_t S, Z, part_m, part_s, zy, tc, keys, offs, ctr, db, total;
 };
-BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need_db) {
+// fused = 1: the single fwd+bwd call, which also keeps the chunk's FP32
+// logits Z and the forward partials.
+BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need_db,
+                     int fused = 0) {
     BwdLayout L;
     L.ldS = round_up(V, 8);
-    const size_t row_bytes = size_t(L.ldS) * esize(dtype);
+    L.ldZ = round_up(V, 8);
+    L.n_segs = cdiv(cdiv(V, kBN), kVocabTilesPerSeg);
+    const size_t row_bytes =
+        size_t(L.ldS) * esize(dtype) + (fused ? size_t(L.ldZ) * 4 + size_t(L.n_segs) * 8 + 4 : 0);
     const int64_t n1 = N > 0 ? N : 1;
     int64_t k = token_chunks;
     if (k <= 0) {
@@ -182,7 +188,18 @@ BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need
     L.chunks = cdiv(n1, L.Nc);
     size_t off = 0;
     L.S = off;
-    off = align_up(off + size_t(L.Nc) * row_bytes);
+    off = align_up(off + size_t(L.Nc) * size_t(L.ldS) * esize(dtype));
+    L.Z = L.part_m = L.part_s = L.zy = off;
+    if (fused) {
+        L.Z = off;
+        off = align_up(off + size_t(L.Nc) * size_t(L.ldZ) * 4);
+        L.part_m = off;
+        off = align_up(off + size_t(L.n_segs) * size_t(L.Nc) * 4);
+        L.part_s = off;
+        off = align_up(off + size_t(L.n_segs) * size_t(L.Nc) * 4);
+        L.zy = off;
+        off = align_up(off + size_t(L.Nc) * 4);
+    }
     L.tc = off;
     off = align_up(off + size_t(n1) * 4);
     L.keys = off;
@@ -233,7 +250,7 @@ size_t ll_workspace_size(int64_t N, int64_t D, int64_t V, int dtype, int token_c
     (void)D;
     if (N < 0 || V < 1 || !dtype_ok(dtype)) return 0;
     if (!is_backward) return fwd_layout(N, V).total;
-    return bwd_layout(N, V, dtype, token_chunks, flags & 1).total;
+    return bwd_layout(N, V, dtype, token_chunks, flags & 1, is_backward == 2).total;
 }
 
 void ll_set_wait_limit_ns(int64_t ns) { g_wait_limit_ns = ns > 0 ? uint64_t(ns) : 2000000000ull; }
@@ -302,11 +319,19 @@ int ll_forward(const void* hidden, const void* weight, const void* bias, const i
     return cuda_status(e);
 }
 
-int ll_backward(const float* grad_logp, const void* hidden, const void* weight, const void* bias,
-                const int64_t* targets, const float* lse, int64_t N, int64_t D, int64_t V,
-                int dtype, int need_dh, int need_dw, int need_db, void* grad_hidden,
-                int dh_dtype, void* grad_weight, int dw_dtype, void* grad_bias,
-                int token_chunks, void* workspace, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace ll {
+namespace {
+// The backward, or (fused = 1) the forward and backward in one call when
+// grad_logp is known up front: the chunk's forward GEMM then keeps its FP32
+// logits and the softmax part is formed from them, instead of recomputing z.
+int backward_impl(const float* grad_logp, const void* hidden, const void* weight,
+                  const void* bias, const int64_t* targets, const float* lse, int64_t N,
+                  int64_t D, int64_t V, int dtype, int need_dh, int need_dw, int need_db,
+                  void* grad_hidden, int dh_dtype, void* grad_weight, int dw_dtype,
+                  void* grad_bias, int token_chunks, void* workspace, size_t ws_bytes,
+                  void* stream, int fused, float* logp_out, float* lse_out) {
     int st = check_sizes(N, D, V);
     if (st) return st;
     if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
@@ -320,7 +345,8 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight, 
     if (need_dh && N > 0 && !grad_hidden) return LL_ERR_INVALID_ARG;
     if (D % 8 != 0 || !aligned16(weight)) return LL_ERR_ALIGN;
     if (need_dw && !aligned16(grad_weight)) return LL_ERR_ALIGN;
-    if (!need_dh && !need_dw && !need_db) return LL_OK;
+    if (fused && N > 0 && (!logp_out || !lse_out)) return LL_ERR_INVALID_ARG;
+    if (!fused && !need_dh && !need_dw && !need_db) return LL_OK;
 
     DeviceGuard guard(weight);
     if (guard.err) return guard.err;
@@ -334,9 +360,9 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight, 
         if (e == cudaSuccess && need_db) e = launch_fill_zero(grad_bias, V, dw_dtype, s);
         return cuda_status(e);
     }
-    if (!grad_logp || !hidden || !targets || !lse) return LL_ERR_INVALID_ARG;
+    if (!grad_logp || !hidden || !targets || (!fused && !lse)) return LL_ERR_INVALID_ARG;
     if (!aligned16(hidden) || (need_dh && !aligned16(grad_hidden))) return LL_ERR_ALIGN;
-    const BwdLayout L = bwd_layout(N, V, dtype, token_chunks, need_db);
+    const BwdLayout L = bwd_layout(N, V, dtype, token_chunks, need_db, fused);
     if (!workspace || ws_bytes < L.total) return LL_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return LL_ERR_WORKSPACE;
 
@@ -350,10 +376,15 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight, 
     const int64_t db_groups_v = (L.Nc < 64 ? L.Nc : 64) * V;
     float* db_acc = db_part + db_groups_v;
     const size_t es = esize(dtype);
+    float* Z = reinterpret_cast<float*>(ws + L.Z);
+    float* part_m = reinterpret_cast<float*>(ws + L.part_m);
+    float* part_s = reinterpret_cast<float*>(ws + L.part_s);
+    float* zy = reinterpret_cast<float*>(ws + L.zy);
+    if (fused) lse = lse_out;
 
     // The token sort (only the last chunk's grad_weight / grad_bias epilogue
-    // reads it) runs on a side stream, overlapping the first recompute GEMM,
-    // which leaves kSideSms SMs free for it.
+    // reads it) runs on a side stream, overlapping the first recompute (or
+    // forward) GEMM, which leaves kSideSms SMs free for it.
     cudaEvent_t sort_done = nullptr;
     const bool need_sort = need_dw || need_db;
     bool overlap = false;
@@ -392,7 +423,7 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight, 
         const char* h_c = static_cast<const char*>(hidden) + size_t(r0) * size_t(D) * es;
 
         // (1) recompute z for the chunk, store S = -grad * p off target and c
-        {
+        if (!fused) {
             GemmLaunch G;
             memset(&G, 0, sizeof(G));
             G.dtype = dtype;
@@ -421,6 +452,53 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight, 
             if (overlap && c == 0) G.max_ctas = dev.num_sms - kSideSms;
             Phase ph(dtype == LL_F32 ? "recompute_gemm_f32" : "recompute_gemm", s);
             e = launch_gemm(G, dev, s);
+            if (e != cudaSuccess) return cuda_status(e);
+        } else {
+            // (1') forward GEMM of the chunk keeping its FP32 logits, the
+            // ordered LSE merge (logp, lse), then S and c from the logits
+            GemmLaunch G;
+            memset(&G, 0, sizeof(G));
+            G.dtype = dtype;
+            G.nkinds = 1;
+            G.kind[0] = EpiKind::Fwd;
+            G.op[0] = GemmOperands{h_c, D, 0, weight, D, 0, rows, V, D};
+            GemmShape& sh = G.shape[0];
+            sh.m_blocks = cdiv(rows, kBM);
+            sh.n_tiles = cdiv(V, kBN);
+            sh.tiles_per_unit = kVocabTilesPerSeg;
+            sh.n_segs = L.n_segs;
+            sh.k_blocks = cdiv(D, 64);
+            sh.unit_order = 0;
+            EpiArgs& ea = G.ea[0];
+            ea = base;
+            ea.M = rows;
+            ea.Ncols = V;
+            ea.targets = targets + r0;
+            ea.part_m = part_m;
+            ea.part_s = part_s;
+            ea.zy = zy;
+            ea.part_ld = L.Nc;
+            ea.Z = Z;
+            ea.ldZ = L.ldZ;
+            G.out[0] = OutDesc{Z, LL_F32, rows, V, L.ldZ};
+            G.zero_counter = counter;
+            if (overlap && c == 0) G.max_ctas = dev.num_sms - kSideSms;
+            {
+                Phase ph(dtype == LL_F32 ? "fwd_gemm_f32" : "fwd_gemm", s);
+                e = launch_gemm(G, dev, s);
+            }
+            if (e != cudaSuccess) return cuda_status(e);
+            {
+                Phase ph("lse_merge", s);
+                e = launch_lse_merge(part_m, part_s, zy, L.Nc, L.n_segs, targets + r0, rows, V,
+                                     logp_out + r0, lse_out + r0, s);
+            }
+            if (e != cudaSuccess) return cuda_status(e);
+            {
+                Phase ph("softmax_part", s);
+                e = launch_softmax_part(Z, L.ldZ, rows, V, targets + r0, grad_logp + r0,
+                                        lse_out + r0, S, L.ldS, dtype, tc + r0, s);
+            }
             if (e != cudaSuccess) return cuda_status(e);
         }
         if (overlap && c == L.chunks - 1) {  // the last chunk's epilogues read the sort
@@ -503,7 +581,37 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight, 
             if (e != cudaSuccess) return cuda_status(e);
         }
     }
+    if (overlap) {  // nothing read the sort (no chunk needed it): still join it
+        cudaStreamWaitEvent(s, sort_done, 0);
+        cudaEventDestroy(sort_done);
+    }
     return LL_OK;
+}
+}  // namespace
+}  // namespace ll
+
+extern "C" {
+
+int ll_backward(const float* grad_logp, const void* hidden, const void* weight, const void* bias,
+                const int64_t* targets, const float* lse, int64_t N, int64_t D, int64_t V,
+                int dtype, int need_dh, int need_dw, int need_db, void* grad_hidden,
+                int dh_dtype, void* grad_weight, int dw_dtype, void* grad_bias,
+                int token_chunks, void* workspace, size_t ws_bytes, void* stream) {
+    return backward_impl(grad_logp, hidden, weight, bias, targets, lse, N, D, V, dtype, need_dh,
+                         need_dw, need_db, grad_hidden, dh_dtype, grad_weight, dw_dtype,
+                         grad_bias, token_chunks, workspace, ws_bytes, stream, 0, nullptr,
+                         nullptr);
+}
+
+int ll_forward_backward(const float* grad_logp, const void* hidden, const void* weight,
+                        const void* bias, const int64_t* targets, int64_t N, int64_t D,
+                        int64_t V, int dtype, float* logp, float* lse, int need_dh,
+                        int need_dw, int need_db, void* grad_hidden, int dh_dtype,
+                        void* grad_weight, int dw_dtype, void* grad_bias, int token_chunks,
+                        void* workspace, size_t ws_bytes, void* stream) {
+    return backward_impl(grad_logp, hidden, weight, bias, targets, nullptr, N, D, V, dtype,
+                         need_dh, need_dw, need_db, grad_hidden, dh_dtype, grad_weight, dw_dtype,
+                         grad_bias, token_chunks, workspace, ws_bytes, stream, 1, logp, lse);
 }
 
 int logits_logp_fwd(const void* logits, int64_t ld, int dtype, const int64_t* targets, int64_t N,

@@ -19,7 +19,8 @@
 //   warp 1      allocates 512 TMEM columns, issues tcgen05.mma (128x256x16)
 //   warps 2..5  epilogue: tcgen05.ld of its 32 TMEM lanes, fused epilogue,
 //               output rows staged in swizzled shared memory and written by
-//               TMA bulk-tensor stores (or reduce-adds)
+//               TMA bulk-tensor stores (or reduce-adds); the forward may also
+//               store its FP32 logits tile (single fwd+bwd call)
 // One launch may carry two tile kinds (grad_hidden and grad_weight tiles of
 // the same chunk), the long kind first, so that the dynamic scheduler evens
 // out the SMs' work.  Two 256-column accumulators in TMEM let the epilogue
@@ -412,7 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const CUtensorMap* tmO = kind == 0 ? &tmO0 : &tmO1;
             const bool out16 = P.out16[kind] != 0;
             const bool reduce = P.reduce[kind] != 0;
-            const bool stores = (kind == 0 ? K0::kEpi : K1::kEpi) != EpiKind::Fwd;
+            // every kind but the plain forward stores its tile; the forward
+            // stores its logits tile too when given an output (one fwd+bwd call)
+            const bool stores = P.out_rows[kind] > 0;
             const int64_t row0 = un.mb * kBM + q * 32;  // first output row of this warp
             if (kind == 0)
                 epi0.begin_unit(ea, un.mb * kBM + r_in_tile);

@@ -54,6 +54,8 @@ struct EpiArgs {
     float* part_s;           // [n_segs, part_ld] running sum
     float* zy;               // [M] target logit
     int64_t part_ld;
+    float* Z;                // forward of the single fwd+bwd call: FP32 logits [M, ldZ]
+    int64_t ldZ;
     const float* lse;        // [M]
     const float* grad;       // [M] grad_logp
     void* S;                 // [M, ldS] off-target part of g (0 at the target)
@@ -102,7 +104,7 @@ struct GemmOperands {
 
 // Tile output written by the epilogue ([rows, cols], row stride ld).
 struct OutDesc {
-    void* ptr;  // nullptr: the kind stores nothing (forward)
+    void* ptr;  // nullptr: the kind stores nothing (plain forward)
     int dtype;
     int64_t rows, cols, ld;
 };
@@ -142,6 +144,13 @@ cudaError_t launch_db_chunk(const void* S, int64_t ldS, int s_dtype, int64_t row
                             const int64_t* keys, const float* tc_all, void* grad_bias,
                             int out_dtype, cudaStream_t s);
 cudaError_t launch_fill_zero(void* p, int64_t n_elems, int dtype, cudaStream_t s);
+// Softmax part from stored FP32 logits Z [rows, ldZ] (bias included):
+// S = -grad * exp(z - lse) off target (S dtype s_dtype), S = 0 and
+// tc = grad * (1 - p) at the target, +0 rows when the target is invalid or
+// the gradient zero.  Same arithmetic as the recompute epilogue.
+cudaError_t launch_softmax_part(const float* Z, int64_t ldZ, int64_t rows, int64_t V,
+                                const int64_t* targets, const float* grad, const float* lse,
+                                void* S, int64_t ldS, int s_dtype, float* tc, cudaStream_t s);
 cudaError_t launch_unsatisfied_wait(int* flag, int* status, uint64_t wait_ns, cudaStream_t s);
 
 }  // namespace ll

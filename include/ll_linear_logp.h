@@ -75,9 +75,10 @@ const char* ll_status_string(int status);
 int ll_version(void);
 
 /*
- * Workspace bytes needed by ll_forward (is_backward = 0) or ll_backward
- * (is_backward = 1) for these sizes; `flags` is the need_db flag for the
- * backward (bias gradient partials) and ignored for the forward.
+ * Workspace bytes needed by ll_forward (is_backward = 0), ll_backward
+ * (is_backward = 1) or ll_forward_backward (is_backward = 2) for these
+ * sizes; `flags` is the need_db flag for the backward (bias gradient
+ * partials) and ignored for the forward.
  * token_chunks: number of token chunks the backward splits N into (0 =
  * automatic, see ll_backward).  Returns 0 only for N == 0 in the forward.
  * The workspace pointer must be 256-byte aligned.
@@ -129,6 +130,24 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight,
                 void* grad_weight, int dw_dtype,
                 void* grad_bias, int token_chunks,
                 void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Forward and backward in one call, for when grad_logp is known before the
+ * forward (a fixed loss weighting such as a mean cross entropy, as in the
+ * fused linear cross entropy of Liger-Kernel PR #1324, "Summary").  Same
+ * arguments and results as ll_forward followed by ll_backward (logp and lse
+ * are written as the forward's outputs), bitwise: each token chunk's forward
+ * GEMM keeps its FP32 logits in the workspace (one chunk's worth, bounded by
+ * the same 2 GiB automatic budget, never the whole [N, V] beyond it), and
+ * the softmax part is formed from them instead of recomputing the logits.
+ * Workspace: ll_workspace_size(..., is_backward = 2, need_db).
+ */
+int ll_forward_backward(const float* grad_logp, const void* hidden, const void* weight,
+                        const void* bias, const int64_t* targets, int64_t N, int64_t D,
+                        int64_t V, int dtype, float* logp, float* lse, int need_dh,
+                        int need_dw, int need_db, void* grad_hidden, int dh_dtype,
+                        void* grad_weight, int dw_dtype, void* grad_bias, int token_chunks,
+                        void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Forward without a caller workspace.  No counterpart on the source pages:
@@ -184,8 +203,9 @@ int ll_check_status(void* stream);
  * Tracing.  ll_launch_count(): number of kernels this library has launched
  * in the process.  ll_profile_enable(1) clears earlier records and brackets
  * every phase of later calls (fwd_gemm, lse_merge, token_sort,
- * recompute_gemm, grad_gemm (grad_hidden and grad_weight tiles), db_sums,
- * logits_fwd, logits_bwd; an _f32 suffix for the CUDA-core FP32 GEMMs) with CUDA events on the call's
+ * recompute_gemm, softmax_part, grad_gemm (grad_hidden and grad_weight
+ * tiles), db_sums, logits_fwd, logits_bwd; an _f32 suffix for the
+ * CUDA-core FP32 GEMMs) with CUDA events on the call's
  * stream; ll_profile_enable(0) stops recording.  ll_profile_summary()
  * synchronises on the recorded events and writes one line per phase,
  * "label count total_ms", into buf (NUL-terminated, truncated to len);

@@ -253,3 +253,51 @@ def test_requested_gradients_only(lib, need):
     for k, want in zip(("dh", "dW", "db"), need):
         assert (got[k] is not None) == bool(want), k
     compare(p, got, full_ref(p))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("N,D,V,bias,chunks", [
+    (300, 136, 1031, True, 0), (513, 264, 4099, True, 3), (1000, 128, 2048, False, 2)])
+def test_single_call_forward_backward_is_bitwise_the_two_calls(lib, dt, N, D, V, bias, chunks):
+    """ll_forward_backward (grad_logp known up front, no logits recompute)
+    gives bitwise the outputs of ll_forward + ll_backward, and so the oracle's."""
+    p = synth.linear_inputs(N, D, V, dtype=dt, bias=bias, seed=N + 7)
+    two = run(lib, p, token_chunks=chunks)
+    h, W, b = dev(p["h"], dt), dev(p["W"], dt), dev(p["b"], dt)
+    logp, lse, dh, dW, db = lib.forward_backward(dev(p["gl"]), h, W, b, dev(p["y"]),
+                                                 token_chunks=chunks)
+    torch.cuda.synchronize()
+    assert lib.check_status() == 0
+    one = dict(logp=logp, lse=lse, dh=dh, dW=dW, db=db)
+    for k in ("logp", "lse", "dh", "dW") + (("db",) if bias else ()):
+        assert bits_equal(one[k], two[k]), k
+    compare(p, one, full_ref(p))
+
+
+@pytest.mark.slow
+def test_single_call_bf16_4k_2k_32k_matches_two_calls(lib):
+    p = synth.linear_inputs(**synth.WORKLOADS["bf16_4k_2k_32k"], seed=0)
+    two = run(lib, p)
+    h, W = dev(p["h"], "bf16"), dev(p["W"], "bf16")
+    logp, lse, dh, dW, _ = lib.forward_backward(dev(p["gl"]), h, W, None, dev(p["y"]))
+    torch.cuda.synchronize()
+    for k, v in (("logp", logp), ("lse", lse), ("dh", dh), ("dW", dW)):
+        assert bits_equal(v, two[k]), k
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_gradients_into_given_16bit_buffers(lib, dt):
+    """Caller-given grad buffers decide the output dtypes (grad_weight and
+    grad_bias in the operand dtype here, as in the dtype sweep)."""
+    p = synth.linear_inputs(640, 256, 3000, dtype=dt, bias=True, seed=37, grad="mean")
+    h, W, b = dev(p["h"], dt), dev(p["W"], dt), dev(p["b"], dt)
+    y, g = dev(p["y"]), dev(p["gl"])
+    logp, lse = lib.forward(h, W, b, y)
+    t = TORCH[dt]
+    dh = torch.empty(640, 256, dtype=t, device="cuda")
+    dW = torch.empty(3000, 256, dtype=t, device="cuda")
+    db = torch.empty(3000, dtype=t, device="cuda")
+    lib.backward(g, h, W, b, y, lse, out=(dh, dW, db))
+    torch.cuda.synchronize()
+    assert lib.check_status() == 0
+    compare(p, dict(logp=logp, lse=lse, dh=dh, dW=dW, db=db), full_ref(p))

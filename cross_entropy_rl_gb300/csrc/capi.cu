@@ -284,7 +284,7 @@ int ll_forward(const void* hidden, const void* weight, const void* bias, const i
     sh.tiles_per_unit = kVocabTilesPerSeg;
     sh.n_segs = L.n_segs;
     sh.k_blocks = cdiv(D, 64);
-    sh.unit_order = 0;
+    sh.unit_order = 2;
     EpiArgs ea;
     memset(&ea, 0, sizeof(ea));
     ea.M = N;
@@ -436,7 +436,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             sh.tiles_per_unit = kVocabTilesPerSeg;
             sh.n_segs = cdiv(sh.n_tiles, sh.tiles_per_unit);
             sh.k_blocks = cdiv(D, 64);
-            sh.unit_order = 0;
+            sh.unit_order = 2;
             EpiArgs& ea = G.ea[0];
             ea = base;
             ea.M = rows;
@@ -468,7 +468,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             sh.tiles_per_unit = kVocabTilesPerSeg;
             sh.n_segs = L.n_segs;
             sh.k_blocks = cdiv(D, 64);
-            sh.unit_order = 0;
+            sh.unit_order = 2;
             EpiArgs& ea = G.ea[0];
             ea = base;
             ea.M = rows;

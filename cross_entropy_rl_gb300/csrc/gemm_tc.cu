@@ -119,9 +119,16 @@ __device__ __forceinline__ Unit decode_unit(const KParams& P, int64_t u) {
     if (sh.unit_order == 0) {
         r.seg = v / sh.m_blocks;
         r.mb = v % sh.m_blocks;
-    } else {
+    } else if (sh.unit_order == 1) {
         r.mb = v / sh.n_segs;
         r.seg = v % sh.n_segs;
+    } else {
+        const int64_t per_group = kGroupM * sh.n_segs;
+        const int64_t g = v / per_group;
+        const int64_t in_g = v % per_group;
+        const int64_t gm = min(kGroupM, sh.m_blocks - g * kGroupM);
+        r.seg = in_g / gm;
+        r.mb = g * kGroupM + in_g % gm;
     }
     r.t0 = r.seg * sh.tiles_per_unit;
     r.t1 = min(r.t0 + sh.tiles_per_unit, sh.n_tiles);
@@ -604,7 +611,7 @@ cudaError_t dispatch(const GemmLaunch& L, const CUtensorMap* m, const KParams& P
 cudaError_t launch_gemm_f32(EpiKind kind, const void* A, int64_t lda, int a_mn, const void* B,
                             int64_t ldb, int b_mn, int64_t M, int64_t N, int64_t K,
                             const GemmShape& shape, const EpiArgs& ea, const DevInfo& dev,
-                            cudaStream_t s);
+                            int max_ctas, cudaStream_t s);
 
 cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s) {
     if (L.dtype == LL_F32) {
@@ -613,7 +620,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
             EpiArgs ea = L.ea[k];
             ea.dw_add_prev = !ea.first_chunk;
             cudaError_t e = launch_gemm_f32(L.kind[k], g.A, g.lda, g.a_mn, g.B, g.ldb, g.b_mn,
-                                            g.M, g.N, g.K, L.shape[k], ea, dev, s);
+                                            g.M, g.N, g.K, L.shape[k], ea, dev, L.max_ctas, s);
             if (e != cudaSuccess) return e;
         }
         return cudaSuccess;

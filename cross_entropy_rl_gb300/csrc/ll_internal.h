@@ -86,8 +86,13 @@ struct GemmShape {
     int64_t tiles_per_unit;  // N tiles per work unit (forward segments), else 1
     int64_t n_segs;          // ceil(n_tiles / tiles_per_unit)
     int64_t k_blocks;        // K / BK, rounded up
-    int unit_order;          // 0: segment-major, 1: m-major
+    int unit_order;          // 0: segment-major, 1: m-major, 2: segment-major within
+                             //    groups of kGroupM row blocks (L2 rasterisation)
 };
+
+// Row blocks per group of the grouped unit order: the units in flight then
+// share ~kGroupM row blocks of A and a few segments of B, which fit in L2.
+constexpr int64_t kGroupM = 32;
 
 // Operands of one GEMM kind:
 //   A: [M, K] (a_mn = 0, row stride lda) or [K, M] (a_mn = 1)

@@ -36,9 +36,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (sh.unit_order == 0) {
             seg = u / sh.m_blocks;
             mb = u % sh.m_blocks;
-        } else {
+        } else if (sh.unit_order == 1) {
             mb = u / sh.n_segs;
             seg = u % sh.n_segs;
+        } else {
+            const int64_t per_group = kGroupM * sh.n_segs;
+            const int64_t g = u / per_group;
+            const int64_t in_g = u % per_group;
+            const int64_t gm = min(kGroupM, sh.m_blocks - g * kGroupM);
+            seg = in_g / gm;
+            mb = g * kGroupM + in_g % gm;
         }
         const int64_t t0 = seg * sh.tiles_per_unit;
         const int64_t t1 = min(t0 + sh.tiles_per_unit, sh.n_tiles);
@@ -105,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <EpiKind E, bool A_MN, bool B_MN>
 cudaError_t launch_simt(const float* A, int64_t lda, const float* B, int64_t ldb, int64_t M,
                         int64_t N, int64_t K, const GemmShape& sh, const EpiArgs& ea,
-                        const DevInfo& dev, cudaStream_t s) {
+                        const DevInfo& dev, int max_ctas, cudaStream_t s) {
     auto kern = simt_gemm_kernel<E, A_MN, B_MN>;
     static int configured[64] = {0};
     if (dev.device < 64 && !configured[dev.device]) {
@@ -115,7 +122,8 @@ cudaError_t launch_simt(const float* A, int64_t lda, const float* B, int64_t ldb
         configured[dev.device] = 1;
     }
     const int64_t units = sh.m_blocks * sh.n_segs;
-    const int grid = static_cast<int>(units < dev.num_sms ? units : dev.num_sms);
+    const int cap = (max_ctas > 0 && max_ctas < dev.num_sms) ? max_ctas : dev.num_sms;
+    const int grid = static_cast<int>(units < cap ? units : cap);
     note_launches(1);
     kern<<<grid, kThreads, kSmemBytes, s>>>(A, lda, B, ldb, M, N, K, sh, ea);
     return cudaGetLastError();
@@ -126,19 +134,19 @@ cudaError_t launch_simt(const float* A, int64_t lda, const float* B, int64_t ldb
 cudaError_t launch_gemm_f32(EpiKind kind, const void* A, int64_t lda, int a_mn, const void* B,
                             int64_t ldb, int b_mn, int64_t M, int64_t N, int64_t K,
                             const GemmShape& sh, const EpiArgs& ea, const DevInfo& dev,
-                            cudaStream_t s) {
+                            int max_ctas, cudaStream_t s) {
     const float* a = static_cast<const float*>(A);
     const float* b = static_cast<const float*>(B);
     switch (kind) {
         case EpiKind::Fwd:
-            return launch_simt<EpiKind::Fwd, false, false>(a, lda, b, ldb, M, N, K, sh, ea, dev, s);
+            return launch_simt<EpiKind::Fwd, false, false>(a, lda, b, ldb, M, N, K, sh, ea, dev, max_ctas, s);
         case EpiKind::Recomp:
             return launch_simt<EpiKind::Recomp, false, false>(a, lda, b, ldb, M, N, K, sh, ea, dev,
-                                                              s);
+                                                              max_ctas, s);
         case EpiKind::Dh:
-            return launch_simt<EpiKind::Dh, false, true>(a, lda, b, ldb, M, N, K, sh, ea, dev, s);
+            return launch_simt<EpiKind::Dh, false, true>(a, lda, b, ldb, M, N, K, sh, ea, dev, max_ctas, s);
         case EpiKind::Dw:
-            return launch_simt<EpiKind::Dw, true, true>(a, lda, b, ldb, M, N, K, sh, ea, dev, s);
+            return launch_simt<EpiKind::Dw, true, true>(a, lda, b, ldb, M, N, K, sh, ea, dev, max_ctas, s);
     }
     (void)a_mn;
     (void)b_mn;

@@ -328,6 +328,26 @@ def run_ours(args, rank, world, local_rank):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_e2e = float(t.item())
 
+    # single call (upstream gradient known before the forward): no logits recompute
+    ws_fb = torch.empty(max(256, ll.workspace_size(N, D, V, tdt, args.token_chunks,
+                                                   backward=2, need_db=has_bias)),
+                        dtype=torch.uint8, device=device)
+
+    def fb_step():
+        ll.forward_backward(gl, h, W, b, y, need_dh=True, need_dw=True, need_db=has_bias,
+                            dh_dtype=tdt, dw_dtype=dw_dt, token_chunks=args.token_chunks,
+                            workspace=ws_fb, out=(logp, lse, dh, dW, db))
+
+    for _ in range(args.warmup):
+        fb_step()
+    ms_fb = timed_loop(fb_step, args.steps)
+    assert ll.check_status() == 0
+    if dist is not None:
+        t = torch.tensor([ms_fb], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_fb = float(t.item())
+    del ws_fb
+
     if rank != 0:
         return
     pk, pk_kind = peaks()
@@ -370,6 +390,12 @@ def run_ours(args, rank, world, local_rank):
                      "flops_per_launch": flops[dom]},
         "kernels_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},
         "gpu_launches": launches,
+        "single_call": {"value": world * N / (ms_fb * 1e-3), "unit": "tokens/s",
+                        "ms_per_step": ms_fb,
+                        "useful_frac_of_bf16_peak": 6.0 * N * D * V / (ms_fb * 1e-3) / 1e12
+                        / pk["bf16_tflops"],
+                        "call": "ll_forward_backward (grad_logp known before the forward; "
+                                "bitwise the outputs of ll_forward + ll_backward)"},
         "e2e": {"value": world * N / (ms_e2e * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h.numel() * h.element_size() + y.numel() * 8 + gl.numel() * 4,
                 "d2h_bytes_per_step": logp.numel() * 4, "ms_per_step": ms_e2e},

@@ -49,6 +49,8 @@ EXPORTS = {
     "logits_logp_fwd": (_c_int, [_c_p, _c_i64, _c_int, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_p]),
     "logits_logp_bwd": (_c_int, [_c_p, _c_p, _c_i64, _c_int, _c_p, _c_p, _c_i64, _c_i64,
                                  _c_p, _c_p]),
+    "logits_logp_fwd_bwd": (_c_int, [_c_p, _c_p, _c_i64, _c_int, _c_p, _c_i64, _c_i64, _c_p,
+                                     _c_p, _c_p, _c_p]),
     "ll_check_status": (_c_int, [_c_p]),
     "ll_set_wait_limit_ns": (None, [_c_i64]),
     "ll_debug_unsatisfied_wait": (_c_int, [_c_p, _c_p]),
@@ -359,6 +361,34 @@ def profile_summary() -> dict:
         name, cnt, ms = line.split()
         out[name] = (int(cnt), float(ms))
     return out
+
+
+def logits_fwd_bwd(grad_logp, logits, targets, V=None, *, out=None, stream=None):
+    """(logp, lse, grad_logits) in one pass over the logits (grad_logp known
+    before the forward)."""
+    torch = _torch()
+    L = load()
+    N, ld = logits.shape
+    V = ld if V is None else V
+    dev = logits.device
+    _need(logits, "logits", (N, ld), device=dev,
+          dtypes=(torch.float32, torch.float16, torch.bfloat16))
+    _need(targets, "targets", (N,), torch.int64, dev)
+    _need(grad_logp, "grad_logp", (N,), torch.float32, dev)
+    if out is None:
+        logp = torch.empty(N, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+        g = torch.empty_like(logits)
+    else:
+        logp, lse, g = out
+    _need(logp, "logp", (N,), torch.float32, dev)
+    _need(lse, "lse", (N,), torch.float32, dev)
+    _need(g, "grad_logits", (N, ld), logits.dtype, dev)
+    st = L.logits_logp_fwd_bwd(_ptr(grad_logp), _ptr(logits), ld, _code(logits.dtype),
+                               _ptr(targets), N, V, _ptr(logp), _ptr(lse), _ptr(g),
+                               _stream(stream))
+    _check("logits_logp_fwd_bwd", st)
+    return logp, lse, g
 
 
 def check_status(stream=None) -> int:

@@ -655,6 +655,47 @@ int logits_logp_bwd(const float* grad_logp, const void* logits, int64_t ld, int 
                                          grad_logits, static_cast<cudaStream_t>(stream)));
 }
 
+int logits_logp_fwd_bwd(const float* grad_logp, const void* logits, int64_t ld, int dtype,
+                        const int64_t* targets, int64_t N, int64_t V, float* logp, float* lse,
+                        void* grad_logits, void* stream) {
+    if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
+    if (N < 0 || V < 1 || V > kMaxV || ld < V || N > (int64_t(1) << 31) - 1) return LL_ERR_SHAPE;
+    if (N == 0) return LL_OK;
+    if (!grad_logp || !logits || !targets || !logp || !lse || !grad_logits)
+        return LL_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(logits) % esize(dtype) ||
+        reinterpret_cast<uintptr_t>(grad_logits) % esize(dtype))
+        return LL_ERR_ALIGN;
+    const char* a = static_cast<const char*>(logits);
+    const char* b = static_cast<const char*>(grad_logits);
+    const size_t span = size_t(N) * size_t(ld) * esize(dtype);
+    if (a < b + span && b < a + span) return LL_ERR_INVALID_ARG;  // no aliasing
+    DeviceGuard guard(logits);
+    if (guard.err) return guard.err;
+    DevInfo dev;
+    int st = device_info(guard.dev, &dev);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool used = false;
+    {
+        Phase ph("logits_fused", s);
+        cudaError_t e = launch_logits_fused(grad_logp, logits, ld, dtype, targets, N, V, logp,
+                                            lse, grad_logits, dev, s, &used);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    if (used) return LL_OK;
+    // shape or alignment the one-pass kernel does not take: the two kernels
+    cudaError_t e;
+    {
+        Phase ph("logits_fwd", s);
+        e = launch_logits_fwd(logits, ld, dtype, targets, N, V, logp, lse, s);
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    Phase ph("logits_bwd", s);
+    return cuda_status(launch_logits_bwd(grad_logp, logits, ld, dtype, targets, lse, N, V,
+                                         grad_logits, s));
+}
+
 int ll_check_status(void* stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return LL_ERR_CUDA;

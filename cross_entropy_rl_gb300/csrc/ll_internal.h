@@ -39,6 +39,14 @@ cudaError_t launch_logits_bwd(const float* grad, const void* logits, int64_t ld,
                               const int64_t* targets, const float* lse, int64_t N, int64_t V,
                               void* grad_logits, cudaStream_t s);
 
+// Logits forward + backward in one pass for a known upstream gradient
+// (logits_fused.cu).  *used = false (nothing launched) when the shape or
+// alignment does not suit it; the caller then runs the two kernels.
+cudaError_t launch_logits_fused(const float* grad, const void* logits, int64_t ld, int dtype,
+                                const int64_t* targets, int64_t N, int64_t V, float* logp,
+                                float* lse, void* grad_logits, const DevInfo& dev,
+                                cudaStream_t s, bool* used);
+
 // --- GEMM-based linear path -------------------------------------------------
 enum class EpiKind : int { Fwd = 0, Recomp = 1, Dh = 2, Dw = 3 };
 

@@ -193,6 +193,21 @@ int logits_logp_bwd(const float* grad_logp, const void* logits, int64_t ld, int 
                     void* grad_logits, void* stream);
 
 /*
+ * Logits-input forward and backward in one pass, for a grad_logp known
+ * before the forward.  Same arguments as logits_logp_fwd plus
+ * logits_logp_bwd together; logp, lse and grad_logits are written.  Each
+ * row is read once and its gradient written once (4 V bytes per row instead
+ * of 6 V): a cluster of CTAs holds the row in shared memory, combines the
+ * slices' (max, sum-exp) in a fixed order and overwrites the row with its
+ * gradient.  Deterministic and batch-invariant; equal to the two calls
+ * within rounding (the reduction order differs).  Rows whose logits or
+ * gradient are not 16-byte aligned, or V % 8 != 0, use the two kernels.
+ */
+int logits_logp_fwd_bwd(const float* grad_logp, const void* logits, int64_t ld, int dtype,
+                        const int64_t* targets, int64_t N, int64_t V, float* logp, float* lse,
+                        void* grad_logits, void* stream);
+
+/*
  * Device status word of the current device: synchronises `stream`, returns
  * LL_OK or the first device-side error recorded since the last call
  * (LL_ERR_DEVICE_TIMEOUT), and clears it.
@@ -204,8 +219,8 @@ int ll_check_status(void* stream);
  * in the process.  ll_profile_enable(1) clears earlier records and brackets
  * every phase of later calls (fwd_gemm, lse_merge, token_sort,
  * recompute_gemm, softmax_part, grad_gemm (grad_hidden and grad_weight
- * tiles), db_sums, logits_fwd, logits_bwd; an _f32 suffix for the
- * CUDA-core FP32 GEMMs) with CUDA events on the call's
+ * tiles), db_sums, logits_fwd, logits_bwd, logits_fused; an _f32 suffix
+ * for the CUDA-core FP32 GEMMs) with CUDA events on the call's
  * stream; ll_profile_enable(0) stops recording.  ll_profile_summary()
  * synchronises on the recorded events and writes one line per phase,
  * "label count total_ms", into buf (NUL-terminated, truncated to len);

@@ -146,3 +146,66 @@ def test_logits_32k_151936_sampled(lib):
     # the probe rows of the sweep are position independent at full size too
     alone = run(lib, x[-1:], y[-1:], gl[-1:])
     assert bits_equal(alone[2], got[2][-1:]) and bits_equal(alone[1], got[1][-1:])
+
+
+# ------------------------------------------------ one pass (known upstream) --
+
+def run_fused(ll, x, y, gl, V=None):
+    logp, lse, g = ll.logits_fwd_bwd(gl, x, y, V)
+    torch.cuda.synchronize()
+    assert ll.check_status() == 0
+    return logp, lse, g
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("V,ld", [(151936, 151936), (1024, 1024), (4096, 4104),
+                                  (1031, 1031), (1031, 1040), (8, 8)])
+def test_fused_full_parity(lib, dt, V, ld):
+    """One-pass fwd+bwd vs the oracle, on shapes the cluster kernel takes and
+    on ones that go to the two kernels (V % 8 != 0, unaligned rows)."""
+    N = 48 if V > 10000 else 150
+    p = synth.logits_inputs(N, V, seed=V + ld, dtype=dt, ld=ld)
+    x, y, gl = dev(p["logits"], dt), dev(p["y"]), dev(p["gl"])
+    compare(p, run_fused(lib, x, y, gl, V=V), V=V)
+
+
+def test_fused_invalid_targets_and_zero_rows(lib):
+    N, V = 40, 4096
+    p = synth.logits_inputs(N, V, seed=5)
+    x = dev(p["logits"], "bf16")
+    x[:, 3000:] = -float("inf")
+    x[11, :] = -float("inf")
+    y = p["y"] % 1000
+    y[[2, 9, 11, 30]] = [-100, V, -100, V + 5]
+    gl = p["gl"].copy()
+    gl[[4, 20]] = [0.0, -0.0]
+    q = dict(p, y=y, gl=gl, logits=x.view(torch.int16).cpu().numpy().view(np.uint16))
+    got = run_fused(lib, x, dev(y), dev(gl))
+    compare(q, got)
+    logp, lse, g = got
+    for r in (2, 9, 11, 30, 4, 20):
+        assert_pos_zero(f"g[{r}]", g[r])
+    assert float(logp[11]) == 0.0 and float(lse[11]) == -float("inf")
+
+
+def test_fused_batch_invariance_and_determinism(lib):
+    V = 151936
+    p = synth.logits_inputs(300, V, seed=41)
+    x, y, gl = dev(p["logits"], "bf16"), dev(p["y"]), dev(p["gl"])
+    full = run_fused(lib, x, y, gl)
+    again = run_fused(lib, x, y, gl)
+    for a, b in zip(full, again):
+        assert bits_equal(a, b)
+    for rows in ([0], [299], [7, 150, 3], list(range(100, 257))):
+        idx = torch.tensor(rows, device="cuda")
+        part = run_fused(lib, x[idx].contiguous(), y[idx], gl[idx])
+        for a, b in zip(part, full):
+            assert bits_equal(a, b[idx])
+
+
+@pytest.mark.slow
+def test_fused_logits_32k_151936_sampled(lib):
+    p = synth.logits_inputs(**synth.WORKLOADS["logits_32k_151936"], seed=0)
+    x, y, gl = dev(p["logits"], "bf16"), dev(p["y"]), dev(p["gl"])
+    got = run_fused(lib, x, y, gl)
+    compare(p, got, rows=synth.sample_rows(0, p["N"]))

@@ -449,6 +449,21 @@ def logits_path(args, device, pk):
     prof = ll.profile_summary()
     ll.profile(False)
     assert ll.check_status() == 0
+
+    # one pass over the logits when grad_logp is known before the forward
+    def fused_step():
+        ll.logits_fwd_bwd(gl, x, y, out=(logp, lse, dx))
+
+    for _ in range(3):
+        fused_step()
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        fused_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms_fused = a.elapsed_time(b) / steps
+    assert ll.check_status() == 0
     fwd_ms = prof["logits_fwd"][1] / prof["logits_fwd"][0]
     bwd_ms = prof["logits_bwd"][1] / prof["logits_bwd"][0]
     fwd_b, bwd_b = 2.0 * N * V, 4.0 * N * V
@@ -464,7 +479,12 @@ def logits_path(args, device, pk):
                          "frac": bwd_b / (bwd_ms * 1e-3) / 1e9 / peak,
                          "traffic": ncu_traffic("logits_bwd"), "avg_launch_ms": bwd_ms},
             "logits_fwd": {"ms": fwd_ms, "gbs": fwd_b / (fwd_ms * 1e-3) / 1e9,
-                           "frac": fwd_b / (fwd_ms * 1e-3) / 1e9 / peak}}
+                           "frac": fwd_b / (fwd_ms * 1e-3) / 1e9 / peak},
+            "single_pass": {"call": "logits_logp_fwd_bwd (grad_logp known before the forward)",
+                            "ms_per_step": ms_fused, "value": N / (ms_fused * 1e-3),
+                            "unit": "tokens/s", "bytes_per_token": 4 * V,
+                            "gbs": 4.0 * N * V / (ms_fused * 1e-3) / 1e9,
+                            "frac": 4.0 * N * V / (ms_fused * 1e-3) / 1e9 / peak}}
 
 
 def main():

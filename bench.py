@@ -133,25 +133,35 @@ class Clocks:
                 "reasons": sorted(reasons)}
 
 
-def kernel_source_hash() -> str:
+# source files each timed kernel is built from (a change to any of them
+# invalidates a stored ncu traffic figure for that kernel)
+KERNEL_SOURCES = {
+    "gemm": ["gemm_tc.cu", "epilogue.cuh", "ll_device.cuh", "ll_internal.h"],
+    "logits": ["logits_kernels.cu", "ll_device.cuh", "ll_internal.h"],
+}
+PHASE_SOURCES = {"fwd_gemm": "gemm", "recompute_gemm": "gemm", "grad_gemm": "gemm",
+                 "logits_fwd": "logits", "logits_bwd": "logits"}
+
+
+def kernel_source_hash(phase: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "cross_entropy_rl_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[PHASE_SOURCES[phase]]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(phase: str):
+def ncu_traffic(phase: str, workload: str = WORKLOAD):
     """DRAM bytes per launch of `phase` from the committed ncu summary, if it
-    was taken on the current kernel sources; else None."""
+    was taken on the current sources of that kernel; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(p):
+    if not os.path.exists(p) or phase not in PHASE_SOURCES:
         return None
     with open(p) as f:
         d = json.load(f)
-    ent = d.get(WORKLOAD, {}).get(phase)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    ent = d.get(workload, {}).get(phase)
+    if not ent or ent.get("source_hash") != kernel_source_hash(phase):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -386,7 +396,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
                      "frac_of_sustained": achieved / pk.get("bf16_tflops_sustained", peak),
-                     "traffic": ncu_traffic(dom), "avg_launch_ms": avg_ms,
+                     "traffic": ncu_traffic(dom, args.workload), "avg_launch_ms": avg_ms,
                      "flops_per_launch": flops[dom]},
         "kernels_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},
         "gpu_launches": launches,

@@ -162,6 +162,14 @@ FwdLayout fwd_layout(int64_t N, int64_t V) {
 
 constexpr size_t kAutoChunkBytes = size_t(2) << 30;  // softmax workspace budget
 
+// Rows of grad_bias partials a chunk of Nc tokens may write: one per 32 rows
+// (recompute epilogue) or up to 64 row groups (sums over the stored S).
+int64_t db_groups(int64_t Nc) {
+    const int64_t per32 = cdiv(Nc, 32);
+    const int64_t from_s = Nc < 64 ? (Nc > 0 ? Nc : 1) : 64;
+    return per32 > from_s ? per32 : from_s;
+}
+
 struct BwdLayout {
     int64_t chunks, Nc, ldS, ldZ, n_segs;
     size_t S, Z, part_m, part_s, zy, tc, keys, offs, ctr, db, total;
@@ -209,7 +217,7 @@ BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need
     L.ctr = off;
     off = align_up(off + 64);
     L.db = off;
-    if (need_db) off = align_up(off + db_partial_bytes(L.Nc, V));
+    if (need_db) off = align_up(off + size_t(db_groups(L.Nc) + 1) * size_t(V) * 4);
     L.total = off;
     return L;
 }
@@ -373,8 +381,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
     int* offs = reinterpret_cast<int*>(ws + L.offs);
     int* counter = reinterpret_cast<int*>(ws + L.ctr);
     float* db_part = reinterpret_cast<float*>(ws + L.db);
-    const int64_t db_groups_v = (L.Nc < 64 ? L.Nc : 64) * V;
-    float* db_acc = db_part + db_groups_v;
+    float* db_acc = db_part + db_groups(L.Nc) * V;  // after the partial rows
     const size_t es = esize(dtype);
     float* Z = reinterpret_cast<float*>(ws + L.Z);
     float* part_m = reinterpret_cast<float*>(ws + L.part_m);
@@ -447,6 +454,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             ea.S = S;
             ea.ldS = L.ldS;
             ea.tc = tc + r0;
+            ea.db_part = need_db ? db_part : nullptr;
             G.out[0] = OutDesc{S, dtype, rows, V, L.ldS};
             G.zero_counter = counter;  // for the gradient launch that follows
             if (overlap && c == 0) G.max_ctas = dev.num_sms - kSideSms;
@@ -576,8 +584,12 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
         // (4) grad_bias: fixed-order column sums of S (+ one-hot part at the end)
         if (need_db) {
             Phase ph("db_sums", s);
-            e = launch_db_chunk(S, L.ldS, dtype, rows, V, db_part, db_acc, c == 0,
-                                c == L.chunks - 1, offs, keys, tc, grad_bias, dw_dtype, s);
+            if (!fused)  // partials from the recompute epilogue, per 32 rows
+                e = launch_db_finish(db_part, cdiv(rows, 32), V, db_acc, c == 0,
+                                     c == L.chunks - 1, offs, keys, tc, grad_bias, dw_dtype, s);
+            else
+                e = launch_db_chunk(S, L.ldS, dtype, rows, V, db_part, db_acc, c == 0,
+                                    c == L.chunks - 1, offs, keys, tc, grad_bias, dw_dtype, s);
             if (e != cudaSuccess) return cuda_status(e);
         }
     }

@@ -151,7 +151,11 @@ struct RowEpilogue {
                     s += acc;
                 }
             } else {  // Recomp: S = -grad * exp(z - lse), target entry apart
-                if (!rvalid) return;
+                if (!rvalid) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                    return;
+                }
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = ex2(fmaf(v[j], kLog2e, -lse2));
                 const int64_t off = y - col0;
@@ -202,6 +206,36 @@ struct RowEpilogue {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = fmaf(g, hv[j], v[j]);
             }
+        }
+    }
+
+    // grad_bias partials of the recompute: the sums over this warp's 32 rows
+    // of each of the chunk's 32 columns of S (off-target entries, FP32, rows
+    // outside the problem count 0), by a fixed butterfly over the lanes: at
+    // each step a lane keeps the half of its columns selected by its lane
+    // bit and adds the partner's copy of that half; lane l ends with the sum
+    // of column l.  Written to db_part[row / 32][col].  All 32 lanes of the
+    // warp must call it (consecutive rows); v is consumed.
+    __device__ __forceinline__ void db_partials(const EpiArgs& ea, float (&v)[32],
+                                                int64_t col0) {
+        if constexpr (E == EpiKind::Recomp) {
+            if (!ea.db_part) return;
+            const int lane = threadIdx.x & 31;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) {
+                const bool up = (lane & off) != 0;
+#pragma unroll
+                for (int j = 0; j < off; ++j) {
+                    const float keep = up ? v[j + off] : v[j];
+                    const float send = up ? v[j] : v[j + off];
+                    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                }
+            }
+            const int64_t col = col0 + lane;
+            // warps whose 32 rows all lie past the problem write nothing, so
+            // partial rows stay within ceil(M / 32)
+            if (col < ea.Ncols && (row & ~int64_t(31)) < ea.M)
+                ea.db_part[(row >> 5) * ea.Ncols + col] = v[0];
         }
     }
 

@@ -458,6 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __syncwarp();
                     }
                     stage_row<T>(sb, lane, v, out16, h);
+                    if (kind == 0)  // grad_bias partials (recompute only), consumes v
+                        epi0.db_partials(ea, v, col0);
                     if (!out16 || h == 1) {
                         fence_proxy_async_smem();
                         __syncwarp();

@@ -70,6 +70,7 @@ struct EpiArgs {
     int64_t ldS;
     float* tc;               // [M] target entry of g: grad * (1 - p[y]) (Recomp writes,
                              //     Dh reads; offset to the launch's rows)
+    float* db_part;          // Recomp: [ceil(M / 32), V] grad_bias partials, or nullptr
     // dh (M = tokens, N = D): adds gl * W[y] and stores
     const void* W;
     int64_t ldW;
@@ -156,6 +157,12 @@ cudaError_t launch_db_chunk(const void* S, int64_t ldS, int s_dtype, int64_t row
                             float* partial, float* db_acc, int first, int last, const int* offs,
                             const int64_t* keys, const float* tc_all, void* grad_bias,
                             int out_dtype, cudaStream_t s);
+// The finishing half of it, for partials [groups, V] written elsewhere (the
+// recompute epilogue): db_acc (+)= sum over groups in order, then on `last`
+// the target entries and the store.
+cudaError_t launch_db_finish(const float* partial, int64_t groups, int64_t V, float* db_acc,
+                             int first, int last, const int* offs, const int64_t* keys,
+                             const float* tc_all, void* grad_bias, int out_dtype, cudaStream_t s);
 cudaError_t launch_fill_zero(void* p, int64_t n_elems, int dtype, cudaStream_t s);
 // Softmax part from stored FP32 logits Z [rows, ldZ] (bias included):
 // S = -grad * exp(z - lse) off target (S dtype s_dtype), S = 0 and

@@ -7,8 +7,8 @@
 // A row does not fit in one SM's shared memory (151936 bf16 = 297 KB), so a
 // thread-block cluster of C CTAs takes one row at a time: CTA j holds the
 // contiguous slice j of the row (slice boundaries depend only on V and C),
-// loaded by one bulk copy into a double-buffered shared-memory slice (the
-// next row is prefetched while the current one is processed).  Each CTA
+// loaded by one bulk copy into a ring of shared-memory slice buffers (the
+// next rows are prefetched while the current one is processed).  Each CTA
 // folds its slice into a running (max, sum-exp) pair with a fixed reduction
 // tree, the C pairs are combined in ascending rank order through distributed
 // shared memory (every CTA computes the same lse), the gradient
@@ -25,12 +25,14 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 8;
-constexpr size_t kSliceBudget = 200 * 1024;  // two slice buffers
+constexpr int kMaxBufs = 6;                   // slice buffers per CTA (ring)
+constexpr size_t kSliceBudget = 200 * 1024;   // shared memory for the ring
 
 struct FusedArgs {
     const void* logits;
     void* grad_out;
     int64_t ld, N, V, L;  // L: slice length in elements (multiple of 8)
+    int nbuf;             // ring depth: rows in flight = nbuf - 2 loads + 2 stores
     const int64_t* targets;
     const float* grad;
     float* logp;
@@ -88,8 +90,9 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t 
                  : "memory");
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-__device__ __forceinline__ void bulk_wait_read_all() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+// at most one bulk store (the latest) may still be reading shared memory
+__device__ __forceinline__ void bulk_wait_read_but_one() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -109,14 +112,13 @@ __global__ void __launch_bounds__(kThreads, 1) logits_fused_kernel(const FusedAr
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const uint32_t C = cluster_size();
     const uint32_t rank = cluster_rank();
-    const int64_t slice_elems_max = a.L;
-    T* buf[2] = {reinterpret_cast<T*>(smem_raw),
-                 reinterpret_cast<T*>(smem_raw + slice_elems_max * sizeof(T))};
-    uint8_t* tail = smem_raw + 2 * slice_elems_max * sizeof(T);
-    uint64_t* full = reinterpret_cast<uint64_t*>(tail);  // [2]
-    float2* slot = reinterpret_cast<float2*>(tail + 16);  // [2] this CTA's (m, s) per parity
-    MS* wred = reinterpret_cast<MS*>(tail + 32);          // [kWarps]
-    float* lse_sh = reinterpret_cast<float*>(tail + 32 + kWarps * sizeof(MS));
+    const int nbuf = a.nbuf;
+    const size_t slice_bytes = size_t(a.L) * sizeof(T);
+    uint8_t* tail = smem_raw + nbuf * slice_bytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(tail);                 // [kMaxBufs]
+    float2* slot = reinterpret_cast<float2*>(tail + 8 * kMaxBufs);      // [2] (m, s) per parity
+    MS* wred = reinterpret_cast<MS*>(tail + 8 * kMaxBufs + 16);         // [kWarps]
+    float* lse_sh = reinterpret_cast<float*>(tail + 8 * kMaxBufs + 16 + kWarps * sizeof(MS));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     const int64_t c0 = int64_t(rank) * a.L;  // this CTA's slice [c0, c1)
@@ -126,8 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) logits_fused_kernel(const FusedAr
     const int64_t nvec = len / 8;
 
     if (tid == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
+        for (int i = 0; i < nbuf; ++i) mbar_init(&full[i], 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -135,25 +136,39 @@ __global__ void __launch_bounds__(kThreads, 1) logits_fused_kernel(const FusedAr
     const T* X = static_cast<const T*>(a.logits);
     T* G = static_cast<T*>(a.grad_out);
     const int64_t first = cluster_id(), step = cluster_count();
+    // rows of this cluster: first, first + step, ...; the ring keeps the
+    // loads of the next nbuf - 2 rows in flight; a buffer is refilled two
+    // rows after its store was issued, so only the latest store may still
+    // be reading shared memory then
+    const int ahead = nbuf - 2;
+    auto buf_of = [&](int64_t kk) {
+        return reinterpret_cast<T*>(smem_raw + (kk % nbuf) * slice_bytes);
+    };
     bool ok = true;
-    if (tid == 0 && len > 0 && first < a.N) {
-        mbar_arrive_expect_tx(&full[0], bytes);
-        bulk_load(buf[0], X + first * a.ld + c0, bytes, &full[0]);
+    if (tid == 0 && len > 0) {
+        for (int kk = 0; kk < ahead; ++kk) {
+            const int64_t r = first + kk * step;
+            if (r >= a.N) break;
+            mbar_arrive_expect_tx(&full[kk], bytes);
+            bulk_load(buf_of(kk), X + r * a.ld + c0, bytes, &full[kk]);
+        }
     }
     int64_t k = 0;
     for (int64_t row = first; row < a.N; row += step, ++k) {
-        const int b = static_cast<int>(k & 1);
-        const int64_t next = row + step;
-        if (tid == 0 && len > 0 && next < a.N) {
-            bulk_wait_read_all();  // the store that used buf[b ^ 1] has read it
-            mbar_arrive_expect_tx(&full[b ^ 1], bytes);
-            bulk_load(buf[b ^ 1], X + next * a.ld + c0, bytes, &full[b ^ 1]);
+        const int bi = static_cast<int>(k % nbuf);
+        const int b = static_cast<int>(k & 1);  // partial-slot parity
+        const int64_t pre = row + ahead * step;
+        if (tid == 0 && len > 0 && pre < a.N) {
+            bulk_wait_read_but_one();  // the store of row k - 2 has read its buffer
+            const int pb = static_cast<int>((k + ahead) % nbuf);
+            mbar_arrive_expect_tx(&full[pb], bytes);
+            bulk_load(buf_of(k + ahead), X + pre * a.ld + c0, bytes, &full[pb]);
         }
-        if (len > 0 && !mbar_wait(&full[b], static_cast<uint32_t>((k >> 1) & 1), a.wait_ns,
+        if (len > 0 && !mbar_wait(&full[bi], static_cast<uint32_t>((k / nbuf) & 1), a.wait_ns,
                                   nullptr))
             ok = false;
         ok = __syncthreads_and(ok);
-        const T* z = buf[b];
+        const T* z = buf_of(k);
         // ---- this slice's (max, sum-exp), fixed assignment and tree
         MS st = {-INFINITY, 0.f};
         if (ok) {
@@ -217,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) logits_fused_kernel(const FusedAr
         const float lse = *lse_sh;
         // ---- gradient in place, then one bulk store of the slice
         const float lse2 = lse * kLog2e;
-        T* zw = buf[b];
+        T* zw = buf_of(k);
         if (ok) {
             for (int64_t i = tid; i < nvec; i += kThreads) {
                 float f[8];
@@ -246,17 +261,26 @@ __global__ void __launch_bounds__(kThreads, 1) logits_fused_kernel(const FusedAr
 
 }  // namespace
 
-// Cluster size for V: the smallest C in {1, 2, 4, 8} whose two slice buffers
-// fit the shared-memory budget, or 0 when the fused kernel does not apply.
-static int fused_cluster(int64_t V, size_t es, int64_t* L_out) {
-    for (int C = 1; C <= kMaxCluster; C <<= 1) {
+// Cluster size and ring depth for V: the smallest C in {2, 4, 8} whose
+// slices fit at least 4 buffers in the shared-memory budget (else the
+// deepest ring C = 8 allows, at least 2), or 0 when the kernel does not apply.
+static int fused_cluster(int64_t V, size_t es, int64_t* L_out, int* nbuf_out) {
+    int bestC = 0, bestN = 0;
+    int64_t bestL = 0;
+    for (int C = 2; C <= kMaxCluster; C <<= 1) {
         const int64_t L = (((V + C - 1) / C) + 7) / 8 * 8;
-        if (size_t(2 * L) * es + 1024 <= kSliceBudget) {
-            *L_out = L;
-            return C;
+        int64_t n = static_cast<int64_t>((kSliceBudget - 1024) / (size_t(L) * es));
+        if (n > kMaxBufs) n = kMaxBufs;
+        if (n >= 4 || (C == kMaxCluster && n >= 2)) {
+            bestC = C;
+            bestN = static_cast<int>(n);
+            bestL = L;
+            break;
         }
     }
-    return 0;
+    *L_out = bestL;
+    *nbuf_out = bestN;
+    return bestC;
 }
 
 cudaError_t launch_logits_fused(const float* grad, const void* logits, int64_t ld, int dtype,
@@ -266,7 +290,8 @@ cudaError_t launch_logits_fused(const float* grad, const void* logits, int64_t l
     *used = false;
     const size_t es = dtype == LL_F32 ? 4 : 2;
     int64_t L = 0;
-    const int C = fused_cluster(V, es, &L);
+    int nbuf = 0;
+    const int C = fused_cluster(V, es, &L, &nbuf);
     // bulk copies: 16-byte aligned rows; slices of whole 8-element vectors
     const bool aligned = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) &&
                          (reinterpret_cast<uintptr_t>(grad_logits) % 16 == 0) &&
@@ -279,13 +304,14 @@ cudaError_t launch_logits_fused(const float* grad, const void* logits, int64_t l
     a.N = N;
     a.V = V;
     a.L = L;
+    a.nbuf = nbuf;
     a.targets = targets;
     a.grad = grad;
     a.logp = logp;
     a.lse = lse;
     a.status = dev.status;
     a.wait_ns = wait_limit_ns();
-    const size_t smem = size_t(2 * L) * es + 1024;
+    const size_t smem = size_t(nbuf) * size_t(L) * es + 1024;
     void (*kern)(const FusedArgs) = dtype == LL_BF16  ? logits_fused_kernel<__nv_bfloat16>
                                     : dtype == LL_F16 ? logits_fused_kernel<__half>
                                                       : logits_fused_kernel<float>;

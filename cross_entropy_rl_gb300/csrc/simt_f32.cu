@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 32; ++j) v[j] = Cs[tid * kCld + c * 32 + j];
                     epi.chunk(ea, v, t * kBN + c * 32);
                     epi.store_direct(ea, v, t * kBN + c * 32);
+                    epi.db_partials(ea, v, t * kBN + c * 32);
                 }
             }
         }

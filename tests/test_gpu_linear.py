@@ -301,3 +301,19 @@ def test_gradients_into_given_16bit_buffers(lib, dt):
     torch.cuda.synchronize()
     assert lib.check_status() == 0
     compare(p, dict(logp=logp, lse=lse, dh=dh, dW=dW, db=db), full_ref(p))
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_16bit_grad_weight_several_chunks(lib, dt):
+    """A 16-bit grad_weight over 3 token chunks: each later chunk reads the
+    running table, adds its FP32 contribution and rounds once more."""
+    p = synth.linear_inputs(700, 128, 1500, dtype=dt, bias=True, seed=43, grad="mean")
+    got = run(lib, p, token_chunks=3, dw_dtype=TORCH[dt])
+    ref = full_ref(p)
+    # three roundings of a value of size |r|: allow three output ulps
+    from gpu_util import ulp
+    ga, gr = TOL[dt]["grad"]
+    sb = s_rounding_bounds(p)
+    for k in ("dW", "db"):
+        check(k, got[k], ref[k], ga, gr, extra=sb[k] + 3 * ulp(ref[k], got[k].dtype))
+    check("dh", got["dh"], ref["dh"], ga, gr, out_dtype=got["dh"].dtype, extra=sb["dh"])

@@ -144,49 +144,92 @@ __global__ void db_finish_kernel(const float* __restrict__ partial, int64_t grou
     }
 }
 
-// One CTA per row: p = 2^(z * log2e - lse * log2e) exactly as the recompute
-// epilogue forms it, S = -grad * p off target, S = 0 / tc = grad * (1 - p)
-// at the target.
+// Softmax part from stored FP32 logits, tile by tile exactly as the
+// recompute epilogue forms it: a warp takes 32 rows x 32 columns with lane =
+// row, p = 2^(z * log2e - lse * log2e), S = -grad * p off target, S = 0 and
+// tc = grad * (1 - p) at the target, and (with db_part) the same butterfly
+// column sums over the 32 rows.  Grid: x = row groups of 32, y = column
+// blocks of 4 warps x 32 columns (strided).
 template <typename T>
-__global__ void __launch_bounds__(256) softmax_part_kernel(
-    const float* __restrict__ Z, int64_t ldZ, int64_t V, const int64_t* __restrict__ targets,
-    const float* __restrict__ grad, const float* __restrict__ lse, T* __restrict__ S,
-    int64_t ldS, float* __restrict__ tc) {
-    const int64_t row = blockIdx.x;
-    const int64_t y = targets[row];
-    const float g = grad[row];
-    const bool live = y >= 0 && y < V && g != 0.f;
+__global__ void __launch_bounds__(128) softmax_part_kernel(
+    const float* __restrict__ Z, int64_t ldZ, int64_t rows, int64_t V,
+    const int64_t* __restrict__ targets, const float* __restrict__ grad,
+    const float* __restrict__ lse, T* __restrict__ S, int64_t ldS, float* __restrict__ tc,
+    float* __restrict__ db_part) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = blockIdx.x * int64_t(32) + lane;
+    const bool rvalid = row < rows;
+    const int64_t y = rvalid ? targets[row] : -1;
+    const float g = rvalid ? grad[row] : 0.f;
+    const bool live = rvalid && y >= 0 && y < V && g != 0.f;
     const float coef = live ? -g : 0.f;
-    const float lse2 = lse[row] * kLog2e;
-    const float* z = Z + row * ldZ;
-    T* out = S + row * ldS;
-    for (int64_t c = int64_t(threadIdx.x) * 8; c < V; c += int64_t(blockDim.x) * 8) {
-        float f[8];
-        if (c + 8 <= V) {
-            load8(z + c, f);
-        } else {
+    const float lse2 = rvalid ? lse[row] * kLog2e : 0.f;
+    const int64_t nchunks = (V + 31) / 32;
+    for (int64_t ch = blockIdx.y * 4 + (threadIdx.x >> 5); ch < nchunks; ch += gridDim.y * 4) {
+        const int64_t col0 = ch * 32;
+        float v[32];
+        if (rvalid) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) f[j] = (c + j < V) ? z[c + j] : 0.f;
-        }
+            for (int q = 0; q < 4; ++q) {
+                float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                if (col0 + 8 * q + 8 <= V) {
+                    load8(Z + row * ldZ + col0 + 8 * q, f);
+                } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = ex2(fmaf(f[j], kLog2e, -lse2));
-        if (y >= c && y < c + 8) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (c + j == y) {
-                    tc[row] = coef != 0.f ? -coef * (1.f - f[j]) : 0.f;
-                    f[j] = 0.f;
+                    for (int j = 0; j < 8; ++j)
+                        if (col0 + 8 * q + j < V) f[j] = Z[row * ldZ + col0 + 8 * q + j];
                 }
-        }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = coef * f[j];
-        if (c + 8 <= V) {
-            store8(out + c, f);
+                for (int j = 0; j < 8; ++j) v[8 * q + j] = f[j];
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = ex2(fmaf(v[j], kLog2e, -lse2));
+            const int64_t off = y - col0;
+            if (off >= 0 && off < 32) {
+                float py = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j == off) py = v[j];
+                tc[row] = coef != 0.f ? -coef * (1.f - py) : 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j == off) v[j] = 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = coef * v[j];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if (col0 + 8 * q >= V) break;
+                float f[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) f[j] = v[8 * q + j];
+                if (col0 + 8 * q + 8 <= V) {
+                    store8(S + row * ldS + col0 + 8 * q, f);
+                } else {
+                    for (int j = 0; j < 8 && col0 + 8 * q + j < V; ++j)
+                        S[row * ldS + col0 + 8 * q + j] = Elem<T>::from_f(f[j]);
+                }
+            }
         } else {
-            for (int j = 0; j < 8 && c + j < V; ++j) out[c + j] = Elem<T>::from_f(f[j]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        }
+        if (db_part) {  // column sums over the 32 rows, the recompute's butterfly
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                const bool up = (lane & o) != 0;
+#pragma unroll
+                for (int j = 0; j < o; ++j) {
+                    const float keep = up ? v[j + o] : v[j];
+                    const float send = up ? v[j] : v[j + o];
+                    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            const int64_t col = col0 + lane;
+            if (col < V && blockIdx.x * int64_t(32) < rows) db_part[blockIdx.x * V + col] = v[0];
         }
     }
-    if (!(y >= 0 && y < V) && threadIdx.x == 0) tc[row] = 0.f;
+    if (rvalid && !(y >= 0 && y < V) && blockIdx.y == 0 && threadIdx.x < 32) tc[row] = 0.f;
 }
 
 __global__ void fill_zero_kernel(uint32_t* p, int64_t n_words) {
@@ -296,38 +339,23 @@ cudaError_t launch_db_chunk(const void* S, int64_t ldS, int s_dtype, int64_t row
 
 cudaError_t launch_softmax_part(const float* Z, int64_t ldZ, int64_t rows, int64_t V,
                                 const int64_t* targets, const float* grad, const float* lse,
-                                void* S, int64_t ldS, int s_dtype, float* tc, cudaStream_t s) {
+                                void* S, int64_t ldS, int s_dtype, float* tc, float* db_part,
+                                cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
     note_launches(1);
-    const unsigned grid = static_cast<unsigned>(rows);
+    const int64_t nchunks = (V + 31) / 32;
+    int64_t gy = (nchunks + 3) / 4;
+    if (gy > 64) gy = 64;
+    const dim3 grid(static_cast<unsigned>((rows + 31) / 32), static_cast<unsigned>(gy));
     if (s_dtype == LL_BF16)
-        softmax_part_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-            Z, ldZ, V, targets, grad, lse, static_cast<__nv_bfloat16*>(S), ldS, tc);
+        softmax_part_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(
+            Z, ldZ, rows, V, targets, grad, lse, static_cast<__nv_bfloat16*>(S), ldS, tc, db_part);
     else if (s_dtype == LL_F16)
-        softmax_part_kernel<__half><<<grid, 256, 0, s>>>(Z, ldZ, V, targets, grad, lse,
-                                                         static_cast<__half*>(S), ldS, tc);
+        softmax_part_kernel<__half><<<grid, 128, 0, s>>>(Z, ldZ, rows, V, targets, grad, lse,
+                                                         static_cast<__half*>(S), ldS, tc, db_part);
     else
-        softmax_part_kernel<float><<<grid, 256, 0, s>>>(Z, ldZ, V, targets, grad, lse,
-                                                        static_cast<float*>(S), ldS, tc);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_db_finish(const float* partial, int64_t groups, int64_t V, float* db_acc,
-                             int first, int last, const int* offs, const int64_t* keys,
-                             const float* tc_all, void* grad_bias, int out_dtype, cudaStream_t s) {
-    note_launches(1);
-    const unsigned fb = static_cast<unsigned>((V + 255) / 256);
-    const unsigned long long* k = reinterpret_cast<const unsigned long long*>(keys);
-    if (out_dtype == LL_F32)
-        db_finish_kernel<float><<<fb, 256, 0, s>>>(partial, groups, V, db_acc, first, last, offs,
-                                                   k, tc_all, static_cast<float*>(grad_bias));
-    else if (out_dtype == LL_F16)
-        db_finish_kernel<__half><<<fb, 256, 0, s>>>(partial, groups, V, db_acc, first, last, offs,
-                                                    k, tc_all, static_cast<__half*>(grad_bias));
-    else
-        db_finish_kernel<__nv_bfloat16><<<fb, 256, 0, s>>>(
-            partial, groups, V, db_acc, first, last, offs, k, tc_all,
-            static_cast<__nv_bfloat16*>(grad_bias));
+        softmax_part_kernel<float><<<grid, 128, 0, s>>>(Z, ldZ, rows, V, targets, grad, lse,
+                                                        static_cast<float*>(S), ldS, tc, db_part);
     return cudaGetLastError();
 }
 

@@ -505,7 +505,8 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             {
                 Phase ph("softmax_part", s);
                 e = launch_softmax_part(Z, L.ldZ, rows, V, targets + r0, grad_logp + r0,
-                                        lse_out + r0, S, L.ldS, dtype, tc + r0, s);
+                                        lse_out + r0, S, L.ldS, dtype, tc + r0,
+                                        need_db ? db_part : nullptr, s);
             }
             if (e != cudaSuccess) return cuda_status(e);
         }
@@ -584,12 +585,10 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
         // (4) grad_bias: fixed-order column sums of S (+ one-hot part at the end)
         if (need_db) {
             Phase ph("db_sums", s);
-            if (!fused)  // partials from the recompute epilogue, per 32 rows
-                e = launch_db_finish(db_part, cdiv(rows, 32), V, db_acc, c == 0,
-                                     c == L.chunks - 1, offs, keys, tc, grad_bias, dw_dtype, s);
-            else
-                e = launch_db_chunk(S, L.ldS, dtype, rows, V, db_part, db_acc, c == 0,
-                                    c == L.chunks - 1, offs, keys, tc, grad_bias, dw_dtype, s);
+            // partials per 32 rows from the recompute epilogue (or, in the
+            // single call, from the softmax-part kernel with the same sums)
+            e = launch_db_finish(db_part, cdiv(rows, 32), V, db_acc, c == 0, c == L.chunks - 1,
+                                 offs, keys, tc, grad_bias, dw_dtype, s);
             if (e != cudaSuccess) return cuda_status(e);
         }
     }

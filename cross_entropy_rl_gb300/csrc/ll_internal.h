@@ -168,9 +168,12 @@ cudaError_t launch_fill_zero(void* p, int64_t n_elems, int dtype, cudaStream_t s
 // S = -grad * exp(z - lse) off target (S dtype s_dtype), S = 0 and
 // tc = grad * (1 - p) at the target, +0 rows when the target is invalid or
 // the gradient zero.  Same arithmetic as the recompute epilogue.
+// With db_part (not null) it also writes the grad_bias partials per 32 rows,
+// as the recompute epilogue does.
 cudaError_t launch_softmax_part(const float* Z, int64_t ldZ, int64_t rows, int64_t V,
                                 const int64_t* targets, const float* grad, const float* lse,
-                                void* S, int64_t ldS, int s_dtype, float* tc, cudaStream_t s);
+                                void* S, int64_t ldS, int s_dtype, float* tc, float* db_part,
+                                cudaStream_t s);
 cudaError_t launch_unsatisfied_wait(int* flag, int* status, uint64_t wait_ns, cudaStream_t s);
 
 }  // namespace ll

@@ -68,7 +68,9 @@ def build(verbose: bool = False, ptxas_verbose: bool = False) -> str:
             if log:
                 print(f"--- {s}\n{log}")
     if _stale(LIB_PATH, objs):
-        cmd = [nvcc(), *ARCH, "-shared", "-o", LIB_PATH, *objs]
+        # every symbol must resolve at link time (a missing definition is a
+        # build error, not a load-time error)
+        cmd = [nvcc(), *ARCH, "-shared", "-Xlinker", "--no-undefined", "-o", LIB_PATH, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -359,6 +359,25 @@ cudaError_t launch_softmax_part(const float* Z, int64_t ldZ, int64_t rows, int64
     return cudaGetLastError();
 }
 
+cudaError_t launch_db_finish(const float* partial, int64_t groups, int64_t V, float* db_acc,
+                             int first, int last, const int* offs, const int64_t* keys,
+                             const float* tc_all, void* grad_bias, int out_dtype, cudaStream_t s) {
+    note_launches(1);
+    const unsigned fb = static_cast<unsigned>((V + 255) / 256);
+    const unsigned long long* k = reinterpret_cast<const unsigned long long*>(keys);
+    if (out_dtype == LL_F32)
+        db_finish_kernel<float><<<fb, 256, 0, s>>>(partial, groups, V, db_acc, first, last, offs,
+                                                   k, tc_all, static_cast<float*>(grad_bias));
+    else if (out_dtype == LL_F16)
+        db_finish_kernel<__half><<<fb, 256, 0, s>>>(partial, groups, V, db_acc, first, last, offs,
+                                                    k, tc_all, static_cast<__half*>(grad_bias));
+    else
+        db_finish_kernel<__nv_bfloat16><<<fb, 256, 0, s>>>(
+            partial, groups, V, db_acc, first, last, offs, k, tc_all,
+            static_cast<__nv_bfloat16*>(grad_bias));
+    return cudaGetLastError();
+}
+
 cudaError_t launch_fill_zero(void* p, int64_t n_elems, int dtype, cudaStream_t s) {
     if (n_elems <= 0) return cudaSuccess;
     note_launches(1);

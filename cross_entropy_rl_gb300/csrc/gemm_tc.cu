@@ -141,7 +141,9 @@ struct Kind {
     using Epi = RowEpilogue<E, T>;
     static constexpr EpiKind kEpi = E;
     static constexpr bool kAmn = A_MN, kBmn = B_MN;
-    static constexpr int kFmt = std::is_same<T, __half>::value ? 0 : 1;
+    static constexpr int kFmt = std::is_same<T, __half>::value   ? 0
+                                : std::is_same<T, float>::value ? 2  // tf32
+                                                                : 1;
     static constexpr uint32_t kIdesc = instr_desc(kFmt, A_MN, B_MN, kBM, kBN);
 };
 
@@ -503,6 +505,416 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------ FP32 (3 x TF32)
+// FP32 operands on the tensor cores: each operand x is split exactly into
+// hi = x with its 13 low mantissa bits cleared (a TF32 value) and
+// lo = x - hi, and every K step runs three kind::tf32 MMAs,
+// hi*hi + hi*lo + lo*hi (the lo*lo term, ~2^-22 of the product, is
+// dropped).  A stage holds 16 K-values of A [128 x 16] and B [256 x 16]
+// as loaded (then hi, in place) and their lo parts; four converter warps
+// make the split between the TMA load and the MMAs.  K-major operands use
+// 64-byte rows (64-byte swizzle), MN-major operands 32-wide 128-byte boxes.
+constexpr int kBKf = 16;                       // K values per stage
+constexpr int kAfBytes = kBM * kBKf * 4;       // 8 KB
+constexpr int kBfBytes = kBN * kBKf * 4;       // 16 KB
+constexpr int kRawBytes = kAfBytes + kBfBytes; // 24 KB, lo parts follow
+constexpr int kMnBoxF = 32 * kBKf * 4;         // one 32(MN) x 16(K) box, 2 KB
+constexpr int kThreadsF = 320;                 // 10 warps
+static_assert(2 * kRawBytes == kStageBytes, "tf32 stage = raw + lo");
+
+struct BarsF {
+    uint64_t full[kStages];   // TMA landed
+    uint64_t conv[kStages];   // hi / lo written
+    uint64_t empty[kStages];  // MMAs done with the stage
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t sfull[kSchedDepth];
+    uint64_t sempty[kSchedDepth];
+    uint64_t drain;
+    int sched[kSchedDepth];
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(BarsF) <= 512, "barrier block");
+
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void load_stage_f(uint8_t* st, const CUtensorMap* tmA,
+                                             const CUtensorMap* tmB, uint64_t* fb, int32_t k0,
+                                             int32_t m0, int32_t n0) {
+    uint8_t* sa = st;
+    uint8_t* sb = st + kAfBytes;
+    mbar_arrive_expect_tx(fb, kRawBytes);
+    if constexpr (!A_MN) {
+        tma_load_2d(sa, tmA, fb, k0, m0);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kBM / 32; ++j) tma_load_2d(sa + j * kMnBoxF, tmA, fb, m0 + 32 * j, k0);
+    }
+    if constexpr (!B_MN) {
+        tma_load_2d(sb, tmB, fb, k0, n0);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kBN / 32; ++j) tma_load_2d(sb + j * kMnBoxF, tmB, fb, n0 + 32 * j, k0);
+    }
+}
+
+template <bool MN>
+__device__ __forceinline__ uint64_t desc_f(uint32_t base, int kk) {
+    // K-major: 64-byte rows, 8-row groups of 512 B, K step of 8 values = 32 B.
+    // MN-major: 32-value (128 B) atoms one box (2 KB) apart, 8 K-rows = 1 KB.
+    return MN ? smem_desc_sw128(base + kk * 1024, kMnBoxF, 1024)
+              : smem_desc_sw64(base + kk * 32, 16, 512);
+}
+
+template <bool A_MN, bool B_MN, uint32_t IDESC>
+__device__ __forceinline__ void mma_stage_f(uint32_t d_tmem, uint32_t st, bool first) {
+    const uint32_t a_hi = st, b_hi = st + kAfBytes;
+    const uint32_t a_lo = st + kRawBytes, b_lo = st + kRawBytes + kAfBytes;
+#pragma unroll
+    for (int kk = 0; kk < kBKf / 8; ++kk) {
+        tc_mma<1>(d_tmem, desc_f<A_MN>(a_hi, kk), desc_f<B_MN>(b_hi, kk), IDESC,
+                  (!first || kk > 0) ? 1u : 0u);
+        tc_mma<1>(d_tmem, desc_f<A_MN>(a_hi, kk), desc_f<B_MN>(b_lo, kk), IDESC, 1u);
+        tc_mma<1>(d_tmem, desc_f<A_MN>(a_lo, kk), desc_f<B_MN>(b_hi, kk), IDESC, 1u);
+    }
+}
+
+template <class K0, class K1, int NK>
+__global__ void __launch_bounds__(kThreadsF, 1)
+    gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA0,
+                     const __grid_constant__ CUtensorMap tmB0,
+                     const __grid_constant__ CUtensorMap tmO0,
+                     const __grid_constant__ CUtensorMap tmA1,
+                     const __grid_constant__ CUtensorMap tmB1,
+                     const __grid_constant__ CUtensorMap tmO1, const KParams P,
+                     const EpiArgs ea0, const EpiArgs ea1) {
+    using T = float;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* outbuf = smem + kStages * kStageBytes;
+    BarsF* bars = reinterpret_cast<BarsF*>(outbuf + kOutBytes);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t total = P.n_units[0] + (NK > 1 ? P.n_units[1] : 0);
+    const uint64_t wait_ns = ea0.wait_ns;
+    int* status = ea0.status;
+    volatile int* abort = &bars->abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->conv[s], 4);  // the four converter warps
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->tfull[b], 1);
+            mbar_init(&bars->tempty[b], 4);
+        }
+        for (int s = 0; s < kSchedDepth; ++s) {
+            mbar_init(&bars->sfull[s], 1);
+            mbar_init(&bars->sempty[s], 9);  // MMA + 4 epilogue + 4 converter warps
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA0);
+        tma_prefetch_desc(&tmB0);
+        if (NK > 1) {
+            tma_prefetch_desc(&tmA1);
+            tma_prefetch_desc(&tmB1);
+        }
+        if (P.zero_counter && blockIdx.x == 0) *P.zero_counter = 0;
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    // every role but the producer takes the unit sequence from the ring
+    auto next_unit = [&](int& sslot, uint32_t& sphase, bool& ok) -> int {
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->sfull[sslot], sphase, wait_ns, abort))) {
+            ok = false;
+            return -1;
+        }
+        const int u = *reinterpret_cast<volatile int*>(&bars->sched[sslot]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->sempty[sslot]);
+        if (++sslot == kSchedDepth) {
+            sslot = 0;
+            sphase ^= 1;
+        }
+        return u;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------- scheduler + TMA producer
+        int stage = 0, sslot = 0;
+        uint32_t phase = 0, sphase = 0;
+        uint32_t issued_phase[kStages];
+        bool issued[kStages];
+        for (int s = 0; s < kStages; ++s) issued[s] = false;
+        bool ok = true;
+        int64_t next_static = blockIdx.x;
+        while (ok) {
+            int64_t u;
+            if (P.dynamic) {
+                int got = 0;
+                if (lane == 0) got = atomicAdd(P.counter, 1);
+                u = __shfl_sync(0xffffffffu, got, 0);
+            } else {
+                u = next_static;
+                next_static += gridDim.x;
+            }
+            if (u >= total) u = -1;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(&bars->sempty[sslot], sphase ^ 1, wait_ns, abort))) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                bars->sched[sslot] = static_cast<int>(u);
+                mbar_arrive(&bars->sfull[sslot]);
+            }
+            __syncwarp();
+            if (++sslot == kSchedDepth) {
+                sslot = 0;
+                sphase ^= 1;
+            }
+            if (u < 0) break;
+            const Unit un = decode_unit(P, u);
+            for (int64_t t = un.t0; t < un.t1 && ok; ++t) {
+                for (int64_t kb = 0; kb < un.k_blocks; ++kb) {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(&bars->empty[stage], phase ^ 1, wait_ns, abort))) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        uint8_t* st = smem + stage * kStageBytes;
+                        const int32_t k0 = static_cast<int32_t>(kb * kBKf);
+                        const int32_t m0 = static_cast<int32_t>(un.mb * kBM);
+                        const int32_t n0 = static_cast<int32_t>(t * kBN);
+                        if (NK == 1 || un.kind == 0)
+                            load_stage_f<K0::kAmn, K0::kBmn>(st, &tmA0, &tmB0,
+                                                             &bars->full[stage], k0, m0, n0);
+                        else
+                            load_stage_f<K1::kAmn, K1::kBmn>(st, &tmA1, &tmB1,
+                                                             &bars->full[stage], k0, m0, n0);
+                    }
+                    __syncwarp();
+                    issued[stage] = true;
+                    issued_phase[stage] = phase;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        }
+        if (!ok) {
+            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
+            bars->abort = 1;
+            for (int s = 0; s < kStages; ++s)
+                if (issued[s]) mbar_wait(&bars->full[s], issued_phase[s], wait_ns, nullptr);
+        }
+    } else if (warp >= 6) {
+        // ------------------------------------------------ hi / lo converters
+        const int ct = threadIdx.x - 6 * 32;  // 0..127
+        int stage = 0, sslot = 0;
+        uint32_t phase = 0, sphase = 0;
+        bool ok = true;
+        while (ok) {
+            const int u = next_unit(sslot, sphase, ok);
+            if (!ok || u < 0) break;
+            const Unit un = decode_unit(P, u);
+            const int64_t steps = (un.t1 - un.t0) * un.k_blocks;
+            for (int64_t i = 0; i < steps; ++i) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[stage], phase, wait_ns, abort))) {
+                    ok = false;
+                    break;
+                }
+                uint32_t* raw = reinterpret_cast<uint32_t*>(smem + stage * kStageBytes);
+                uint32_t* lo = raw + kRawBytes / 4;
+#pragma unroll 4
+                for (int e = ct * 4; e < kRawBytes / 4; e += 128 * 4) {
+                    uint4 x = *reinterpret_cast<const uint4*>(raw + e);
+                    uint4 hi, l;
+                    hi.x = x.x & 0xFFFFE000u;
+                    hi.y = x.y & 0xFFFFE000u;
+                    hi.z = x.z & 0xFFFFE000u;
+                    hi.w = x.w & 0xFFFFE000u;
+                    l.x = __float_as_uint(__uint_as_float(x.x) - __uint_as_float(hi.x));
+                    l.y = __float_as_uint(__uint_as_float(x.y) - __uint_as_float(hi.y));
+                    l.z = __float_as_uint(__uint_as_float(x.z) - __uint_as_float(hi.z));
+                    l.w = __float_as_uint(__uint_as_float(x.w) - __uint_as_float(hi.w));
+                    *reinterpret_cast<uint4*>(raw + e) = hi;
+                    *reinterpret_cast<uint4*>(lo + e) = l;
+                }
+                fence_proxy_async_shared_cta();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->conv[stage]);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+        }
+        if (!ok) {
+            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
+            bars->abort = 1;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        int stage = 0, sslot = 0, buf = 0;
+        uint32_t phase = 0, sphase = 0, bphase = 0;
+        bool ok = true;
+        const uint32_t sbase = smem_u32(smem);
+        while (ok) {
+            const int u = next_unit(sslot, sphase, ok);
+            if (!ok || u < 0) break;
+            const Unit un = decode_unit(P, u);
+            for (int64_t t = un.t0; t < un.t1 && ok; ++t) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&bars->tempty[buf], bphase ^ 1, wait_ns, abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + buf * kBN;
+                for (int64_t kb = 0; kb < un.k_blocks; ++kb) {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(&bars->conv[stage], phase, wait_ns, abort))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t st = sbase + stage * kStageBytes;
+                        if (NK == 1 || un.kind == 0)
+                            mma_stage_f<K0::kAmn, K0::kBmn, K0::kIdesc>(d_tmem, st, kb == 0);
+                        else
+                            mma_stage_f<K1::kAmn, K1::kBmn, K1::kIdesc>(d_tmem, st, kb == 0);
+                        tc_commit(&bars->empty[stage]);
+                    }
+                    __syncwarp();
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                if (lane == 0) tc_commit(&bars->tfull[buf]);
+                __syncwarp();
+                if (++buf == 2) {
+                    buf = 0;
+                    bphase ^= 1;
+                }
+            }
+        }
+        if (!ok) {
+            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
+            bars->abort = 1;
+        }
+        if (lane == 0) tc_commit(&bars->drain);
+        __syncwarp();
+        mbar_wait(&bars->drain, 0, wait_ns, nullptr);
+    } else {
+        // ------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const int r_in_tile = q * 32 + lane;
+        uint8_t* wbuf = outbuf + q * 2 * kOutBufBytes;
+        int sslot = 0, buf = 0, sidx = 0;
+        uint32_t sphase = 0, bphase = 0;
+        bool ok = true;
+        typename K0::Epi epi0;
+        typename K1::Epi epi1;
+        while (ok) {
+            const int u = next_unit(sslot, sphase, ok);
+            if (!ok || u < 0) break;
+            const Unit un = decode_unit(P, u);
+            const int kind = (NK == 1) ? 0 : un.kind;
+            const EpiArgs& ea = kind == 0 ? ea0 : ea1;
+            const CUtensorMap* tmO = kind == 0 ? &tmO0 : &tmO1;
+            const bool reduce = P.reduce[kind] != 0;
+            const bool stores = P.out_rows[kind] > 0;
+            const int64_t row0 = un.mb * kBM + q * 32;
+            if (kind == 0)
+                epi0.begin_unit(ea, un.mb * kBM + r_in_tile);
+            else
+                epi1.begin_unit(ea, un.mb * kBM + r_in_tile);
+            for (int64_t t = un.t0; t < un.t1; ++t) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&bars->tfull[buf], bphase, wait_ns, abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem + buf * kBN + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+                for (int c = 0; c < kBN / 32; ++c) {
+                    uint32_t r[32];
+                    __syncwarp();
+                    tmem_ld32(taddr + c * 32, r);
+                    tmem_ld_wait(r);
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    const int64_t col0 = t * kBN + c * 32;
+                    if (kind == 0)
+                        epi0.chunk(ea, v, col0);
+                    else
+                        epi1.chunk(ea, v, col0);
+                    if (!stores) continue;
+                    uint8_t* sb = wbuf + (sidx & 1) * kOutBufBytes;
+                    if (lane == 0) bulk_wait_read_1();
+                    __syncwarp();
+                    stage_row<T>(sb, lane, v, false, 0);
+                    if (kind == 0) epi0.db_partials(ea, v, col0);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && row0 < P.out_rows[kind] && col0 < P.out_cols[kind]) {
+                        if (reduce)
+                            tma_reduce_add_2d(tmO, sb, static_cast<int32_t>(col0),
+                                              static_cast<int32_t>(row0));
+                        else
+                            tma_store_2d(tmO, sb, static_cast<int32_t>(col0),
+                                         static_cast<int32_t>(row0));
+                        bulk_commit();
+                    }
+                    ++sidx;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->tempty[buf]);
+                if (++buf == 2) {
+                    buf = 0;
+                    bphase ^= 1;
+                }
+            }
+            if (!ok) break;
+            if (kind == 0)
+                epi0.end_unit(ea, un.seg);
+            else
+                epi1.end_unit(ea, un.seg);
+        }
+        if (lane == 0) bulk_wait_all();
+        if (!ok) {
+            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
+            bars->abort = 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
 // ---------------------------------------------------------------- host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -532,7 +944,8 @@ CUtensorMapDataType map_type(int dtype) {
 // 2-D map over a row-major [rows, cols] matrix with row stride `ld`
 // elements; box = box_cols x box_rows, 128-byte swizzle, zero fill.
 bool make_map(CUtensorMap* map, const void* base, int dtype, int64_t cols, int64_t rows,
-              int64_t ld, int box_cols, int box_rows) {
+              int64_t ld, int box_cols, int box_rows,
+              CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const int es = dtype == LL_F32 ? 4 : 2;
@@ -542,8 +955,7 @@ bool make_map(CUtensorMap* map, const void* base, int dtype, int64_t cols, int64
                                static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, map_type(dtype), 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -607,16 +1019,71 @@ cudaError_t dispatch(const GemmLaunch& L, const CUtensorMap* m, const KParams& P
     return cudaErrorInvalidValue;
 }
 
-}  // namespace
+// FP32 operands run on the CUDA-core kernel (simt_f32.cu) unless this is set.
+constexpr bool kFp32OnTensorCores = true;
 
-// FP32 operands run on the CUDA-core kernel (simt_f32.cu).
+// FP32 operands on the CUDA cores (simt_f32.cu).
 cudaError_t launch_gemm_f32(EpiKind kind, const void* A, int64_t lda, int a_mn, const void* B,
                             int64_t ldb, int b_mn, int64_t M, int64_t N, int64_t K,
                             const GemmShape& shape, const EpiArgs& ea, const DevInfo& dev,
                             int max_ctas, cudaStream_t s);
 
+template <class K0, class K1, int NK>
+cudaError_t launch_f(const CUtensorMap* m, const KParams& P, const EpiArgs& ea0,
+                     const EpiArgs& ea1, const DevInfo& dev, int max_ctas, cudaStream_t s) {
+    auto kern = gemm_tf32_kernel<K0, K1, NK>;
+    static int configured[64] = {0};
+    if (dev.device < 64 && !configured[dev.device]) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured[dev.device] = 1;
+    }
+    const int64_t units = P.n_units[0] + (NK > 1 ? P.n_units[1] : 0);
+    const int cap = (max_ctas > 0 && max_ctas < dev.num_sms) ? max_ctas : dev.num_sms;
+    int grid = static_cast<int>(units < cap ? units : cap);
+    if (grid < 1) grid = 1;
+    note_launches(1);
+    kern<<<grid, kThreadsF, kSmemBytes, s>>>(m[0], m[1], m[2], m[3], m[4], m[5], P, ea0, ea1);
+    return cudaGetLastError();
+}
+
+// FP32 operand maps: K-major [rows, K] box 16(K) x rows, 64-byte swizzle;
+// MN-major [K, MN] box 32 x 16, 128-byte swizzle.
+bool operand_maps_f32(const GemmOperands& g, CUtensorMap* ma, CUtensorMap* mb) {
+    const bool oka = g.a_mn ? make_map(ma, g.A, LL_F32, g.M, g.K, g.lda, 32, kBKf)
+                            : make_map(ma, g.A, LL_F32, g.K, g.M, g.lda, kBKf, kBM,
+                                       CU_TENSOR_MAP_SWIZZLE_64B);
+    const bool okb = g.b_mn ? make_map(mb, g.B, LL_F32, g.N, g.K, g.ldb, 32, kBKf)
+                            : make_map(mb, g.B, LL_F32, g.K, g.N, g.ldb, kBKf, kBN,
+                                       CU_TENSOR_MAP_SWIZZLE_64B);
+    return oka && okb;
+}
+
+cudaError_t dispatch_f32(const GemmLaunch& L, const CUtensorMap* m, const KParams& P,
+                         const DevInfo& dev, cudaStream_t s) {
+    using Fwd = Kind<float, EpiKind::Fwd, false, false>;
+    using Rec = Kind<float, EpiKind::Recomp, false, false>;
+    using Dh = Kind<float, EpiKind::Dh, false, true>;
+    using Dw = Kind<float, EpiKind::Dw, true, true>;
+    if (L.nkinds == 1) {
+        switch (L.kind[0]) {
+            case EpiKind::Fwd: return launch_f<Fwd, Fwd, 1>(m, P, L.ea[0], L.ea[0], dev, L.max_ctas, s);
+            case EpiKind::Recomp:
+                return launch_f<Rec, Rec, 1>(m, P, L.ea[0], L.ea[0], dev, L.max_ctas, s);
+            case EpiKind::Dh: return launch_f<Dh, Dh, 1>(m, P, L.ea[0], L.ea[0], dev, L.max_ctas, s);
+            case EpiKind::Dw: return launch_f<Dw, Dw, 1>(m, P, L.ea[0], L.ea[0], dev, L.max_ctas, s);
+        }
+    } else if (L.kind[0] == EpiKind::Dh && L.kind[1] == EpiKind::Dw) {
+        return launch_f<Dh, Dw, 2>(m, P, L.ea[0], L.ea[1], dev, L.max_ctas, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
 cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s) {
-    if (L.dtype == LL_F32) {
+    if (L.dtype == LL_F32 && !kFp32OnTensorCores) {
         for (int k = 0; k < L.nkinds; ++k) {
             const GemmOperands& g = L.op[k];
             EpiArgs ea = L.ea[k];
@@ -633,7 +1100,10 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
     memset(&P, 0, sizeof(P));
     GemmLaunch G = L;
     for (int k = 0; k < G.nkinds; ++k) {
-        if (!operand_maps(G.op[k], G.dtype, &m[3 * k], &m[3 * k + 1])) return cudaErrorInvalidValue;
+        const bool okm = G.dtype == LL_F32
+                             ? operand_maps_f32(G.op[k], &m[3 * k], &m[3 * k + 1])
+                             : operand_maps(G.op[k], G.dtype, &m[3 * k], &m[3 * k + 1]);
+        if (!okm) return cudaErrorInvalidValue;
         if (!out_map(&m[3 * k + 2], G.out[k])) return cudaErrorInvalidValue;
         P.sh[k] = G.shape[k];
         P.n_units[k] = G.shape[k].m_blocks * G.shape[k].n_segs;
@@ -655,6 +1125,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
     P.dynamic = G.counter != nullptr;
     P.counter = G.counter;
     P.zero_counter = G.zero_counter;
+    if (G.dtype == LL_F32) return dispatch_f32(G, m, P, dev, s);
     if (G.dtype == LL_BF16) return dispatch<__nv_bfloat16>(G, m, P, dev, s);
     return dispatch<__half>(G, m, P, dev, s);
 }

@@ -1020,7 +1020,7 @@ cudaError_t dispatch(const GemmLaunch& L, const CUtensorMap* m, const KParams& P
 }
 
 // FP32 operands run on the CUDA-core kernel (simt_f32.cu) unless this is set.
-constexpr bool kFp32OnTensorCores = true;
+constexpr bool kFp32OnTensorCores = false;
 
 // FP32 operands on the CUDA cores (simt_f32.cu).
 cudaError_t launch_gemm_f32(EpiKind kind, const void* A, int64_t lda, int a_mn, const void* B,

@@ -1022,12 +1022,6 @@ cudaError_t dispatch(const GemmLaunch& L, const CUtensorMap* m, const KParams& P
 // FP32 operands run on the CUDA-core kernel (simt_f32.cu) unless this is set.
 constexpr bool kFp32OnTensorCores = false;
 
-// FP32 operands on the CUDA cores (simt_f32.cu).
-cudaError_t launch_gemm_f32(EpiKind kind, const void* A, int64_t lda, int a_mn, const void* B,
-                            int64_t ldb, int b_mn, int64_t M, int64_t N, int64_t K,
-                            const GemmShape& shape, const EpiArgs& ea, const DevInfo& dev,
-                            int max_ctas, cudaStream_t s);
-
 template <class K0, class K1, int NK>
 cudaError_t launch_f(const CUtensorMap* m, const KParams& P, const EpiArgs& ea0,
                      const EpiArgs& ea1, const DevInfo& dev, int max_ctas, cudaStream_t s) {

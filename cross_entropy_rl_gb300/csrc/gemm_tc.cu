@@ -510,22 +510,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 // hi = x with its 13 low mantissa bits cleared (a TF32 value) and
 // lo = x - hi, and every K step runs three kind::tf32 MMAs,
 // hi*hi + hi*lo + lo*hi (the lo*lo term, ~2^-22 of the product, is
-// dropped).  A stage holds 16 K-values of A [128 x 16] and B [256 x 16]
-// as loaded (then hi, in place) and their lo parts; four converter warps
-// make the split between the TMA load and the MMAs.  K-major operands use
-// 64-byte rows (64-byte swizzle), MN-major operands 32-wide 128-byte boxes.
+// dropped).  TMA lands 16 K-values of A [128 x 16] and B [256 x 16] in a
+// raw stage as they lie in memory: K-major operands in 64-byte rows
+// (64-byte swizzle), MN-major operands in 32-wide 128-byte boxes.  Four
+// converter warps write the hi and lo parts of both into a converted stage,
+// always K-major with 64-byte rows: kind::tf32 takes no MN-major operand, so
+// the converters transpose MN-major tiles on the way.
 constexpr int kBKf = 16;                       // K values per stage
 constexpr int kAfBytes = kBM * kBKf * 4;       // 8 KB
 constexpr int kBfBytes = kBN * kBKf * 4;       // 16 KB
-constexpr int kRawBytes = kAfBytes + kBfBytes; // 24 KB, lo parts follow
+constexpr int kRawBytes = kAfBytes + kBfBytes; // 24 KB (one raw stage)
+constexpr int kConvBytes = 2 * kRawBytes;      // hi A, hi B, lo A, lo B
+constexpr int kRawStages = 4;
+constexpr int kConvStages = 2;
 constexpr int kMnBoxF = 32 * kBKf * 4;         // one 32(MN) x 16(K) box, 2 KB
 constexpr int kThreadsF = 320;                 // 10 warps
-static_assert(2 * kRawBytes == kStageBytes, "tf32 stage = raw + lo");
+static_assert(kRawStages * kRawBytes + kConvStages * kConvBytes == kStages * kStageBytes,
+              "tf32 rings fill the 16-bit kernel's stage memory");
 
 struct BarsF {
-    uint64_t full[kStages];   // TMA landed
-    uint64_t conv[kStages];   // hi / lo written
-    uint64_t empty[kStages];  // MMAs done with the stage
+    uint64_t full[kRawStages];     // TMA landed in the raw stage
+    uint64_t rempty[kRawStages];   // converters done reading the raw stage
+    uint64_t conv[kConvStages];    // hi / lo written
+    uint64_t empty[kConvStages];   // MMAs done with the converted stage
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t sfull[kSchedDepth];
@@ -558,25 +565,84 @@ __device__ __forceinline__ void load_stage_f(uint8_t* st, const CUtensorMap* tmA
     }
 }
 
-template <bool MN>
+// K-major operand with 64-byte rows: 8-row groups of 512 B, a K step of
+// 8 values is 32 B along the row.
 __device__ __forceinline__ uint64_t desc_f(uint32_t base, int kk) {
-    // K-major: 64-byte rows, 8-row groups of 512 B, K step of 8 values = 32 B.
-    // MN-major: 32-value (128 B) atoms one box (2 KB) apart, 8 K-rows = 1 KB.
-    return MN ? smem_desc_sw128(base + kk * 1024, kMnBoxF, 1024)
-              : smem_desc_sw64(base + kk * 32, 16, 512);
+    return smem_desc_sw64(base + kk * 32, 16, 512);
 }
 
-template <bool A_MN, bool B_MN, uint32_t IDESC>
+constexpr uint32_t kIdescF = instr_desc(2 /*tf32*/, 0, 0, kBM, kBN);
+
 __device__ __forceinline__ void mma_stage_f(uint32_t d_tmem, uint32_t st, bool first) {
     const uint32_t a_hi = st, b_hi = st + kAfBytes;
     const uint32_t a_lo = st + kRawBytes, b_lo = st + kRawBytes + kAfBytes;
 #pragma unroll
     for (int kk = 0; kk < kBKf / 8; ++kk) {
-        tc_mma<1>(d_tmem, desc_f<A_MN>(a_hi, kk), desc_f<B_MN>(b_hi, kk), IDESC,
+        tc_mma<1>(d_tmem, desc_f(a_hi, kk), desc_f(b_hi, kk), kIdescF,
                   (!first || kk > 0) ? 1u : 0u);
-        tc_mma<1>(d_tmem, desc_f<A_MN>(a_hi, kk), desc_f<B_MN>(b_lo, kk), IDESC, 1u);
-        tc_mma<1>(d_tmem, desc_f<A_MN>(a_lo, kk), desc_f<B_MN>(b_hi, kk), IDESC, 1u);
+        tc_mma<1>(d_tmem, desc_f(a_hi, kk), desc_f(b_lo, kk), kIdescF, 1u);
+        tc_mma<1>(d_tmem, desc_f(a_lo, kk), desc_f(b_hi, kk), kIdescF, 1u);
     }
+}
+
+__device__ __forceinline__ void split_tf32(const uint4& x, uint4& hi, uint4& lo) {
+    hi.x = x.x & 0xFFFFE000u;
+    hi.y = x.y & 0xFFFFE000u;
+    hi.z = x.z & 0xFFFFE000u;
+    hi.w = x.w & 0xFFFFE000u;
+    lo.x = __float_as_uint(__uint_as_float(x.x) - __uint_as_float(hi.x));
+    lo.y = __float_as_uint(__uint_as_float(x.y) - __uint_as_float(hi.y));
+    lo.z = __float_as_uint(__uint_as_float(x.z) - __uint_as_float(hi.z));
+    lo.w = __float_as_uint(__uint_as_float(x.w) - __uint_as_float(hi.w));
+}
+
+// One operand of ROWS rows x 16 K-values from its raw stage into hi / lo in
+// K-major 64-byte rows (row r at r * 64, 16-byte chunk c at c ^ ((r >> 1) & 3),
+// the 64-byte swizzle).  ct = converter thread 0..127.
+template <bool MN, int ROWS>
+__device__ __forceinline__ void convert_operand(const uint8_t* raw, uint8_t* hi, uint8_t* lo,
+                                                int ct) {
+    if constexpr (!MN) {
+        // already in that layout: split 16-byte vectors in place
+#pragma unroll
+        for (int e = ct; e < ROWS * 4; e += 128) {
+            const uint4 x = *reinterpret_cast<const uint4*>(raw + e * 16);
+            uint4 h, l;
+            split_tf32(x, h, l);
+            *reinterpret_cast<uint4*>(hi + e * 16) = h;
+            *reinterpret_cast<uint4*>(lo + e * 16) = l;
+        }
+    } else {
+        // box j: K-row k (128 B) holds MN values 32j..32j+31, 16-byte chunk c
+        // (MN values 4c..4c+3) at c ^ (k & 7).  Thread (mn = ct & 31,
+        // q = ct >> 5) gathers K values 4q..4q+3 of one MN index.
+        const int m = ct & 31, q = ct >> 5;
+        const uint32_t src = static_cast<uint32_t>((m & 3) * 4);
+#pragma unroll
+        for (int j = 0; j < ROWS / 32; ++j) {
+            const uint8_t* box = raw + j * kMnBoxF;
+            uint4 x;
+            uint32_t* xv = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int k = 4 * q + i;
+                xv[i] = *reinterpret_cast<const uint32_t*>(box + k * 128 +
+                                                           (((m >> 2) ^ (k & 7)) * 16) + src);
+            }
+            uint4 h, l;
+            split_tf32(x, h, l);
+            const int r = j * 32 + m;
+            const int off = r * 64 + ((q ^ ((r >> 1) & 3)) * 16);
+            *reinterpret_cast<uint4*>(hi + off) = h;
+            *reinterpret_cast<uint4*>(lo + off) = l;
+        }
+    }
+}
+
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void convert_stage(const uint8_t* raw, uint8_t* cv, int ct) {
+    convert_operand<A_MN, kBM>(raw, cv, cv + kRawBytes, ct);
+    convert_operand<B_MN, kBN>(raw + kAfBytes, cv + kAfBytes, cv + kRawBytes + kAfBytes, ct);
 }
 
 template <class K0, class K1, int NK>
@@ -602,8 +668,11 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     volatile int* abort = &bars->abort;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kRawStages; ++s) {
             mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->rempty[s], 4);  // the four converter warps
+        }
+        for (int s = 0; s < kConvStages; ++s) {
             mbar_init(&bars->conv[s], 4);  // the four converter warps
             mbar_init(&bars->empty[s], 1);
         }
@@ -655,9 +724,9 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         // ------------------------------------------- scheduler + TMA producer
         int stage = 0, sslot = 0;
         uint32_t phase = 0, sphase = 0;
-        uint32_t issued_phase[kStages];
-        bool issued[kStages];
-        for (int s = 0; s < kStages; ++s) issued[s] = false;
+        uint32_t issued_phase[kRawStages];
+        bool issued[kRawStages];
+        for (int s = 0; s < kRawStages; ++s) issued[s] = false;
         bool ok = true;
         int64_t next_static = blockIdx.x;
         while (ok) {
@@ -690,12 +759,12 @@ __global__ void __launch_bounds__(kThreadsF, 1)
             for (int64_t t = un.t0; t < un.t1 && ok; ++t) {
                 for (int64_t kb = 0; kb < un.k_blocks; ++kb) {
                     if (!__all_sync(0xffffffffu,
-                                    mbar_wait(&bars->empty[stage], phase ^ 1, wait_ns, abort))) {
+                                    mbar_wait(&bars->rempty[stage], phase ^ 1, wait_ns, abort))) {
                         ok = false;
                         break;
                     }
                     if (lane == 0) {
-                        uint8_t* st = smem + stage * kStageBytes;
+                        uint8_t* st = smem + stage * kRawBytes;
                         const int32_t k0 = static_cast<int32_t>(kb * kBKf);
                         const int32_t m0 = static_cast<int32_t>(un.mb * kBM);
                         const int32_t n0 = static_cast<int32_t>(t * kBN);
@@ -709,7 +778,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                     __syncwarp();
                     issued[stage] = true;
                     issued_phase[stage] = phase;
-                    if (++stage == kStages) {
+                    if (++stage == kRawStages) {
                         stage = 0;
                         phase ^= 1;
                     }
@@ -719,48 +788,47 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         if (!ok) {
             if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
             bars->abort = 1;
-            for (int s = 0; s < kStages; ++s)
+            for (int s = 0; s < kRawStages; ++s)
                 if (issued[s]) mbar_wait(&bars->full[s], issued_phase[s], wait_ns, nullptr);
         }
     } else if (warp >= 6) {
         // ------------------------------------------------ hi / lo converters
         const int ct = threadIdx.x - 6 * 32;  // 0..127
-        int stage = 0, sslot = 0;
-        uint32_t phase = 0, sphase = 0;
+        int rs = 0, cs = 0, sslot = 0;
+        uint32_t rphase = 0, cphase = 0, sphase = 0;
         bool ok = true;
+        uint8_t* conv_base = smem + kRawStages * kRawBytes;
         while (ok) {
             const int u = next_unit(sslot, sphase, ok);
             if (!ok || u < 0) break;
             const Unit un = decode_unit(P, u);
             const int64_t steps = (un.t1 - un.t0) * un.k_blocks;
             for (int64_t i = 0; i < steps; ++i) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&bars->full[stage], phase, wait_ns, abort))) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&bars->full[rs], rphase, wait_ns, abort) &&
+                                    mbar_wait(&bars->empty[cs], cphase ^ 1, wait_ns, abort))) {
                     ok = false;
                     break;
                 }
-                uint32_t* raw = reinterpret_cast<uint32_t*>(smem + stage * kStageBytes);
-                uint32_t* lo = raw + kRawBytes / 4;
-#pragma unroll 4
-                for (int e = ct * 4; e < kRawBytes / 4; e += 128 * 4) {
-                    uint4 x = *reinterpret_cast<const uint4*>(raw + e);
-                    uint4 hi, l;
-                    hi.x = x.x & 0xFFFFE000u;
-                    hi.y = x.y & 0xFFFFE000u;
-                    hi.z = x.z & 0xFFFFE000u;
-                    hi.w = x.w & 0xFFFFE000u;
-                    l.x = __float_as_uint(__uint_as_float(x.x) - __uint_as_float(hi.x));
-                    l.y = __float_as_uint(__uint_as_float(x.y) - __uint_as_float(hi.y));
-                    l.z = __float_as_uint(__uint_as_float(x.z) - __uint_as_float(hi.z));
-                    l.w = __float_as_uint(__uint_as_float(x.w) - __uint_as_float(hi.w));
-                    *reinterpret_cast<uint4*>(raw + e) = hi;
-                    *reinterpret_cast<uint4*>(lo + e) = l;
-                }
+                const uint8_t* raw = smem + rs * kRawBytes;
+                uint8_t* cv = conv_base + cs * kConvBytes;
+                if (NK == 1 || un.kind == 0)
+                    convert_stage<K0::kAmn, K0::kBmn>(raw, cv, ct);
+                else
+                    convert_stage<K1::kAmn, K1::kBmn>(raw, cv, ct);
                 fence_proxy_async_shared_cta();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->conv[stage]);
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1;
+                if (lane == 0) {
+                    mbar_arrive(&bars->rempty[rs]);
+                    mbar_arrive(&bars->conv[cs]);
+                }
+                if (++rs == kRawStages) {
+                    rs = 0;
+                    rphase ^= 1;
+                }
+                if (++cs == kConvStages) {
+                    cs = 0;
+                    cphase ^= 1;
                 }
             }
         }
@@ -773,7 +841,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         int stage = 0, sslot = 0, buf = 0;
         uint32_t phase = 0, sphase = 0, bphase = 0;
         bool ok = true;
-        const uint32_t sbase = smem_u32(smem);
+        const uint32_t sbase = smem_u32(smem) + kRawStages * kRawBytes;
         while (ok) {
             const int u = next_unit(sslot, sphase, ok);
             if (!ok || u < 0) break;
@@ -794,15 +862,11 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                     }
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t st = sbase + stage * kStageBytes;
-                        if (NK == 1 || un.kind == 0)
-                            mma_stage_f<K0::kAmn, K0::kBmn, K0::kIdesc>(d_tmem, st, kb == 0);
-                        else
-                            mma_stage_f<K1::kAmn, K1::kBmn, K1::kIdesc>(d_tmem, st, kb == 0);
+                        mma_stage_f(d_tmem, sbase + stage * kConvBytes, kb == 0);
                         tc_commit(&bars->empty[stage]);
                     }
                     __syncwarp();
-                    if (++stage == kStages) {
+                    if (++stage == kConvStages) {
                         stage = 0;
                         phase ^= 1;
                     }
@@ -1020,7 +1084,7 @@ cudaError_t dispatch(const GemmLaunch& L, const CUtensorMap* m, const KParams& P
 }
 
 // FP32 operands run on the CUDA-core kernel (simt_f32.cu) unless this is set.
-constexpr bool kFp32OnTensorCores = false;
+constexpr bool kFp32OnTensorCores = true;
 
 template <class K0, class K1, int NK>
 cudaError_t launch_f(const CUtensorMap* m, const KParams& P, const EpiArgs& ea0,
@@ -1100,6 +1164,9 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
         if (!okm) return cudaErrorInvalidValue;
         if (!out_map(&m[3 * k + 2], G.out[k])) return cudaErrorInvalidValue;
         P.sh[k] = G.shape[k];
+        // the host sizes K blocks for the 16-bit kernel (64 values); the
+        // tf32 kernel takes 16 per stage
+        if (G.dtype == LL_F32) P.sh[k].k_blocks = (G.op[k].K + kBKf - 1) / kBKf;
         P.n_units[k] = G.shape[k].m_blocks * G.shape[k].n_segs;
         P.out16[k] = G.out[k].dtype != LL_F32;
         P.out_rows[k] = G.out[k].rows;

@@ -140,7 +140,9 @@ KERNEL_SOURCES = {
     "logits": ["logits_kernels.cu", "ll_device.cuh", "ll_internal.h"],
 }
 PHASE_SOURCES = {"fwd_gemm": "gemm", "recompute_gemm": "gemm", "grad_gemm": "gemm",
-                 "logits_fwd": "logits", "logits_bwd": "logits"}
+                 "fwd_gemm_f32": "gemm", "recompute_gemm_f32": "gemm",
+                 "grad_gemm_f32": "gemm", "logits_fwd": "logits", "logits_bwd": "logits",
+                 "logits_fused": "logits"}
 
 
 def kernel_source_hash(phase: str) -> str:
@@ -369,10 +371,14 @@ def run_ours(args, rank, world, local_rank):
     cnt, tot = gemms[dom]
     avg_ms = tot / cnt
     achieved = flops[dom] / (avg_ms * 1e-3) / 1e12
+    simt_peak = 152 * 128 * 2 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
     if dt == "f32":
-        # FP32 FFMA on the CUDA cores: 152 SMs x 128 lanes x 2 flops x max SM clock
-        peak, bound = 152 * 128 * 2 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12, "alu"
-        pk_kind = "derived (152 SMs x 128 FP32 lanes x 2 x max clock)"
+        # FP32 operands run as three TF32 MMAs per product (hi*hi + hi*lo +
+        # lo*hi): the tensor peak for FP32 work is the TF32 rate / 3, the TF32
+        # rate being the measured BF16 one times the nominal 1.1 / 2.25 ratio
+        peak, bound = pk["bf16_tflops"] * (1.1 / 2.25) / 3.0, "tensor"
+        pk_kind = (f"{pk_kind} bf16 x 1.1/2.25 (nominal tf32/bf16) / 3 "
+                   "(3 x TF32 per FP32 product)")
     else:
         # fp16 has the same dense tensor rate as bf16
         peak, bound = pk["bf16_tflops"], "tensor"
@@ -391,11 +397,14 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"dp{world}"},
         "useful_tflops": useful, "useful_frac_of_bf16_peak": useful / pk["bf16_tflops"],
         "useful_frac_of_peak": useful / peak, "peak_tflops": peak,
+        "useful_frac_of_fp32_cuda_core_peak": useful / simt_peak if dt == "f32" else None,
         "executed_tflops_incl_recompute": executed,
         "peak_source": pk_kind,
         "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
-                     "frac_of_sustained": achieved / pk.get("bf16_tflops_sustained", peak),
+                     "frac_of_sustained": achieved / (pk.get("bf16_tflops_sustained",
+                                                             pk["bf16_tflops"])
+                                                      * (peak / pk["bf16_tflops"])),
                      "traffic": ncu_traffic(dom, args.workload), "avg_launch_ms": avg_ms,
                      "flops_per_launch": flops[dom]},
         "kernels_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},

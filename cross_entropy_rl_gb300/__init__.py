@@ -18,7 +18,8 @@ import os
 
 __all__ = [
     "LLError", "load", "lib", "forward", "backward", "forward_backward", "logits_fwd",
-    "logits_bwd",
+    "logits_bwd", "logits_fwd_bwd", "shard_segments", "forward_shard", "lse_merge",
+    "backward_shard", "SEGMENT_COLS",
     "workspace_size", "check_status", "DTYPE_CODES", "EXPORTS",
 ]
 
@@ -27,6 +28,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "lib
 
 # ll_dtype codes of the C ABI
 LL_F32, LL_F16, LL_BF16 = 0, 1, 2
+# vocab entries per LSE segment; vocab shards start on a multiple of it
+SEGMENT_COLS = 1024
 
 _c_i64 = ctypes.c_int64
 _c_p = ctypes.c_void_p
@@ -51,6 +54,16 @@ EXPORTS = {
                                  _c_p, _c_p]),
     "logits_logp_fwd_bwd": (_c_int, [_c_p, _c_p, _c_i64, _c_int, _c_p, _c_i64, _c_i64, _c_p,
                                      _c_p, _c_p, _c_p]),
+    "ll_shard_segments": (_c_i64, [_c_i64]),
+    "ll_workspace_size_shard": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_int,
+                                          _c_int]),
+    "ll_forward_shard": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64,
+                                  _c_i64, _c_int, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p]),
+    "ll_lse_merge": (_c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_i64, _c_p,
+                              _c_p, _c_p]),
+    "ll_backward_shard": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64,
+                                   _c_i64, _c_i64, _c_int, _c_int, _c_int, _c_int, _c_p,
+                                   _c_int, _c_p, _c_int, _c_p, _c_int, _c_p, _c_size, _c_p]),
     "ll_check_status": (_c_int, [_c_p]),
     "ll_set_wait_limit_ns": (None, [_c_i64]),
     "ll_debug_unsatisfied_wait": (_c_int, [_c_p, _c_p]),
@@ -394,3 +407,98 @@ def logits_fwd_bwd(grad_logp, logits, targets, V=None, *, out=None, stream=None)
 def check_status(stream=None) -> int:
     """Synchronise and return (and clear) the device-side status word."""
     return int(load().ll_check_status(_stream(stream)))
+
+
+# ---------------------------------------------------------- vocab shards
+
+def shard_segments(Vs: int) -> int:
+    """LSE segments of a vocab shard of Vs entries."""
+    return int(load().ll_shard_segments(int(Vs)))
+
+
+def forward_shard(hidden, weight, bias, targets, v0, V, *, workspace=None, out=None,
+                  stream=None):
+    """Segment partials of the vocab shard [v0, v0 + weight.shape[0]) of a
+    vocab of V entries: (part_m, part_s) [shard_segments(Vs), N] and zy [N]
+    (z of the target where it lies in the shard, -inf elsewhere).  targets
+    are global ids."""
+    torch = _torch()
+    L = load()
+    N, D, Vs, dev = _check_linear(hidden, weight, bias, targets)
+    code = _code(hidden.dtype)
+    S = shard_segments(Vs)
+    if out is None:
+        part_m = torch.empty(S, N, dtype=torch.float32, device=dev)
+        part_s = torch.empty(S, N, dtype=torch.float32, device=dev)
+        zy = torch.empty(N, dtype=torch.float32, device=dev)
+    else:
+        part_m, part_s, zy = out
+    _need(part_m, "part_m", (S, N), torch.float32, dev)
+    _need(part_s, "part_s", (S, N), torch.float32, dev)
+    _need(zy, "zy", (N,), torch.float32, dev)
+    if workspace is None:
+        workspace = _workspace(L.ll_workspace_size_shard(N, D, Vs, code, 0, 0, 0), dev)
+    _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
+    st = L.ll_forward_shard(_ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets), N, D, Vs,
+                            int(v0), int(V), code, _ptr(part_m), _ptr(part_s), _ptr(zy),
+                            _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("ll_forward_shard", st)
+    return part_m, part_s, zy
+
+
+def lse_merge(part_m, part_s, zy, targets, V, *, out=None, stream=None):
+    """(logp, lse) from whole-vocab segment partials [n_segs, N] in ascending
+    segment order (rows of m = -inf, s = 0 change nothing)."""
+    torch = _torch()
+    L = load()
+    if part_m.dim() != 2:
+        raise ValueError("part_m must be 2-D [n_segs, N]")
+    n_segs, N = part_m.shape
+    dev = part_m.device
+    _need(part_m, "part_m", (n_segs, N), torch.float32, dev)
+    _need(part_s, "part_s", (n_segs, N), torch.float32, dev)
+    _need(zy, "zy", (N,), torch.float32, dev)
+    _need(targets, "targets", (N,), torch.int64, dev)
+    if out is None:
+        logp = torch.empty(N, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+    else:
+        logp, lse = out
+    _need(logp, "logp", (N,), torch.float32, dev)
+    _need(lse, "lse", (N,), torch.float32, dev)
+    st = L.ll_lse_merge(_ptr(part_m), _ptr(part_s), n_segs, N, _ptr(zy), _ptr(targets), N,
+                        int(V), _ptr(logp), _ptr(lse), _stream(stream))
+    _check("ll_lse_merge", st)
+    return logp, lse
+
+
+def backward_shard(grad_logp, hidden, weight, bias, targets, lse, v0, V, *, need_dh=True,
+                   need_dw=True, need_db=None, dh_dtype=None, dw_dtype=None, token_chunks=0,
+                   workspace=None, out=None, stream=None):
+    """(grad_hidden part, grad_weight rows, grad_bias rows) of the vocab shard
+    [v0, v0 + weight.shape[0]); lse is the merged whole-vocab lse.  The
+    grad_hidden part defaults to float32 (the shards' parts are summed)."""
+    torch = _torch()
+    L = load()
+    N, D, Vs, dev = _check_linear(hidden, weight, bias, targets)
+    code = _code(hidden.dtype)
+    if need_db is None:
+        need_db = bias is not None
+    if dh_dtype is None and (out is None or out[0] is None):
+        dh_dtype = torch.float32
+    _need(grad_logp, "grad_logp", (N,), torch.float32, dev)
+    _need(lse, "lse", (N,), torch.float32, dev)
+    dh, dW, db, dh_dtype, dw_dtype = _grad_outputs(out, need_dh, need_dw, need_db, N, D, Vs,
+                                                   hidden.dtype, dh_dtype, dw_dtype, dev)
+    if workspace is None:
+        workspace = _workspace(L.ll_workspace_size_shard(N, D, Vs, code, token_chunks, 1,
+                                                         int(bool(need_db))), dev)
+    _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
+    st = L.ll_backward_shard(_ptr(grad_logp), _ptr(hidden), _ptr(weight), _ptr(bias),
+                             _ptr(targets), _ptr(lse), N, D, Vs, int(v0), int(V), code,
+                             int(bool(need_dh)), int(bool(need_dw)), int(bool(need_db)),
+                             _ptr(dh), _code(dh_dtype), _ptr(dW), _code(dw_dtype), _ptr(db),
+                             int(token_chunks), _ptr(workspace), workspace.numel(),
+                             _stream(stream))
+    _check("ll_backward_shard", st)
+    return dh, dW, db

@@ -6,6 +6,7 @@
 //     of tokens that target it in ascending token order (used by the exact
 //     one-hot part of grad_weight and grad_bias);
 //   * fixed-order column sums of the softmax part for grad_bias;
+//   * shard-local targets of a vocab shard;
 //   * a +0 fill and the bounded-wait self test.
 #include <math.h>
 
@@ -31,6 +32,19 @@ __global__ void lse_merge_kernel(const float* __restrict__ pm, const float* __re
     const int64_t y = targets[r];
     logp[r] = (y >= 0 && y < V) ? zy[r] - lse : 0.f;
     lse_out[r] = lse;
+}
+
+// Targets of one vocab shard [v0, v0 + Vs) of a vocab of V entries.
+__global__ void localize_targets_kernel(const int64_t* __restrict__ targets, int64_t N,
+                                        int64_t v0, int64_t Vs, int64_t V,
+                                        int64_t* __restrict__ local, float* __restrict__ zy) {
+    const int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+    if (i >= N) return;
+    const int64_t y = targets[i];
+    int64_t l = -1;
+    if (y >= 0 && y < V) l = (y >= v0 && y < v0 + Vs) ? y - v0 : kTargetInOtherShard;
+    local[i] = l;
+    if (zy) zy[i] = -INFINITY;
 }
 
 constexpr int kSortSeg = 4096;  // keys sorted per CTA in shared memory
@@ -275,6 +289,16 @@ cudaError_t launch_lse_merge(const float* part_m, const float* part_s, const flo
     note_launches(1);
     lse_merge_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
         part_m, part_s, zy, part_ld, n_segs, targets, N, V, logp, lse);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_localize_targets(const int64_t* targets, int64_t N, int64_t v0, int64_t Vs,
+                                    int64_t V, int64_t* local, float* zy, cudaStream_t s) {
+    if (N <= 0) return cudaSuccess;
+    const int threads = 256;
+    note_launches(1);
+    localize_targets_kernel<<<static_cast<unsigned>((N + threads - 1) / threads), threads, 0, s>>>(
+        targets, N, v0, Vs, V, local, zy);
     return cudaGetLastError();
 }
 

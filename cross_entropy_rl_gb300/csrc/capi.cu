@@ -229,6 +229,18 @@ int check_sizes(int64_t N, int64_t D, int64_t V) {
     return LL_OK;
 }
 
+// A vocab shard [v0, v0 + Vs) of V: starts on a segment boundary and ends on
+// one unless it is the last shard.
+int check_shard(int64_t Vs, int64_t v0, int64_t V) {
+    if (V < 1 || V > kMaxV || Vs < 1 || v0 < 0 || v0 > V - Vs) return LL_ERR_SHAPE;
+    if (v0 % kSegCols != 0) return LL_ERR_SHAPE;
+    if (v0 + Vs != V && Vs % kSegCols != 0) return LL_ERR_SHAPE;
+    return LL_OK;
+}
+
+// Shard-local targets after the backward's (or at the forward's) workspace.
+size_t local_targets_bytes(int64_t N) { return align_up(size_t(N > 0 ? N : 1) * 8); }
+
 }  // namespace
 }  // namespace ll
 
@@ -263,34 +275,21 @@ size_t ll_workspace_size(int64_t N, int64_t D, int64_t V, int dtype, int token_c
 
 void ll_set_wait_limit_ns(int64_t ns) { g_wait_limit_ns = ns > 0 ? uint64_t(ns) : 2000000000ull; }
 
-int ll_forward(const void* hidden, const void* weight, const void* bias, const int64_t* targets,
-               int64_t N, int64_t D, int64_t V, int dtype, float* logp, float* lse,
-               void* workspace, size_t ws_bytes, void* stream) {
-    int st = check_sizes(N, D, V);
-    if (st) return st;
-    if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
-    if (!weight) return LL_ERR_INVALID_ARG;
-    if (N == 0) return LL_OK;
-    if (!hidden || !targets || !logp || !lse) return LL_ERR_INVALID_ARG;
-    if (D % 8 != 0 || !aligned16(hidden) || !aligned16(weight)) return LL_ERR_ALIGN;
-    const FwdLayout L = fwd_layout(N, V);
-    if (!workspace || ws_bytes < L.total) return LL_ERR_WORKSPACE;
-    if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return LL_ERR_WORKSPACE;
-    DeviceGuard guard(hidden);
-    if (guard.err) return guard.err;
-    DevInfo dev;
-    if ((st = device_info(guard.dev, &dev))) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    char* ws = static_cast<char*>(workspace);
-    float* part_m = reinterpret_cast<float*>(ws + L.part_m);
-    float* part_s = reinterpret_cast<float*>(ws + L.part_s);
-    float* zy = reinterpret_cast<float*>(ws + L.zy);
+}  // extern "C"
 
+namespace ll {
+namespace {
+// The forward GEMM: per (row, vocab segment) partials [n_segs, N] and the
+// target logit of rows whose target lies in [0, V).
+cudaError_t forward_gemm(const void* hidden, const void* weight, const void* bias,
+                         const int64_t* targets, int64_t N, int64_t D, int64_t V, int dtype,
+                         float* part_m, float* part_s, float* zy, int shard, const DevInfo& dev,
+                         cudaStream_t s) {
     GemmShape sh;
     sh.m_blocks = cdiv(N, kBM);
     sh.n_tiles = cdiv(V, kBN);
     sh.tiles_per_unit = kVocabTilesPerSeg;
-    sh.n_segs = L.n_segs;
+    sh.n_segs = cdiv(sh.n_tiles, kVocabTilesPerSeg);
     sh.k_blocks = cdiv(D, 64);
     sh.unit_order = 2;
     EpiArgs ea;
@@ -306,6 +305,7 @@ int ll_forward(const void* hidden, const void* weight, const void* bias, const i
     ea.part_ld = N;
     ea.status = dev.status;
     ea.wait_ns = wait_limit_ns();
+    ea.shard = shard;
     GemmLaunch G;
     memset(&G, 0, sizeof(G));
     G.dtype = dtype;
@@ -314,11 +314,47 @@ int ll_forward(const void* hidden, const void* weight, const void* bias, const i
     G.op[0] = GemmOperands{hidden, D, 0, weight, D, 0, N, V, D};
     G.shape[0] = sh;
     G.ea[0] = ea;
-    cudaError_t e;
-    {
-        Phase ph(dtype == LL_F32 ? "fwd_gemm_f32" : "fwd_gemm", s);
-        e = launch_gemm(G, dev, s);
-    }
+    Phase ph(dtype == LL_F32 ? "fwd_gemm_f32" : "fwd_gemm", s);
+    return launch_gemm(G, dev, s);
+}
+
+// Validation shared by the forward entry points.
+int forward_checks(const void* hidden, const void* weight, const int64_t* targets, int64_t N,
+                   int64_t D, int64_t V, int dtype) {
+    int st = check_sizes(N, D, V);
+    if (st) return st;
+    if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
+    if (!weight) return LL_ERR_INVALID_ARG;
+    if (N == 0) return LL_OK;
+    if (!hidden || !targets) return LL_ERR_INVALID_ARG;
+    if (D % 8 != 0 || !aligned16(hidden) || !aligned16(weight)) return LL_ERR_ALIGN;
+    return LL_OK;
+}
+}  // namespace
+}  // namespace ll
+
+extern "C" {
+
+int ll_forward(const void* hidden, const void* weight, const void* bias, const int64_t* targets,
+               int64_t N, int64_t D, int64_t V, int dtype, float* logp, float* lse,
+               void* workspace, size_t ws_bytes, void* stream) {
+    int st = forward_checks(hidden, weight, targets, N, D, V, dtype);
+    if (st || N == 0) return st;
+    if (!logp || !lse) return LL_ERR_INVALID_ARG;
+    const FwdLayout L = fwd_layout(N, V);
+    if (!workspace || ws_bytes < L.total) return LL_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return LL_ERR_WORKSPACE;
+    DeviceGuard guard(hidden);
+    if (guard.err) return guard.err;
+    DevInfo dev;
+    if ((st = device_info(guard.dev, &dev))) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    float* part_m = reinterpret_cast<float*>(ws + L.part_m);
+    float* part_s = reinterpret_cast<float*>(ws + L.part_s);
+    float* zy = reinterpret_cast<float*>(ws + L.zy);
+    cudaError_t e = forward_gemm(hidden, weight, bias, targets, N, D, V, dtype, part_m, part_s,
+                                 zy, 0, dev, s);
     if (e != cudaSuccess) return cuda_status(e);
     {
         Phase ph("lse_merge", s);
@@ -339,7 +375,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
                   int64_t D, int64_t V, int dtype, int need_dh, int need_dw, int need_db,
                   void* grad_hidden, int dh_dtype, void* grad_weight, int dw_dtype,
                   void* grad_bias, int token_chunks, void* workspace, size_t ws_bytes,
-                  void* stream, int fused, float* logp_out, float* lse_out) {
+                  void* stream, int fused, float* logp_out, float* lse_out, int shard = 0) {
     int st = check_sizes(N, D, V);
     if (st) return st;
     if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
@@ -423,6 +459,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
     base.bias = bias;
     base.status = dev.status;
     base.wait_ns = wait_limit_ns();
+    base.shard = shard;
 
     for (int64_t c = 0; c < L.chunks; ++c) {
         const int64_t r0 = c * L.Nc;
@@ -625,6 +662,98 @@ int ll_forward_backward(const float* grad_logp, const void* hidden, const void* 
                          grad_bias, token_chunks, workspace, ws_bytes, stream, 1, logp, lse);
 }
 
+int64_t ll_shard_segments(int64_t Vs) { return Vs > 0 ? cdiv(Vs, kSegCols) : 0; }
+
+size_t ll_workspace_size_shard(int64_t N, int64_t D, int64_t Vs, int dtype, int token_chunks,
+                               int is_backward, int flags) {
+    (void)D;
+    if (N < 0 || Vs < 1 || !dtype_ok(dtype)) return 0;
+    if (N == 0) return 0;
+    if (!is_backward) return local_targets_bytes(N);
+    return bwd_layout(N, Vs, dtype, token_chunks, flags & 1).total + local_targets_bytes(N);
+}
+
+int ll_forward_shard(const void* hidden, const void* weight, const void* bias,
+                     const int64_t* targets, int64_t N, int64_t D, int64_t Vs, int64_t v0,
+                     int64_t V, int dtype, float* part_m, float* part_s, float* zy,
+                     void* workspace, size_t ws_bytes, void* stream) {
+    int st = check_shard(Vs, v0, V);
+    if (st) return st;
+    st = forward_checks(hidden, weight, targets, N, D, Vs, dtype);
+    if (st || N == 0) return st;
+    if (!part_m || !part_s || !zy) return LL_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < local_targets_bytes(N)) return LL_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return LL_ERR_WORKSPACE;
+    DeviceGuard guard(hidden);
+    if (guard.err) return guard.err;
+    DevInfo dev;
+    if ((st = device_info(guard.dev, &dev))) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int64_t* local = static_cast<int64_t*>(workspace);
+    cudaError_t e = launch_localize_targets(targets, N, v0, Vs, V, local, zy, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    return cuda_status(forward_gemm(hidden, weight, bias, local, N, D, Vs, dtype, part_m, part_s,
+                                    zy, 1, dev, s));
+}
+
+int ll_lse_merge(const float* part_m, const float* part_s, int64_t n_segs, int64_t part_ld,
+                 const float* zy, const int64_t* targets, int64_t N, int64_t V, float* logp,
+                 float* lse, void* stream) {
+    if (N < 0 || V < 1 || V > kMaxV || n_segs < 1 || part_ld < N) return LL_ERR_SHAPE;
+    if (N == 0) return LL_OK;
+    if (!part_m || !part_s || !zy || !targets || !logp || !lse) return LL_ERR_INVALID_ARG;
+    DeviceGuard guard(part_m);
+    if (guard.err) return guard.err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Phase ph("lse_merge", s);
+    return cuda_status(launch_lse_merge(part_m, part_s, zy, part_ld, n_segs, targets, N, V, logp,
+                                        lse, s));
+}
+
+int ll_backward_shard(const float* grad_logp, const void* hidden, const void* weight,
+                      const void* bias, const int64_t* targets, const float* lse, int64_t N,
+                      int64_t D, int64_t Vs, int64_t v0, int64_t V, int dtype, int need_dh,
+                      int need_dw, int need_db, void* grad_hidden, int dh_dtype,
+                      void* grad_weight, int dw_dtype, void* grad_bias, int token_chunks,
+                      void* workspace, size_t ws_bytes, void* stream) {
+    int st = check_shard(Vs, v0, V);
+    if (st) return st;
+    if ((st = check_sizes(N, D, Vs))) return st;
+    if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
+    if (N == 0 || !(need_dh | need_dw | need_db))
+        return backward_impl(grad_logp, hidden, weight, bias, targets, lse, N, D, Vs, dtype,
+                             need_dh, need_dw, need_db, grad_hidden, dh_dtype, grad_weight,
+                             dw_dtype, grad_bias, token_chunks, workspace, ws_bytes, stream, 0,
+                             nullptr, nullptr, 1);
+    if (!targets || !weight) return LL_ERR_INVALID_ARG;
+    const size_t tail = local_targets_bytes(N);
+    if (!workspace || ws_bytes < tail) return LL_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return LL_ERR_WORKSPACE;
+    const size_t body = ws_bytes - tail;
+    const BwdLayout L = bwd_layout(N, Vs, dtype, token_chunks, need_db);
+    if (body < L.total) return LL_ERR_WORKSPACE;
+    // checks of backward_impl that must pass before anything is launched
+    if ((need_dh | need_dw | need_db) & ~1 || token_chunks < 0) return LL_ERR_INVALID_ARG;
+    if (need_dh && !(dh_dtype == dtype || dh_dtype == LL_F32)) return LL_ERR_DTYPE;
+    if ((need_dw || need_db) && !(dw_dtype == dtype || dw_dtype == LL_F32)) return LL_ERR_DTYPE;
+    if ((need_dw && !grad_weight) || (need_db && !grad_bias) || (need_dh && !grad_hidden))
+        return LL_ERR_INVALID_ARG;
+    if (!grad_logp || !hidden || !lse) return LL_ERR_INVALID_ARG;
+    if (D % 8 != 0 || !aligned16(weight) || !aligned16(hidden) ||
+        (need_dw && !aligned16(grad_weight)) || (need_dh && !aligned16(grad_hidden)))
+        return LL_ERR_ALIGN;
+    DeviceGuard guard(weight);
+    if (guard.err) return guard.err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int64_t* local = reinterpret_cast<int64_t*>(static_cast<char*>(workspace) + body);
+    cudaError_t e = launch_localize_targets(targets, N, v0, Vs, V, local, nullptr, s);
+    if (e != cudaSuccess) return cuda_status(e);
+    return backward_impl(grad_logp, hidden, weight, bias, local, lse, N, D, Vs, dtype, need_dh,
+                         need_dw, need_db, grad_hidden, dh_dtype, grad_weight, dw_dtype,
+                         grad_bias, token_chunks, workspace, body, stream, 0, nullptr, nullptr,
+                         1);
+}
+
 int logits_logp_fwd(const void* logits, int64_t ld, int dtype, const int64_t* targets, int64_t N,
                     int64_t V, float* logp, float* lse, void* stream) {
     if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
@@ -680,31 +809,17 @@ int logits_logp_fwd_bwd(const float* grad_logp, const void* logits, int64_t ld, 
     const char* a = static_cast<const char*>(logits);
     const char* b = static_cast<const char*>(grad_logits);
     const size_t span = size_t(N) * size_t(ld) * esize(dtype);
-    if (a < b + span && b < a + span) return LL_ERR_INVALID_ARG;  // no aliasing
+    // in place (the same buffer) or apart; a partial overlap is refused
+    if (a != b && a < b + span && b < a + span) return LL_ERR_INVALID_ARG;
     DeviceGuard guard(logits);
     if (guard.err) return guard.err;
     DevInfo dev;
     int st = device_info(guard.dev, &dev);
     if (st) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    bool used = false;
-    {
-        Phase ph("logits_fused", s);
-        cudaError_t e = launch_logits_fused(grad_logp, logits, ld, dtype, targets, N, V, logp,
-                                            lse, grad_logits, dev, s, &used);
-        if (e != cudaSuccess) return cuda_status(e);
-    }
-    if (used) return LL_OK;
-    // shape or alignment the one-pass kernel does not take: the two kernels
-    cudaError_t e;
-    {
-        Phase ph("logits_fwd", s);
-        e = launch_logits_fwd(logits, ld, dtype, targets, N, V, logp, lse, s);
-    }
-    if (e != cudaSuccess) return cuda_status(e);
-    Phase ph("logits_bwd", s);
-    return cuda_status(launch_logits_bwd(grad_logp, logits, ld, dtype, targets, lse, N, V,
-                                         grad_logits, s));
+    Phase ph("logits_fused", s);
+    return cuda_status(launch_logits_fused(grad_logp, logits, ld, dtype, targets, N, V, logp, lse,
+                                           grad_logits, dev, s));
 }
 
 int ll_check_status(void* stream) {

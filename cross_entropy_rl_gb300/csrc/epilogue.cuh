@@ -23,9 +23,11 @@
 // in FP32 (c), and the off-target entries S, stored in 16 bits.  The 16-bit
 // rounding then only touches the entries -grad * p[n, v], v != y, whose sum
 // over v is grad * (1 - p[n, y]); a sharp distribution (p[n, y] -> 1) makes
-// that error vanish instead of leaving a 2^-9 * |grad| error at the target.  Zero rules (issue #261, "Correctness boundary"):
-// rows with an invalid target or a zero upstream gradient store exact +0;
-// sums start from +0.
+// that error vanish instead of leaving a 2^-9 * |grad| error at the target.
+// Zero rules (issue #261, "Correctness boundary"): rows with an invalid
+// target or a zero upstream gradient store exact +0; sums start from +0.
+// In a vocab shard (ea.shard) a row whose target lies in another shard keeps
+// its softmax part and has no target column here.
 #pragma once
 #include "ll_device.cuh"
 
@@ -82,6 +84,7 @@ struct RowEpilogue {
     int64_t y;
     float coef;    // Recomp: -grad (0 for dead rows); Dh: c[row] (0 for dead rows)
     bool live;     // Recomp / Dh: valid target and non-zero upstream gradient
+    bool onehot;   // Dh: the target column lies in this launch's vocab
     float lse2;    // Recomp: lse * log2(e)
     float m2, s;   // Fwd: running max (log2 units) and sum
     float zyv;
@@ -100,11 +103,13 @@ struct RowEpilogue {
         } else if constexpr (E == EpiKind::Recomp || E == EpiKind::Dh) {
             y = rvalid ? ea.targets[row] : -1;
             const float g = rvalid ? ea.grad[row] : 0.f;
-            live = rvalid && y >= 0 && y < ea.V && g != 0.f;
+            const bool here = y >= 0 && y < ea.V;
+            live = rvalid && (here || (ea.shard && y == kTargetInOtherShard)) && g != 0.f;
+            onehot = live && here;
             if constexpr (E == EpiKind::Recomp)
                 coef = live ? -g : 0.f;
             else
-                coef = live ? ea.tc[row] : 0.f;
+                coef = onehot ? ea.tc[row] : 0.f;
             if constexpr (E == EpiKind::Recomp) lse2 = rvalid ? ea.lse[row] * kLog2e : 0.f;
         } else {  // Dw: row is a vocab index
             oh_beg = oh_end = 0;
@@ -176,11 +181,14 @@ struct RowEpilogue {
         } else if constexpr (E == EpiKind::Dh) {
             if (!rvalid) return;
             const int64_t D = ea.Ncols;
-            if (live) {
+            if (onehot) {
                 float w[32];
                 load_row32<T>(ea.W, y * ea.ldW + col0, w, col0, D, own_tag<T>());
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = fmaf(coef, w[j], v[j]) + 0.f;
+            } else if (live) {  // target in another vocab shard: softmax part only
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = v[j] + 0.f;
             } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.f;

@@ -266,4 +266,62 @@ __device__ __forceinline__ void store8(T* p, const float (&f)[8]) {
     }
 }
 
+// ------------------------------------------------- L2 eviction-hinted access
+// Cache policies for ld / st .L2::cache_hint: evict_last keeps the lines
+// (a row read again soon), evict_first lets them go first (last use).
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint4 ld16_hint(const void* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void st16_hint(void* p, const uint4& v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+                 : "memory");
+}
+// load8 / store8 with an L2 policy.
+template <typename T>
+__device__ __forceinline__ void load8_hint(const T* p, float (&f)[8], uint64_t pol) {
+    if constexpr (sizeof(T) == 4) {
+        const uint4 a = ld16_hint(p, pol), b = ld16_hint(p + 4, pol);
+        f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y);
+        f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
+        f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y);
+        f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
+    } else {
+        const uint4 u = ld16_hint(p, pol);
+        const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = Elem<T>::to_f(e[j]);
+    }
+}
+template <typename T>
+__device__ __forceinline__ void store8_hint(T* p, const float (&f)[8], uint64_t pol) {
+    if constexpr (sizeof(T) == 4) {
+        st16_hint(p, make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]),
+                                __float_as_uint(f[2]), __float_as_uint(f[3])), pol);
+        st16_hint(p + 4, make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]),
+                                    __float_as_uint(f[6]), __float_as_uint(f[7])), pol);
+    } else {
+        uint4 u;
+        T* e = reinterpret_cast<T*>(&u);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) e[j] = Elem<T>::from_f(f[j]);
+        st16_hint(p, u, pol);
+    }
+}
+
 }  // namespace ll

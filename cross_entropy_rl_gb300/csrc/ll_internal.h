@@ -19,6 +19,15 @@ constexpr int kVocabTilesPerSeg = 4;  // vocab tiles per LSE segment (1024 vocab
 // Maximum vocab size: inner indices within a row stay below 2^31.
 constexpr int64_t kMaxV = (int64_t(1) << 31) - 1 - 256;
 
+// Vocab-parallel shards: a shard covers vocab [v0, v0 + Vs) with v0 and (but
+// for the last shard) Vs multiples of one LSE segment, so its segment
+// partials are those of the whole-vocab run.  Inside a shard's launches a
+// target is the local index y - v0, or kTargetInOtherShard for a valid
+// target of another shard: the row keeps its softmax part, it has no
+// one-hot entry here (EpiArgs::shard set).  Invalid targets become -1.
+constexpr int64_t kSegCols = int64_t(kBN) * kVocabTilesPerSeg;
+constexpr int64_t kTargetInOtherShard = -(int64_t(1) << 62);
+
 struct DevInfo {
     int device;
     int num_sms;
@@ -40,12 +49,12 @@ cudaError_t launch_logits_bwd(const float* grad, const void* logits, int64_t ld,
                               void* grad_logits, cudaStream_t s);
 
 // Logits forward + backward in one pass for a known upstream gradient
-// (logits_fused.cu).  *used = false (nothing launched) when the shape or
-// alignment does not suit it; the caller then runs the two kernels.
+// (logits_kernels.cu): per row the forward then the backward, bitwise the
+// results of the two kernels; grad_logits may be the logits buffer.
 cudaError_t launch_logits_fused(const float* grad, const void* logits, int64_t ld, int dtype,
                                 const int64_t* targets, int64_t N, int64_t V, float* logp,
                                 float* lse, void* grad_logits, const DevInfo& dev,
-                                cudaStream_t s, bool* used);
+                                cudaStream_t s);
 
 // --- GEMM-based linear path -------------------------------------------------
 enum class EpiKind : int { Fwd = 0, Recomp = 1, Dh = 2, Dw = 3 };
@@ -87,6 +96,7 @@ struct EpiArgs {
     int64_t ld_h;
     int* status;
     uint64_t wait_ns;
+    int shard;               // targets may be kTargetInOtherShard (vocab shard)
 };
 
 struct GemmShape {
@@ -146,6 +156,10 @@ cudaError_t launch_gemm_f32(EpiKind kind, const void* A, int64_t lda, int a_mn, 
                             int max_ctas, cudaStream_t s);
 
 // --- small kernels (aux_kernels.cu) ------------------------------------------
+// Shard-local targets: y - v0 for y in [v0, v0 + Vs), kTargetInOtherShard
+// for other valid y in [0, V), -1 for invalid ones; zy (if given) = -inf.
+cudaError_t launch_localize_targets(const int64_t* targets, int64_t N, int64_t v0, int64_t Vs,
+                                    int64_t V, int64_t* local, float* zy, cudaStream_t s);
 cudaError_t launch_lse_merge(const float* part_m, const float* part_s, const float* zy,
                              int64_t part_ld, int64_t n_segs, const int64_t* targets, int64_t N,
                              int64_t V, float* logp, float* lse, cudaStream_t s);

@@ -10,6 +10,10 @@
 //
 // Element-to-thread assignment depends only on the column index and the
 // block size, never on the row index or N, which gives batch invariance.
+//
+// With a known upstream gradient, logits_fwd_bwd_kernel runs both per row,
+// back to back, so the row's second read is served by L2: one HBM read and
+// one write per row (4 V bytes instead of the two kernels' 6 V).
 #include <math.h>
 
 #include "ll_device.cuh"
@@ -79,6 +83,104 @@ __device__ __forceinline__ MS block_reduce(MS st, MS* sh) {
     return r;
 }
 
+// Plain or L2-hinted 8-element access (HINT selects the policy versions).
+template <typename T, bool HINT>
+__device__ __forceinline__ void ld8(const T* p, float (&f)[8], uint64_t pol) {
+    if constexpr (HINT)
+        load8_hint(p, f, pol);
+    else
+        load8(p, f);
+}
+template <typename T, bool HINT>
+__device__ __forceinline__ void st8(T* p, const float (&f)[8], uint64_t pol) {
+    if constexpr (HINT)
+        store8_hint(p, f, pol);
+    else
+        store8(p, f);
+}
+
+// This thread's (max, sum-exp) of row x: 8-element vectors tid, tid + T,
+// tid + 2T, ... (T = block size) in that order, U of them loaded at a time
+// (the order, hence the result, does not depend on U), then the scalar tail.
+template <typename T, int U, bool HINT>
+__device__ __forceinline__ MS row_partial(const T* x, int64_t V, int vec_ok, uint64_t pol) {
+    MS st = {-INFINITY, 0.f};
+    int64_t done = 0;
+    if (vec_ok) {
+        const int64_t nvec = V / 8;
+        int64_t i = threadIdx.x;
+        for (; i + (U - 1) * kThreads < nvec; i += U * kThreads) {
+            float f[U][8];
+#pragma unroll
+            for (int u = 0; u < U; ++u) ld8<T, HINT>(x + (i + u * kThreads) * 8, f[u], pol);
+#pragma unroll
+            for (int u = 0; u < U; ++u) ms_fold8(st, f[u]);
+        }
+        for (; i < nvec; i += kThreads) {
+            float f[8];
+            ld8<T, HINT>(x + i * 8, f, pol);
+            ms_fold8(st, f);
+        }
+        done = nvec * 8;
+    }
+    for (int64_t j = done + threadIdx.x; j < V; j += kThreads) ms_fold1(st, Elem<T>::to_f(x[j]));
+    return st;
+}
+
+// lse of a row from thread 0's block result.
+__device__ __forceinline__ float lse_of(const MS& r) {
+    return (r.m == -INFINITY) ? -INFINITY : r.m * kLn2 + logf(r.s);
+}
+
+__device__ __forceinline__ float grad_elem(float z, int64_t c, int64_t y, float g, float lse2) {
+    const float p = ex2(fmaf(z, kLog2e, -lse2));
+    const float oh = (c == y) ? 1.f : 0.f;
+    return fmaf(g, oh - p, 0.f);  // + 0 keeps empty results at +0
+}
+
+// Gradient row o = g * (onehot(y) - exp(x - lse)) (all +0 when !live); each
+// thread reads a vector of x and writes the same vector of o, so o may be x.
+template <typename T, int U, bool HINT>
+__device__ __forceinline__ void row_grad(const T* x, T* o, int64_t V, int vec_ok, int64_t y,
+                                         float g, bool live, float lse2, uint64_t pol_ld,
+                                         uint64_t pol_st) {
+    int64_t done = 0;
+    if (vec_ok) {
+        const int64_t nvec = V / 8;
+        if (!live) {
+            const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int64_t i = threadIdx.x; i < nvec; i += kThreads) st8<T, HINT>(o + i * 8, z, pol_st);
+        } else {
+            int64_t i = threadIdx.x;
+            for (; i + (U - 1) * kThreads < nvec; i += U * kThreads) {
+                float f[U][8];
+#pragma unroll
+                for (int u = 0; u < U; ++u) ld8<T, HINT>(x + (i + u * kThreads) * 8, f[u], pol_ld);
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t c0 = (i + u * kThreads) * 8;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) f[u][j] = grad_elem(f[u][j], c0 + j, y, g, lse2);
+                    st8<T, HINT>(o + c0, f[u], pol_st);
+                }
+            }
+            for (; i < nvec; i += kThreads) {
+                float f[8];
+                const int64_t c0 = i * 8;
+                ld8<T, HINT>(x + c0, f, pol_ld);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) f[j] = grad_elem(f[j], c0 + j, y, g, lse2);
+                st8<T, HINT>(o + c0, f, pol_st);
+            }
+        }
+        done = nvec * 8;
+    }
+    for (int64_t j = done + threadIdx.x; j < V; j += kThreads) {
+        const float v = live ? grad_elem(Elem<T>::to_f(x[j]), j, y, g, lse2) : 0.f;
+        o[j] = Elem<T>::from_f(v);
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) logits_fwd_kernel(const T* __restrict__ logits,
                                                               int64_t ld,
@@ -89,29 +191,9 @@ __global__ void __launch_bounds__(kThreads) logits_fwd_kernel(const T* __restric
     __shared__ MS sh[kWarps];
     const int64_t row = blockIdx.x;
     const T* x = logits + row * ld;
-    MS st = {-INFINITY, 0.f};
-    int64_t done = 0;
-    if (vec_ok) {
-        const int64_t nvec = V / 8;
-        int64_t i = threadIdx.x;
-        for (; i + (kUnroll - 1) * kThreads < nvec; i += kUnroll * kThreads) {
-            float f[kUnroll][8];
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) load8(x + (i + u * kThreads) * 8, f[u]);
-#pragma unroll
-            for (int u = 0; u < kUnroll; ++u) ms_fold8(st, f[u]);
-        }
-        for (; i < nvec; i += kThreads) {
-            float f[8];
-            load8(x + i * 8, f);
-            ms_fold8(st, f);
-        }
-        done = nvec * 8;
-    }
-    for (int64_t j = done + threadIdx.x; j < V; j += kThreads) ms_fold1(st, Elem<T>::to_f(x[j]));
-    const MS r = block_reduce(st, sh);
+    const MS r = block_reduce(row_partial<T, kUnroll, false>(x, V, vec_ok, 0), sh);
     if (threadIdx.x == 0) {
-        const float lse = (r.m == -INFINITY) ? -INFINITY : r.m * kLn2 + logf(r.s);
+        const float lse = lse_of(r);
         const int64_t y = targets[row];
         const bool valid = (y >= 0) && (y < V);
         logp[row] = valid ? Elem<T>::to_f(x[y]) - lse : 0.f;
@@ -125,58 +207,44 @@ __global__ void __launch_bounds__(kThreads) logits_bwd_kernel(
     const int64_t* __restrict__ targets, const float* __restrict__ lse, int64_t V,
     T* __restrict__ out, int vec_ok) {
     const int64_t row = blockIdx.x;
-    const T* x = logits + row * ld;
-    T* o = out + row * ld;
     const int64_t y = targets[row];
     const float g = grad[row];
     const bool live = (y >= 0) && (y < V) && (g != 0.f);
-    const float lse2 = lse[row] * kLog2e;
-    int64_t done = 0;
-    if (vec_ok) {
-        const int64_t nvec = V / 8;
-        if (!live) {
-            const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int64_t i = threadIdx.x; i < nvec; i += kThreads) store8(o + i * 8, z);
-        } else {
-            int64_t i = threadIdx.x;
-            for (; i + (kUnroll - 1) * kThreads < nvec; i += kUnroll * kThreads) {
-                float f[kUnroll][8];
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) load8(x + (i + u * kThreads) * 8, f[u]);
-#pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
-                    const int64_t c0 = (i + u * kThreads) * 8;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float p = ex2(fmaf(f[u][j], kLog2e, -lse2));
-                        const float oh = (c0 + j == y) ? 1.f : 0.f;
-                        f[u][j] = fmaf(g, oh - p, 0.f);  // + 0 keeps empty results at +0
-                    }
-                    store8(o + c0, f[u]);
-                }
-            }
-            for (; i < nvec; i += kThreads) {
-                float f[8];
-                const int64_t c0 = i * 8;
-                load8(x + c0, f);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float p = ex2(fmaf(f[j], kLog2e, -lse2));
-                    const float oh = (c0 + j == y) ? 1.f : 0.f;
-                    f[j] = fmaf(g, oh - p, 0.f);
-                }
-                store8(o + c0, f);
-            }
+    row_grad<T, kUnroll, false>(logits + row * ld, out + row * ld, V, vec_ok, y, g, live,
+                                lse[row] * kLog2e, 0, 0);
+}
+
+// Forward and backward of each row in turn (a known upstream gradient): the
+// row's second read, right after its first, finds it in L2, so HBM sees one
+// read and one write per row.  The blocks are persistent (rows blockIdx.x,
+// blockIdx.x + gridDim.x, ...), which bounds the rows in flight, hence the
+// L2 footprint; the first read keeps its lines (evict_last), the second read
+// and the gradient stores release theirs (evict_first).  The row code is the
+// one of logits_fwd_kernel and logits_bwd_kernel, so every result is bitwise
+// theirs.  grad_logits may be the logits buffer itself.
+template <typename T, int U>
+__global__ void __launch_bounds__(kThreads) logits_fwd_bwd_kernel(
+    const float* __restrict__ grad, const T* logits, int64_t ld,
+    const int64_t* __restrict__ targets, int64_t N, int64_t V, float* __restrict__ logp,
+    float* __restrict__ lse_out, T* out, int vec_ok) {
+    __shared__ MS sh[kWarps];
+    __shared__ float lse_sh;
+    const uint64_t keep = l2_evict_last(), drop = l2_evict_first();
+    for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
+        const T* x = logits + row * ld;
+        const MS r = block_reduce(row_partial<T, U, true>(x, V, vec_ok, keep), sh);
+        const int64_t y = targets[row];
+        const float g = grad[row];
+        const bool valid = (y >= 0) && (y < V);
+        if (threadIdx.x == 0) {
+            const float lse = lse_of(r);
+            logp[row] = valid ? Elem<T>::to_f(x[y]) - lse : 0.f;
+            lse_out[row] = lse;
+            lse_sh = lse;
         }
-        done = nvec * 8;
-    }
-    for (int64_t j = done + threadIdx.x; j < V; j += kThreads) {
-        float v = 0.f;
-        if (live) {
-            const float p = ex2(fmaf(Elem<T>::to_f(x[j]), kLog2e, -lse2));
-            v = fmaf(g, (j == y ? 1.f : 0.f) - p, 0.f);
-        }
-        o[j] = Elem<T>::from_f(v);
+        __syncthreads();  // lse_sh; also thread 0 is done with sh and x[y]
+        row_grad<T, U, true>(x, out + row * ld, V, vec_ok, y, g, valid && g != 0.f,
+                             lse_sh * kLog2e, drop, drop);
     }
 }
 
@@ -234,6 +302,43 @@ cudaError_t launch_logits_bwd(const float* grad, const void* logits, int64_t ld,
             const int ok = vec_ok<float>(logits, ld) && vec_ok<float>(grad_logits, ld);
             logits_bwd_kernel<float><<<grid, kThreads, 0, s>>>(
                 grad, static_cast<const float*>(logits), ld, targets, lse, V,
+                static_cast<float*>(grad_logits), ok);
+        }
+    }
+    return cudaGetLastError();
+}
+
+// Resident blocks of the fused kernel per SM (rows in flight per SM).
+constexpr int kFusedBlocksPerSm = 2;
+constexpr int kFusedUnroll = 8;
+
+cudaError_t launch_logits_fused(const float* grad, const void* logits, int64_t ld, int dtype,
+                                const int64_t* targets, int64_t N, int64_t V, float* logp,
+                                float* lse, void* grad_logits, const DevInfo& dev,
+                                cudaStream_t s) {
+    int64_t blocks = int64_t(dev.num_sms) * kFusedBlocksPerSm;
+    if (blocks > N) blocks = N;
+    const dim3 grid(static_cast<unsigned>(blocks));
+    note_launches(1);
+    switch (dtype) {
+        case LL_BF16: {
+            const int ok = vec_ok<__nv_bfloat16>(logits, ld) && vec_ok<__nv_bfloat16>(grad_logits, ld);
+            logits_fwd_bwd_kernel<__nv_bfloat16, kFusedUnroll><<<grid, kThreads, 0, s>>>(
+                grad, static_cast<const __nv_bfloat16*>(logits), ld, targets, N, V, logp, lse,
+                static_cast<__nv_bfloat16*>(grad_logits), ok);
+            break;
+        }
+        case LL_F16: {
+            const int ok = vec_ok<__half>(logits, ld) && vec_ok<__half>(grad_logits, ld);
+            logits_fwd_bwd_kernel<__half, kFusedUnroll><<<grid, kThreads, 0, s>>>(
+                grad, static_cast<const __half*>(logits), ld, targets, N, V, logp, lse,
+                static_cast<__half*>(grad_logits), ok);
+            break;
+        }
+        default: {
+            const int ok = vec_ok<float>(logits, ld) && vec_ok<float>(grad_logits, ld);
+            logits_fwd_bwd_kernel<float, kFusedUnroll><<<grid, kThreads, 0, s>>>(
+                grad, static_cast<const float*>(logits), ld, targets, N, V, logp, lse,
                 static_cast<float*>(grad_logits), ok);
         }
     }

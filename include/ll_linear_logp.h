@@ -150,6 +150,79 @@ int ll_forward_backward(const float* grad_logp, const void* hidden, const void* 
                         void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Vocab-parallel (tensor-parallel) pieces: the vocab split over ranks into
+ * contiguous shards [v0, v0 + Vs) (RL-Kernel PR #495, the coordinated
+ * cross entropy experiment and its follow-up commit: each tensor-parallel
+ * shard must start and end on a fixed vocab tile boundary, and training
+ * and rollout scoring must agree bitwise across tensor-parallel layouts,
+ * which a shard-local merge broke for 282 of 1200 rows).
+ *   v0 must be a multiple of LL_SEGMENT_COLS; Vs too, except for the last
+ *   shard (v0 + Vs == V).  Anything else is LL_ERR_SHAPE.
+ * The forward's lse is an ascending-order merge of per-segment (max,
+ * sum-exp) partials, segments of LL_SEGMENT_COLS vocab entries.  A shard's
+ * partials are exactly the whole-vocab run's partials of its segments, so
+ * the shards' partials stacked in shard order, merged by ll_lse_merge, give
+ * the logp and lse of ll_forward bitwise, for any number of shards.
+ * Targets are global vocab ids throughout.
+ */
+#define LL_SEGMENT_COLS 1024
+
+/* Segments of a shard of Vs vocab entries: ceil(Vs / LL_SEGMENT_COLS). */
+int64_t ll_shard_segments(int64_t Vs);
+
+/* Workspace bytes of ll_forward_shard (is_backward = 0) or
+ * ll_backward_shard (is_backward = 1; flags = need_db), 256-byte aligned. */
+size_t ll_workspace_size_shard(int64_t N, int64_t D, int64_t Vs, int dtype, int token_chunks,
+                               int is_backward, int flags);
+
+/*
+ * Forward of one vocab shard: the shard's segment partials, no lse.
+ *   weight [Vs, D], bias [Vs] or NULL: the shard's rows of W and b.
+ *   targets [N] int64, global ids.
+ *   part_m, part_s [ll_shard_segments(Vs), N] float, device (written): for
+ *     the shard's segment j and row n, m = max over the segment of
+ *     z * log2(e) and s = sum over the segment of 2^(z * log2(e) - m).
+ *   zy [N] float, device (written): z[n, y_n] where y_n lies in the shard,
+ *     -inf elsewhere; the elementwise max over the shards is z[n, y_n].
+ */
+int ll_forward_shard(const void* hidden, const void* weight, const void* bias,
+                     const int64_t* targets, int64_t N, int64_t D, int64_t Vs, int64_t v0,
+                     int64_t V, int dtype, float* part_m, float* part_s, float* zy,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Ordered merge of whole-vocab segment partials: lse[n] = M + log sum_j
+ * s[j, n] 2^(m[j, n] - M) (M = max_j m[j, n], j ascending; in natural units),
+ * logp[n] = zy[n] - lse[n] if 0 <= targets[n] < V, else 0.
+ *   part_m, part_s [n_segs, part_ld] float, device, part_ld >= N; rows with
+ *     m = -inf, s = 0 (padding between shards) change nothing, bitwise.
+ *   zy [N] float: z[n, y_n] (for instance the max over the shards' zy).
+ *   logp, lse [N] float, device (written).  No workspace.
+ */
+int ll_lse_merge(const float* part_m, const float* part_s, int64_t n_segs, int64_t part_ld,
+                 const float* zy, const int64_t* targets, int64_t N, int64_t V, float* logp,
+                 float* lse, void* stream);
+
+/*
+ * Backward of one vocab shard, given the merged lse.  Arguments as in
+ * ll_backward with weight/bias/grad_weight/grad_bias being the shard's rows
+ * ([Vs, D], [Vs]) and targets global ids.
+ *   grad_hidden [N, D] (written): this shard's part, sum over v in the shard
+ *     of g[n, v] W[v, :]; grad_hidden is the sum of the shards' parts (add
+ *     them in a fixed order; LL_F32 keeps that sum accurate).
+ *   grad_weight / grad_bias: the shard's rows of the whole gradients,
+ *     bitwise those of ll_backward for the same token_chunks.
+ * A row whose target lies in another shard has no one-hot entry here and
+ * keeps its softmax part; invalid targets or grad_logp = 0 give +0 rows.
+ */
+int ll_backward_shard(const float* grad_logp, const void* hidden, const void* weight,
+                      const void* bias, const int64_t* targets, const float* lse, int64_t N,
+                      int64_t D, int64_t Vs, int64_t v0, int64_t V, int dtype, int need_dh,
+                      int need_dw, int need_db, void* grad_hidden, int dh_dtype,
+                      void* grad_weight, int dw_dtype, void* grad_bias, int token_chunks,
+                      void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Forward without a caller workspace.  No counterpart on the source pages:
  * it exists for callers that cannot allocate device memory (a framework
  * that forbids allocation during a step, plugin code without access to the
@@ -195,13 +268,11 @@ int logits_logp_bwd(const float* grad_logp, const void* logits, int64_t ld, int 
 /*
  * Logits-input forward and backward in one pass, for a grad_logp known
  * before the forward.  Same arguments as logits_logp_fwd plus
- * logits_logp_bwd together; logp, lse and grad_logits are written.  Each
- * row is read once and its gradient written once (4 V bytes per row instead
- * of 6 V): a cluster of CTAs holds the row in shared memory, combines the
- * slices' (max, sum-exp) in a fixed order and overwrites the row with its
- * gradient.  Deterministic and batch-invariant; equal to the two calls
- * within rounding (the reduction order differs).  Rows whose logits or
- * gradient are not 16-byte aligned, or V % 8 != 0, use the two kernels.
+ * logits_logp_bwd together; logp, lse and grad_logits are written, bitwise
+ * the results of the two calls.  Each row's gradient is computed right after
+ * its lse, so the row's second read is served by L2: HBM sees 4 V bytes per
+ * row instead of 6 V.  grad_logits may be the logits buffer itself (in
+ * place); a partial overlap is LL_ERR_INVALID_ARG.
  */
 int logits_logp_fwd_bwd(const float* grad_logp, const void* logits, int64_t ld, int dtype,
                         const int64_t* targets, int64_t N, int64_t V, float* logp, float* lse,

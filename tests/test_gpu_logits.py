@@ -161,12 +161,38 @@ def run_fused(ll, x, y, gl, V=None):
 @pytest.mark.parametrize("V,ld", [(151936, 151936), (1024, 1024), (4096, 4104),
                                   (1031, 1031), (1031, 1040), (8, 8)])
 def test_fused_full_parity(lib, dt, V, ld):
-    """One-pass fwd+bwd vs the oracle, on shapes the cluster kernel takes and
-    on ones that go to the two kernels (V % 8 != 0, unaligned rows)."""
+    """One-pass fwd+bwd vs the oracle (vector rows, V % 8 != 0, unaligned
+    rows), and bitwise the two calls."""
     N = 48 if V > 10000 else 150
     p = synth.logits_inputs(N, V, seed=V + ld, dtype=dt, ld=ld)
     x, y, gl = dev(p["logits"], dt), dev(p["y"]), dev(p["gl"])
-    compare(p, run_fused(lib, x, y, gl, V=V), V=V)
+    got = run_fused(lib, x, y, gl, V=V)
+    compare(p, got, V=V)
+    two = run(lib, x, y, gl, V=V)
+    for a, b in zip(got, two):
+        assert bits_equal(a[:, :V] if a.dim() == 2 else a, b[:, :V] if b.dim() == 2 else b)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_fused_in_place(lib, dt):
+    """grad_logits written over the logits buffer: the same bits as out of
+    place; a partially overlapping output is refused."""
+    N, V = 300, 151936 if dt == "bf16" else 4104
+    p = synth.logits_inputs(N, V, seed=13, dtype=dt)
+    x, y, gl = dev(p["logits"], dt), dev(p["y"]), dev(p["gl"])
+    ref = run_fused(lib, x, y, gl)
+    xi = x.clone()
+    got = lib.logits_fwd_bwd(gl, xi, y, out=(torch.empty(N, device="cuda"),
+                                             torch.empty(N, device="cuda"), xi))
+    torch.cuda.synchronize()
+    for a, b in zip(got, ref):
+        assert bits_equal(a, b)
+    assert got[2].data_ptr() == xi.data_ptr()
+    big = torch.empty(N + 1, V, dtype=x.dtype, device="cuda")
+    big[:N] = x
+    with pytest.raises(lib.LLError, match="status 1"):
+        lib.logits_fwd_bwd(gl, big[:N], y, out=(torch.empty(N, device="cuda"),
+                                                torch.empty(N, device="cuda"), big[1:]))
 
 
 def test_fused_invalid_targets_and_zero_rows(lib):

@@ -20,6 +20,12 @@ reordered beyond that):
                outside [0, V)
       dh     = g . W,   dW = g^T . h,   db = sum_n g_nv
 * the same two steps with the logits given directly (logits-input variant).
+* temperature T > 0 (the sampling temperature of RL rollouts; RL-Kernel PR
+  #495, the vLLM provider evidence runs temperatures 1.0 and 0.7): every
+  function takes ``temperature``; the distribution is softmax(z / T), so
+  logp_n = z_{n, y_n} / T - logsumexp_v(z_nv / T) and the gradient with
+  respect to z is gl_n * ([v == y_n] - p_nv) / T, p = softmax(z / T).
+  T = 1 is the plain definition above.
 
 Signed zeros: the correctness boundary of issue #261 keeps a +0-initialised
 gradient table, so an entry that receives no non-zero contribution is +0.  The
@@ -121,21 +127,35 @@ def linear_logits(h, W, b=None) -> np.ndarray:
     return z
 
 
-def linear_forward(h, W, b, y, dtype: str):
-    """(logp, lse) for hidden h [N, D], weight W [V, D], optional bias b [V]."""
+def _tempered(z: np.ndarray, temperature: float) -> np.ndarray:
+    """z / T (the logits of the temperature-scaled distribution)."""
+    if not temperature > 0:
+        raise ValueError("temperature must be > 0")
+    return z if temperature == 1.0 else z / temperature
+
+
+def _tempered_grad(zT, y, gl, temperature: float, lse=None) -> np.ndarray:
+    """d(sum gl logp_T)/dz = grad_logits(z / T) / T."""
+    g = grad_logits(zT, y, gl, lse)
+    return g if temperature == 1.0 else g / temperature + 0.0
+
+
+def linear_forward(h, W, b, y, dtype: str, temperature: float = 1.0):
+    """(logp, lse) for hidden h [N, D], weight W [V, D], optional bias b [V];
+    lse is the one of the tempered logits z / T."""
     h64, W64, b64 = decode(h, dtype), decode(W, dtype), decode(b, dtype)
-    return logp_from_logits(linear_logits(h64, W64, b64), y)
+    return logp_from_logits(_tempered(linear_logits(h64, W64, b64), temperature), y)
 
 
-def linear_backward(gl, h, W, b, y, dtype: str, dw_rows=None):
+def linear_backward(gl, h, W, b, y, dtype: str, dw_rows=None, temperature: float = 1.0):
     """(dh, dW, db) of sum_n gl_n * logp_n.
 
     dw_rows: optional index array; dW is then returned only for those vocab
     rows (each is a full sum over tokens, nothing is truncated).
     """
     h64, W64, b64 = decode(h, dtype), decode(W, dtype), decode(b, dtype)
-    z = linear_logits(h64, W64, b64)
-    g = grad_logits(z, y, gl)
+    z = _tempered(linear_logits(h64, W64, b64), temperature)
+    g = _tempered_grad(z, y, gl, temperature)
     dh = g @ W64 + 0.0
     gT = g.T if dw_rows is None else g.T[np.asarray(dw_rows)]
     dW = gT @ h64 + 0.0
@@ -143,12 +163,13 @@ def linear_backward(gl, h, W, b, y, dtype: str, dw_rows=None):
     return dh, dW, db
 
 
-def linear_forward_backward(gl, h, W, b, y, dtype: str, dw_rows=None):
+def linear_forward_backward(gl, h, W, b, y, dtype: str, dw_rows=None,
+                            temperature: float = 1.0):
     """Forward and backward of one problem, sharing the float64 logits."""
     h64, W64, b64 = decode(h, dtype), decode(W, dtype), decode(b, dtype)
-    z = linear_logits(h64, W64, b64)
+    z = _tempered(linear_logits(h64, W64, b64), temperature)
     logp, lse = logp_from_logits(z, y)
-    g = grad_logits(z, y, gl, lse)
+    g = _tempered_grad(z, y, gl, temperature, lse)
     dh = g @ W64 + 0.0
     gT = g.T if dw_rows is None else g.T[np.asarray(dw_rows)]
     dW = gT @ h64 + 0.0
@@ -156,7 +177,7 @@ def linear_forward_backward(gl, h, W, b, y, dtype: str, dw_rows=None):
     return dict(logp=logp, lse=lse, dh=dh, dW=dW, db=db)
 
 
-def linear_rows(gl, h, W, b, y, dtype: str, rows, dw_rows=None):
+def linear_rows(gl, h, W, b, y, dtype: str, rows, dw_rows=None, temperature: float = 1.0):
     """Outputs restricted to the token rows ``rows``.
 
     logp, lse and dh of those rows are exactly the full problem's rows
@@ -168,20 +189,21 @@ def linear_rows(gl, h, W, b, y, dtype: str, rows, dw_rows=None):
     h_r = np.asarray(h)[rows]
     y_r = np.asarray(y)[rows]
     gl_r = np.asarray(gl)[rows]
-    return linear_forward_backward(gl_r, h_r, W, b, y_r, dtype, dw_rows=dw_rows)
+    return linear_forward_backward(gl_r, h_r, W, b, y_r, dtype, dw_rows=dw_rows,
+                                   temperature=temperature)
 
 
-def logits_forward(x, y, dtype: str, V=None):
+def logits_forward(x, y, dtype: str, V=None, temperature: float = 1.0):
     """(logp, lse) from stored logits x [N, ld]; columns >= V are ignored."""
     z = decode(x, dtype)
     if V is not None:
         z = z[:, :V]
-    return logp_from_logits(z, y)
+    return logp_from_logits(_tempered(z, temperature), y)
 
 
-def logits_backward(gl, x, y, dtype: str, V=None):
+def logits_backward(gl, x, y, dtype: str, V=None, temperature: float = 1.0):
     """Gradient w.r.t. the logits [N, V] (float64) of sum_n gl_n * logp_n."""
     z = decode(x, dtype)
     if V is not None:
         z = z[:, :V]
-    return grad_logits(z, y, gl)
+    return _tempered_grad(_tempered(z, temperature), y, gl, temperature)

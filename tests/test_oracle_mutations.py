@@ -20,6 +20,9 @@ PINS = [
     pins.test_zero_upstream_gives_positive_zeros,
     pins.test_empty_input,
     pins.test_masked_tail_logits,
+    pins.test_temperature_two_class_softplus,
+    pins.test_temperature_limits,
+    lambda: pins.test_temperature_finite_differences(0.7),
 ]
 
 
@@ -94,7 +97,27 @@ def _logits_transposed_weight(h, W, b=None):
     return z if b is None else z + b[None, :]
 
 
+_orig_tempered = OL._tempered
+_orig_tgrad = OL._tempered_grad
+
+
+def _temper_multiplies(z, temperature):
+    _orig_tempered(z, temperature)  # keeps the argument check
+    return z * temperature
+
+
+def _tgrad_no_inverse(zT, y, gl, temperature, lse=None):
+    return _orig_grad(zT, y, gl, lse)  # the 1 / T factor dropped
+
+
+def _tgrad_squared(zT, y, gl, temperature, lse=None):
+    return _orig_grad(zT, y, gl, lse) / temperature ** 2 + 0.0
+
+
 MUTATIONS = {
+    "temperature_multiplies": ("_tempered", _temper_multiplies),
+    "temperature_grad_no_inverse": ("_tempered_grad", _tgrad_no_inverse),
+    "temperature_grad_squared": ("_tempered_grad", _tgrad_squared),
     "drop_bias": ("linear_logits", _drop_bias),
     "bias_twice": ("linear_logits", _bias_twice),
     "transposed_weight": ("linear_logits", _logits_transposed_weight),

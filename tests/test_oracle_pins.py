@@ -277,3 +277,67 @@ def test_masked_tail_logits():
     assert (g[3] == 0).all()
     np.testing.assert_allclose(g[:3, :8], O.logits_backward(gl[:3], z[:3, :8], y[:3], "f64"),
                                atol=1e-16)
+
+
+# ---------------------------------------------------------- temperature ----
+
+def test_temperature_two_class_softplus():
+    """V = 2: logp_T of class 0 is -softplus((z1 - z0) / T) (closed form)."""
+    z = np.array([[0.3, -1.1], [2.0, 2.5], [-4.0, 3.0]])
+    y = np.array([0, 0, 1])
+    for T in (0.7, 1.0, 2.5):
+        logp, _ = O.logits_forward(z, y, "f64", temperature=T)
+        d = np.array([z[0, 1] - z[0, 0], z[1, 1] - z[1, 0], z[2, 0] - z[2, 1]]) / T
+        assert np.allclose(logp, -np.log1p(np.exp(d)), rtol=0, atol=1e-15)
+
+
+def test_temperature_limits():
+    """T -> inf: every class has probability 1/V; T -> 0: the argmax class
+    has logp -> 0 and the others -> -inf."""
+    z = _rand((4, 9), 120)
+    y = np.array([0, 3, 8, 5])
+    logp, _ = O.logits_forward(z, y, "f64", temperature=1e9)
+    assert np.allclose(logp, -np.log(9.0), atol=1e-8)
+    am = z.argmax(axis=1)
+    logp, _ = O.logits_forward(z, am, "f64", temperature=1e-3)
+    assert np.all(logp > -1e-10) and np.all(logp <= 0.0)
+    other = (am + 1) % 9
+    logp, _ = O.logits_forward(z, other, "f64", temperature=1e-3)
+    assert np.all(logp < -10.0)
+
+
+@pytest.mark.parametrize("T", [0.7, 1.6])
+def test_temperature_finite_differences(T):
+    """Central differences of sum_n gl_n logp_T,n (the oracle's forward) match
+    its dh, dW, db and logits gradients: this pins the 1 / T factor."""
+    N, D, V = 3, 4, 6
+    h, W, b = _rand((N, D), 130), _rand((V, D), 131, 0.8), _rand((V,), 132)
+    y = np.array([1, 5, 0])
+    gl = _rand((N,), 133)
+    dh, dW, db = O.linear_backward(gl, h, W, b, y, "f64", temperature=T)
+    eps = 1e-6
+
+    def loss():
+        return float(np.dot(gl, O.linear_forward(h, W, b, y, "f64", temperature=T)[0]))
+
+    for arr, grad in ((h, dh), (W, dW), (b, db)):
+        num = np.zeros(arr.shape)
+        for i in np.ndindex(arr.shape):
+            a0 = arr[i]
+            arr[i] = a0 + eps
+            lp = loss()
+            arr[i] = a0 - eps
+            lm = loss()
+            arr[i] = a0
+            num[i] = (lp - lm) / (2 * eps)
+        assert np.abs(num - grad).max() / max(1.0, np.abs(grad).max()) < 1e-6
+    z = _rand((N, V), 134)
+    g = O.logits_backward(gl, z, y, "f64", temperature=T)
+    for n in range(N):
+        for v in range(V):
+            zp, zm = z.copy(), z.copy()
+            zp[n, v] += eps
+            zm[n, v] -= eps
+            lp = np.dot(gl, O.logits_forward(zp, y, "f64", temperature=T)[0])
+            lm = np.dot(gl, O.logits_forward(zm, y, "f64", temperature=T)[0])
+            assert (lp - lm) / (2 * eps) == pytest.approx(g[n, v], abs=1e-8)

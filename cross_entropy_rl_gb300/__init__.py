@@ -58,12 +58,28 @@ EXPORTS = {
     "ll_workspace_size_shard": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_int,
                                           _c_int]),
     "ll_forward_shard": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_i64,
-                                  _c_i64, _c_int, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p]),
+                                  _c_i64, _c_int, _c_p, _c_p, _c_p, _c_p, _c_size, _c_p, _c_p]),
     "ll_lse_merge": (_c_int, [_c_p, _c_p, _c_i64, _c_i64, _c_p, _c_p, _c_i64, _c_i64, _c_p,
                               _c_p, _c_p]),
     "ll_backward_shard": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64,
                                    _c_i64, _c_i64, _c_int, _c_int, _c_int, _c_int, _c_p,
-                                   _c_int, _c_p, _c_int, _c_p, _c_int, _c_p, _c_size, _c_p]),
+                                   _c_int, _c_p, _c_int, _c_p, _c_int, _c_p, _c_size, _c_p,
+                                   _c_p]),
+    "ll_forward_ex": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64, _c_int,
+                               _c_p, _c_p, _c_p, _c_size, _c_p, _c_p]),
+    "ll_backward_ex": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64,
+                                _c_int, _c_int, _c_int, _c_int, _c_p, _c_int, _c_p, _c_int,
+                                _c_p, _c_int, _c_p, _c_size, _c_p, _c_p]),
+    "ll_forward_backward_ex": (_c_int, [_c_p, _c_p, _c_p, _c_p, _c_p, _c_i64, _c_i64, _c_i64,
+                                        _c_int, _c_p, _c_p, _c_int, _c_int, _c_int, _c_p,
+                                        _c_int, _c_p, _c_int, _c_p, _c_int, _c_p, _c_size,
+                                        _c_p, _c_p]),
+    "logits_logp_fwd_ex": (_c_int, [_c_p, _c_i64, _c_int, _c_p, _c_i64, _c_i64, _c_p, _c_p,
+                                    _c_p, _c_p]),
+    "logits_logp_bwd_ex": (_c_int, [_c_p, _c_p, _c_i64, _c_int, _c_p, _c_p, _c_i64, _c_i64,
+                                    _c_p, _c_p, _c_p]),
+    "logits_logp_fwd_bwd_ex": (_c_int, [_c_p, _c_p, _c_i64, _c_int, _c_p, _c_i64, _c_i64,
+                                        _c_p, _c_p, _c_p, _c_p, _c_p]),
     "ll_check_status": (_c_int, [_c_p]),
     "ll_set_wait_limit_ns": (None, [_c_i64]),
     "ll_debug_unsatisfied_wait": (_c_int, [_c_p, _c_p]),
@@ -73,6 +89,22 @@ EXPORTS = {
     "ll_profile_enable": (None, [_c_int]),
     "ll_profile_summary": (_c_int, [ctypes.c_char_p, _c_size]),
 }
+
+
+class Options(ctypes.Structure):
+    """ll_options of the C ABI."""
+    _fields_ = [("temperature", ctypes.c_float), ("split_s", ctypes.c_int),
+                ("reserved", ctypes.c_int * 6)]
+
+
+def _opts(temperature=1.0, split_s=False):
+    """ll_options pointer for a call (None when every option is default)."""
+    t = 1.0 if temperature is None else float(temperature)
+    if not t > 0:
+        raise ValueError("temperature must be > 0")
+    if t == 1.0 and not split_s:
+        return None
+    return ctypes.byref(Options(temperature=t, split_s=int(bool(split_s))))
 
 
 class LLError(RuntimeError):
@@ -219,8 +251,10 @@ def _grad_outputs(out, need_dh, need_dw, need_db, N, D, V, op_dtype, dh_dtype, d
     return dh, dW, db, dh_dtype, dw_dtype
 
 
-def forward(hidden, weight, bias, targets, *, workspace=None, out=None, stream=None):
-    """(logp [N] fp32, lse [N] fp32) of z = hidden . weight^T (+ bias)."""
+def forward(hidden, weight, bias, targets, *, temperature=1.0, workspace=None, out=None,
+            stream=None):
+    """(logp [N] fp32, lse [N] fp32) of z = hidden . weight^T (+ bias); with a
+    temperature T the distribution is softmax(z / T)."""
     torch = _torch()
     L = load()
     N, D, V, dev = _check_linear(hidden, weight, bias, targets)
@@ -236,15 +270,16 @@ def forward(hidden, weight, bias, targets, *, workspace=None, out=None, stream=N
     if workspace is None:
         workspace = _workspace(ws_need, dev)
     _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
-    st = L.ll_forward(_ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets), N, D, V, code,
-                      _ptr(logp), _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream))
+    st = L.ll_forward_ex(_ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets), N, D, V, code,
+                         _ptr(logp), _ptr(lse), _ptr(workspace), workspace.numel(),
+                         _opts(temperature), _stream(stream))
     _check("ll_forward", st)
     return logp, lse
 
 
 def backward(grad_logp, hidden, weight, bias, targets, lse, *, need_dh=True, need_dw=True,
-             need_db=None, dh_dtype=None, dw_dtype=None, token_chunks=0, workspace=None,
-             out=None, stream=None):
+             need_db=None, dh_dtype=None, dw_dtype=None, token_chunks=0, temperature=1.0,
+             split_s=False, workspace=None, out=None, stream=None):
     """(grad_hidden, grad_weight, grad_bias); entries not requested are None.
 
     dw_dtype defaults to float32; grad_bias uses dw_dtype.
@@ -259,22 +294,24 @@ def backward(grad_logp, hidden, weight, bias, targets, lse, *, need_dh=True, nee
     _need(lse, "lse", (N,), torch.float32, dev)
     dh, dW, db, dh_dtype, dw_dtype = _grad_outputs(out, need_dh, need_dw, need_db, N, D, V,
                                                    hidden.dtype, dh_dtype, dw_dtype, dev)
-    ws_need = L.ll_workspace_size(N, D, V, code, token_chunks, 1, int(bool(need_db)))
+    ws_need = L.ll_workspace_size(N, D, V, code, token_chunks, 1,
+                                  int(bool(need_db)) | (int(bool(split_s)) << 1))
     if workspace is None:
         workspace = _workspace(ws_need, dev)
     _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
-    st = L.ll_backward(_ptr(grad_logp), _ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets),
-                       _ptr(lse), N, D, V, code, int(bool(need_dh)), int(bool(need_dw)),
-                       int(bool(need_db)), _ptr(dh), _code(dh_dtype), _ptr(dW), _code(dw_dtype),
-                       _ptr(db), int(token_chunks), _ptr(workspace), workspace.numel(),
-                       _stream(stream))
+    st = L.ll_backward_ex(_ptr(grad_logp), _ptr(hidden), _ptr(weight), _ptr(bias),
+                          _ptr(targets), _ptr(lse), N, D, V, code, int(bool(need_dh)),
+                          int(bool(need_dw)), int(bool(need_db)), _ptr(dh), _code(dh_dtype),
+                          _ptr(dW), _code(dw_dtype), _ptr(db), int(token_chunks),
+                          _ptr(workspace), workspace.numel(), _opts(temperature, split_s),
+                          _stream(stream))
     _check("ll_backward", st)
     return dh, dW, db
 
 
 def forward_backward(grad_logp, hidden, weight, bias, targets, *, need_dh=True, need_dw=True,
                      need_db=None, dh_dtype=None, dw_dtype=None, token_chunks=0,
-                     workspace=None, out=None, stream=None):
+                     temperature=1.0, split_s=False, workspace=None, out=None, stream=None):
     """(logp, lse, grad_hidden, grad_weight, grad_bias) in one call, for a
     grad_logp known before the forward; bitwise equal to forward + backward."""
     torch = _torch()
@@ -295,21 +332,23 @@ def forward_backward(grad_logp, hidden, weight, bias, targets, *, need_dh=True, 
     _need(lse, "lse", (N,), torch.float32, dev)
     dh, dW, db, dh_dtype, dw_dtype = _grad_outputs(grads, need_dh, need_dw, need_db, N, D, V,
                                                    hidden.dtype, dh_dtype, dw_dtype, dev)
-    ws_need = L.ll_workspace_size(N, D, V, code, token_chunks, 2, int(bool(need_db)))
+    ws_need = L.ll_workspace_size(N, D, V, code, token_chunks, 2,
+                                  int(bool(need_db)) | (int(bool(split_s)) << 1))
     if workspace is None:
         workspace = _workspace(ws_need, dev)
     _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
-    st = L.ll_forward_backward(_ptr(grad_logp), _ptr(hidden), _ptr(weight), _ptr(bias),
-                               _ptr(targets), N, D, V, code, _ptr(logp), _ptr(lse),
-                               int(bool(need_dh)), int(bool(need_dw)), int(bool(need_db)),
-                               _ptr(dh), _code(dh_dtype), _ptr(dW), _code(dw_dtype), _ptr(db),
-                               int(token_chunks), _ptr(workspace), workspace.numel(),
-                               _stream(stream))
+    st = L.ll_forward_backward_ex(_ptr(grad_logp), _ptr(hidden), _ptr(weight), _ptr(bias),
+                                  _ptr(targets), N, D, V, code, _ptr(logp), _ptr(lse),
+                                  int(bool(need_dh)), int(bool(need_dw)), int(bool(need_db)),
+                                  _ptr(dh), _code(dh_dtype), _ptr(dW), _code(dw_dtype),
+                                  _ptr(db), int(token_chunks), _ptr(workspace),
+                                  workspace.numel(), _opts(temperature, split_s),
+                                  _stream(stream))
     _check("ll_forward_backward", st)
     return logp, lse, dh, dW, db
 
 
-def logits_fwd(logits, targets, V=None, *, out=None, stream=None):
+def logits_fwd(logits, targets, V=None, *, temperature=1.0, out=None, stream=None):
     """(logp, lse) from logits [N, ld]; columns >= V (default ld) ignored."""
     torch = _torch()
     L = load()
@@ -326,13 +365,14 @@ def logits_fwd(logits, targets, V=None, *, out=None, stream=None):
         logp, lse = out
     _need(logp, "logp", (N,), torch.float32, dev)
     _need(lse, "lse", (N,), torch.float32, dev)
-    st = L.logits_logp_fwd(_ptr(logits), ld, _code(logits.dtype), _ptr(targets), N, V,
-                           _ptr(logp), _ptr(lse), _stream(stream))
+    st = L.logits_logp_fwd_ex(_ptr(logits), ld, _code(logits.dtype), _ptr(targets), N, V,
+                              _ptr(logp), _ptr(lse), _opts(temperature), _stream(stream))
     _check("logits_logp_fwd", st)
     return logp, lse
 
 
-def logits_bwd(grad_logp, logits, targets, lse, V=None, *, out=None, stream=None):
+def logits_bwd(grad_logp, logits, targets, lse, V=None, *, temperature=1.0, out=None,
+               stream=None):
     """grad_logits [N, ld] in the logits dtype (columns [0, V) written)."""
     torch = _torch()
     L = load()
@@ -347,8 +387,9 @@ def logits_bwd(grad_logp, logits, targets, lse, V=None, *, out=None, stream=None
     if out is None:
         out = torch.empty_like(logits)
     _need(out, "grad_logits", (N, ld), logits.dtype, dev)
-    st = L.logits_logp_bwd(_ptr(grad_logp), _ptr(logits), ld, _code(logits.dtype),
-                           _ptr(targets), _ptr(lse), N, V, _ptr(out), _stream(stream))
+    st = L.logits_logp_bwd_ex(_ptr(grad_logp), _ptr(logits), ld, _code(logits.dtype),
+                              _ptr(targets), _ptr(lse), N, V, _ptr(out), _opts(temperature),
+                              _stream(stream))
     _check("logits_logp_bwd", st)
     return out
 
@@ -376,7 +417,8 @@ def profile_summary() -> dict:
     return out
 
 
-def logits_fwd_bwd(grad_logp, logits, targets, V=None, *, out=None, stream=None):
+def logits_fwd_bwd(grad_logp, logits, targets, V=None, *, temperature=1.0, out=None,
+                   stream=None):
     """(logp, lse, grad_logits) in one pass over the logits (grad_logp known
     before the forward)."""
     torch = _torch()
@@ -397,9 +439,9 @@ def logits_fwd_bwd(grad_logp, logits, targets, V=None, *, out=None, stream=None)
     _need(logp, "logp", (N,), torch.float32, dev)
     _need(lse, "lse", (N,), torch.float32, dev)
     _need(g, "grad_logits", (N, ld), logits.dtype, dev)
-    st = L.logits_logp_fwd_bwd(_ptr(grad_logp), _ptr(logits), ld, _code(logits.dtype),
-                               _ptr(targets), N, V, _ptr(logp), _ptr(lse), _ptr(g),
-                               _stream(stream))
+    st = L.logits_logp_fwd_bwd_ex(_ptr(grad_logp), _ptr(logits), ld, _code(logits.dtype),
+                                  _ptr(targets), N, V, _ptr(logp), _ptr(lse), _ptr(g),
+                                  _opts(temperature), _stream(stream))
     _check("logits_logp_fwd_bwd", st)
     return logp, lse, g
 
@@ -416,8 +458,8 @@ def shard_segments(Vs: int) -> int:
     return int(load().ll_shard_segments(int(Vs)))
 
 
-def forward_shard(hidden, weight, bias, targets, v0, V, *, workspace=None, out=None,
-                  stream=None):
+def forward_shard(hidden, weight, bias, targets, v0, V, *, temperature=1.0, workspace=None,
+                  out=None, stream=None):
     """Segment partials of the vocab shard [v0, v0 + weight.shape[0]) of a
     vocab of V entries: (part_m, part_s) [shard_segments(Vs), N] and zy [N]
     (z of the target where it lies in the shard, -inf elsewhere).  targets
@@ -441,7 +483,8 @@ def forward_shard(hidden, weight, bias, targets, v0, V, *, workspace=None, out=N
     _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
     st = L.ll_forward_shard(_ptr(hidden), _ptr(weight), _ptr(bias), _ptr(targets), N, D, Vs,
                             int(v0), int(V), code, _ptr(part_m), _ptr(part_s), _ptr(zy),
-                            _ptr(workspace), workspace.numel(), _stream(stream))
+                            _ptr(workspace), workspace.numel(), _opts(temperature),
+                            _stream(stream))
     _check("ll_forward_shard", st)
     return part_m, part_s, zy
 
@@ -474,7 +517,7 @@ def lse_merge(part_m, part_s, zy, targets, V, *, out=None, stream=None):
 
 def backward_shard(grad_logp, hidden, weight, bias, targets, lse, v0, V, *, need_dh=True,
                    need_dw=True, need_db=None, dh_dtype=None, dw_dtype=None, token_chunks=0,
-                   workspace=None, out=None, stream=None):
+                   temperature=1.0, split_s=False, workspace=None, out=None, stream=None):
     """(grad_hidden part, grad_weight rows, grad_bias rows) of the vocab shard
     [v0, v0 + weight.shape[0]); lse is the merged whole-vocab lse.  The
     grad_hidden part defaults to float32 (the shards' parts are summed)."""
@@ -491,14 +534,14 @@ def backward_shard(grad_logp, hidden, weight, bias, targets, lse, v0, V, *, need
     dh, dW, db, dh_dtype, dw_dtype = _grad_outputs(out, need_dh, need_dw, need_db, N, D, Vs,
                                                    hidden.dtype, dh_dtype, dw_dtype, dev)
     if workspace is None:
-        workspace = _workspace(L.ll_workspace_size_shard(N, D, Vs, code, token_chunks, 1,
-                                                         int(bool(need_db))), dev)
+        workspace = _workspace(L.ll_workspace_size_shard(
+            N, D, Vs, code, token_chunks, 1, int(bool(need_db)) | (int(bool(split_s)) << 1)), dev)
     _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
     st = L.ll_backward_shard(_ptr(grad_logp), _ptr(hidden), _ptr(weight), _ptr(bias),
                              _ptr(targets), _ptr(lse), N, D, Vs, int(v0), int(V), code,
                              int(bool(need_dh)), int(bool(need_dw)), int(bool(need_db)),
                              _ptr(dh), _code(dh_dtype), _ptr(dW), _code(dw_dtype), _ptr(db),
                              int(token_chunks), _ptr(workspace), workspace.numel(),
-                             _stream(stream))
+                             _opts(temperature, split_s), _stream(stream))
     _check("ll_backward_shard", st)
     return dh, dW, db

@@ -169,14 +169,14 @@ __global__ void __launch_bounds__(128) softmax_part_kernel(
     const float* __restrict__ Z, int64_t ldZ, int64_t rows, int64_t V,
     const int64_t* __restrict__ targets, const float* __restrict__ grad,
     const float* __restrict__ lse, T* __restrict__ S, int64_t ldS, float* __restrict__ tc,
-    float* __restrict__ db_part) {
+    float* __restrict__ db_part, float inv_temp, T* __restrict__ S_lo) {
     const int lane = threadIdx.x & 31;
     const int64_t row = blockIdx.x * int64_t(32) + lane;
     const bool rvalid = row < rows;
     const int64_t y = rvalid ? targets[row] : -1;
     const float g = rvalid ? grad[row] : 0.f;
     const bool live = rvalid && y >= 0 && y < V && g != 0.f;
-    const float coef = live ? -g : 0.f;
+    const float coef = live ? -g * inv_temp : 0.f;
     const float lse2 = rvalid ? lse[row] * kLog2e : 0.f;
     const int64_t nchunks = (V + 31) / 32;
     for (int64_t ch = blockIdx.y * 4 + (threadIdx.x >> 5); ch < nchunks; ch += gridDim.y * 4) {
@@ -222,6 +222,16 @@ __global__ void __launch_bounds__(128) softmax_part_kernel(
                 } else {
                     for (int j = 0; j < 8 && col0 + 8 * q + j < V; ++j)
                         S[row * ldS + col0 + 8 * q + j] = Elem<T>::from_f(f[j]);
+                }
+                if (S_lo) {  // hi / lo split: the rounding rest S - S_hi
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) f[j] -= Elem<T>::to_f(Elem<T>::from_f(f[j]));
+                    if (col0 + 8 * q + 8 <= V) {
+                        store8(S_lo + row * ldS + col0 + 8 * q, f);
+                    } else {
+                        for (int j = 0; j < 8 && col0 + 8 * q + j < V; ++j)
+                            S_lo[row * ldS + col0 + 8 * q + j] = Elem<T>::from_f(f[j]);
+                    }
                 }
             }
         } else {
@@ -364,7 +374,7 @@ cudaError_t launch_db_chunk(const void* S, int64_t ldS, int s_dtype, int64_t row
 cudaError_t launch_softmax_part(const float* Z, int64_t ldZ, int64_t rows, int64_t V,
                                 const int64_t* targets, const float* grad, const float* lse,
                                 void* S, int64_t ldS, int s_dtype, float* tc, float* db_part,
-                                cudaStream_t s) {
+                                float inv_temp, void* S_lo, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
     note_launches(1);
     const int64_t nchunks = (V + 31) / 32;
@@ -373,13 +383,16 @@ cudaError_t launch_softmax_part(const float* Z, int64_t ldZ, int64_t rows, int64
     const dim3 grid(static_cast<unsigned>((rows + 31) / 32), static_cast<unsigned>(gy));
     if (s_dtype == LL_BF16)
         softmax_part_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(
-            Z, ldZ, rows, V, targets, grad, lse, static_cast<__nv_bfloat16*>(S), ldS, tc, db_part);
+            Z, ldZ, rows, V, targets, grad, lse, static_cast<__nv_bfloat16*>(S), ldS, tc, db_part,
+            inv_temp, static_cast<__nv_bfloat16*>(S_lo));
     else if (s_dtype == LL_F16)
         softmax_part_kernel<__half><<<grid, 128, 0, s>>>(Z, ldZ, rows, V, targets, grad, lse,
-                                                         static_cast<__half*>(S), ldS, tc, db_part);
+                                                         static_cast<__half*>(S), ldS, tc, db_part,
+                                                         inv_temp, static_cast<__half*>(S_lo));
     else
         softmax_part_kernel<float><<<grid, 128, 0, s>>>(Z, ldZ, rows, V, targets, grad, lse,
-                                                        static_cast<float*>(S), ldS, tc, db_part);
+                                                        static_cast<float*>(S), ldS, tc, db_part,
+                                                        inv_temp, nullptr);
     return cudaGetLastError();
 }
 

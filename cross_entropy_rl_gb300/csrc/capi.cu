@@ -172,18 +172,21 @@ int64_t db_groups(int64_t Nc) {
 
 struct BwdLayout {
     int64_t chunks, Nc, ldS, ldZ, n_segs;
-    size_t S, Z, part_m, part_s, zy, tc, keys, offs, ctr, db, total;
+    size_t S, S_lo, Z, part_m, part_s, zy, tc, keys, offs, ctr, db, total;
 };
 // fused = 1: the single fwd+bwd call, which also keeps the chunk's FP32
 // logits Z and the forward partials.
+// split = 1: the softmax part is kept as a hi / lo pair (16-bit dtypes).
 BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need_db,
-                     int fused = 0) {
+                     int fused = 0, int split = 0) {
     BwdLayout L;
     L.ldS = round_up(V, 8);
     L.ldZ = round_up(V, 8);
     L.n_segs = cdiv(cdiv(V, kBN), kVocabTilesPerSeg);
+    split = split && dtype != LL_F32;
     const size_t row_bytes =
-        size_t(L.ldS) * esize(dtype) + (fused ? size_t(L.ldZ) * 4 + size_t(L.n_segs) * 8 + 4 : 0);
+        size_t(L.ldS) * esize(dtype) * (split ? 2 : 1) +
+        (fused ? size_t(L.ldZ) * 4 + size_t(L.n_segs) * 8 + 4 : 0);
     const int64_t n1 = N > 0 ? N : 1;
     int64_t k = token_chunks;
     if (k <= 0) {
@@ -197,6 +200,8 @@ BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need
     size_t off = 0;
     L.S = off;
     off = align_up(off + size_t(L.Nc) * size_t(L.ldS) * esize(dtype));
+    L.S_lo = off;
+    if (split) off = align_up(off + size_t(L.Nc) * size_t(L.ldS) * esize(dtype));
     L.Z = L.part_m = L.part_s = L.zy = off;
     if (fused) {
         L.Z = off;
@@ -238,6 +243,24 @@ int check_shard(int64_t Vs, int64_t v0, int64_t V) {
     return LL_OK;
 }
 
+// Options of a call: *inv_temp = 1 / temperature, *split = hi / lo S.
+// NULL = defaults.
+int read_options(const ll_options* o, float* inv_temp, int* split = nullptr) {
+    *inv_temp = 1.f;
+    if (split) *split = 0;
+    if (!o) return LL_OK;
+    for (int r : o->reserved)
+        if (r != 0) return LL_ERR_INVALID_ARG;
+    if (o->split_s != 0 && o->split_s != 1) return LL_ERR_INVALID_ARG;
+    if (split) *split = o->split_s;
+    const float T = o->temperature;
+    if (!(T > 0.f) || !(T < INFINITY)) return LL_ERR_INVALID_ARG;
+    const float it = 1.f / T;
+    if (!(it > 0.f) || !(it < INFINITY)) return LL_ERR_INVALID_ARG;
+    *inv_temp = it;
+    return LL_OK;
+}
+
 // Shard-local targets after the backward's (or at the forward's) workspace.
 size_t local_targets_bytes(int64_t N) { return align_up(size_t(N > 0 ? N : 1) * 8); }
 
@@ -270,7 +293,8 @@ size_t ll_workspace_size(int64_t N, int64_t D, int64_t V, int dtype, int token_c
     (void)D;
     if (N < 0 || V < 1 || !dtype_ok(dtype)) return 0;
     if (!is_backward) return fwd_layout(N, V).total;
-    return bwd_layout(N, V, dtype, token_chunks, flags & 1, is_backward == 2).total;
+    return bwd_layout(N, V, dtype, token_chunks, flags & 1, is_backward == 2, (flags >> 1) & 1)
+        .total;
 }
 
 void ll_set_wait_limit_ns(int64_t ns) { g_wait_limit_ns = ns > 0 ? uint64_t(ns) : 2000000000ull; }
@@ -283,8 +307,8 @@ namespace {
 // target logit of rows whose target lies in [0, V).
 cudaError_t forward_gemm(const void* hidden, const void* weight, const void* bias,
                          const int64_t* targets, int64_t N, int64_t D, int64_t V, int dtype,
-                         float* part_m, float* part_s, float* zy, int shard, const DevInfo& dev,
-                         cudaStream_t s) {
+                         float* part_m, float* part_s, float* zy, int shard, float inv_temp,
+                         const DevInfo& dev, cudaStream_t s) {
     GemmShape sh;
     sh.m_blocks = cdiv(N, kBM);
     sh.n_tiles = cdiv(V, kBN);
@@ -306,6 +330,7 @@ cudaError_t forward_gemm(const void* hidden, const void* weight, const void* bia
     ea.status = dev.status;
     ea.wait_ns = wait_limit_ns();
     ea.shard = shard;
+    ea.inv_temp = inv_temp;
     GemmLaunch G;
     memset(&G, 0, sizeof(G));
     G.dtype = dtype;
@@ -338,7 +363,18 @@ extern "C" {
 int ll_forward(const void* hidden, const void* weight, const void* bias, const int64_t* targets,
                int64_t N, int64_t D, int64_t V, int dtype, float* logp, float* lse,
                void* workspace, size_t ws_bytes, void* stream) {
-    int st = forward_checks(hidden, weight, targets, N, D, V, dtype);
+    return ll_forward_ex(hidden, weight, bias, targets, N, D, V, dtype, logp, lse, workspace,
+                         ws_bytes, nullptr, stream);
+}
+
+int ll_forward_ex(const void* hidden, const void* weight, const void* bias,
+                  const int64_t* targets, int64_t N, int64_t D, int64_t V, int dtype,
+                  float* logp, float* lse, void* workspace, size_t ws_bytes,
+                  const ll_options* opt, void* stream) {
+    float it;
+    int st = read_options(opt, &it);
+    if (st) return st;
+    st = forward_checks(hidden, weight, targets, N, D, V, dtype);
     if (st || N == 0) return st;
     if (!logp || !lse) return LL_ERR_INVALID_ARG;
     const FwdLayout L = fwd_layout(N, V);
@@ -354,7 +390,7 @@ int ll_forward(const void* hidden, const void* weight, const void* bias, const i
     float* part_s = reinterpret_cast<float*>(ws + L.part_s);
     float* zy = reinterpret_cast<float*>(ws + L.zy);
     cudaError_t e = forward_gemm(hidden, weight, bias, targets, N, D, V, dtype, part_m, part_s,
-                                 zy, 0, dev, s);
+                                 zy, 0, it, dev, s);
     if (e != cudaSuccess) return cuda_status(e);
     {
         Phase ph("lse_merge", s);
@@ -375,7 +411,8 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
                   int64_t D, int64_t V, int dtype, int need_dh, int need_dw, int need_db,
                   void* grad_hidden, int dh_dtype, void* grad_weight, int dw_dtype,
                   void* grad_bias, int token_chunks, void* workspace, size_t ws_bytes,
-                  void* stream, int fused, float* logp_out, float* lse_out, int shard = 0) {
+                  void* stream, int fused, float* logp_out, float* lse_out, int shard = 0,
+                  float inv_temp = 1.f, int split = 0) {
     int st = check_sizes(N, D, V);
     if (st) return st;
     if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
@@ -406,12 +443,14 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
     }
     if (!grad_logp || !hidden || !targets || (!fused && !lse)) return LL_ERR_INVALID_ARG;
     if (!aligned16(hidden) || (need_dh && !aligned16(grad_hidden))) return LL_ERR_ALIGN;
-    const BwdLayout L = bwd_layout(N, V, dtype, token_chunks, need_db, fused);
+    split = split && dtype != LL_F32;  // FP32 keeps S in FP32: nothing to split
+    const BwdLayout L = bwd_layout(N, V, dtype, token_chunks, need_db, fused, split);
     if (!workspace || ws_bytes < L.total) return LL_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return LL_ERR_WORKSPACE;
 
     char* ws = static_cast<char*>(workspace);
     void* S = ws + L.S;
+    void* S_lo = split ? static_cast<void*>(ws + L.S_lo) : nullptr;
     float* tc = reinterpret_cast<float*>(ws + L.tc);
     int64_t* keys = reinterpret_cast<int64_t*>(ws + L.keys);
     int* offs = reinterpret_cast<int*>(ws + L.offs);
@@ -460,6 +499,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
     base.status = dev.status;
     base.wait_ns = wait_limit_ns();
     base.shard = shard;
+    base.inv_temp = inv_temp;
 
     for (int64_t c = 0; c < L.chunks; ++c) {
         const int64_t r0 = c * L.Nc;
@@ -489,6 +529,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             ea.lse = lse + r0;
             ea.grad = grad_logp + r0;
             ea.S = S;
+            ea.S_lo = S_lo;
             ea.ldS = L.ldS;
             ea.tc = tc + r0;
             ea.db_part = need_db ? db_part : nullptr;
@@ -543,7 +584,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
                 Phase ph("softmax_part", s);
                 e = launch_softmax_part(Z, L.ldZ, rows, V, targets + r0, grad_logp + r0,
                                         lse_out + r0, S, L.ldS, dtype, tc + r0,
-                                        need_db ? db_part : nullptr, s);
+                                        need_db ? db_part : nullptr, inv_temp, S_lo, s);
             }
             if (e != cudaSuccess) return cuda_status(e);
         }
@@ -562,7 +603,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             int k = 0;
             if (need_dh) {
                 G.kind[k] = EpiKind::Dh;
-                G.op[k] = GemmOperands{S, L.ldS, 0, weight, D, 1, rows, D, V};
+                G.op[k] = GemmOperands{S, L.ldS, 0, weight, D, 1, rows, D, V, S_lo};
                 GemmShape& sh = G.shape[k];
                 sh.m_blocks = cdiv(rows, kBM);
                 sh.n_tiles = cdiv(D, kBN);
@@ -587,7 +628,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             }
             if (need_dw) {
                 G.kind[k] = EpiKind::Dw;
-                G.op[k] = GemmOperands{S, L.ldS, 1, h_c, D, 1, V, D, rows};
+                G.op[k] = GemmOperands{S, L.ldS, 1, h_c, D, 1, V, D, rows, S_lo};
                 GemmShape& sh = G.shape[k];
                 sh.m_blocks = cdiv(V, kBM);
                 sh.n_tiles = cdiv(D, kBN);
@@ -640,15 +681,47 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
 
 extern "C" {
 
+int ll_backward_ex(const float* grad_logp, const void* hidden, const void* weight,
+                   const void* bias, const int64_t* targets, const float* lse, int64_t N,
+                   int64_t D, int64_t V, int dtype, int need_dh, int need_dw, int need_db,
+                   void* grad_hidden, int dh_dtype, void* grad_weight, int dw_dtype,
+                   void* grad_bias, int token_chunks, void* workspace, size_t ws_bytes,
+                   const ll_options* opt, void* stream) {
+    float it;
+    int split;
+    int st = read_options(opt, &it, &split);
+    if (st) return st;
+    return backward_impl(grad_logp, hidden, weight, bias, targets, lse, N, D, V, dtype, need_dh,
+                         need_dw, need_db, grad_hidden, dh_dtype, grad_weight, dw_dtype,
+                         grad_bias, token_chunks, workspace, ws_bytes, stream, 0, nullptr,
+                         nullptr, 0, it, split);
+}
+
 int ll_backward(const float* grad_logp, const void* hidden, const void* weight, const void* bias,
                 const int64_t* targets, const float* lse, int64_t N, int64_t D, int64_t V,
                 int dtype, int need_dh, int need_dw, int need_db, void* grad_hidden,
                 int dh_dtype, void* grad_weight, int dw_dtype, void* grad_bias,
                 int token_chunks, void* workspace, size_t ws_bytes, void* stream) {
-    return backward_impl(grad_logp, hidden, weight, bias, targets, lse, N, D, V, dtype, need_dh,
-                         need_dw, need_db, grad_hidden, dh_dtype, grad_weight, dw_dtype,
-                         grad_bias, token_chunks, workspace, ws_bytes, stream, 0, nullptr,
-                         nullptr);
+    return ll_backward_ex(grad_logp, hidden, weight, bias, targets, lse, N, D, V, dtype, need_dh,
+                          need_dw, need_db, grad_hidden, dh_dtype, grad_weight, dw_dtype,
+                          grad_bias, token_chunks, workspace, ws_bytes, nullptr, stream);
+}
+
+int ll_forward_backward_ex(const float* grad_logp, const void* hidden, const void* weight,
+                           const void* bias, const int64_t* targets, int64_t N, int64_t D,
+                           int64_t V, int dtype, float* logp, float* lse, int need_dh,
+                           int need_dw, int need_db, void* grad_hidden, int dh_dtype,
+                           void* grad_weight, int dw_dtype, void* grad_bias,
+                           int token_chunks, void* workspace, size_t ws_bytes,
+                           const ll_options* opt, void* stream) {
+    float it;
+    int split;
+    int st = read_options(opt, &it, &split);
+    if (st) return st;
+    return backward_impl(grad_logp, hidden, weight, bias, targets, nullptr, N, D, V, dtype,
+                         need_dh, need_dw, need_db, grad_hidden, dh_dtype, grad_weight, dw_dtype,
+                         grad_bias, token_chunks, workspace, ws_bytes, stream, 1, logp, lse, 0,
+                         it, split);
 }
 
 int ll_forward_backward(const float* grad_logp, const void* hidden, const void* weight,
@@ -657,9 +730,10 @@ int ll_forward_backward(const float* grad_logp, const void* hidden, const void* 
                         int need_dw, int need_db, void* grad_hidden, int dh_dtype,
                         void* grad_weight, int dw_dtype, void* grad_bias, int token_chunks,
                         void* workspace, size_t ws_bytes, void* stream) {
-    return backward_impl(grad_logp, hidden, weight, bias, targets, nullptr, N, D, V, dtype,
-                         need_dh, need_dw, need_db, grad_hidden, dh_dtype, grad_weight, dw_dtype,
-                         grad_bias, token_chunks, workspace, ws_bytes, stream, 1, logp, lse);
+    return ll_forward_backward_ex(grad_logp, hidden, weight, bias, targets, N, D, V, dtype, logp,
+                                  lse, need_dh, need_dw, need_db, grad_hidden, dh_dtype,
+                                  grad_weight, dw_dtype, grad_bias, token_chunks, workspace,
+                                  ws_bytes, nullptr, stream);
 }
 
 int64_t ll_shard_segments(int64_t Vs) { return Vs > 0 ? cdiv(Vs, kSegCols) : 0; }
@@ -670,15 +744,18 @@ size_t ll_workspace_size_shard(int64_t N, int64_t D, int64_t Vs, int dtype, int 
     if (N < 0 || Vs < 1 || !dtype_ok(dtype)) return 0;
     if (N == 0) return 0;
     if (!is_backward) return local_targets_bytes(N);
-    return bwd_layout(N, Vs, dtype, token_chunks, flags & 1).total + local_targets_bytes(N);
+    return bwd_layout(N, Vs, dtype, token_chunks, flags & 1, 0, (flags >> 1) & 1).total +
+           local_targets_bytes(N);
 }
 
 int ll_forward_shard(const void* hidden, const void* weight, const void* bias,
                      const int64_t* targets, int64_t N, int64_t D, int64_t Vs, int64_t v0,
                      int64_t V, int dtype, float* part_m, float* part_s, float* zy,
-                     void* workspace, size_t ws_bytes, void* stream) {
-    int st = check_shard(Vs, v0, V);
+                     void* workspace, size_t ws_bytes, const ll_options* opt, void* stream) {
+    float it;
+    int st = read_options(opt, &it);
     if (st) return st;
+    if ((st = check_shard(Vs, v0, V))) return st;
     st = forward_checks(hidden, weight, targets, N, D, Vs, dtype);
     if (st || N == 0) return st;
     if (!part_m || !part_s || !zy) return LL_ERR_INVALID_ARG;
@@ -693,7 +770,7 @@ int ll_forward_shard(const void* hidden, const void* weight, const void* bias,
     cudaError_t e = launch_localize_targets(targets, N, v0, Vs, V, local, zy, s);
     if (e != cudaSuccess) return cuda_status(e);
     return cuda_status(forward_gemm(hidden, weight, bias, local, N, D, Vs, dtype, part_m, part_s,
-                                    zy, 1, dev, s));
+                                    zy, 1, it, dev, s));
 }
 
 int ll_lse_merge(const float* part_m, const float* part_s, int64_t n_segs, int64_t part_ld,
@@ -715,22 +792,25 @@ int ll_backward_shard(const float* grad_logp, const void* hidden, const void* we
                       int64_t D, int64_t Vs, int64_t v0, int64_t V, int dtype, int need_dh,
                       int need_dw, int need_db, void* grad_hidden, int dh_dtype,
                       void* grad_weight, int dw_dtype, void* grad_bias, int token_chunks,
-                      void* workspace, size_t ws_bytes, void* stream) {
-    int st = check_shard(Vs, v0, V);
+                      void* workspace, size_t ws_bytes, const ll_options* opt, void* stream) {
+    float it;
+    int split;
+    int st = read_options(opt, &it, &split);
     if (st) return st;
+    if ((st = check_shard(Vs, v0, V))) return st;
     if ((st = check_sizes(N, D, Vs))) return st;
     if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
     if (N == 0 || !(need_dh | need_dw | need_db))
         return backward_impl(grad_logp, hidden, weight, bias, targets, lse, N, D, Vs, dtype,
                              need_dh, need_dw, need_db, grad_hidden, dh_dtype, grad_weight,
                              dw_dtype, grad_bias, token_chunks, workspace, ws_bytes, stream, 0,
-                             nullptr, nullptr, 1);
+                             nullptr, nullptr, 1, it, split);
     if (!targets || !weight) return LL_ERR_INVALID_ARG;
     const size_t tail = local_targets_bytes(N);
     if (!workspace || ws_bytes < tail) return LL_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return LL_ERR_WORKSPACE;
     const size_t body = ws_bytes - tail;
-    const BwdLayout L = bwd_layout(N, Vs, dtype, token_chunks, need_db);
+    const BwdLayout L = bwd_layout(N, Vs, dtype, token_chunks, need_db, 0, split);
     if (body < L.total) return LL_ERR_WORKSPACE;
     // checks of backward_impl that must pass before anything is launched
     if ((need_dh | need_dw | need_db) & ~1 || token_chunks < 0) return LL_ERR_INVALID_ARG;
@@ -751,11 +831,19 @@ int ll_backward_shard(const float* grad_logp, const void* hidden, const void* we
     return backward_impl(grad_logp, hidden, weight, bias, local, lse, N, D, Vs, dtype, need_dh,
                          need_dw, need_db, grad_hidden, dh_dtype, grad_weight, dw_dtype,
                          grad_bias, token_chunks, workspace, body, stream, 0, nullptr, nullptr,
-                         1);
+                         1, it, split);
 }
 
 int logits_logp_fwd(const void* logits, int64_t ld, int dtype, const int64_t* targets, int64_t N,
                     int64_t V, float* logp, float* lse, void* stream) {
+    return logits_logp_fwd_ex(logits, ld, dtype, targets, N, V, logp, lse, nullptr, stream);
+}
+
+int logits_logp_fwd_ex(const void* logits, int64_t ld, int dtype, const int64_t* targets,
+                       int64_t N, int64_t V, float* logp, float* lse, const ll_options* opt,
+                       void* stream) {
+    float it;
+    if (read_options(opt, &it)) return LL_ERR_INVALID_ARG;
     if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
     if (N < 0 || V < 1 || V > kMaxV || ld < V || N > (int64_t(1) << 31) - 1) return LL_ERR_SHAPE;
     if (N == 0) return LL_OK;
@@ -767,13 +855,22 @@ int logits_logp_fwd(const void* logits, int64_t ld, int dtype, const int64_t* ta
     int st = device_info(guard.dev, &dev);
     if (st) return st;
     Phase ph("logits_fwd", static_cast<cudaStream_t>(stream));
-    return cuda_status(launch_logits_fwd(logits, ld, dtype, targets, N, V, logp, lse,
+    return cuda_status(launch_logits_fwd(logits, ld, dtype, targets, N, V, logp, lse, it,
                                          static_cast<cudaStream_t>(stream)));
 }
 
 int logits_logp_bwd(const float* grad_logp, const void* logits, int64_t ld, int dtype,
                     const int64_t* targets, const float* lse, int64_t N, int64_t V,
                     void* grad_logits, void* stream) {
+    return logits_logp_bwd_ex(grad_logp, logits, ld, dtype, targets, lse, N, V, grad_logits,
+                              nullptr, stream);
+}
+
+int logits_logp_bwd_ex(const float* grad_logp, const void* logits, int64_t ld, int dtype,
+                       const int64_t* targets, const float* lse, int64_t N, int64_t V,
+                       void* grad_logits, const ll_options* opt, void* stream) {
+    float it;
+    if (read_options(opt, &it)) return LL_ERR_INVALID_ARG;
     if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
     if (N < 0 || V < 1 || V > kMaxV || ld < V || N > (int64_t(1) << 31) - 1) return LL_ERR_SHAPE;
     if (N == 0) return LL_OK;
@@ -792,12 +889,22 @@ int logits_logp_bwd(const float* grad_logp, const void* logits, int64_t ld, int 
     if (st) return st;
     Phase ph("logits_bwd", static_cast<cudaStream_t>(stream));
     return cuda_status(launch_logits_bwd(grad_logp, logits, ld, dtype, targets, lse, N, V,
-                                         grad_logits, static_cast<cudaStream_t>(stream)));
+                                         grad_logits, it, static_cast<cudaStream_t>(stream)));
 }
 
 int logits_logp_fwd_bwd(const float* grad_logp, const void* logits, int64_t ld, int dtype,
                         const int64_t* targets, int64_t N, int64_t V, float* logp, float* lse,
                         void* grad_logits, void* stream) {
+    return logits_logp_fwd_bwd_ex(grad_logp, logits, ld, dtype, targets, N, V, logp, lse,
+                                  grad_logits, nullptr, stream);
+}
+
+int logits_logp_fwd_bwd_ex(const float* grad_logp, const void* logits, int64_t ld, int dtype,
+                           const int64_t* targets, int64_t N, int64_t V, float* logp,
+                           float* lse, void* grad_logits, const ll_options* opt,
+                           void* stream) {
+    float it;
+    if (read_options(opt, &it)) return LL_ERR_INVALID_ARG;
     if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
     if (N < 0 || V < 1 || V > kMaxV || ld < V || N > (int64_t(1) << 31) - 1) return LL_ERR_SHAPE;
     if (N == 0) return LL_OK;
@@ -819,7 +926,7 @@ int logits_logp_fwd_bwd(const float* grad_logp, const void* logits, int64_t ld, 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     Phase ph("logits_fused", s);
     return cuda_status(launch_logits_fused(grad_logp, logits, ld, dtype, targets, N, V, logp, lse,
-                                           grad_logits, dev, s));
+                                           grad_logits, it, dev, s));
 }
 
 int ll_check_status(void* stream) {

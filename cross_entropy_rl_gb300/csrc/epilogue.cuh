@@ -82,7 +82,7 @@ struct RowEpilogue {
     int64_t row;   // row in the M dimension of the launch
     bool rvalid;
     int64_t y;
-    float coef;    // Recomp: -grad (0 for dead rows); Dh: c[row] (0 for dead rows)
+    float coef;    // Recomp: -grad / T (0 for dead rows); Dh: c[row] (0 for dead rows)
     bool live;     // Recomp / Dh: valid target and non-zero upstream gradient
     bool onehot;   // Dh: the target column lies in this launch's vocab
     float lse2;    // Recomp: lse * log2(e)
@@ -107,7 +107,7 @@ struct RowEpilogue {
             live = rvalid && (here || (ea.shard && y == kTargetInOtherShard)) && g != 0.f;
             onehot = live && here;
             if constexpr (E == EpiKind::Recomp)
-                coef = live ? -g : 0.f;
+                coef = live ? -g * ea.inv_temp : 0.f;  // d(z / T)/dz = 1 / T
             else
                 coef = onehot ? ea.tc[row] : 0.f;
             if constexpr (E == EpiKind::Recomp) lse2 = rvalid ? ea.lse[row] * kLog2e : 0.f;
@@ -127,6 +127,10 @@ struct RowEpilogue {
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     if (col0 + j < V) v[j] += ld_elem<T>(ea.bias, col0 + j);
+            }
+            if (ea.inv_temp != 1.f) {  // the tempered logits z / T
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] *= ea.inv_temp;
             }
             if constexpr (E == EpiKind::Fwd) {
                 if (col0 + 32 > V) {
@@ -244,6 +248,20 @@ struct RowEpilogue {
             // partial rows stay within ceil(M / 32)
             if (col < ea.Ncols && (row & ~int64_t(31)) < ea.M)
                 ea.db_part[(row >> 5) * ea.Ncols + col] = v[0];
+        }
+    }
+
+    // Recomp with a hi / lo split of S: S_lo = S - S_hi, S_hi being S rounded
+    // to T (what the tile store writes), in direct row stores.  The two 16-bit
+    // parts carry S to ~2^-17 relative instead of 2^-9.
+    __device__ __forceinline__ void store_lo(const EpiArgs& ea, const float (&v)[32],
+                                             int64_t col0) {
+        if constexpr (E == EpiKind::Recomp && sizeof(T) == 2) {
+            if (!ea.S_lo || !rvalid) return;
+            float lo[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) lo[j] = v[j] - Elem<T>::to_f(Elem<T>::from_f(v[j]));
+            store_row32<T>(ea.S_lo, row * ea.ldS + col0, lo, col0, ea.Ncols, own_tag<T>());
         }
     }
 

@@ -74,6 +74,8 @@ struct KParams {
     int out16[2];        // output element of the kind is 16-bit
     int reduce[2];       // TMA reduce-add instead of store
     int64_t out_rows[2], out_cols[2];
+    int64_t k_split[2];  // 16-bit: K blocks from the first A map; later blocks read the
+                         // second A map (A_lo) at K block kb - k_split (0 = one A)
 };
 
 // ----------------------------------------------------------- bulk stores
@@ -211,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO1,
+                   const __grid_constant__ CUtensorMap tmL0, const __grid_constant__ CUtensorMap tmL1,
                    const KParams P, const EpiArgs ea0, const EpiArgs ea1) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -302,15 +305,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (lane == 0) {
                         uint8_t* sa = smem + stage * kStageBytes;
-                        const int32_t k0 = static_cast<int32_t>(kb * kBK);
+                        // a hi / lo split runs K twice: A, then A_lo, against the same B
+                        const int64_t ks = P.k_split[un.kind];
+                        const bool lo = ks > 0 && kb >= ks;
+                        const int32_t k0 = static_cast<int32_t>((lo ? kb - ks : kb) * kBK);
                         const int32_t m0 = static_cast<int32_t>(un.mb * kBM);
                         const int32_t n0 = static_cast<int32_t>(t * kBN);
                         if (NK == 1 || un.kind == 0)
-                            load_stage<K0::kAmn, K0::kBmn>(sa, &tmA0, &tmB0, &bars->full[stage],
-                                                           k0, m0, n0);
+                            load_stage<K0::kAmn, K0::kBmn>(sa, lo ? &tmL0 : &tmA0, &tmB0,
+                                                           &bars->full[stage], k0, m0, n0);
                         else
-                            load_stage<K1::kAmn, K1::kBmn>(sa, &tmA1, &tmB1, &bars->full[stage],
-                                                           k0, m0, n0);
+                            load_stage<K1::kAmn, K1::kBmn>(sa, lo ? &tmL1 : &tmA1, &tmB1,
+                                                           &bars->full[stage], k0, m0, n0);
                     }
                     __syncwarp();
                     issued[stage] = true;
@@ -460,8 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __syncwarp();
                     }
                     stage_row<T>(sb, lane, v, out16, h);
-                    if (kind == 0)  // grad_bias partials (recompute only), consumes v
-                        epi0.db_partials(ea, v, col0);
+                    if (kind == 0) {
+                        epi0.store_lo(ea, v, col0);  // hi / lo split of S (recompute only)
+                        epi0.db_partials(ea, v, col0);  // grad_bias partials, consumes v
+                    }
                     if (!out16 || h == 1) {
                         fence_proxy_async_smem();
                         __syncwarp();
@@ -1059,7 +1067,8 @@ cudaError_t launch_k(const CUtensorMap* m, const KParams& P, const EpiArgs& ea0,
     int grid = static_cast<int>(units < cap ? units : cap);
     if (grid < 1) grid = 1;
     note_launches(1);
-    kern<<<grid, kThreads, kSmemBytes, s>>>(m[0], m[1], m[2], m[3], m[4], m[5], P, ea0, ea1);
+    kern<<<grid, kThreads, kSmemBytes, s>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7], P,
+                                            ea0, ea1);
     return cudaGetLastError();
 }
 
@@ -1152,7 +1161,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
         }
         return cudaSuccess;
     }
-    CUtensorMap m[6];
+    CUtensorMap m[8];  // A, B, out of kind 0; of kind 1; A_lo of kind 0, 1
     memset(m, 0, sizeof(m));
     KParams P;
     memset(&P, 0, sizeof(P));
@@ -1167,6 +1176,15 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
         // the host sizes K blocks for the 16-bit kernel (64 values); the
         // tf32 kernel takes 16 per stage
         if (G.dtype == LL_F32) P.sh[k].k_blocks = (G.op[k].K + kBKf - 1) / kBKf;
+        if (G.op[k].A_lo) {  // hi / lo split: A_lo after A along K
+            if (G.dtype == LL_F32) return cudaErrorInvalidValue;
+            GemmOperands lo = G.op[k];
+            lo.A = lo.A_lo;
+            CUtensorMap unused;
+            if (!operand_maps(lo, G.dtype, &m[6 + k], &unused)) return cudaErrorInvalidValue;
+            P.k_split[k] = P.sh[k].k_blocks;
+            P.sh[k].k_blocks *= 2;
+        }
         P.n_units[k] = G.shape[k].m_blocks * G.shape[k].n_segs;
         P.out16[k] = G.out[k].dtype != LL_F32;
         P.out_rows[k] = G.out[k].rows;
@@ -1182,6 +1200,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
         m[3] = m[0];
         m[4] = m[1];
         m[5] = m[2];
+        m[7] = m[6];
+        P.k_split[1] = P.k_split[0];
     }
     P.dynamic = G.counter != nullptr;
     P.counter = G.counter;

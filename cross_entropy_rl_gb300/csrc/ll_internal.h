@@ -42,19 +42,21 @@ uint64_t wait_limit_ns();
 void note_launches(int n);
 
 // --- logits-input kernels (logits_kernels.cu) --------------------------------
+// inv_temp: the logits are scaled by 1 / temperature (1 = none).
 cudaError_t launch_logits_fwd(const void* logits, int64_t ld, int dtype, const int64_t* targets,
-                              int64_t N, int64_t V, float* logp, float* lse, cudaStream_t s);
+                              int64_t N, int64_t V, float* logp, float* lse, float inv_temp,
+                              cudaStream_t s);
 cudaError_t launch_logits_bwd(const float* grad, const void* logits, int64_t ld, int dtype,
                               const int64_t* targets, const float* lse, int64_t N, int64_t V,
-                              void* grad_logits, cudaStream_t s);
+                              void* grad_logits, float inv_temp, cudaStream_t s);
 
 // Logits forward + backward in one pass for a known upstream gradient
 // (logits_kernels.cu): per row the forward then the backward, bitwise the
 // results of the two kernels; grad_logits may be the logits buffer.
 cudaError_t launch_logits_fused(const float* grad, const void* logits, int64_t ld, int dtype,
                                 const int64_t* targets, int64_t N, int64_t V, float* logp,
-                                float* lse, void* grad_logits, const DevInfo& dev,
-                                cudaStream_t s);
+                                float* lse, void* grad_logits, float inv_temp,
+                                const DevInfo& dev, cudaStream_t s);
 
 // --- GEMM-based linear path -------------------------------------------------
 enum class EpiKind : int { Fwd = 0, Recomp = 1, Dh = 2, Dw = 3 };
@@ -97,6 +99,9 @@ struct EpiArgs {
     int* status;
     uint64_t wait_ns;
     int shard;               // targets may be kTargetInOtherShard (vocab shard)
+    float inv_temp;          // Fwd / Recomp: logits scaled by 1 / temperature (1 = none)
+    void* S_lo;              // Recomp, 16-bit: S - S_hi (the rounding rest of S) [M, ldS],
+                             //   or nullptr (no hi / lo split)
 };
 
 struct GemmShape {
@@ -124,6 +129,8 @@ struct GemmOperands {
     int64_t ldb;
     int b_mn;
     int64_t M, N, K;
+    const void* A_lo;  // 16-bit only: a second A of A's layout; the contraction then
+                       // runs over K twice, A then A_lo, against the same B (nullptr: no)
 };
 
 // Tile output written by the epilogue ([rows, cols], row stride ld).
@@ -192,7 +199,7 @@ cudaError_t launch_fill_zero(void* p, int64_t n_elems, int dtype, cudaStream_t s
 cudaError_t launch_softmax_part(const float* Z, int64_t ldZ, int64_t rows, int64_t V,
                                 const int64_t* targets, const float* grad, const float* lse,
                                 void* S, int64_t ldS, int s_dtype, float* tc, float* db_part,
-                                cudaStream_t s);
+                                float inv_temp, void* S_lo, cudaStream_t s);
 cudaError_t launch_unsatisfied_wait(int* flag, int* status, uint64_t wait_ns, cudaStream_t s);
 
 }  // namespace ll

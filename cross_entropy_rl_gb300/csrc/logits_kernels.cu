@@ -65,6 +65,7 @@ __device__ __forceinline__ void ms_fold1(MS& st, float z) {
 
 // Block-wide combine in a fixed order: butterfly within each warp (lane 0's
 // value is used), then warp results in ascending warp order by thread 0.
+template <int NT = kThreads>
 __device__ __forceinline__ MS block_reduce(MS st, MS* sh) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -78,18 +79,41 @@ __device__ __forceinline__ MS block_reduce(MS st, MS* sh) {
     __syncthreads();
     MS r = {-INFINITY, 0.f};
     if (threadIdx.x == 0) {
-        for (int w = 0; w < kWarps; ++w) r = ms_combine(r, sh[w]);
+        for (int w = 0; w < NT / 32; ++w) r = ms_combine(r, sh[w]);
     }
     return r;
 }
 
-// Plain or L2-hinted 8-element access (HINT selects the policy versions).
+// 8 elements as loaded (16-bit types: one 16-byte vector, kept packed until
+// used, so a deep unroll costs 4 registers per vector; float: two vectors).
+template <typename T>
+struct Raw8 {
+    uint4 a, b;  // b unused for 16-bit types
+};
 template <typename T, bool HINT>
-__device__ __forceinline__ void ld8(const T* p, float (&f)[8], uint64_t pol) {
-    if constexpr (HINT)
-        load8_hint(p, f, pol);
-    else
-        load8(p, f);
+__device__ __forceinline__ Raw8<T> ld_raw(const T* p, uint64_t pol) {
+    Raw8<T> r;
+    if constexpr (HINT) {
+        r.a = ld16_hint(p, pol);
+        if constexpr (sizeof(T) == 4) r.b = ld16_hint(p + 4, pol);
+    } else {
+        r.a = *reinterpret_cast<const uint4*>(p);
+        if constexpr (sizeof(T) == 4) r.b = *reinterpret_cast<const uint4*>(p + 4);
+    }
+    return r;
+}
+template <typename T>
+__device__ __forceinline__ void unpack(const Raw8<T>& r, float (&f)[8]) {
+    if constexpr (sizeof(T) == 4) {
+        f[0] = __uint_as_float(r.a.x); f[1] = __uint_as_float(r.a.y);
+        f[2] = __uint_as_float(r.a.z); f[3] = __uint_as_float(r.a.w);
+        f[4] = __uint_as_float(r.b.x); f[5] = __uint_as_float(r.b.y);
+        f[6] = __uint_as_float(r.b.z); f[7] = __uint_as_float(r.b.w);
+    } else {
+        const T* e = reinterpret_cast<const T*>(&r.a);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = Elem<T>::to_f(e[j]);
+    }
 }
 template <typename T, bool HINT>
 __device__ __forceinline__ void st8(T* p, const float (&f)[8], uint64_t pol) {
@@ -99,31 +123,45 @@ __device__ __forceinline__ void st8(T* p, const float (&f)[8], uint64_t pol) {
         store8(p, f);
 }
 
+__device__ __forceinline__ void scale8(float (&f)[8], float it) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] *= it;
+}
+
 // This thread's (max, sum-exp) of row x: 8-element vectors tid, tid + T,
 // tid + 2T, ... (T = block size) in that order, U of them loaded at a time
 // (the order, hence the result, does not depend on U), then the scalar tail.
-template <typename T, int U, bool HINT>
-__device__ __forceinline__ MS row_partial(const T* x, int64_t V, int vec_ok, uint64_t pol) {
+// it = 1 / temperature: the fold sees the tempered logits x * it (exact for it = 1).
+template <typename T, int U, bool HINT, int NT = kThreads>
+__device__ __forceinline__ MS row_partial(const T* x, int64_t V, int vec_ok, uint64_t pol,
+                                          float it) {
     MS st = {-INFINITY, 0.f};
     int64_t done = 0;
     if (vec_ok) {
         const int64_t nvec = V / 8;
         int64_t i = threadIdx.x;
-        for (; i + (U - 1) * kThreads < nvec; i += U * kThreads) {
-            float f[U][8];
+        for (; i + (U - 1) * NT < nvec; i += U * NT) {
+            Raw8<T> r[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) ld8<T, HINT>(x + (i + u * kThreads) * 8, f[u], pol);
+            for (int u = 0; u < U; ++u) r[u] = ld_raw<T, HINT>(x + (i + u * NT) * 8, pol);
 #pragma unroll
-            for (int u = 0; u < U; ++u) ms_fold8(st, f[u]);
+            for (int u = 0; u < U; ++u) {
+                float f[8];
+                unpack(r[u], f);
+                scale8(f, it);
+                ms_fold8(st, f);
+            }
         }
-        for (; i < nvec; i += kThreads) {
+        for (; i < nvec; i += NT) {
             float f[8];
-            ld8<T, HINT>(x + i * 8, f, pol);
+            unpack(ld_raw<T, HINT>(x + i * 8, pol), f);
+            scale8(f, it);
             ms_fold8(st, f);
         }
         done = nvec * 8;
     }
-    for (int64_t j = done + threadIdx.x; j < V; j += kThreads) ms_fold1(st, Elem<T>::to_f(x[j]));
+    for (int64_t j = done + threadIdx.x; j < V; j += NT)
+        ms_fold1(st, Elem<T>::to_f(x[j]) * it);
     return st;
 }
 
@@ -140,43 +178,48 @@ __device__ __forceinline__ float grad_elem(float z, int64_t c, int64_t y, float 
 
 // Gradient row o = g * (onehot(y) - exp(x - lse)) (all +0 when !live); each
 // thread reads a vector of x and writes the same vector of o, so o may be x.
-template <typename T, int U, bool HINT>
+// With a temperature (it = 1 / T) the caller passes g * it and the tempered
+// lse; the logits are scaled by it here.
+template <typename T, int U, bool HINT, int NT = kThreads>
 __device__ __forceinline__ void row_grad(const T* x, T* o, int64_t V, int vec_ok, int64_t y,
                                          float g, bool live, float lse2, uint64_t pol_ld,
-                                         uint64_t pol_st) {
+                                         uint64_t pol_st, float it) {
     int64_t done = 0;
     if (vec_ok) {
         const int64_t nvec = V / 8;
         if (!live) {
             const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int64_t i = threadIdx.x; i < nvec; i += kThreads) st8<T, HINT>(o + i * 8, z, pol_st);
+            for (int64_t i = threadIdx.x; i < nvec; i += NT) st8<T, HINT>(o + i * 8, z, pol_st);
         } else {
             int64_t i = threadIdx.x;
-            for (; i + (U - 1) * kThreads < nvec; i += U * kThreads) {
-                float f[U][8];
+            for (; i + (U - 1) * NT < nvec; i += U * NT) {
+                Raw8<T> r[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u) ld8<T, HINT>(x + (i + u * kThreads) * 8, f[u], pol_ld);
+                for (int u = 0; u < U; ++u)
+                    r[u] = ld_raw<T, HINT>(x + (i + u * NT) * 8, pol_ld);
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
-                    const int64_t c0 = (i + u * kThreads) * 8;
+                    const int64_t c0 = (i + u * NT) * 8;
+                    float f[8];
+                    unpack(r[u], f);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) f[u][j] = grad_elem(f[u][j], c0 + j, y, g, lse2);
-                    st8<T, HINT>(o + c0, f[u], pol_st);
+                    for (int j = 0; j < 8; ++j) f[j] = grad_elem(f[j] * it, c0 + j, y, g, lse2);
+                    st8<T, HINT>(o + c0, f, pol_st);
                 }
             }
-            for (; i < nvec; i += kThreads) {
+            for (; i < nvec; i += NT) {
                 float f[8];
                 const int64_t c0 = i * 8;
-                ld8<T, HINT>(x + c0, f, pol_ld);
+                unpack(ld_raw<T, HINT>(x + c0, pol_ld), f);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) f[j] = grad_elem(f[j], c0 + j, y, g, lse2);
+                for (int j = 0; j < 8; ++j) f[j] = grad_elem(f[j] * it, c0 + j, y, g, lse2);
                 st8<T, HINT>(o + c0, f, pol_st);
             }
         }
         done = nvec * 8;
     }
-    for (int64_t j = done + threadIdx.x; j < V; j += kThreads) {
-        const float v = live ? grad_elem(Elem<T>::to_f(x[j]), j, y, g, lse2) : 0.f;
+    for (int64_t j = done + threadIdx.x; j < V; j += NT) {
+        const float v = live ? grad_elem(Elem<T>::to_f(x[j]) * it, j, y, g, lse2) : 0.f;
         o[j] = Elem<T>::from_f(v);
     }
 }
@@ -187,16 +230,16 @@ __global__ void __launch_bounds__(kThreads) logits_fwd_kernel(const T* __restric
                                                               const int64_t* __restrict__ targets,
                                                               int64_t V, float* __restrict__ logp,
                                                               float* __restrict__ lse_out,
-                                                              int vec_ok) {
+                                                              int vec_ok, float it) {
     __shared__ MS sh[kWarps];
     const int64_t row = blockIdx.x;
     const T* x = logits + row * ld;
-    const MS r = block_reduce(row_partial<T, kUnroll, false>(x, V, vec_ok, 0), sh);
+    const MS r = block_reduce(row_partial<T, kUnroll, false>(x, V, vec_ok, 0, it), sh);
     if (threadIdx.x == 0) {
         const float lse = lse_of(r);
         const int64_t y = targets[row];
         const bool valid = (y >= 0) && (y < V);
-        logp[row] = valid ? Elem<T>::to_f(x[y]) - lse : 0.f;
+        logp[row] = valid ? Elem<T>::to_f(x[y]) * it - lse : 0.f;
         lse_out[row] = lse;
     }
 }
@@ -205,13 +248,13 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) logits_bwd_kernel(
     const float* __restrict__ grad, const T* __restrict__ logits, int64_t ld,
     const int64_t* __restrict__ targets, const float* __restrict__ lse, int64_t V,
-    T* __restrict__ out, int vec_ok) {
+    T* __restrict__ out, int vec_ok, float it) {
     const int64_t row = blockIdx.x;
     const int64_t y = targets[row];
     const float g = grad[row];
     const bool live = (y >= 0) && (y < V) && (g != 0.f);
-    row_grad<T, kUnroll, false>(logits + row * ld, out + row * ld, V, vec_ok, y, g, live,
-                                lse[row] * kLog2e, 0, 0);
+    row_grad<T, kUnroll, false>(logits + row * ld, out + row * ld, V, vec_ok, y, g * it, live,
+                                lse[row] * kLog2e, 0, 0, it);
 }
 
 // Forward and backward of each row in turn (a known upstream gradient): the
@@ -222,29 +265,41 @@ __global__ void __launch_bounds__(kThreads) logits_bwd_kernel(
 // and the gradient stores release theirs (evict_first).  The row code is the
 // one of logits_fwd_kernel and logits_bwd_kernel, so every result is bitwise
 // theirs.  grad_logits may be the logits buffer itself.
-template <typename T, int U>
-__global__ void __launch_bounds__(kThreads) logits_fwd_bwd_kernel(
+// Ask L2 for the 128-byte lines of [p, p + bytes), spread over the block.
+template <int NT>
+__device__ __forceinline__ void prefetch_l2(const void* p, int64_t bytes) {
+    const char* c = static_cast<const char*>(p);
+    for (int64_t o = int64_t(threadIdx.x) * 128; o < bytes; o += int64_t(NT) * 128)
+        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(c + o));
+}
+
+template <typename T, int U, bool PF = false, int NT = kThreads>
+__global__ void __launch_bounds__(NT) logits_fwd_bwd_kernel(
     const float* __restrict__ grad, const T* logits, int64_t ld,
     const int64_t* __restrict__ targets, int64_t N, int64_t V, float* __restrict__ logp,
-    float* __restrict__ lse_out, T* out, int vec_ok) {
-    __shared__ MS sh[kWarps];
+    float* __restrict__ lse_out, T* out, int vec_ok, float it) {
+    __shared__ MS sh[NT / 32];
     __shared__ float lse_sh;
     const uint64_t keep = l2_evict_last(), drop = l2_evict_first();
+    const int64_t row_bytes = V * int64_t(sizeof(T));
+    if (PF && blockIdx.x < N) prefetch_l2<NT>(logits + blockIdx.x * ld, row_bytes);
     for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
         const T* x = logits + row * ld;
-        const MS r = block_reduce(row_partial<T, U, true>(x, V, vec_ok, keep), sh);
+        const MS r = block_reduce<NT>(row_partial<T, U, true, NT>(x, V, vec_ok, keep, it), sh);
+        // the next row of this block streams into L2 during this row's second pass
+        if (PF && row + gridDim.x < N) prefetch_l2<NT>(logits + (row + gridDim.x) * ld, row_bytes);
         const int64_t y = targets[row];
         const float g = grad[row];
         const bool valid = (y >= 0) && (y < V);
         if (threadIdx.x == 0) {
             const float lse = lse_of(r);
-            logp[row] = valid ? Elem<T>::to_f(x[y]) - lse : 0.f;
+            logp[row] = valid ? Elem<T>::to_f(x[y]) * it - lse : 0.f;
             lse_out[row] = lse;
             lse_sh = lse;
         }
         __syncthreads();  // lse_sh; also thread 0 is done with sh and x[y]
-        row_grad<T, U, true>(x, out + row * ld, V, vec_ok, y, g, valid && g != 0.f,
-                             lse_sh * kLog2e, drop, drop);
+        row_grad<T, U, true, NT>(x, out + row * ld, V, vec_ok, y, g * it, valid && g != 0.f,
+                             lse_sh * kLog2e, drop, drop, it);
     }
 }
 
@@ -256,31 +311,32 @@ bool vec_ok(const void* p, int64_t ld) {
 }  // namespace
 
 cudaError_t launch_logits_fwd(const void* logits, int64_t ld, int dtype, const int64_t* targets,
-                              int64_t N, int64_t V, float* logp, float* lse, cudaStream_t s) {
+                              int64_t N, int64_t V, float* logp, float* lse, float it,
+                              cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>(N));
     note_launches(1);
     switch (dtype) {
         case LL_BF16:
             logits_fwd_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
                 static_cast<const __nv_bfloat16*>(logits), ld, targets, V, logp, lse,
-                vec_ok<__nv_bfloat16>(logits, ld));
+                vec_ok<__nv_bfloat16>(logits, ld), it);
             break;
         case LL_F16:
             logits_fwd_kernel<__half><<<grid, kThreads, 0, s>>>(
                 static_cast<const __half*>(logits), ld, targets, V, logp, lse,
-                vec_ok<__half>(logits, ld));
+                vec_ok<__half>(logits, ld), it);
             break;
         default:
             logits_fwd_kernel<float><<<grid, kThreads, 0, s>>>(
                 static_cast<const float*>(logits), ld, targets, V, logp, lse,
-                vec_ok<float>(logits, ld));
+                vec_ok<float>(logits, ld), it);
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_logits_bwd(const float* grad, const void* logits, int64_t ld, int dtype,
                               const int64_t* targets, const float* lse, int64_t N, int64_t V,
-                              void* grad_logits, cudaStream_t s) {
+                              void* grad_logits, float it, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>(N));
     note_launches(1);
     switch (dtype) {
@@ -288,21 +344,21 @@ cudaError_t launch_logits_bwd(const float* grad, const void* logits, int64_t ld,
             const int ok = vec_ok<__nv_bfloat16>(logits, ld) && vec_ok<__nv_bfloat16>(grad_logits, ld);
             logits_bwd_kernel<__nv_bfloat16><<<grid, kThreads, 0, s>>>(
                 grad, static_cast<const __nv_bfloat16*>(logits), ld, targets, lse, V,
-                static_cast<__nv_bfloat16*>(grad_logits), ok);
+                static_cast<__nv_bfloat16*>(grad_logits), ok, it);
             break;
         }
         case LL_F16: {
             const int ok = vec_ok<__half>(logits, ld) && vec_ok<__half>(grad_logits, ld);
             logits_bwd_kernel<__half><<<grid, kThreads, 0, s>>>(
                 grad, static_cast<const __half*>(logits), ld, targets, lse, V,
-                static_cast<__half*>(grad_logits), ok);
+                static_cast<__half*>(grad_logits), ok, it);
             break;
         }
         default: {
             const int ok = vec_ok<float>(logits, ld) && vec_ok<float>(grad_logits, ld);
             logits_bwd_kernel<float><<<grid, kThreads, 0, s>>>(
                 grad, static_cast<const float*>(logits), ld, targets, lse, V,
-                static_cast<float*>(grad_logits), ok);
+                static_cast<float*>(grad_logits), ok, it);
         }
     }
     return cudaGetLastError();
@@ -314,7 +370,7 @@ constexpr int kFusedUnroll = 8;
 
 cudaError_t launch_logits_fused(const float* grad, const void* logits, int64_t ld, int dtype,
                                 const int64_t* targets, int64_t N, int64_t V, float* logp,
-                                float* lse, void* grad_logits, const DevInfo& dev,
+                                float* lse, void* grad_logits, float it, const DevInfo& dev,
                                 cudaStream_t s) {
     int64_t blocks = int64_t(dev.num_sms) * kFusedBlocksPerSm;
     if (blocks > N) blocks = N;
@@ -325,21 +381,21 @@ cudaError_t launch_logits_fused(const float* grad, const void* logits, int64_t l
             const int ok = vec_ok<__nv_bfloat16>(logits, ld) && vec_ok<__nv_bfloat16>(grad_logits, ld);
             logits_fwd_bwd_kernel<__nv_bfloat16, kFusedUnroll><<<grid, kThreads, 0, s>>>(
                 grad, static_cast<const __nv_bfloat16*>(logits), ld, targets, N, V, logp, lse,
-                static_cast<__nv_bfloat16*>(grad_logits), ok);
+                static_cast<__nv_bfloat16*>(grad_logits), ok, it);
             break;
         }
         case LL_F16: {
             const int ok = vec_ok<__half>(logits, ld) && vec_ok<__half>(grad_logits, ld);
             logits_fwd_bwd_kernel<__half, kFusedUnroll><<<grid, kThreads, 0, s>>>(
                 grad, static_cast<const __half*>(logits), ld, targets, N, V, logp, lse,
-                static_cast<__half*>(grad_logits), ok);
+                static_cast<__half*>(grad_logits), ok, it);
             break;
         }
         default: {
             const int ok = vec_ok<float>(logits, ld) && vec_ok<float>(grad_logits, ld);
             logits_fwd_bwd_kernel<float, kFusedUnroll><<<grid, kThreads, 0, s>>>(
                 grad, static_cast<const float*>(logits), ld, targets, N, V, logp, lse,
-                static_cast<float*>(grad_logits), ok);
+                static_cast<float*>(grad_logits), ok, it);
         }
     }
     return cudaGetLastError();

@@ -56,7 +56,8 @@ def _impl(impl):
     return binding
 
 
-def forward(hidden, weight, bias, targets, v0: int, V: int, group=None, impl=None):
+def forward(hidden, weight, bias, targets, v0: int, V: int, group=None, impl=None,
+            temperature=1.0):
     """(logp, lse) [N] of the whole vocab on every rank of `group`.
 
     weight / bias: this rank's shard rows (weight.shape[0] may be 0 for an
@@ -75,7 +76,7 @@ def forward(hidden, weight, bias, targets, v0: int, V: int, group=None, impl=Non
     zy = torch.full((N,), -float("inf"), dtype=torch.float32, device=dev)
     if Vs > 0 and N > 0:
         S = -(-Vs // SEGMENT_COLS)
-        f.forward_shard(hidden, weight, bias, targets, v0, V,
+        f.forward_shard(hidden, weight, bias, targets, v0, V, temperature=temperature,
                         out=(part_m[:S], part_s[:S], zy))
     gm = [torch.empty_like(part_m) for _ in range(world)]
     gs = [torch.empty_like(part_s) for _ in range(world)]
@@ -88,7 +89,7 @@ def forward(hidden, weight, bias, targets, v0: int, V: int, group=None, impl=Non
 
 
 def backward(grad_logp, hidden, weight, bias, targets, lse, v0: int, V: int, group=None,
-             impl=None, need_db=None, token_chunks=0):
+             impl=None, need_db=None, token_chunks=0, temperature=1.0):
     """(grad_hidden [N, D] float32, equal on every rank; this shard's
     grad_weight rows; its grad_bias rows or None)."""
     import torch
@@ -100,7 +101,8 @@ def backward(grad_logp, hidden, weight, bias, targets, lse, v0: int, V: int, gro
         need_db = bias is not None
     if Vs > 0:
         dh, dW, db = f.backward_shard(grad_logp, hidden, weight, bias, targets, lse, v0, V,
-                                      need_db=need_db, token_chunks=token_chunks)
+                                      need_db=need_db, token_chunks=token_chunks,
+                                      temperature=temperature)
     else:
         dh = torch.zeros(N, D, dtype=torch.float32, device=hidden.device)
         dW = torch.zeros(0, D, dtype=torch.float32, device=hidden.device)

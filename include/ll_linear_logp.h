@@ -68,6 +68,37 @@ typedef enum {
 
 typedef enum { LL_F32 = 0, LL_F16 = 1, LL_BF16 = 2 } ll_dtype;
 
+/*
+ * Per-call options of the *_ex entry points (and of the vocab-shard calls).
+ * A NULL pointer means every default.  An entry point without _ex is its
+ * _ex form with NULL.
+ *   temperature  > 0 and finite; default 1.  The distribution is
+ *                softmax(z / T): logp = z[y] / T - logsumexp(z / T), lse is
+ *                that of z / T, and every gradient carries the 1 / T factor
+ *                of d(z / T)/dz (the sampling temperature of RL rollouts;
+ *                RL-Kernel PR #495, the vLLM provider evidence at
+ *                temperatures 1.0 and 0.7).  T = 1 gives bitwise the
+ *                results of the calls without options.
+ *   split_s      0 or 1; backward with 16-bit operands: the off-target part
+ *                S = -grad_logp * p / T of g is stored as a hi / lo pair of
+ *                the operand dtype (S_hi = S rounded, S_lo = S - S_hi
+ *                rounded) and the grad_hidden / grad_weight contractions run
+ *                over both, twice their work: S is then carried to ~2^-17
+ *                relative instead of 2^-9, which matters for peaked
+ *                distributions whose large off-target probabilities would
+ *                otherwise lose 2^-9 * |grad| at that entry.  The workspace
+ *                grows by one more S buffer (flags bit 1 of
+ *                ll_workspace_size).  Ignored for FP32 operands (S is FP32).
+ *   reserved     must be 0.
+ * A bad temperature, split_s not 0 / 1 or a non-zero reserved field is
+ * LL_ERR_INVALID_ARG.
+ */
+typedef struct {
+    float temperature;
+    int split_s;
+    int reserved[6];
+} ll_options;
+
 /* Human-readable name of a status code (static storage). */
 const char* ll_status_string(int status);
 
@@ -77,8 +108,9 @@ int ll_version(void);
 /*
  * Workspace bytes needed by ll_forward (is_backward = 0), ll_backward
  * (is_backward = 1) or ll_forward_backward (is_backward = 2) for these
- * sizes; `flags` is the need_db flag for the backward (bias gradient
- * partials) and ignored for the forward.
+ * sizes; `flags` bit 0 is the need_db flag of the backward (bias gradient
+ * partials), bit 1 the split_s option (ll_options); both are ignored for
+ * the forward.
  * token_chunks: number of token chunks the backward splits N into (0 =
  * automatic, see ll_backward).  Returns 0 only for N == 0 in the forward.
  * The workspace pointer must be 256-byte aligned.
@@ -149,6 +181,28 @@ int ll_forward_backward(const float* grad_logp, const void* hidden, const void* 
                         void* grad_weight, int dw_dtype, void* grad_bias, int token_chunks,
                         void* workspace, size_t ws_bytes, void* stream);
 
+/* ll_forward, ll_backward and ll_forward_backward with options (see
+ * ll_options); same workspaces. */
+int ll_forward_ex(const void* hidden, const void* weight, const void* bias,
+                  const int64_t* targets, int64_t N, int64_t D, int64_t V, int dtype,
+                  float* logp, float* lse, void* workspace, size_t ws_bytes,
+                  const ll_options* opt, void* stream);
+int ll_backward_ex(const float* grad_logp, const void* hidden, const void* weight,
+                   const void* bias, const int64_t* targets, const float* lse,
+                   int64_t N, int64_t D, int64_t V, int dtype,
+                   int need_dh, int need_dw, int need_db,
+                   void* grad_hidden, int dh_dtype,
+                   void* grad_weight, int dw_dtype,
+                   void* grad_bias, int token_chunks,
+                   void* workspace, size_t ws_bytes, const ll_options* opt, void* stream);
+int ll_forward_backward_ex(const float* grad_logp, const void* hidden, const void* weight,
+                           const void* bias, const int64_t* targets, int64_t N, int64_t D,
+                           int64_t V, int dtype, float* logp, float* lse, int need_dh,
+                           int need_dw, int need_db, void* grad_hidden, int dh_dtype,
+                           void* grad_weight, int dw_dtype, void* grad_bias,
+                           int token_chunks, void* workspace, size_t ws_bytes,
+                           const ll_options* opt, void* stream);
+
 /*
  * Vocab-parallel (tensor-parallel) pieces: the vocab split over ranks into
  * contiguous shards [v0, v0 + Vs) (RL-Kernel PR #495, the coordinated
@@ -171,7 +225,8 @@ int ll_forward_backward(const float* grad_logp, const void* hidden, const void* 
 int64_t ll_shard_segments(int64_t Vs);
 
 /* Workspace bytes of ll_forward_shard (is_backward = 0) or
- * ll_backward_shard (is_backward = 1; flags = need_db), 256-byte aligned. */
+ * ll_backward_shard (is_backward = 1; flags as for ll_workspace_size),
+ * 256-byte aligned. */
 size_t ll_workspace_size_shard(int64_t N, int64_t D, int64_t Vs, int dtype, int token_chunks,
                                int is_backward, int flags);
 
@@ -188,7 +243,8 @@ size_t ll_workspace_size_shard(int64_t N, int64_t D, int64_t Vs, int dtype, int 
 int ll_forward_shard(const void* hidden, const void* weight, const void* bias,
                      const int64_t* targets, int64_t N, int64_t D, int64_t Vs, int64_t v0,
                      int64_t V, int dtype, float* part_m, float* part_s, float* zy,
-                     void* workspace, size_t ws_bytes, void* stream);
+                     void* workspace, size_t ws_bytes, const ll_options* opt,
+                     void* stream);
 
 /*
  * Ordered merge of whole-vocab segment partials: lse[n] = M + log sum_j
@@ -220,7 +276,8 @@ int ll_backward_shard(const float* grad_logp, const void* hidden, const void* we
                       int64_t D, int64_t Vs, int64_t v0, int64_t V, int dtype, int need_dh,
                       int need_dw, int need_db, void* grad_hidden, int dh_dtype,
                       void* grad_weight, int dw_dtype, void* grad_bias, int token_chunks,
-                      void* workspace, size_t ws_bytes, void* stream);
+                      void* workspace, size_t ws_bytes, const ll_options* opt,
+                      void* stream);
 
 /*
  * Forward without a caller workspace.  No counterpart on the source pages:
@@ -277,6 +334,18 @@ int logits_logp_bwd(const float* grad_logp, const void* logits, int64_t ld, int 
 int logits_logp_fwd_bwd(const float* grad_logp, const void* logits, int64_t ld, int dtype,
                         const int64_t* targets, int64_t N, int64_t V, float* logp, float* lse,
                         void* grad_logits, void* stream);
+
+/* The logits-input calls with options (see ll_options). */
+int logits_logp_fwd_ex(const void* logits, int64_t ld, int dtype, const int64_t* targets,
+                       int64_t N, int64_t V, float* logp, float* lse, const ll_options* opt,
+                       void* stream);
+int logits_logp_bwd_ex(const float* grad_logp, const void* logits, int64_t ld, int dtype,
+                       const int64_t* targets, const float* lse, int64_t N, int64_t V,
+                       void* grad_logits, const ll_options* opt, void* stream);
+int logits_logp_fwd_bwd_ex(const float* grad_logp, const void* logits, int64_t ld, int dtype,
+                           const int64_t* targets, int64_t N, int64_t V, float* logp,
+                           float* lse, void* grad_logits, const ll_options* opt,
+                           void* stream);
 
 /*
  * Device status word of the current device: synchronises `stream`, returns

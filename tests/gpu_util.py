@@ -59,8 +59,8 @@ def ulp(ref, tdtype):
     return np.exp2(e - m)
 
 
-def s_rounding_bounds(p):
-    """Worst-case effect of storing S = -grad * p (off-target) in 16 bits."""
+def s_rounding_bounds(p, temperature=1.0):
+    """Worst-case effect of storing S = -grad * p / T (off-target) in 16 bits."""
     import oracle as O
 
     dt = p["dtype"]
@@ -68,9 +68,9 @@ def s_rounding_bounds(p):
         return {}
     u = 2.0 ** -8 if dt == "bf16" else 2.0 ** -11
     h, W, b = O.decode(p["h"], dt), O.decode(p["W"], dt), O.decode(p["b"], dt)
-    z = O.linear_logits(h, W, b)
+    z = O.linear_logits(h, W, b) / temperature
     lse = O.logsumexp_rows(z)
-    S = np.abs(np.asarray(p["gl"], np.float64))[:, None] * np.exp(z - lse[:, None])
+    S = np.abs(np.asarray(p["gl"], np.float64))[:, None] * np.exp(z - lse[:, None]) / temperature
     y = np.asarray(p["y"])
     V = W.shape[0]
     ok = (y >= 0) & (y < V) & (np.asarray(p["gl"]) != 0)

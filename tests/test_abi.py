@@ -153,3 +153,21 @@ def test_binding_fails_loudly_without_library(tmp_path):
             mod.load(str(tmp_path / "missing.so"))
     finally:
         importlib.reload(ll)
+
+
+def test_options_are_validated_before_any_device_work(L):
+    """A bad temperature or a non-zero reserved field is LL_ERR_INVALID_ARG,
+    returned before any pointer is touched (all pointers here are NULL)."""
+    for T in (0.0, -1.0, float("inf"), float("nan")):
+        o = ll.Options(temperature=T)
+        assert L.ll_forward_ex(None, None, None, None, 4, 8, 16, ll.LL_BF16, None, None, None,
+                               0, ctypes.byref(o), None) == 1
+        assert L.logits_logp_fwd_ex(None, 16, ll.LL_BF16, None, 4, 16, None, None,
+                                    ctypes.byref(o), None) == 1
+    o = ll.Options(temperature=1.0)
+    o.reserved[3] = 7
+    assert L.ll_backward_ex(None, None, None, None, None, None, 4, 8, 16, ll.LL_BF16, 1, 1, 0,
+                            None, ll.LL_BF16, None, ll.LL_F32, None, 0, None, 0,
+                            ctypes.byref(o), None) == 1
+    with pytest.raises(ValueError, match="temperature"):
+        ll._opts(-2.0)

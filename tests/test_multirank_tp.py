@@ -24,14 +24,14 @@ class OracleShards:
     with the ABI's semantics (partials per 1024-column segment, -inf zy
     outside the shard, ascending-order merge)."""
 
-    def forward_shard(self, hidden, weight, bias, targets, v0, V, out):
+    def forward_shard(self, hidden, weight, bias, targets, v0, V, out, temperature=1.0):
         import oracle
 
         part_m, part_s, zy = out
         h = hidden.double().numpy()
         W = weight.double().numpy()
         b = None if bias is None else bias.double().numpy()
-        z = oracle.linear_logits(h, W, b) * LOG2E
+        z = oracle.linear_logits(h, W, b) / temperature * LOG2E
         Vs = W.shape[0]
         for j in range(-(-Vs // tp.SEGMENT_COLS)):
             seg = z[:, j * tp.SEGMENT_COLS:(j + 1) * tp.SEGMENT_COLS]
@@ -58,13 +58,13 @@ class OracleShards:
         return torch.from_numpy(logp), torch.from_numpy(lse)
 
     def backward_shard(self, grad_logp, hidden, weight, bias, targets, lse, v0, V, need_db,
-                       token_chunks):
+                       token_chunks, temperature=1.0):
         import oracle
 
         h = hidden.double().numpy()
         W = weight.double().numpy()
         b = None if bias is None else bias.double().numpy()
-        z = oracle.linear_logits(h, W, b)
+        z = oracle.linear_logits(h, W, b) / temperature
         p = np.exp(z - lse.double().numpy()[:, None])
         y = targets.numpy()
         gl = grad_logp.double().numpy()
@@ -72,7 +72,7 @@ class OracleShards:
         onehot = np.zeros_like(p)
         mine = np.nonzero((y >= v0) & (y < v0 + Vs))[0]
         onehot[mine, y[mine] - v0] = 1.0
-        g = gl[:, None] * (onehot - p)
+        g = gl[:, None] * (onehot - p) / temperature
         g[(y < 0) | (y >= V)] = 0.0
         db = torch.from_numpy(g.sum(axis=0)) if need_db else None
         return torch.from_numpy(g @ W), torch.from_numpy(g.T @ h), db
@@ -97,7 +97,7 @@ def _inputs():
     return p, y
 
 
-def _worker(rank, world, port, out_dir):
+def _worker(rank, world, port, out_dir, T=1.0):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world,
                             timeout=__import__("datetime").timedelta(seconds=30))
@@ -110,8 +110,9 @@ def _worker(rank, world, port, out_dir):
         gl = torch.from_numpy(p["gl"])
         v0, v1 = tp.shard_bounds(V, world)[rank]
         impl = OracleShards()
-        logp, lse = tp.forward(h, W[v0:v1], b[v0:v1], yt, v0, V, impl=impl)
-        dh, dW, db = tp.backward(gl, h, W[v0:v1], b[v0:v1], yt, lse.float(), v0, V, impl=impl)
+        logp, lse = tp.forward(h, W[v0:v1], b[v0:v1], yt, v0, V, impl=impl, temperature=T)
+        dh, dW, db = tp.backward(gl, h, W[v0:v1], b[v0:v1], yt, lse.float(), v0, V, impl=impl,
+                                 temperature=T)
         np.save(os.path.join(out_dir, f"logp{rank}.npy"), logp.numpy())
         np.save(os.path.join(out_dir, f"lse{rank}.npy"), lse.numpy())
         np.save(os.path.join(out_dir, f"dh{rank}.npy"), dh.numpy())
@@ -135,7 +136,7 @@ def test_shard_bounds_are_whole_segments():
             assert max(sizes) - min(sizes) <= 1 and max(sizes) == tp.max_segments(V_, world)
 
 
-def _single_process_merge():
+def _single_process_merge(T=1.0):
     """Every segment's partial in one process, merged: the reference bits."""
     p, y = _inputs()
     impl = OracleShards()
@@ -144,20 +145,22 @@ def _single_process_merge():
     s = torch.empty(S, N, dtype=torch.float32)
     zy = torch.empty(N, dtype=torch.float32)
     impl.forward_shard(torch.from_numpy(p["h"]), torch.from_numpy(p["W"]),
-                       torch.from_numpy(p["b"]), torch.from_numpy(y), 0, V, out=(m, s, zy))
+                       torch.from_numpy(p["b"]), torch.from_numpy(y), 0, V, out=(m, s, zy),
+                       temperature=T)
     return impl.lse_merge(m, s, zy, torch.from_numpy(y), V)
 
 
-@pytest.mark.parametrize("world", [2, 3, 4])
-def test_vocab_parallel_composition(tmp_path, world):
+@pytest.mark.parametrize("world,T", [(2, 1.0), (3, 1.0), (4, 1.0), (3, 0.7)])
+def test_vocab_parallel_composition(tmp_path, world, T):
     import oracle
 
     port = _free_port()
-    mp.start_processes(_worker, args=(world, port, str(tmp_path)), nprocs=world, join=True,
+    mp.start_processes(_worker, args=(world, port, str(tmp_path), T), nprocs=world, join=True,
                        start_method="spawn")
     p, y = _inputs()
-    logp1, lse1 = _single_process_merge()
-    full = oracle.linear_forward_backward(p["gl"], p["h"], p["W"], p["b"], y, "f32")
+    logp1, lse1 = _single_process_merge(T)
+    full = oracle.linear_forward_backward(p["gl"], p["h"], p["W"], p["b"], y, "f32",
+                                          temperature=T)
     ld = lambda k, r: np.load(tmp_path / f"{k}{r}.npy")
     for r in range(world):
         # bitwise the one-process merge of all segments, on every rank

@@ -147,6 +147,7 @@ struct Kind {
                                 : std::is_same<T, float>::value ? 2  // tf32
                                                                 : 1;
     static constexpr uint32_t kIdesc = instr_desc(kFmt, A_MN, B_MN, kBM, kBN);
+    static constexpr uint32_t kIdescPair = instr_desc(kFmt, A_MN, B_MN, 2 * kBM, kBN);
 };
 
 template <bool A_MN, bool B_MN>
@@ -511,6 +512,389 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ------------------------------------------- CTA pairs (cta_group::2)
+// The same GEMM on a pair of CTAs (a cluster of two SMs): one 256 x 256
+// output tile per pair, each CTA holding 128 rows of A and 128 of the 256
+// columns of B in its shared memory and 128 rows x 256 columns of the
+// accumulator in its TMEM.  The even CTA (the leader) runs the scheduler and
+// issues the M = 256 MMAs (tcgen05.mma.cta_group::2), which read both CTAs'
+// operand tiles; every CTA loads its own tiles, their transaction bytes
+// counted on the leader's stage barrier.  MMA completion is multicast to both
+// CTAs (stage free, accumulator ready); each CTA's epilogue then works on its
+// own 128 rows exactly like the single-CTA kernel.  Per SM, a k-step moves
+// A 16 KB + B 16 KB instead of 16 + 32 KB: a third less operand traffic for
+// the same tensor work.
+constexpr int kPairStages = 6;
+constexpr int kBHalf = kBN / 2;
+constexpr int kPairStageBytes = kABytes + kBHalf * kBK * 2;  // 32 KB
+static_assert(kPairStages * kPairStageBytes == kStages * kStageBytes, "same stage memory");
+
+struct BarsPair {
+    uint64_t full[kPairStages];   // leader: both CTAs' tiles landed
+    uint64_t empty[kPairStages];  // both: the pair MMAs are done with the stage
+    uint64_t tfull[2];            // both: accumulator ready
+    uint64_t tempty[2];           // leader: both CTAs' epilogues drained it
+    uint64_t sfull[kSchedDepth];  // both: unit id written
+    uint64_t sempty[kSchedDepth]; // leader: every consumer of the pair read it
+    uint64_t drain;
+    int sched[kSchedDepth];
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(BarsPair) <= 512, "barrier block");
+
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void load_stage_pair(uint8_t* sa, const CUtensorMap* tmA,
+                                                const CUtensorMap* tmB, uint32_t bar_cl,
+                                                int32_t k0, int32_t m0, int32_t n0) {
+    uint8_t* sb = sa + kABytes;
+    if constexpr (!A_MN) {
+        tma_load_2d_pair(sa, tmA, bar_cl, k0, m0);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kBM / 64; ++j)
+            tma_load_2d_pair(sa + j * kMnBoxBytes, tmA, bar_cl, m0 + 64 * j, k0);
+    }
+    if constexpr (!B_MN) {
+        tma_load_2d_pair(sb, tmB, bar_cl, k0, n0);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kBHalf / 64; ++j)
+            tma_load_2d_pair(sb + j * kMnBoxBytes, tmB, bar_cl, n0 + 64 * j, k0);
+    }
+}
+
+template <bool A_MN, bool B_MN, uint32_t IDESC>
+__device__ __forceinline__ void mma_stage_pair(uint32_t d_tmem, uint32_t sa, bool first) {
+    const uint32_t sb = sa + kABytes;
+#pragma unroll
+    for (int kk = 0; kk < kBK / 16; ++kk) {
+        const uint64_t ad = A_MN ? smem_desc_sw128(sa + kk * 2048, kMnBoxBytes, 1024)
+                                 : smem_desc_sw128(sa + kk * 32, 16, 1024);
+        const uint64_t bd = B_MN ? smem_desc_sw128(sb + kk * 2048, kMnBoxBytes, 1024)
+                                 : smem_desc_sw128(sb + kk * 32, 16, 1024);
+        tc_mma_pair(d_tmem, ad, bd, IDESC, (!first || kk > 0) ? 1u : 0u);
+    }
+}
+
+template <typename T, class K0, class K1, int NK>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA0,
+                     const __grid_constant__ CUtensorMap tmB0,
+                     const __grid_constant__ CUtensorMap tmO0,
+                     const __grid_constant__ CUtensorMap tmA1,
+                     const __grid_constant__ CUtensorMap tmB1,
+                     const __grid_constant__ CUtensorMap tmO1,
+                     const __grid_constant__ CUtensorMap tmL0,
+                     const __grid_constant__ CUtensorMap tmL1, const KParams P,
+                     const EpiArgs ea0, const EpiArgs ea1) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* outbuf = smem + kPairStages * kPairStageBytes;
+    BarsPair* bars = reinterpret_cast<BarsPair*>(outbuf + kOutBytes);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int64_t pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+    const int64_t total = P.n_units[0] + (NK > 1 ? P.n_units[1] : 0);
+    const uint64_t wait_ns = ea0.wait_ns;
+    int* status = ea0.status;
+    volatile int* abort = &bars->abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->tfull[b], 1);
+            mbar_init(&bars->tempty[b], 8);  // 4 epilogue warps in each CTA
+        }
+        for (int s = 0; s < kSchedDepth; ++s) {
+            mbar_init(&bars->sfull[s], 1);
+            // leader: its MMA warp and 4 epilogue warps, the peer's producer
+            // and 4 epilogue warps
+            mbar_init(&bars->sempty[s], 10);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA0);
+        tma_prefetch_desc(&tmB0);
+        if (NK > 1) {
+            tma_prefetch_desc(&tmA1);
+            tma_prefetch_desc(&tmB1);
+        }
+        if (P.zero_counter && blockIdx.x == 0) *P.zero_counter = 0;
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(&bars->tmem_base, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_barrier();  // both CTAs' barriers exist before either signals the other's
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    // every consumer of the unit ring arrives on the leader's slot barrier
+    auto next_unit = [&](int& sslot, uint32_t& sphase, bool& ok) -> int {
+        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->sfull[sslot], sphase, wait_ns, abort))) {
+            ok = false;
+            return -1;
+        }
+        const int u = *reinterpret_cast<volatile int*>(&bars->sched[sslot]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(cluster_addr(&bars->sempty[sslot], 0));
+        if (++sslot == kSchedDepth) {
+            sslot = 0;
+            sphase ^= 1;
+        }
+        return u;
+    };
+
+    if (warp == 0) {
+        // ------------------- scheduler (leader) + TMA producer (both CTAs)
+        int stage = 0, sslot = 0;
+        uint32_t phase = 0, sphase = 0;
+        bool ok = true;
+        int64_t next_static = pair;
+        while (ok) {
+            int64_t u;
+            if (leader) {
+                if (P.dynamic) {
+                    int got = 0;
+                    if (lane == 0) got = atomicAdd(P.counter, 1);
+                    u = __shfl_sync(0xffffffffu, got, 0);
+                } else {
+                    u = next_static;
+                    next_static += n_pairs;
+                }
+                if (u >= total) u = -1;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_cl(&bars->sempty[sslot], sphase ^ 1, wait_ns, abort))) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {  // the slot in both CTAs, then its barrier in both
+                    bars->sched[sslot] = static_cast<int>(u);
+                    st_cluster_u32(cluster_addr(&bars->sched[sslot], 1), static_cast<uint32_t>(u));
+                    mbar_arrive(&bars->sfull[sslot]);
+                    mbar_arrive_cluster(cluster_addr(&bars->sfull[sslot], 1));
+                }
+                __syncwarp();
+                if (++sslot == kSchedDepth) {
+                    sslot = 0;
+                    sphase ^= 1;
+                }
+            } else {
+                u = next_unit(sslot, sphase, ok);
+                if (!ok) break;
+            }
+            if (u < 0) break;
+            const Unit un = decode_unit(P, u);
+            const uint32_t full_cl0 = cluster_addr(&bars->full[0], 0);
+            for (int64_t t = un.t0; t < un.t1 && ok; ++t) {
+                for (int64_t kb = 0; kb < un.k_blocks; ++kb) {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait_cl(&bars->empty[stage], phase ^ 1, wait_ns, abort))) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        uint8_t* sa = smem + stage * kPairStageBytes;
+                        const uint32_t bar_cl = full_cl0 + stage * 8u;
+                        // the leader expects both CTAs' bytes on its stage barrier
+                        if (leader) mbar_arrive_expect_tx(&bars->full[stage], 2 * kPairStageBytes);
+                        const int64_t ks = P.k_split[un.kind];
+                        const bool lo = ks > 0 && kb >= ks;
+                        const int32_t k0 = static_cast<int32_t>((lo ? kb - ks : kb) * kBK);
+                        const int32_t m0 = static_cast<int32_t>(un.mb * 2 * kBM + rank * kBM);
+                        const int32_t n0 = static_cast<int32_t>(t * kBN + rank * kBHalf);
+                        if (NK == 1 || un.kind == 0)
+                            load_stage_pair<K0::kAmn, K0::kBmn>(sa, lo ? &tmL0 : &tmA0, &tmB0,
+                                                                bar_cl, k0, m0, n0);
+                        else
+                            load_stage_pair<K1::kAmn, K1::kBmn>(sa, lo ? &tmL1 : &tmA1, &tmB1,
+                                                                bar_cl, k0, m0, n0);
+                    }
+                    __syncwarp();
+                    if (++stage == kPairStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+        }
+        if (!ok) {
+            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
+            bars->abort = 1;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------- MMA issuer (leader only)
+        if (leader) {
+            int stage = 0, sslot = 0, buf = 0;
+            uint32_t phase = 0, sphase = 0, bphase = 0;
+            bool ok = true;
+            const uint32_t sbase = smem_u32(smem);
+            while (ok) {
+                const int u = next_unit(sslot, sphase, ok);
+                if (!ok || u < 0) break;
+                const Unit un = decode_unit(P, u);
+                for (int64_t t = un.t0; t < un.t1 && ok; ++t) {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait_cl(&bars->tempty[buf], bphase ^ 1, wait_ns, abort))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem + buf * kBN;
+                    for (int64_t kb = 0; kb < un.k_blocks; ++kb) {
+                        if (!__all_sync(0xffffffffu,
+                                        mbar_wait_cl(&bars->full[stage], phase, wait_ns, abort))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (lane == 0) {
+                            const uint32_t sa = sbase + stage * kPairStageBytes;
+                            if (NK == 1 || un.kind == 0)
+                                mma_stage_pair<K0::kAmn, K0::kBmn, K0::kIdescPair>(d_tmem, sa,
+                                                                                   kb == 0);
+                            else
+                                mma_stage_pair<K1::kAmn, K1::kBmn, K1::kIdescPair>(d_tmem, sa,
+                                                                                   kb == 0);
+                            tc_commit_pair_both(&bars->empty[stage]);
+                        }
+                        __syncwarp();
+                        if (++stage == kPairStages) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                    }
+                    if (!ok) break;
+                    if (lane == 0) tc_commit_pair_both(&bars->tfull[buf]);
+                    __syncwarp();
+                    if (++buf == 2) {
+                        buf = 0;
+                        bphase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
+                bars->abort = 1;
+            }
+            if (lane == 0) tc_commit_pair_local(&bars->drain);
+            __syncwarp();
+            mbar_wait(&bars->drain, 0, wait_ns, nullptr);
+        }
+    } else {
+        // ------------------------------------------- epilogue (both CTAs)
+        const int q = warp & 3;
+        const int r_in_tile = q * 32 + lane;
+        uint8_t* wbuf = outbuf + q * 2 * kOutBufBytes;
+        int sslot = 0, buf = 0, sidx = 0;
+        uint32_t sphase = 0, bphase = 0;
+        bool ok = true;
+        typename K0::Epi epi0;
+        typename K1::Epi epi1;
+        while (ok) {
+            const int u = next_unit(sslot, sphase, ok);
+            if (!ok || u < 0) break;
+            const Unit un = decode_unit(P, u);
+            const int kind = (NK == 1) ? 0 : un.kind;
+            const EpiArgs& ea = kind == 0 ? ea0 : ea1;
+            const CUtensorMap* tmO = kind == 0 ? &tmO0 : &tmO1;
+            const bool out16 = P.out16[kind] != 0;
+            const bool reduce = P.reduce[kind] != 0;
+            const bool stores = P.out_rows[kind] > 0;
+            const int64_t base_row = un.mb * 2 * kBM + rank * kBM;  // this CTA's 128 rows
+            const int64_t row0 = base_row + q * 32;
+            if (kind == 0)
+                epi0.begin_unit(ea, base_row + r_in_tile);
+            else
+                epi1.begin_unit(ea, base_row + r_in_tile);
+            for (int64_t t = un.t0; t < un.t1; ++t) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_cl(&bars->tfull[buf], bphase, wait_ns, abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem + buf * kBN + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+                for (int c = 0; c < kBN / 32; ++c) {
+                    uint32_t r[32];
+                    __syncwarp();
+                    tmem_ld32(taddr + c * 32, r);
+                    tmem_ld_wait(r);
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    const int64_t col0 = t * kBN + c * 32;
+                    if (kind == 0)
+                        epi0.chunk(ea, v, col0);
+                    else
+                        epi1.chunk(ea, v, col0);
+                    if (!stores) continue;
+                    const int h = out16 ? (c & 1) : 0;
+                    uint8_t* sb = wbuf + (sidx & 1) * kOutBufBytes;
+                    if (h == 0) {
+                        if (lane == 0) bulk_wait_read_1();
+                        __syncwarp();
+                    }
+                    stage_row<T>(sb, lane, v, out16, h);
+                    if (kind == 0) {
+                        epi0.store_lo(ea, v, col0);
+                        epi0.db_partials(ea, v, col0);
+                    }
+                    if (!out16 || h == 1) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        const int64_t x0 = out16 ? col0 - 32 : col0;
+                        if (lane == 0 && row0 < P.out_rows[kind] && x0 < P.out_cols[kind]) {
+                            if (reduce)
+                                tma_reduce_add_2d(tmO, sb, static_cast<int32_t>(x0),
+                                                  static_cast<int32_t>(row0));
+                            else
+                                tma_store_2d(tmO, sb, static_cast<int32_t>(x0),
+                                             static_cast<int32_t>(row0));
+                            bulk_commit();
+                        }
+                        ++sidx;
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(cluster_addr(&bars->tempty[buf], 0));
+                if (++buf == 2) {
+                    buf = 0;
+                    bphase ^= 1;
+                }
+            }
+            if (!ok) break;
+            if (kind == 0)
+                epi0.end_unit(ea, un.seg);
+            else
+                epi1.end_unit(ea, un.seg);
+        }
+        if (lane == 0) bulk_wait_all();
+        if (!ok) {
+            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
+            bars->abort = 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_barrier();  // the leader's MMAs are done with both CTAs' memory
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
 
 // ------------------------------------------------------ FP32 (3 x TF32)
@@ -1031,12 +1415,15 @@ bool make_map(CUtensorMap* map, const void* base, int dtype, int64_t cols, int64
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool operand_maps(const GemmOperands& g, int dtype, CUtensorMap* ma, CUtensorMap* mb) {
+// pair = 1: B tiles of a CTA pair's half (128 columns) for a K-major B.
+bool operand_maps(const GemmOperands& g, int dtype, CUtensorMap* ma, CUtensorMap* mb,
+                  int pair = 0) {
     // K-major operand: [rows, K], box 64(K) x rows; MN-major: [K, MN], box 64 x 64.
     const bool oka = g.a_mn ? make_map(ma, g.A, dtype, g.M, g.K, g.lda, 64, kBK)
                             : make_map(ma, g.A, dtype, g.K, g.M, g.lda, kBK, kBM);
     const bool okb = g.b_mn ? make_map(mb, g.B, dtype, g.N, g.K, g.ldb, 64, kBK)
-                            : make_map(mb, g.B, dtype, g.K, g.N, g.ldb, kBK, kBN);
+                            : make_map(mb, g.B, dtype, g.K, g.N, g.ldb, kBK,
+                                       pair ? kBHalf : kBN);
     return oka && okb;
 }
 
@@ -1072,28 +1459,62 @@ cudaError_t launch_k(const CUtensorMap* m, const KParams& P, const EpiArgs& ea0,
     return cudaGetLastError();
 }
 
+// CTA pairs: 2 x pairs CTAs (clusters of two), one pair per two SMs.
+template <typename T, class K0, class K1, int NK>
+cudaError_t launch_p(const CUtensorMap* m, const KParams& P, const EpiArgs& ea0,
+                     const EpiArgs& ea1, const DevInfo& dev, int max_ctas, cudaStream_t s) {
+    auto kern = gemm_pair_kernel<T, K0, K1, NK>;
+    static int configured[64] = {0};
+    if (dev.device < 64 && !configured[dev.device]) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured[dev.device] = 1;
+    }
+    const int64_t units = P.n_units[0] + (NK > 1 ? P.n_units[1] : 0);
+    const int cap = ((max_ctas > 0 && max_ctas < dev.num_sms) ? max_ctas : dev.num_sms) / 2;
+    int pairs = static_cast<int>(units < cap ? units : cap);
+    if (pairs < 1) pairs = 1;
+    note_launches(1);
+    kern<<<2 * pairs, kThreads, kSmemBytes, s>>>(m[0], m[1], m[2], m[3], m[4], m[5], m[6], m[7],
+                                                 P, ea0, ea1);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t dispatch(const GemmLaunch& L, const CUtensorMap* m, const KParams& P,
-                     const DevInfo& dev, cudaStream_t s) {
+                     const DevInfo& dev, cudaStream_t s, bool pair) {
     using Fwd = Kind<T, EpiKind::Fwd, false, false>;
     using Rec = Kind<T, EpiKind::Recomp, false, false>;
     using Dh = Kind<T, EpiKind::Dh, false, true>;
     using Dw = Kind<T, EpiKind::Dw, true, true>;
+    const int mc = L.max_ctas;
     if (L.nkinds == 1) {
         switch (L.kind[0]) {
-            case EpiKind::Fwd: return launch_k<T, Fwd, Fwd, 1>(m, P, L.ea[0], L.ea[0], dev, L.max_ctas, s);
-            case EpiKind::Recomp: return launch_k<T, Rec, Rec, 1>(m, P, L.ea[0], L.ea[0], dev, L.max_ctas, s);
-            case EpiKind::Dh: return launch_k<T, Dh, Dh, 1>(m, P, L.ea[0], L.ea[0], dev, L.max_ctas, s);
-            case EpiKind::Dw: return launch_k<T, Dw, Dw, 1>(m, P, L.ea[0], L.ea[0], dev, L.max_ctas, s);
+            case EpiKind::Fwd:
+                return pair ? launch_p<T, Fwd, Fwd, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s)
+                            : launch_k<T, Fwd, Fwd, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
+            case EpiKind::Recomp:
+                return pair ? launch_p<T, Rec, Rec, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s)
+                            : launch_k<T, Rec, Rec, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
+            case EpiKind::Dh:
+                return pair ? launch_p<T, Dh, Dh, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s)
+                            : launch_k<T, Dh, Dh, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
+            case EpiKind::Dw:
+                return pair ? launch_p<T, Dw, Dw, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s)
+                            : launch_k<T, Dw, Dw, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
         }
     } else if (L.kind[0] == EpiKind::Dh && L.kind[1] == EpiKind::Dw) {
-        return launch_k<T, Dh, Dw, 2>(m, P, L.ea[0], L.ea[1], dev, L.max_ctas, s);
+        return pair ? launch_p<T, Dh, Dw, 2>(m, P, L.ea[0], L.ea[1], dev, mc, s)
+                    : launch_k<T, Dh, Dw, 2>(m, P, L.ea[0], L.ea[1], dev, mc, s);
     }
     return cudaErrorInvalidValue;
 }
 
 // FP32 operands run on the CUDA-core kernel (simt_f32.cu) unless this is set.
 constexpr bool kFp32OnTensorCores = true;
+// 16-bit operands on CTA pairs (gemm_pair_kernel) for problems of >= 256 rows.
+constexpr bool kUsePairs = true;
 
 template <class K0, class K1, int NK>
 cudaError_t launch_f(const CUtensorMap* m, const KParams& P, const EpiArgs& ea0,
@@ -1166,13 +1587,18 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
     KParams P;
     memset(&P, 0, sizeof(P));
     GemmLaunch G = L;
+    // 16-bit operands run on CTA pairs (256 x 256 tiles) when every kind has
+    // at least 256 rows; smaller problems keep the single-CTA kernel
+    bool pair = G.dtype != LL_F32 && kUsePairs;
+    for (int k = 0; k < G.nkinds; ++k) pair = pair && G.op[k].M >= 2 * kBM;
     for (int k = 0; k < G.nkinds; ++k) {
         const bool okm = G.dtype == LL_F32
                              ? operand_maps_f32(G.op[k], &m[3 * k], &m[3 * k + 1])
-                             : operand_maps(G.op[k], G.dtype, &m[3 * k], &m[3 * k + 1]);
+                             : operand_maps(G.op[k], G.dtype, &m[3 * k], &m[3 * k + 1], pair);
         if (!okm) return cudaErrorInvalidValue;
         if (!out_map(&m[3 * k + 2], G.out[k])) return cudaErrorInvalidValue;
         P.sh[k] = G.shape[k];
+        if (pair) P.sh[k].m_blocks = (G.op[k].M + 2 * kBM - 1) / (2 * kBM);
         // the host sizes K blocks for the 16-bit kernel (64 values); the
         // tf32 kernel takes 16 per stage
         if (G.dtype == LL_F32) P.sh[k].k_blocks = (G.op[k].K + kBKf - 1) / kBKf;
@@ -1181,11 +1607,11 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
             GemmOperands lo = G.op[k];
             lo.A = lo.A_lo;
             CUtensorMap unused;
-            if (!operand_maps(lo, G.dtype, &m[6 + k], &unused)) return cudaErrorInvalidValue;
+            if (!operand_maps(lo, G.dtype, &m[6 + k], &unused, pair)) return cudaErrorInvalidValue;
             P.k_split[k] = P.sh[k].k_blocks;
             P.sh[k].k_blocks *= 2;
         }
-        P.n_units[k] = G.shape[k].m_blocks * G.shape[k].n_segs;
+        P.n_units[k] = P.sh[k].m_blocks * P.sh[k].n_segs;
         P.out16[k] = G.out[k].dtype != LL_F32;
         P.out_rows[k] = G.out[k].rows;
         P.out_cols[k] = G.out[k].cols;
@@ -1207,8 +1633,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
     P.counter = G.counter;
     P.zero_counter = G.zero_counter;
     if (G.dtype == LL_F32) return dispatch_f32(G, m, P, dev, s);
-    if (G.dtype == LL_BF16) return dispatch<__nv_bfloat16>(G, m, P, dev, s);
-    return dispatch<__half>(G, m, P, dev, s);
+    if (G.dtype == LL_BF16) return dispatch<__nv_bfloat16>(G, m, P, dev, s, pair);
+    return dispatch<__half>(G, m, P, dev, s, pair);
 }
 
 }  // namespace ll

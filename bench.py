@@ -370,7 +370,9 @@ def run_ours(args, rank, world, local_rank):
     dom = max(gemms, key=lambda k: gemms[k][1])
     cnt, tot = gemms[dom]
     avg_ms = tot / cnt
-    achieved = flops[dom] / (avg_ms * 1e-3) / 1e12
+    # flops[] are per step; a step launches the kernel once per token chunk
+    launch_flops = flops[dom] * args.steps / cnt
+    achieved = launch_flops / (avg_ms * 1e-3) / 1e12
     simt_peak = 152 * 128 * 2 * pk.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
     if dt == "f32":
         # FP32 operands run as three TF32 MMAs per product (hi*hi + hi*lo +
@@ -406,7 +408,7 @@ def run_ours(args, rank, world, local_rank):
                                                              pk["bf16_tflops"])
                                                       * (peak / pk["bf16_tflops"])),
                      "traffic": ncu_traffic(dom, args.workload), "avg_launch_ms": avg_ms,
-                     "flops_per_launch": flops[dom]},
+                     "flops_per_launch": launch_flops, "launches_per_step": cnt / args.steps},
         "kernels_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},
         "gpu_launches": launches,
         "single_call": {"value": world * N / (ms_fb * 1e-3), "unit": "tokens/s",

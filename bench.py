@@ -291,17 +291,37 @@ def run_ours(args, rank, world, local_rank):
             evs[i][1].record(stream)
         torch.cuda.synchronize()
         barrier()
-        return sum(a.elapsed_time(b) for a, b in evs) / k
+        times = [a.elapsed_time(b) for a, b in evs]
+        step_times.clear()
+        step_times.extend(times)
+        return sum(times) / k
 
+    step_times = []
     for _ in range(args.warmup):
         step(h, y, gl)
     torch.cuda.synchronize()
     assert ll.check_status() == 0
 
+    # device memory of one fwd + bwd through the binding (outputs and workspaces
+    # allocated by the calls), above what is resident before it
+    torch.cuda.synchronize()
+    mem_base = torch.cuda.memory_allocated(device)
+    torch.cuda.reset_peak_memory_stats(device)
+    m_logp, m_lse = ll.forward(h, W, b, y)
+    m_out = ll.backward(gl, h, W, b, y, m_lse, need_db=has_bias, dh_dtype=tdt, dw_dtype=dw_dt,
+                        token_chunks=args.token_chunks)
+    torch.cuda.synchronize()
+    mem_peak = torch.cuda.max_memory_allocated(device) - mem_base
+    del m_logp, m_lse, m_out
+    torch.cuda.empty_cache()
+
     clocks = Clocks(local_rank)
     clocks.start()
     n0 = ll.launch_count()
     ms = timed_loop(lambda: step(h, y, gl), args.steps)
+    st_sorted = sorted(step_times)
+    pct = {q: st_sorted[min(len(st_sorted) - 1, int(round(q / 100 * (len(st_sorted) - 1))))]
+           for q in (20, 50, 80)}
     launches = ll.launch_count() - n0
     clk = clocks.stop()
     assert ll.check_status() == 0
@@ -421,6 +441,11 @@ def run_ours(args, rank, world, local_rank):
                 "h2d_bytes_per_step": h.numel() * h.element_size() + y.numel() * 8 + gl.numel() * 4,
                 "d2h_bytes_per_step": logp.numel() * 4, "ms_per_step": ms_e2e},
         "clocks": clk,
+        "step_ms_percentiles": {"p20": pct[20], "p50": pct[50], "p80": pct[80]},
+        "memory": {"peak_bytes_above_resident": mem_peak,
+                   "workspace_bytes": {"forward": ws_f.numel(), "backward": ws_b.numel()},
+                   "note": "one ll_forward + ll_backward allocating its outputs and "
+                           "workspaces, max_memory_allocated above the resident inputs"},
     }
     if not args.no_logits and args.workload == WORKLOAD:
         del ws_b, flush_buf

@@ -265,19 +265,6 @@ struct RowEpilogue {
         }
     }
 
-    // Direct row stores (CUDA-core path); the tensor-core path stages the
-    // values in shared memory and writes them with TMA instead.
-    __device__ __forceinline__ void store_direct(const EpiArgs& ea, const float (&v)[32],
-                                                 int64_t col0) {
-        if constexpr (E == EpiKind::Fwd) {
-            if (rvalid && ea.Z) store_row32<T>(ea.Z, row * ea.ldZ + col0, v, col0, ea.Ncols, LL_F32);
-        } else if constexpr (E == EpiKind::Recomp) {
-            if (rvalid) store_row32<T>(ea.S, row * ea.ldS + col0, v, col0, ea.Ncols, own_tag<T>());
-        } else if constexpr (E == EpiKind::Dh || E == EpiKind::Dw) {
-            if (rvalid) store_row32<T>(ea.out, row * ea.ld_out + col0, v, col0, ea.Ncols, ea.out_dtype);
-        }
-    }
-
     __device__ __forceinline__ void end_unit(const EpiArgs& ea, int64_t seg) {
         if constexpr (E == EpiKind::Fwd) {
             if (!rvalid) return;

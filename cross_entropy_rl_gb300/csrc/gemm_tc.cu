@@ -1371,429 +1371,6 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
-// ------------------------------------------------ 3 x TF32 on CTA pairs
-// The FP32-operand GEMM on a CTA pair: each CTA TMA-loads and converts its
-// 128 rows of A and its 128 of the 256 columns of B (raw and converted rings
-// are local to the CTA); the even CTA issues the M = 256 kind::tf32 MMAs once
-// the converter warps of both CTAs have filled the converted stage (its
-// barrier counts the 8 converter warps of the pair).  Per SM a k-step moves
-// and converts 16 KB instead of 24 KB and the MMAs read 48 KB instead of
-// 72 KB of shared memory.
-constexpr int kRawPairBytes = kAfBytes + kBHalf * kBKf * 4;  // 16 KB
-constexpr int kConvPairBytes = 2 * kRawPairBytes;             // hi A, hi B, lo A, lo B
-constexpr int kRawPairStages = 4;
-constexpr int kConvPairStages = 4;
-static_assert(kRawPairStages * kRawPairBytes + kConvPairStages * kConvPairBytes ==
-                  kStages * kStageBytes,
-              "tf32 pair rings fill the stage memory");
-constexpr uint32_t kIdescFPair = instr_desc(2 /*tf32*/, 0, 0, 2 * kBM, kBN);
-
-struct BarsFPair {
-    uint64_t full[kRawPairStages];    // local TMA landed
-    uint64_t rempty[kRawPairStages];  // local converters done reading
-    uint64_t conv[kConvPairStages];   // leader: the pair's 8 converter warps wrote hi / lo
-    uint64_t empty[kConvPairStages];  // both: the pair MMAs are done with the stage
-    uint64_t tfull[2];
-    uint64_t tempty[2];               // leader: 8 epilogue warps of the pair
-    uint64_t sfull[kSchedDepth];
-    uint64_t sempty[kSchedDepth];     // leader: every consumer of the pair
-    uint64_t drain;
-    int sched[kSchedDepth];
-    uint32_t tmem_base;
-    int abort;
-};
-static_assert(sizeof(BarsFPair) <= 512, "barrier block");
-
-template <bool A_MN, bool B_MN>
-__device__ __forceinline__ void load_stage_fpair(uint8_t* st, const CUtensorMap* tmA,
-                                                 const CUtensorMap* tmB, uint64_t* fb,
-                                                 int32_t k0, int32_t m0, int32_t n0) {
-    uint8_t* sa = st;
-    uint8_t* sb = st + kAfBytes;
-    mbar_arrive_expect_tx(fb, kRawPairBytes);
-    if constexpr (!A_MN) {
-        tma_load_2d(sa, tmA, fb, k0, m0);
-    } else {
-#pragma unroll
-        for (int j = 0; j < kBM / 32; ++j) tma_load_2d(sa + j * kMnBoxF, tmA, fb, m0 + 32 * j, k0);
-    }
-    if constexpr (!B_MN) {
-        tma_load_2d(sb, tmB, fb, k0, n0);
-    } else {
-#pragma unroll
-        for (int j = 0; j < kBHalf / 32; ++j)
-            tma_load_2d(sb + j * kMnBoxF, tmB, fb, n0 + 32 * j, k0);
-    }
-}
-
-template <bool A_MN, bool B_MN>
-__device__ __forceinline__ void convert_stage_pair(const uint8_t* raw, uint8_t* cv, int ct) {
-    convert_operand<A_MN, kBM>(raw, cv, cv + kRawPairBytes, ct);
-    convert_operand<B_MN, kBHalf>(raw + kAfBytes, cv + kAfBytes, cv + kRawPairBytes + kAfBytes,
-                                  ct);
-}
-
-__device__ __forceinline__ void mma_stage_fpair(uint32_t d_tmem, uint32_t st, bool first) {
-    const uint32_t a_hi = st, b_hi = st + kAfBytes;
-    const uint32_t a_lo = st + kRawPairBytes, b_lo = st + kRawPairBytes + kAfBytes;
-#pragma unroll
-    for (int kk = 0; kk < kBKf / 8; ++kk) {
-        tc_mma_pair<1>(d_tmem, desc_f(a_hi, kk), desc_f(b_hi, kk), kIdescFPair,
-                       (!first || kk > 0) ? 1u : 0u);
-        tc_mma_pair<1>(d_tmem, desc_f(a_hi, kk), desc_f(b_lo, kk), kIdescFPair, 1u);
-        tc_mma_pair<1>(d_tmem, desc_f(a_lo, kk), desc_f(b_hi, kk), kIdescFPair, 1u);
-    }
-}
-
-template <class K0, class K1, int NK>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsF, 1)
-    gemm_tf32_pair_kernel(const __grid_constant__ CUtensorMap tmA0,
-                          const __grid_constant__ CUtensorMap tmB0,
-                          const __grid_constant__ CUtensorMap tmO0,
-                          const __grid_constant__ CUtensorMap tmA1,
-                          const __grid_constant__ CUtensorMap tmB1,
-                          const __grid_constant__ CUtensorMap tmO1, const KParams P,
-                          const EpiArgs ea0, const EpiArgs ea1) {
-    using T = float;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* conv_base = smem + kRawPairStages * kRawPairBytes;
-    uint8_t* outbuf = smem + kStages * kStageBytes;
-    BarsFPair* bars = reinterpret_cast<BarsFPair*>(outbuf + kOutBytes);
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const bool leader = rank == 0;
-    const int64_t pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
-    const int64_t total = P.n_units[0] + (NK > 1 ? P.n_units[1] : 0);
-    const uint64_t wait_ns = ea0.wait_ns;
-    int* status = ea0.status;
-    volatile int* abort = &bars->abort;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kRawPairStages; ++s) {
-            mbar_init(&bars->full[s], 1);
-            mbar_init(&bars->rempty[s], 4);
-        }
-        for (int s = 0; s < kConvPairStages; ++s) {
-            mbar_init(&bars->conv[s], 8);  // 4 converter warps in each CTA
-            mbar_init(&bars->empty[s], 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&bars->tfull[b], 1);
-            mbar_init(&bars->tempty[b], 8);
-        }
-        for (int s = 0; s < kSchedDepth; ++s) {
-            mbar_init(&bars->sfull[s], 1);
-            // leader: MMA, 4 epilogue, 4 converter warps; peer: producer, 4 + 4
-            mbar_init(&bars->sempty[s], 18);
-        }
-        mbar_init(&bars->drain, 1);
-        bars->abort = 0;
-        fence_mbar_init();
-        tma_prefetch_desc(&tmA0);
-        tma_prefetch_desc(&tmB0);
-        if (NK > 1) {
-            tma_prefetch_desc(&tmA1);
-            tma_prefetch_desc(&tmB1);
-        }
-        if (P.zero_counter && blockIdx.x == 0) *P.zero_counter = 0;
-    }
-    if (warp == 1) {
-        tmem_alloc_pair(&bars->tmem_base, kTmemCols);
-        tmem_relinquish_pair();
-    }
-    tc_fence_before();
-    __syncthreads();
-    cluster_barrier();
-    tc_fence_after();
-    const uint32_t tmem = bars->tmem_base;
-
-    auto next_unit = [&](int& sslot, uint32_t& sphase, bool& ok) -> int {
-        if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->sfull[sslot], sphase, wait_ns, abort))) {
-            ok = false;
-            return -1;
-        }
-        const int u = *reinterpret_cast<volatile int*>(&bars->sched[sslot]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(cluster_addr(&bars->sempty[sslot], 0));
-        if (++sslot == kSchedDepth) {
-            sslot = 0;
-            sphase ^= 1;
-        }
-        return u;
-    };
-
-    if (warp == 0) {
-        // ------------------- scheduler (leader) + TMA producer (both CTAs)
-        int stage = 0, sslot = 0;
-        uint32_t phase = 0, sphase = 0;
-        uint32_t issued_phase[kRawPairStages];
-        bool issued[kRawPairStages];
-        for (int s = 0; s < kRawPairStages; ++s) issued[s] = false;
-        bool ok = true;
-        int64_t next_static = pair;
-        while (ok) {
-            int64_t u;
-            if (leader) {
-                if (P.dynamic) {
-                    int got = 0;
-                    if (lane == 0) got = atomicAdd(P.counter, 1);
-                    u = __shfl_sync(0xffffffffu, got, 0);
-                } else {
-                    u = next_static;
-                    next_static += n_pairs;
-                }
-                if (u >= total) u = -1;
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait_cl(&bars->sempty[sslot], sphase ^ 1, wait_ns, abort))) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
-                    bars->sched[sslot] = static_cast<int>(u);
-                    st_cluster_u32(cluster_addr(&bars->sched[sslot], 1), static_cast<uint32_t>(u));
-                    mbar_arrive(&bars->sfull[sslot]);
-                    mbar_arrive_cluster(cluster_addr(&bars->sfull[sslot], 1));
-                }
-                __syncwarp();
-                if (++sslot == kSchedDepth) {
-                    sslot = 0;
-                    sphase ^= 1;
-                }
-            } else {
-                u = next_unit(sslot, sphase, ok);
-                if (!ok) break;
-            }
-            if (u < 0) break;
-            const Unit un = decode_unit(P, u);
-            for (int64_t t = un.t0; t < un.t1 && ok; ++t) {
-                for (int64_t kb = 0; kb < un.k_blocks; ++kb) {
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait(&bars->rempty[stage], phase ^ 1, wait_ns, abort))) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) {
-                        uint8_t* st = smem + stage * kRawPairBytes;
-                        const int32_t k0 = static_cast<int32_t>(kb * kBKf);
-                        const int32_t m0 = static_cast<int32_t>(un.mb * 2 * kBM + rank * kBM);
-                        const int32_t n0 = static_cast<int32_t>(t * kBN + rank * kBHalf);
-                        if (NK == 1 || un.kind == 0)
-                            load_stage_fpair<K0::kAmn, K0::kBmn>(st, &tmA0, &tmB0,
-                                                                 &bars->full[stage], k0, m0, n0);
-                        else
-                            load_stage_fpair<K1::kAmn, K1::kBmn>(st, &tmA1, &tmB1,
-                                                                 &bars->full[stage], k0, m0, n0);
-                    }
-                    __syncwarp();
-                    issued[stage] = true;
-                    issued_phase[stage] = phase;
-                    if (++stage == kRawPairStages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-            }
-        }
-        if (!ok) {
-            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
-            bars->abort = 1;
-            for (int s = 0; s < kRawPairStages; ++s)
-                if (issued[s]) mbar_wait(&bars->full[s], issued_phase[s], wait_ns, nullptr);
-        }
-    } else if (warp >= 6) {
-        // --------------------------------- hi / lo converters (both CTAs)
-        const int ct = threadIdx.x - 6 * 32;
-        int rs = 0, cs = 0, sslot = 0;
-        uint32_t rphase = 0, cphase = 0, sphase = 0;
-        bool ok = true;
-        while (ok) {
-            const int u = next_unit(sslot, sphase, ok);
-            if (!ok || u < 0) break;
-            const Unit un = decode_unit(P, u);
-            const int64_t steps = (un.t1 - un.t0) * un.k_blocks;
-            for (int64_t i = 0; i < steps; ++i) {
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(&bars->full[rs], rphase, wait_ns, abort) &&
-                                    mbar_wait_cl(&bars->empty[cs], cphase ^ 1, wait_ns, abort))) {
-                    ok = false;
-                    break;
-                }
-                const uint8_t* raw = smem + rs * kRawPairBytes;
-                uint8_t* cv = conv_base + cs * kConvPairBytes;
-                if (NK == 1 || un.kind == 0)
-                    convert_stage_pair<K0::kAmn, K0::kBmn>(raw, cv, ct);
-                else
-                    convert_stage_pair<K1::kAmn, K1::kBmn>(raw, cv, ct);
-                fence_proxy_async_shared_cta();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&bars->rempty[rs]);
-                    mbar_arrive_cluster(cluster_addr(&bars->conv[cs], 0));
-                }
-                if (++rs == kRawPairStages) {
-                    rs = 0;
-                    rphase ^= 1;
-                }
-                if (++cs == kConvPairStages) {
-                    cs = 0;
-                    cphase ^= 1;
-                }
-            }
-        }
-        if (!ok) {
-            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
-            bars->abort = 1;
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------- MMA issuer (leader only)
-        if (leader) {
-            int stage = 0, sslot = 0, buf = 0;
-            uint32_t phase = 0, sphase = 0, bphase = 0;
-            bool ok = true;
-            const uint32_t sbase = smem_u32(conv_base);
-            while (ok) {
-                const int u = next_unit(sslot, sphase, ok);
-                if (!ok || u < 0) break;
-                const Unit un = decode_unit(P, u);
-                for (int64_t t = un.t0; t < un.t1 && ok; ++t) {
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait_cl(&bars->tempty[buf], bphase ^ 1, wait_ns, abort))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem + buf * kBN;
-                    for (int64_t kb = 0; kb < un.k_blocks; ++kb) {
-                        if (!__all_sync(0xffffffffu,
-                                        mbar_wait_cl(&bars->conv[stage], phase, wait_ns, abort))) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        if (lane == 0) {
-                            mma_stage_fpair(d_tmem, sbase + stage * kConvPairBytes, kb == 0);
-                            tc_commit_pair_both(&bars->empty[stage]);
-                        }
-                        __syncwarp();
-                        if (++stage == kConvPairStages) {
-                            stage = 0;
-                            phase ^= 1;
-                        }
-                    }
-                    if (!ok) break;
-                    if (lane == 0) tc_commit_pair_both(&bars->tfull[buf]);
-                    __syncwarp();
-                    if (++buf == 2) {
-                        buf = 0;
-                        bphase ^= 1;
-                    }
-                }
-            }
-            if (!ok) {
-                if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
-                bars->abort = 1;
-            }
-            if (lane == 0) tc_commit_pair_local(&bars->drain);
-            __syncwarp();
-            mbar_wait(&bars->drain, 0, wait_ns, nullptr);
-        }
-    } else {
-        // ------------------------------------------- epilogue (both CTAs)
-        const int q = warp & 3;
-        const int r_in_tile = q * 32 + lane;
-        uint8_t* wbuf = outbuf + q * 2 * kOutBufBytes;
-        int sslot = 0, buf = 0, sidx = 0;
-        uint32_t sphase = 0, bphase = 0;
-        bool ok = true;
-        typename K0::Epi epi0;
-        typename K1::Epi epi1;
-        while (ok) {
-            const int u = next_unit(sslot, sphase, ok);
-            if (!ok || u < 0) break;
-            const Unit un = decode_unit(P, u);
-            const int kind = (NK == 1) ? 0 : un.kind;
-            const EpiArgs& ea = kind == 0 ? ea0 : ea1;
-            const CUtensorMap* tmO = kind == 0 ? &tmO0 : &tmO1;
-            const bool reduce = P.reduce[kind] != 0;
-            const bool stores = P.out_rows[kind] > 0;
-            const int64_t base_row = un.mb * 2 * kBM + rank * kBM;
-            const int64_t row0 = base_row + q * 32;
-            if (kind == 0)
-                epi0.begin_unit(ea, base_row + r_in_tile);
-            else
-                epi1.begin_unit(ea, base_row + r_in_tile);
-            for (int64_t t = un.t0; t < un.t1; ++t) {
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait_cl(&bars->tfull[buf], bphase, wait_ns, abort))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t taddr = tmem + buf * kBN + (static_cast<uint32_t>(q * 32) << 16);
-#pragma unroll 1
-                for (int c = 0; c < kBN / 32; ++c) {
-                    uint32_t r[32];
-                    __syncwarp();
-                    tmem_ld32(taddr + c * 32, r);
-                    tmem_ld_wait(r);
-                    float v[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    const int64_t col0 = t * kBN + c * 32;
-                    if (kind == 0)
-                        epi0.chunk(ea, v, col0);
-                    else
-                        epi1.chunk(ea, v, col0);
-                    if (!stores) continue;
-                    uint8_t* sb = wbuf + (sidx & 1) * kOutBufBytes;
-                    if (lane == 0) bulk_wait_read_1();
-                    __syncwarp();
-                    stage_row<T>(sb, lane, v, false, 0);
-                    if (kind == 0) epi0.db_partials(ea, v, col0);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0 && row0 < P.out_rows[kind] && col0 < P.out_cols[kind]) {
-                        if (reduce)
-                            tma_reduce_add_2d(tmO, sb, static_cast<int32_t>(col0),
-                                              static_cast<int32_t>(row0));
-                        else
-                            tma_store_2d(tmO, sb, static_cast<int32_t>(col0),
-                                         static_cast<int32_t>(row0));
-                        bulk_commit();
-                    }
-                    ++sidx;
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(cluster_addr(&bars->tempty[buf], 0));
-                if (++buf == 2) {
-                    buf = 0;
-                    bphase ^= 1;
-                }
-            }
-            if (!ok) break;
-            if (kind == 0)
-                epi0.end_unit(ea, un.seg);
-            else
-                epi1.end_unit(ea, un.seg);
-        }
-        if (lane == 0) bulk_wait_all();
-        if (!ok) {
-            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
-            bars->abort = 1;
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    cluster_barrier();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
-}
-
 // ---------------------------------------------------------------- host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1934,12 +1511,8 @@ cudaError_t dispatch(const GemmLaunch& L, const CUtensorMap* m, const KParams& P
     return cudaErrorInvalidValue;
 }
 
-// FP32 operands run on the CUDA-core kernel (simt_f32.cu) unless this is set.
-constexpr bool kFp32OnTensorCores = true;
-// 16-bit operands on CTA pairs (gemm_pair_kernel), FP32 operands on 3 x TF32
-// CTA pairs (gemm_tf32_pair_kernel), for problems of >= 256 rows.
+// 16-bit operands on CTA pairs (gemm_pair_kernel) for problems of >= 256 rows.
 constexpr bool kUsePairs = true;
-constexpr bool kUseTf32Pairs = true;
 
 template <class K0, class K1, int NK>
 cudaError_t launch_f(const CUtensorMap* m, const KParams& P, const EpiArgs& ea0,
@@ -1963,39 +1536,18 @@ cudaError_t launch_f(const CUtensorMap* m, const KParams& P, const EpiArgs& ea0,
 
 // FP32 operand maps: K-major [rows, K] box 16(K) x rows, 64-byte swizzle;
 // MN-major [K, MN] box 32 x 16, 128-byte swizzle.
-bool operand_maps_f32(const GemmOperands& g, CUtensorMap* ma, CUtensorMap* mb, int pair = 0) {
+bool operand_maps_f32(const GemmOperands& g, CUtensorMap* ma, CUtensorMap* mb) {
     const bool oka = g.a_mn ? make_map(ma, g.A, LL_F32, g.M, g.K, g.lda, 32, kBKf)
                             : make_map(ma, g.A, LL_F32, g.K, g.M, g.lda, kBKf, kBM,
                                        CU_TENSOR_MAP_SWIZZLE_64B);
     const bool okb = g.b_mn ? make_map(mb, g.B, LL_F32, g.N, g.K, g.ldb, 32, kBKf)
-                            : make_map(mb, g.B, LL_F32, g.K, g.N, g.ldb, kBKf,
-                                       pair ? kBHalf : kBN, CU_TENSOR_MAP_SWIZZLE_64B);
+                            : make_map(mb, g.B, LL_F32, g.K, g.N, g.ldb, kBKf, kBN,
+                                       CU_TENSOR_MAP_SWIZZLE_64B);
     return oka && okb;
 }
 
-template <class K0, class K1, int NK>
-cudaError_t launch_fp(const CUtensorMap* m, const KParams& P, const EpiArgs& ea0,
-                      const EpiArgs& ea1, const DevInfo& dev, int max_ctas, cudaStream_t s) {
-    auto kern = gemm_tf32_pair_kernel<K0, K1, NK>;
-    static int configured[64] = {0};
-    if (dev.device < 64 && !configured[dev.device]) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        configured[dev.device] = 1;
-    }
-    const int64_t units = P.n_units[0] + (NK > 1 ? P.n_units[1] : 0);
-    const int cap = ((max_ctas > 0 && max_ctas < dev.num_sms) ? max_ctas : dev.num_sms) / 2;
-    int pairs = static_cast<int>(units < cap ? units : cap);
-    if (pairs < 1) pairs = 1;
-    note_launches(1);
-    kern<<<2 * pairs, kThreadsF, kSmemBytes, s>>>(m[0], m[1], m[2], m[3], m[4], m[5], P, ea0,
-                                                  ea1);
-    return cudaGetLastError();
-}
-
 cudaError_t dispatch_f32(const GemmLaunch& L, const CUtensorMap* m, const KParams& P,
-                         const DevInfo& dev, cudaStream_t s, bool pair) {
+                         const DevInfo& dev, cudaStream_t s) {
     using Fwd = Kind<float, EpiKind::Fwd, false, false>;
     using Rec = Kind<float, EpiKind::Recomp, false, false>;
     using Dh = Kind<float, EpiKind::Dh, false, true>;
@@ -2003,22 +1555,13 @@ cudaError_t dispatch_f32(const GemmLaunch& L, const CUtensorMap* m, const KParam
     const int mc = L.max_ctas;
     if (L.nkinds == 1) {
         switch (L.kind[0]) {
-            case EpiKind::Fwd:
-                return pair ? launch_fp<Fwd, Fwd, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s)
-                            : launch_f<Fwd, Fwd, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
-            case EpiKind::Recomp:
-                return pair ? launch_fp<Rec, Rec, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s)
-                            : launch_f<Rec, Rec, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
-            case EpiKind::Dh:
-                return pair ? launch_fp<Dh, Dh, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s)
-                            : launch_f<Dh, Dh, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
-            case EpiKind::Dw:
-                return pair ? launch_fp<Dw, Dw, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s)
-                            : launch_f<Dw, Dw, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
+            case EpiKind::Fwd: return launch_f<Fwd, Fwd, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
+            case EpiKind::Recomp: return launch_f<Rec, Rec, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
+            case EpiKind::Dh: return launch_f<Dh, Dh, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
+            case EpiKind::Dw: return launch_f<Dw, Dw, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
         }
     } else if (L.kind[0] == EpiKind::Dh && L.kind[1] == EpiKind::Dw) {
-        return pair ? launch_fp<Dh, Dw, 2>(m, P, L.ea[0], L.ea[1], dev, mc, s)
-                    : launch_f<Dh, Dw, 2>(m, P, L.ea[0], L.ea[1], dev, mc, s);
+        return launch_f<Dh, Dw, 2>(m, P, L.ea[0], L.ea[1], dev, mc, s);
     }
     return cudaErrorInvalidValue;
 }
@@ -2026,17 +1569,6 @@ cudaError_t dispatch_f32(const GemmLaunch& L, const CUtensorMap* m, const KParam
 }  // namespace
 
 cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s) {
-    if (L.dtype == LL_F32 && !kFp32OnTensorCores) {
-        for (int k = 0; k < L.nkinds; ++k) {
-            const GemmOperands& g = L.op[k];
-            EpiArgs ea = L.ea[k];
-            ea.dw_add_prev = !ea.first_chunk;
-            cudaError_t e = launch_gemm_f32(L.kind[k], g.A, g.lda, g.a_mn, g.B, g.ldb, g.b_mn,
-                                            g.M, g.N, g.K, L.shape[k], ea, dev, L.max_ctas, s);
-            if (e != cudaSuccess) return e;
-        }
-        return cudaSuccess;
-    }
     CUtensorMap m[8];  // A, B, out of kind 0; of kind 1; A_lo of kind 0, 1
     memset(m, 0, sizeof(m));
     KParams P;
@@ -2044,11 +1576,11 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
     GemmLaunch G = L;
     // 16-bit operands run on CTA pairs (256 x 256 tiles) when every kind has
     // at least 256 rows; smaller problems keep the single-CTA kernel
-    bool pair = G.dtype == LL_F32 ? kUseTf32Pairs : kUsePairs;
+    bool pair = G.dtype != LL_F32 && kUsePairs;
     for (int k = 0; k < G.nkinds; ++k) pair = pair && G.op[k].M >= 2 * kBM;
     for (int k = 0; k < G.nkinds; ++k) {
         const bool okm = G.dtype == LL_F32
-                             ? operand_maps_f32(G.op[k], &m[3 * k], &m[3 * k + 1], pair)
+                             ? operand_maps_f32(G.op[k], &m[3 * k], &m[3 * k + 1])
                              : operand_maps(G.op[k], G.dtype, &m[3 * k], &m[3 * k + 1], pair);
         if (!okm) return cudaErrorInvalidValue;
         if (!out_map(&m[3 * k + 2], G.out[k])) return cudaErrorInvalidValue;
@@ -2087,7 +1619,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
     P.dynamic = G.counter != nullptr;
     P.counter = G.counter;
     P.zero_counter = G.zero_counter;
-    if (G.dtype == LL_F32) return dispatch_f32(G, m, P, dev, s, pair);
+    if (G.dtype == LL_F32) return dispatch_f32(G, m, P, dev, s);
     if (G.dtype == LL_BF16) return dispatch<__nv_bfloat16>(G, m, P, dev, s, pair);
     return dispatch<__half>(G, m, P, dev, s, pair);
 }

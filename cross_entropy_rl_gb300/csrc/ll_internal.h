@@ -156,11 +156,6 @@ struct GemmLaunch {
     int max_ctas;       // grid cap (0 = one CTA per SM), leaves SMs to a side stream
 };
 cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s);
-// FP32 operands on the CUDA cores (simt_f32.cu): one GEMM of kind `kind`.
-cudaError_t launch_gemm_f32(EpiKind kind, const void* A, int64_t lda, int a_mn, const void* B,
-                            int64_t ldb, int b_mn, int64_t M, int64_t N, int64_t K,
-                            const GemmShape& shape, const EpiArgs& ea, const DevInfo& dev,
-                            int max_ctas, cudaStream_t s);
 
 // --- small kernels (aux_kernels.cu) ------------------------------------------
 // Shard-local targets: y - v0 for y in [v0, v0 + Vs), kTargetInOtherShard

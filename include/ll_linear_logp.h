@@ -360,7 +360,8 @@ int ll_check_status(void* stream);
  * every phase of later calls (fwd_gemm, lse_merge, token_sort,
  * recompute_gemm, softmax_part, grad_gemm (grad_hidden and grad_weight
  * tiles), db_sums, logits_fwd, logits_bwd, logits_fused; an _f32 suffix
- * for the CUDA-core FP32 GEMMs) with CUDA events on the call's
+ * marks the GEMMs of FP32 operands, 3 x TF32 on the tensor cores) with CUDA
+ * events on the call's
  * stream; ll_profile_enable(0) stops recording.  ll_profile_summary()
  * synchronises on the recorded events and writes one line per phase,
  * "label count total_ms", into buf (NUL-terminated, truncated to len);

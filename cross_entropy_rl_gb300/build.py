@@ -21,7 +21,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libll_gb300.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 
-SOURCES = ["capi.cu", "logits_kernels.cu", "logits_cluster.cu", "gemm_tc.cu",
+SOURCES = ["capi.cu", "logits_kernels.cu", "gemm_tc.cu",
            "aux_kernels.cu", "noalloc.cu"]
 HEADERS = ["ll_device.cuh", "ll_internal.h", "epilogue.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -243,10 +243,6 @@ int check_shard(int64_t Vs, int64_t v0, int64_t V) {
     return LL_OK;
 }
 
-// One-pass logits: rows held on chip by a thread-block cluster where they are
-// whole 16-byte vectors (logits_cluster.cu).
-constexpr bool kLogitsOnChip = true;
-
 // Options of a call: *inv_temp = 1 / temperature, *split = hi / lo S.
 // NULL = defaults.
 int read_options(const ll_options* o, float* inv_temp, int* split = nullptr) {
@@ -929,13 +925,6 @@ int logits_logp_fwd_bwd_ex(const float* grad_logp, const void* logits, int64_t l
     if (st) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     Phase ph("logits_fused", s);
-    if (kLogitsOnChip) {
-        bool used = false;
-        cudaError_t e = launch_logits_cluster(grad_logp, logits, ld, dtype, targets, N, V, logp,
-                                              lse, grad_logits, it, dev, s, &used);
-        if (e != cudaSuccess || used) return cuda_status(e);
-    }
-    // rows that are not whole 16-byte vectors: per row, the second read from L2
     return cuda_status(launch_logits_fused(grad_logp, logits, ld, dtype, targets, N, V, logp, lse,
                                            grad_logits, it, dev, s));
 }

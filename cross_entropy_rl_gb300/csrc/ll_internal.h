@@ -57,13 +57,6 @@ cudaError_t launch_logits_fused(const float* grad, const void* logits, int64_t l
                                 const int64_t* targets, int64_t N, int64_t V, float* logp,
                                 float* lse, void* grad_logits, float inv_temp,
                                 const DevInfo& dev, cudaStream_t s);
-// The same one pass with each row held on chip by a thread-block cluster
-// (logits_cluster.cu): 4 V bytes per row whatever L2 holds.  *used = false
-// (nothing launched) when rows are not 16-byte vectors or no cluster fits.
-cudaError_t launch_logits_cluster(const float* grad, const void* logits, int64_t ld, int dtype,
-                                  const int64_t* targets, int64_t N, int64_t V, float* logp,
-                                  float* lse, void* grad_logits, float inv_temp,
-                                  const DevInfo& dev, cudaStream_t s, bool* used);
 
 // --- GEMM-based linear path -------------------------------------------------
 enum class EpiKind : int { Fwd = 0, Recomp = 1, Dh = 2, Dw = 3 };

@@ -325,16 +325,11 @@ int logits_logp_bwd(const float* grad_logp, const void* logits, int64_t ld, int 
 /*
  * Logits-input forward and backward in one pass, for a grad_logp known
  * before the forward.  Same arguments as logits_logp_fwd plus
- * logits_logp_bwd together; logp, lse and grad_logits are written.  Each
- * row is read from HBM once and its gradient written once (4 V bytes per
- * row instead of 6 V): when rows are whole 16-byte vectors (16-byte aligned
- * logits and gradient, ld and V multiples of the vector), a thread-block
- * cluster holds the row in shared memory and combines the slices'
- * (max, sum-exp) pairs in a fixed order; otherwise each row's gradient is
- * computed right after its lse, the second read served by L2, with bitwise
- * the results of the two calls.  Deterministic and batch-invariant in both
- * cases; equal to the two calls within rounding.  grad_logits may be the
- * logits buffer itself (in place); a partial overlap is LL_ERR_INVALID_ARG.
+ * logits_logp_bwd together; logp, lse and grad_logits are written, bitwise
+ * the results of the two calls.  Each row's gradient is computed right after
+ * its lse, so the row's second read is served (mostly) by L2: HBM sees about
+ * 4 V bytes per row instead of 6 V.  grad_logits may be the logits buffer
+ * itself (in place); a partial overlap is LL_ERR_INVALID_ARG.
  */
 int logits_logp_fwd_bwd(const float* grad_logp, const void* logits, int64_t ld, int dtype,
                         const int64_t* targets, int64_t N, int64_t V, float* logp, float* lse,

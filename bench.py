@@ -136,7 +136,7 @@ class Clocks:
 # source files each timed kernel is built from (a change to any of them
 # invalidates a stored ncu traffic figure for that kernel)
 KERNEL_SOURCES = {
-    "gemm": ["gemm_tc.cu", "epilogue.cuh", "ll_device.cuh", "ll_internal.h"],
+    "gemm": ["gemm_tc.cu", "epilogue.cuh", "ll_device.cuh", "ll_internal.h", "capi.cu"],
     "logits": ["logits_kernels.cu", "ll_device.cuh", "ll_internal.h"],
 }
 PHASE_SOURCES = {"fwd_gemm": "gemm", "recompute_gemm": "gemm", "grad_gemm": "gemm",

@@ -610,7 +610,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
                 sh.tiles_per_unit = 1;
                 sh.n_segs = sh.n_tiles;
                 sh.k_blocks = cdiv(V, 64);
-                sh.unit_order = 0;
+                sh.unit_order = 1;  // a row block's D tiles run together and share its S rows in L2
                 EpiArgs& ea = G.ea[k];
                 ea = base;
                 ea.M = rows;

@@ -125,135 +125,176 @@ __global__ void offsets_kernel(const unsigned long long* __restrict__ keys, int6
     offs[v] = static_cast<int>(lo);
 }
 
-template <typename T>
-__global__ void db_partial_kernel(const T* __restrict__ S, int64_t ldS, int64_t rows, int64_t V,
-                                  int64_t rows_per_group, float* __restrict__ partial) {
-    const int64_t v = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
-    const int64_t g = blockIdx.y;
-    if (v >= V) return;
-    const int64_t r0 = g * rows_per_group;
-    const int64_t r1 = min(rows, r0 + rows_per_group);
-    float acc = 0.f;
-    for (int64_t r = r0; r < r1; ++r) acc += Elem<T>::to_f(S[r * ldS + v]);
-    partial[g * V + v] = acc;
-}
-
+// grad_bias from the chunk's partial rows (one per 32 rows of S): a block
+// takes 32 columns; warp w sums rows w, w + 8, w + 16, ... in ascending
+// order, and the block adds the running sum of the earlier chunks and then
+// warps 0..7 in that order -- a fixed order for given rows per chunk.  On the
+// last chunk the exact one-hot part (tc of the tokens whose target is v, in
+// ascending token order) is added and the result stored.
 template <typename TO>
-__global__ void db_finish_kernel(const float* __restrict__ partial, int64_t groups, int64_t V,
-                                 float* __restrict__ db_acc, int first, int last,
-                                 const int* __restrict__ offs,
-                                 const unsigned long long* __restrict__ keys,
-                                 const float* __restrict__ tc_all, TO* __restrict__ out) {
-    const int64_t v = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
-    if (v >= V) return;
-    float acc = first ? 0.f : db_acc[v];
-    for (int64_t g = 0; g < groups; ++g) acc = acc + partial[g * V + v];
+__global__ void __launch_bounds__(256) db_finish_kernel(
+    const float* __restrict__ partial, int64_t groups, int64_t V, float* __restrict__ db_acc,
+    int first, int last, const int* __restrict__ offs,
+    const unsigned long long* __restrict__ keys, const float* __restrict__ tc_all,
+    TO* __restrict__ out) {
+    __shared__ float part[8][32];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int64_t v = blockIdx.x * int64_t(32) + lane;
+    float acc = 0.f;
+    if (v < V) {
+#pragma unroll 4
+        for (int64_t g = warp; g < groups; g += 8) acc = acc + partial[g * V + v];
+    }
+    part[warp][lane] = acc;
+    __syncthreads();
+    if (warp != 0 || v >= V) return;
+    float t = first ? 0.f : db_acc[v];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) t = t + part[w][lane];
     if (last) {
-        for (int i = offs[v]; i < offs[v + 1]; ++i) {
-            acc = acc + tc_all[keys[i] & 0xffffffffull];
-        }
-        out[v] = Elem<TO>::from_f(acc + 0.f);
+        for (int i = offs[v]; i < offs[v + 1]; ++i) t = t + tc_all[keys[i] & 0xffffffffull];
+        out[v] = Elem<TO>::from_f(t + 0.f);
     } else {
-        db_acc[v] = acc;
+        db_acc[v] = t;
     }
 }
 
-// Softmax part from stored FP32 logits, tile by tile exactly as the
-// recompute epilogue forms it: a warp takes 32 rows x 32 columns with lane =
-// row, p = 2^(z * log2e - lse * log2e), S = -grad * p off target, S = 0 and
-// tc = grad * (1 - p) at the target, and (with db_part) the same butterfly
-// column sums over the 32 rows.  Grid: x = row groups of 32, y = column
-// blocks of 4 warps x 32 columns (strided).
-template <typename T>
-__global__ void __launch_bounds__(128) softmax_part_kernel(
+// 5-bit bit reversal: the order in which a 32-row group's rows enter the
+// column sums below.
+__host__ __device__ constexpr int brev5(int i) {
+    return ((i & 1) << 4) | ((i & 2) << 2) | (i & 4) | ((i & 8) >> 2) | ((i & 16) >> 4);
+}
+
+// Softmax part from the stored FP32 logits of a chunk, with the values the
+// recompute epilogue forms: p = 2^(z * log2e - lse * log2e), S = -grad * p off
+// target, S = 0 and tc = grad * (1 - p) at the target.
+//
+// A block takes one group of 32 rows; each warp a 128-column slice of it
+// (4 columns a lane, so every row's slice is one coalesced 512-byte read and a
+// 256-byte 16-bit store), column slices strided over grid.y and the warps.
+// The rows are visited in bit-reversed order, and (with db_part) each lane
+// folds them into its columns' sums like a binary counter: entries 2k and
+// 2k + 1 of that order are rows r and r + 16, then pairs of pairs are rows
+// r, r + 8, and so on.  The sum of a column is thus the same binary tree
+// (rows paired across bit 4 of the row, then bit 3, ..., bit 0) that the
+// recompute epilogue's lane butterfly builds, and so bitwise its value.
+template <typename T, bool DB>
+__global__ void __launch_bounds__(256, 3) softmax_part_kernel(
     const float* __restrict__ Z, int64_t ldZ, int64_t rows, int64_t V,
     const int64_t* __restrict__ targets, const float* __restrict__ grad,
     const float* __restrict__ lse, T* __restrict__ S, int64_t ldS, float* __restrict__ tc,
     float* __restrict__ db_part, float inv_temp, T* __restrict__ S_lo) {
+    constexpr int kAhead = 8;  // rows whose loads are in flight together
     const int lane = threadIdx.x & 31;
-    const int64_t row = blockIdx.x * int64_t(32) + lane;
-    const bool rvalid = row < rows;
-    const int64_t y = rvalid ? targets[row] : -1;
-    const float g = rvalid ? grad[row] : 0.f;
-    const bool live = rvalid && y >= 0 && y < V && g != 0.f;
-    const float coef = live ? -g * inv_temp : 0.f;
-    const float lse2 = rvalid ? lse[row] * kLog2e : 0.f;
-    const int64_t nchunks = (V + 31) / 32;
-    for (int64_t ch = blockIdx.y * 4 + (threadIdx.x >> 5); ch < nchunks; ch += gridDim.y * 4) {
-        const int64_t col0 = ch * 32;
-        float v[32];
-        if (rvalid) {
+    const int warp = threadIdx.x >> 5;
+    const int64_t r0 = blockIdx.x * int64_t(32);
+    // lane r holds the parameters of row r0 + r
+    const int64_t my_row = r0 + lane;
+    const bool rvalid = my_row < rows;
+    const int64_t my_y = rvalid ? targets[my_row] : -1;
+    const float my_g = rvalid ? grad[my_row] : 0.f;
+    const bool live = rvalid && my_y >= 0 && my_y < V && my_g != 0.f;
+    const float my_coef = live ? -my_g * inv_temp : 0.f;
+    const float my_lse2 = rvalid ? lse[my_row] * kLog2e : 0.f;
+    if (rvalid && !(my_y >= 0 && my_y < V) && blockIdx.y == 0 && warp == 0) tc[my_row] = 0.f;
+    const int nr = static_cast<int>(rows - r0 < 32 ? rows - r0 : 32);
+    const int64_t step = int64_t(gridDim.y) * 8 * 128;
+    for (int64_t c = (int64_t(blockIdx.y) * 8 + warp) * 128 + 4 * lane; c - 4 * lane < V;
+         c += step) {
+        float acc[5][4];  // pending subtree sums, one per binary-counter level
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                if (col0 + 8 * q + 8 <= V) {
-                    load8(Z + row * ldZ + col0 + 8 * q, f);
-                } else {
+        for (int i0 = 0; i0 < 32; i0 += kAhead) {
+            float z[kAhead][4];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (col0 + 8 * q + j < V) f[j] = Z[row * ldZ + col0 + 8 * q + j];
+            for (int u = 0; u < kAhead; ++u) {
+                const int r = brev5(i0 + u);
+                z[u][0] = z[u][1] = z[u][2] = z[u][3] = 0.f;
+                if (r < nr && c < V) {
+                    // c + 3 < round_up(V, 4) <= ldZ: the vector stays in the row
+                    const float4 f = *reinterpret_cast<const float4*>(Z + (r0 + r) * ldZ + c);
+                    z[u][0] = f.x;
+                    z[u][1] = f.y;
+                    z[u][2] = f.z;
+                    z[u][3] = f.w;
                 }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) v[8 * q + j] = f[j];
             }
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = ex2(fmaf(v[j], kLog2e, -lse2));
-            const int64_t off = y - col0;
-            if (off >= 0 && off < 32) {
-                float py = 0.f;
+            for (int u = 0; u < kAhead; ++u) {
+                const int k = i0 + u;
+                const int r = brev5(k);
+                const float coef = __shfl_sync(0xffffffffu, my_coef, r);
+                const float lse2 = __shfl_sync(0xffffffffu, my_lse2, r);
+                const int64_t y = __shfl_sync(0xffffffffu, my_y, r);
+                float v[4] = {0.f, 0.f, 0.f, 0.f};
+                if (r < nr && c < V) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (j == off) py = v[j];
-                tc[row] = coef != 0.f ? -coef * (1.f - py) : 0.f;
+                    for (int j = 0; j < 4; ++j) v[j] = ex2(fmaf(z[u][j], kLog2e, -lse2));
+                    const int64_t off = y - c;
+                    if (off >= 0 && off < 4) {
+                        float py = 0.f;
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (j == off) v[j] = 0.f;
-            }
+                        for (int j = 0; j < 4; ++j)
+                            if (j == off) py = v[j];
+                        tc[r0 + r] = coef != 0.f ? -coef * (1.f - py) : 0.f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = coef * v[j];
+                        for (int j = 0; j < 4; ++j)
+                            if (j == off) v[j] = 0.f;
+                    }
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                if (col0 + 8 * q >= V) break;
-                float f[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) f[j] = v[8 * q + j];
-                if (col0 + 8 * q + 8 <= V) {
-                    store8(S + row * ldS + col0 + 8 * q, f);
-                } else {
-                    for (int j = 0; j < 8 && col0 + 8 * q + j < V; ++j)
-                        S[row * ldS + col0 + 8 * q + j] = Elem<T>::from_f(f[j]);
-                }
-                if (S_lo) {  // hi / lo split: the rounding rest S - S_hi
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) f[j] -= Elem<T>::to_f(Elem<T>::from_f(f[j]));
-                    if (col0 + 8 * q + 8 <= V) {
-                        store8(S_lo + row * ldS + col0 + 8 * q, f);
+                    for (int j = 0; j < 4; ++j) v[j] = coef * v[j];
+                    T* srow = S + (r0 + r) * ldS;
+                    T* lrow = S_lo ? S_lo + (r0 + r) * ldS : nullptr;
+                    if constexpr (sizeof(T) == 4) {  // FP32 S, no split
+                        if (c + 4 <= V) {
+                            *reinterpret_cast<float4*>(srow + c) =
+                                make_float4(v[0], v[1], v[2], v[3]);
+                        } else {
+                            for (int j = 0; j < 4 && c + j < V; ++j) srow[c + j] = v[j];
+                        }
                     } else {
-                        for (int j = 0; j < 8 && col0 + 8 * q + j < V; ++j)
-                            S_lo[row * ldS + col0 + 8 * q + j] = Elem<T>::from_f(f[j]);
+                        uint2 hu, lu;  // S rounded to T; the rest S - S_hi rounded to T
+                        T* hi = reinterpret_cast<T*>(&hu);
+                        T* lo = reinterpret_cast<T*>(&lu);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            hi[j] = Elem<T>::from_f(v[j]);
+                            lo[j] = Elem<T>::from_f(v[j] - Elem<T>::to_f(hi[j]));
+                        }
+                        if (c + 4 <= V) {
+                            *reinterpret_cast<uint2*>(srow + c) = hu;
+                            if (lrow) *reinterpret_cast<uint2*>(lrow + c) = lu;
+                        } else {
+                            for (int j = 0; j < 4 && c + j < V; ++j) {
+                                srow[c + j] = hi[j];
+                                if (lrow) lrow[c + j] = lo[j];
+                            }
+                        }
+                    }
+                }
+                if constexpr (DB) {  // binary counter over the visiting order
+                    bool carry = true;
+#pragma unroll
+                    for (int lvl = 0; lvl < 5; ++lvl) {
+                        if (!carry) break;
+                        if ((k >> lvl) & 1) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) v[j] = acc[lvl][j] + v[j];
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) acc[lvl][j] = v[j];
+                            carry = false;
+                        }
+                    }
+                    if (k == 31) {  // v is the sum of all 32 rows
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (c + j < V) db_part[blockIdx.x * V + c + j] = v[j];
                     }
                 }
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0.f;
-        }
-        if (db_part) {  // column sums over the 32 rows, the recompute's butterfly
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                const bool up = (lane & o) != 0;
-#pragma unroll
-                for (int j = 0; j < o; ++j) {
-                    const float keep = up ? v[j + o] : v[j];
-                    const float send = up ? v[j] : v[j + o];
-                    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                }
-            }
-            const int64_t col = col0 + lane;
-            if (col < V && blockIdx.x * int64_t(32) < rows) db_part[blockIdx.x * V + col] = v[0];
         }
     }
-    if (rvalid && !(y >= 0 && y < V) && blockIdx.y == 0 && threadIdx.x < 32) tc[row] = 0.f;
 }
 
 __global__ void fill_zero_kernel(uint32_t* p, int64_t n_words) {
@@ -334,65 +375,44 @@ cudaError_t launch_token_sort(const int64_t* targets, int64_t N, int64_t V, int6
     return cudaGetLastError();
 }
 
-size_t db_partial_bytes(int64_t Nc, int64_t V) {
-    const int64_t groups = Nc < 64 ? (Nc > 0 ? Nc : 1) : 64;
-    return static_cast<size_t>(groups + 1) * static_cast<size_t>(V) * 4;
-}
-
-cudaError_t launch_db_chunk(const void* S, int64_t ldS, int s_dtype, int64_t rows, int64_t V,
-                            float* partial, float* db_acc, int first, int last, const int* offs,
-                            const int64_t* keys, const float* tc_all, void* grad_bias,
-                            int out_dtype, cudaStream_t s) {
-    const int64_t groups = rows < 64 ? (rows > 0 ? rows : 1) : 64;
-    const int64_t rpg = (rows + groups - 1) / groups;
-    const dim3 grid(static_cast<unsigned>((V + 255) / 256), static_cast<unsigned>(groups));
-    note_launches(2);
-    if (s_dtype == LL_F32)
-        db_partial_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(S), ldS, rows, V,
-                                                      rpg, partial);
-    else if (s_dtype == LL_F16)
-        db_partial_kernel<__half><<<grid, 256, 0, s>>>(static_cast<const __half*>(S), ldS, rows,
-                                                       V, rpg, partial);
-    else
-        db_partial_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-            static_cast<const __nv_bfloat16*>(S), ldS, rows, V, rpg, partial);
-    const unsigned fb = static_cast<unsigned>((V + 255) / 256);
-    const unsigned long long* k = reinterpret_cast<const unsigned long long*>(keys);
-    if (out_dtype == LL_F32)
-        db_finish_kernel<float><<<fb, 256, 0, s>>>(partial, groups, V, db_acc, first, last, offs,
-                                                   k, tc_all, static_cast<float*>(grad_bias));
-    else if (out_dtype == LL_F16)
-        db_finish_kernel<__half><<<fb, 256, 0, s>>>(partial, groups, V, db_acc, first, last, offs,
-                                                    k, tc_all, static_cast<__half*>(grad_bias));
-    else
-        db_finish_kernel<__nv_bfloat16><<<fb, 256, 0, s>>>(
-            partial, groups, V, db_acc, first, last, offs, k, tc_all,
-            static_cast<__nv_bfloat16*>(grad_bias));
-    return cudaGetLastError();
-}
-
 cudaError_t launch_softmax_part(const float* Z, int64_t ldZ, int64_t rows, int64_t V,
                                 const int64_t* targets, const float* grad, const float* lse,
                                 void* S, int64_t ldS, int s_dtype, float* tc, float* db_part,
                                 float inv_temp, void* S_lo, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
     note_launches(1);
-    const int64_t nchunks = (V + 31) / 32;
-    int64_t gy = (nchunks + 3) / 4;
-    if (gy > 64) gy = 64;
+    // a block: 32 rows x (8 warps x 128 columns) per step of its column loop
+    int64_t gy = (V + 1023) / 1024;
+    if (gy > 65535) gy = 65535;
     const dim3 grid(static_cast<unsigned>((rows + 31) / 32), static_cast<unsigned>(gy));
-    if (s_dtype == LL_BF16)
-        softmax_part_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(
-            Z, ldZ, rows, V, targets, grad, lse, static_cast<__nv_bfloat16*>(S), ldS, tc, db_part,
-            inv_temp, static_cast<__nv_bfloat16*>(S_lo));
-    else if (s_dtype == LL_F16)
-        softmax_part_kernel<__half><<<grid, 128, 0, s>>>(Z, ldZ, rows, V, targets, grad, lse,
-                                                         static_cast<__half*>(S), ldS, tc, db_part,
-                                                         inv_temp, static_cast<__half*>(S_lo));
-    else
-        softmax_part_kernel<float><<<grid, 128, 0, s>>>(Z, ldZ, rows, V, targets, grad, lse,
-                                                        static_cast<float*>(S), ldS, tc, db_part,
-                                                        inv_temp, nullptr);
+    const bool db = db_part != nullptr;
+    if (s_dtype == LL_BF16) {
+        auto* Sp = static_cast<__nv_bfloat16*>(S);
+        auto* Lp = static_cast<__nv_bfloat16*>(S_lo);
+        if (db)
+            softmax_part_kernel<__nv_bfloat16, true><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, db_part, inv_temp, Lp);
+        else
+            softmax_part_kernel<__nv_bfloat16, false><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, nullptr, inv_temp, Lp);
+    } else if (s_dtype == LL_F16) {
+        auto* Sp = static_cast<__half*>(S);
+        auto* Lp = static_cast<__half*>(S_lo);
+        if (db)
+            softmax_part_kernel<__half, true><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, db_part, inv_temp, Lp);
+        else
+            softmax_part_kernel<__half, false><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, nullptr, inv_temp, Lp);
+    } else {
+        auto* Sp = static_cast<float*>(S);
+        if (db)
+            softmax_part_kernel<float, true><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, db_part, inv_temp, nullptr);
+        else
+            softmax_part_kernel<float, false><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, nullptr, inv_temp, nullptr);
+    }
     return cudaGetLastError();
 }
 
@@ -400,7 +420,7 @@ cudaError_t launch_db_finish(const float* partial, int64_t groups, int64_t V, fl
                              int first, int last, const int* offs, const int64_t* keys,
                              const float* tc_all, void* grad_bias, int out_dtype, cudaStream_t s) {
     note_launches(1);
-    const unsigned fb = static_cast<unsigned>((V + 255) / 256);
+    const unsigned fb = static_cast<unsigned>((V + 31) / 32);
     const unsigned long long* k = reinterpret_cast<const unsigned long long*>(keys);
     if (out_dtype == LL_F32)
         db_finish_kernel<float><<<fb, 256, 0, s>>>(partial, groups, V, db_acc, first, last, offs,

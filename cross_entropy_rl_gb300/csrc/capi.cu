@@ -162,13 +162,8 @@ FwdLayout fwd_layout(int64_t N, int64_t V) {
 
 constexpr size_t kAutoChunkBytes = size_t(2) << 30;  // softmax workspace budget
 
-// Rows of grad_bias partials a chunk of Nc tokens may write: one per 32 rows
-// (recompute epilogue) or up to 64 row groups (sums over the stored S).
-int64_t db_groups(int64_t Nc) {
-    const int64_t per32 = cdiv(Nc, 32);
-    const int64_t from_s = Nc < 64 ? (Nc > 0 ? Nc : 1) : 64;
-    return per32 > from_s ? per32 : from_s;
-}
+// Rows of grad_bias partials a chunk of Nc tokens writes: one per 32 rows.
+int64_t db_groups(int64_t Nc) { return Nc > 32 ? cdiv(Nc, 32) : 1; }
 
 struct BwdLayout {
     int64_t chunks, Nc, ldS, ldZ, n_segs;

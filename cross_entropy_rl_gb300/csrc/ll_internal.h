@@ -170,17 +170,11 @@ cudaError_t launch_lse_merge(const float* part_m, const float* part_s, const flo
 size_t token_sort_bytes(int64_t N);
 cudaError_t launch_token_sort(const int64_t* targets, int64_t N, int64_t V, int64_t* keys,
                               int* offs, cudaStream_t s);
-// db: column sums of S over the chunk's rows added into db_acc (FP32),
-// first chunk starts from +0; with `last`, adds the target entries c[n] of
-// the tokens of each vocab row and writes grad_bias in out_dtype.
-size_t db_partial_bytes(int64_t Nc, int64_t V);
-cudaError_t launch_db_chunk(const void* S, int64_t ldS, int s_dtype, int64_t rows, int64_t V,
-                            float* partial, float* db_acc, int first, int last, const int* offs,
-                            const int64_t* keys, const float* tc_all, void* grad_bias,
-                            int out_dtype, cudaStream_t s);
-// The finishing half of it, for partials [groups, V] written elsewhere (the
-// recompute epilogue): db_acc (+)= sum over groups in order, then on `last`
-// the target entries and the store.
+// grad_bias of a chunk from its partial rows [groups, V] (one per 32 rows
+// of S, written by the recompute epilogue or the softmax-part kernel):
+// db_acc (+)= their sum in a fixed order (the first chunk starts from +0);
+// with `last`, adds the target entries tc[n] of the tokens of each vocab row
+// (ascending token order) and writes grad_bias in out_dtype.
 cudaError_t launch_db_finish(const float* partial, int64_t groups, int64_t V, float* db_acc,
                              int first, int last, const int* offs, const int64_t* keys,
                              const float* tc_all, void* grad_bias, int out_dtype, cudaStream_t s);

@@ -274,6 +274,30 @@ def test_single_call_forward_backward_is_bitwise_the_two_calls(lib, dt, N, D, V,
     compare(p, one, full_ref(p))
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+def test_single_call_bitwise_with_invalid_targets_zero_rows_and_temperature(lib, dt):
+    """Rows with invalid targets or a zero upstream gradient, a ragged last
+    32-row group, a ragged vocab tail and T != 1: the single call's softmax
+    part (and its grad_bias partials) is still bitwise the recompute's."""
+    N, D, V = 389, 72, 2053
+    p = synth.linear_inputs(N, D, V, dtype=dt, bias=True, seed=41)
+    p["y"][[0, 33, 200, 388]] = [-100, V, V + 9, -1]
+    p["gl"][[5, 64, 387]] = [0.0, -0.0, 0.0]
+    T = 0.8
+    h, W, b, y, g = dev(p["h"], dt), dev(p["W"], dt), dev(p["b"], dt), dev(p["y"]), dev(p["gl"])
+    logp2, lse2 = lib.forward(h, W, b, y, temperature=T)
+    dh2, dW2, db2 = lib.backward(g, h, W, b, y, lse2, temperature=T, token_chunks=2)
+    logp1, lse1, dh1, dW1, db1 = lib.forward_backward(g, h, W, b, y, temperature=T,
+                                                      token_chunks=2)
+    torch.cuda.synchronize()
+    assert lib.check_status() == 0
+    for k, a, c in (("logp", logp1, logp2), ("lse", lse1, lse2), ("dh", dh1, dh2),
+                    ("dW", dW1, dW2), ("db", db1, db2)):
+        assert bits_equal(a, c), k
+    for r in (0, 33, 200, 388, 5, 64, 387):
+        assert_pos_zero(f"dh[{r}]", dh1[r])
+
+
 @pytest.mark.slow
 def test_single_call_bf16_4k_2k_32k_matches_two_calls(lib):
     p = synth.linear_inputs(**synth.WORKLOADS["bf16_4k_2k_32k"], seed=0)

@@ -404,6 +404,10 @@ def run_ours(args, rank, world, local_rank):
         fb_step()
     ms_fb = timed_loop(fb_step, args.steps)
     assert ll.check_status() == 0
+    ll.profile(True)
+    timed_loop(fb_step, args.steps)
+    prof_fb = ll.profile_summary()
+    ll.profile(False)
     if dist is not None:
         t = torch.tensor([ms_fb], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -465,6 +469,7 @@ def run_ours(args, rank, world, local_rank):
                         "ms_per_step": ms_fb,
                         "useful_frac_of_bf16_peak": 6.0 * N * D * V / (ms_fb * 1e-3) / 1e12
                         / pk["bf16_tflops"],
+                        "kernels_ms_per_step": {k: v[1] / args.steps for k, v in prof_fb.items()},
                         "call": "ll_forward_backward (grad_logp known before the forward; "
                                 "bitwise the outputs of ll_forward + ll_backward)"},
         "e2e": {"value": world * N / (ms_e2e * 1e-3), "unit": "tokens/s",

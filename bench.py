@@ -65,6 +65,34 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+def fp32_sgemm_tflops(device) -> float:
+    """The FP32 GEMM rate of this GPU through cuBLAS with TF32 off: the
+    denominator an FP32 user compares against."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=device)
+        b = torch.randn(n, n, device=device)
+        c = torch.empty(n, n, device=device)
+        torch.matmul(a, b, out=c)
+        best = float("inf")
+        for _ in range(5):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b, c
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
 def blas_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
@@ -440,6 +468,7 @@ def run_ours(args, rank, world, local_rank):
         peak, bound = pk["bf16_tflops"], "tensor"
     useful = 6.0 * N * D * V / (ms * 1e-3) / 1e12
     executed = 8.0 * N * D * V / (ms * 1e-3) / 1e12
+    sgemm = fp32_sgemm_tflops(device) if dt == "f32" else None
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -454,6 +483,10 @@ def run_ours(args, rank, world, local_rank):
         "useful_tflops": useful, "useful_frac_of_bf16_peak": useful / pk["bf16_tflops"],
         "useful_frac_of_peak": useful / peak, "peak_tflops": peak,
         "useful_frac_of_fp32_cuda_core_peak": useful / simt_peak if dt == "f32" else None,
+        "fp32_sgemm": None if sgemm is None else {
+            "tflops": sgemm, "useful_frac": useful / sgemm,
+            "how": "torch.matmul FP32 8192^3 with TF32 off, best of 5, CUDA events, "
+                   "measured in this run before the timed steps"},
         "executed_tflops_incl_recompute": executed,
         "peak_source": pk_kind,
         "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,

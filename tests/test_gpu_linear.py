@@ -298,6 +298,47 @@ def test_single_call_bitwise_with_invalid_targets_zero_rows_and_temperature(lib,
         assert_pos_zero(f"dh[{r}]", dh1[r])
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("N,V,chunks", [(1024, 1031, 0), (1500, 2053, 0), (2333, 777, 2)])
+def test_single_call_larger_chunks_bitwise_the_two_calls(lib, dt, N, V, chunks):
+    """Chunks of 1000+ rows with bias, invalid targets and zero upstream rows:
+    the single call's outputs are bitwise the two calls'."""
+    D = 136
+    p = synth.linear_inputs(N, D, V, dtype=dt, bias=True, seed=N + 3)
+    p["y"][[1, 700, N - 1]] = [-100, V, -1]
+    p["gl"][[2, 900]] = [0.0, -0.0]
+    two = run(lib, p, token_chunks=chunks)
+    h, W, b = dev(p["h"], dt), dev(p["W"], dt), dev(p["b"], dt)
+    logp, lse, dh, dW, db = lib.forward_backward(dev(p["gl"]), h, W, b, dev(p["y"]),
+                                                 token_chunks=chunks)
+    torch.cuda.synchronize()
+    assert lib.check_status() == 0
+    one = dict(logp=logp, lse=lse, dh=dh, dW=dW, db=db)
+    for k in ("logp", "lse", "dh", "dW", "db"):
+        assert bits_equal(one[k], two[k]), k
+
+
+def test_single_call_split_s_temperature_and_dw_only(lib):
+    """The single call with the hi / lo split of S, T != 1, and with
+    grad_hidden not requested: bitwise the two calls."""
+    N, D, V = 1300, 72, 1500
+    p = synth.linear_inputs(N, D, V, dtype="bf16", bias=True, seed=5)
+    h, W, b, y, g = (dev(p["h"], "bf16"), dev(p["W"], "bf16"), dev(p["b"], "bf16"),
+                     dev(p["y"]), dev(p["gl"]))
+    for need_dh in (True, False):
+        logp2, lse2 = lib.forward(h, W, b, y, temperature=0.9)
+        dh2, dW2, db2 = lib.backward(g, h, W, b, y, lse2, need_dh=need_dh, temperature=0.9,
+                                     split_s=True)
+        logp1, lse1, dh1, dW1, db1 = lib.forward_backward(g, h, W, b, y, need_dh=need_dh,
+                                                          temperature=0.9, split_s=True)
+        torch.cuda.synchronize()
+        assert lib.check_status() == 0
+        pairs = [("logp", logp1, logp2), ("lse", lse1, lse2), ("dW", dW1, dW2),
+                 ("db", db1, db2)] + ([("dh", dh1, dh2)] if need_dh else [])
+        for k, a, c in pairs:
+            assert bits_equal(a, c), (k, need_dh)
+
+
 @pytest.mark.slow
 def test_single_call_bf16_4k_2k_32k_matches_two_calls(lib):
     p = synth.linear_inputs(**synth.WORKLOADS["bf16_4k_2k_32k"], seed=0)

@@ -22,7 +22,12 @@
  * - Every call is asynchronous on `stream` (a cudaStream_t; NULL means the
  *   legacy default stream).  Outputs are valid once the stream reaches the
  *   call.  Arguments are validated on the host before anything is launched;
- *   on an error nothing is launched and no output is touched.
+ *   on an error nothing is launched and no output is touched.  Calls may be
+ *   in flight on several streams at once and may be recorded by CUDA stream
+ *   capture: work that overlaps a GEMM runs on a library side stream that is
+ *   forked from and joined back to `stream` by events.  The first call for a
+ *   given dtype and path sets kernel attributes and is best made outside a
+ *   capture.
  * - The library never allocates device memory.  The caller owns every buffer,
  *   including the scratch `workspace`, whose size ll_workspace_size() gives.
  *   A workspace must not be shared by calls that may overlap on the GPU.

@@ -265,15 +265,7 @@ __global__ void __launch_bounds__(kThreads) logits_bwd_kernel(
 // and the gradient stores release theirs (evict_first).  The row code is the
 // one of logits_fwd_kernel and logits_bwd_kernel, so every result is bitwise
 // theirs.  grad_logits may be the logits buffer itself.
-// Ask L2 for the 128-byte lines of [p, p + bytes), spread over the block.
-template <int NT>
-__device__ __forceinline__ void prefetch_l2(const void* p, int64_t bytes) {
-    const char* c = static_cast<const char*>(p);
-    for (int64_t o = int64_t(threadIdx.x) * 128; o < bytes; o += int64_t(NT) * 128)
-        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(c + o));
-}
-
-template <typename T, int U, bool PF = false, int NT = kThreads>
+template <typename T, int U, int NT = kThreads>
 __global__ void __launch_bounds__(NT) logits_fwd_bwd_kernel(
     const float* __restrict__ grad, const T* logits, int64_t ld,
     const int64_t* __restrict__ targets, int64_t N, int64_t V, float* __restrict__ logp,
@@ -281,13 +273,9 @@ __global__ void __launch_bounds__(NT) logits_fwd_bwd_kernel(
     __shared__ MS sh[NT / 32];
     __shared__ float lse_sh;
     const uint64_t keep = l2_evict_last(), drop = l2_evict_first();
-    const int64_t row_bytes = V * int64_t(sizeof(T));
-    if (PF && blockIdx.x < N) prefetch_l2<NT>(logits + blockIdx.x * ld, row_bytes);
     for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
         const T* x = logits + row * ld;
         const MS r = block_reduce<NT>(row_partial<T, U, true, NT>(x, V, vec_ok, keep, it), sh);
-        // the next row of this block streams into L2 during this row's second pass
-        if (PF && row + gridDim.x < N) prefetch_l2<NT>(logits + (row + gridDim.x) * ld, row_bytes);
         const int64_t y = targets[row];
         const float g = grad[row];
         const bool valid = (y >= 0) && (y < V);

@@ -115,3 +115,26 @@ def assert_pos_zero(name, t):
 def bits_equal(a, b):
     return torch.equal(a.view(torch.int8) if a.dtype != torch.int8 else a,
                        b.view(torch.int8) if b.dtype != torch.int8 else b)
+
+
+def bf16_round(r):
+    """float64 values rounded to the nearest bf16 (ties to even), as float64."""
+    r = np.asarray(r, np.float64)
+    b = r.astype(np.float32).view(np.uint32)
+    lo_bits = b & np.uint32(0xFFFF0000)
+    lo = lo_bits.view(np.float32).astype(np.float64)
+    hi = (lo_bits + np.uint32(0x10000)).view(np.float32).astype(np.float64)
+    dlo, dhi = np.abs(r - lo), np.abs(r - hi)
+    even = ((lo_bits >> np.uint32(16)) & np.uint32(1)) == 0
+    return np.where((dlo < dhi) | ((dlo == dhi) & even), lo, hi)
+
+
+def accuracy(got, ref):
+    """Max abs error, max error / max |ref|, and the fraction of entries equal
+    to the bf16 rounding of the FP64 reference."""
+    g = host64(got)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(g - ref)
+    return dict(max_abs=float(err.max()), max_over_max=float(err.max() / np.abs(ref).max()),
+                correctly_rounded=float(np.mean(g == bf16_round(ref))))
+

@@ -461,21 +461,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         epi1.chunk(ea, v, col0);
                     if (!stores) continue;
                     const int h = out16 ? (c & 1) : 0;
+                    // first column of the staged box (two chunks for 16-bit
+                    // outputs); a box past the output is neither staged nor
+                    // stored, so each staging buffer holds exactly one store
+                    const int64_t x0 = out16 ? col0 - 32 * h : col0;
+                    const bool put = row0 < P.out_rows[kind] && x0 < P.out_cols[kind];
                     uint8_t* sb = wbuf + (sidx & 1) * kOutBufBytes;
-                    if (h == 0) {  // the store that last used this buffer has read it
-                        if (lane == 0) bulk_wait_read_1();
-                        __syncwarp();
+                    if (put) {
+                        if (h == 0) {  // the store that last used this buffer has read it
+                            if (lane == 0) bulk_wait_read_1();
+                            __syncwarp();
+                        }
+                        stage_row<T>(sb, lane, v, out16, h);
                     }
-                    stage_row<T>(sb, lane, v, out16, h);
                     if (kind == 0) {
                         epi0.store_lo(ea, v, col0);  // hi / lo split of S (recompute only)
                         epi0.db_partials(ea, v, col0);  // grad_bias partials, consumes v
                     }
-                    if (!out16 || h == 1) {
+                    if (put && (!out16 || h == 1)) {
                         fence_proxy_async_smem();
                         __syncwarp();
-                        const int64_t x0 = out16 ? col0 - 32 : col0;
-                        if (lane == 0 && row0 < P.out_rows[kind] && x0 < P.out_cols[kind]) {
+                        if (lane == 0) {
                             if (reduce)
                                 tma_reduce_add_2d(tmO, sb, static_cast<int32_t>(x0),
                                                   static_cast<int32_t>(row0));
@@ -843,21 +849,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         epi1.chunk(ea, v, col0);
                     if (!stores) continue;
                     const int h = out16 ? (c & 1) : 0;
+                    const int64_t x0 = out16 ? col0 - 32 * h : col0;  // as in gemm_tc_kernel
+                    const bool put = row0 < P.out_rows[kind] && x0 < P.out_cols[kind];
                     uint8_t* sb = wbuf + (sidx & 1) * kOutBufBytes;
-                    if (h == 0) {
-                        if (lane == 0) bulk_wait_read_1();
-                        __syncwarp();
+                    if (put) {
+                        if (h == 0) {
+                            if (lane == 0) bulk_wait_read_1();
+                            __syncwarp();
+                        }
+                        stage_row<T>(sb, lane, v, out16, h);
                     }
-                    stage_row<T>(sb, lane, v, out16, h);
                     if (kind == 0) {
                         epi0.store_lo(ea, v, col0);
                         epi0.db_partials(ea, v, col0);
                     }
-                    if (!out16 || h == 1) {
+                    if (put && (!out16 || h == 1)) {
                         fence_proxy_async_smem();
                         __syncwarp();
-                        const int64_t x0 = out16 ? col0 - 32 : col0;
-                        if (lane == 0 && row0 < P.out_rows[kind] && x0 < P.out_cols[kind]) {
+                        if (lane == 0) {
                             if (reduce)
                                 tma_reduce_add_2d(tmO, sb, static_cast<int32_t>(x0),
                                                   static_cast<int32_t>(row0));
@@ -1326,14 +1335,20 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                     else
                         epi1.chunk(ea, v, col0);
                     if (!stores) continue;
+                    // a box past the output is neither staged nor stored (each
+                    // staging buffer holds exactly one store in flight)
+                    const bool put = row0 < P.out_rows[kind] && col0 < P.out_cols[kind];
                     uint8_t* sb = wbuf + (sidx & 1) * kOutBufBytes;
-                    if (lane == 0) bulk_wait_read_1();
-                    __syncwarp();
-                    stage_row<T>(sb, lane, v, false, 0);
+                    if (put) {
+                        if (lane == 0) bulk_wait_read_1();
+                        __syncwarp();
+                        stage_row<T>(sb, lane, v, false, 0);
+                    }
                     if (kind == 0) epi0.db_partials(ea, v, col0);
+                    if (!put) continue;
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0 && row0 < P.out_rows[kind] && col0 < P.out_cols[kind]) {
+                    if (lane == 0) {
                         if (reduce)
                             tma_reduce_add_2d(tmO, sb, static_cast<int32_t>(col0),
                                               static_cast<int32_t>(row0));

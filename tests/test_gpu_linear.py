@@ -131,6 +131,23 @@ def test_token_chunks(lib):
         compare(p, o, ref)
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_chunked_gradients_bitwise_whether_fused_or_alone(lib, dt):
+    """Several token chunks, small enough that each gradient launch is mostly
+    partial tiles: grad_hidden and grad_weight tiles launched together (one
+    dynamically scheduled launch) or each alone give the same bits."""
+    N, D, V = 1500, 136, 3001
+    p = synth.linear_inputs(N, D, V, dtype=dt, bias=True, seed=29)
+    p["y"][[3, 700]] = [-100, V]
+    for chunks in (2, 3, 5):
+        both = run(lib, p, token_chunks=chunks)
+        dh_only = run(lib, p, token_chunks=chunks, need=(1, 0, 0))
+        dw_only = run(lib, p, token_chunks=chunks, need=(0, 1, 1))
+        assert bits_equal(both["dh"], dh_only["dh"]), chunks
+        assert bits_equal(both["dW"], dw_only["dW"]), chunks
+        assert bits_equal(both["db"], dw_only["db"]), chunks
+
+
 def test_invalid_targets_and_zero_rows(lib):
     N, D, V = 260, 64, 700
     p = synth.linear_inputs(N, D, V, dtype="bf16", bias=True, seed=17)

@@ -913,7 +913,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // hi*hi + hi*lo + lo*hi (the lo*lo term, ~2^-22 of the product, is
 // dropped).  TMA lands 16 K-values of A [128 x 16] and B [256 x 16] in a
 // raw stage as they lie in memory: K-major operands in 64-byte rows
-// (64-byte swizzle), MN-major operands in 32-wide 128-byte boxes.  Four
+// (64-byte swizzle), MN-major operands in 32-wide 128-byte boxes.  Eight
 // converter warps write the hi and lo parts of both into a converted stage,
 // always K-major with 64-byte rows: kind::tf32 takes no MN-major operand, so
 // the converters transpose MN-major tiles on the way.
@@ -925,7 +925,10 @@ constexpr int kConvBytes = 2 * kRawBytes;      // hi A, hi B, lo A, lo B
 constexpr int kRawStages = 4;
 constexpr int kConvStages = 2;
 constexpr int kMnBoxF = 32 * kBKf * 4;         // one 32(MN) x 16(K) box, 2 KB
-constexpr int kThreadsF = 320;                 // 10 warps
+constexpr int kConvWarps = 8;                  // hi / lo converter warps
+constexpr int kConvThreads = kConvWarps * 32;
+constexpr int kThreadsF = 192 + kConvThreads;  // producer, MMA, 4 epilogue, converters
+static_assert(kConvThreads % 128 == 0, "converters split whole 128-thread groups");
 static_assert(kRawStages * kRawBytes + kConvStages * kConvBytes == kStages * kStageBytes,
               "tf32 rings fill the 16-bit kernel's stage memory");
 
@@ -999,14 +1002,14 @@ __device__ __forceinline__ void split_tf32(const uint4& x, uint4& hi, uint4& lo)
 
 // One operand of ROWS rows x 16 K-values from its raw stage into hi / lo in
 // K-major 64-byte rows (row r at r * 64, 16-byte chunk c at c ^ ((r >> 1) & 3),
-// the 64-byte swizzle).  ct = converter thread 0..127.
+// the 64-byte swizzle).  ct = converter thread 0..kConvThreads - 1.
 template <bool MN, int ROWS>
 __device__ __forceinline__ void convert_operand(const uint8_t* raw, uint8_t* hi, uint8_t* lo,
                                                 int ct) {
     if constexpr (!MN) {
         // already in that layout: split 16-byte vectors in place
 #pragma unroll
-        for (int e = ct; e < ROWS * 4; e += 128) {
+        for (int e = ct; e < ROWS * 4; e += kConvThreads) {
             const uint4 x = *reinterpret_cast<const uint4*>(raw + e * 16);
             uint4 h, l;
             split_tf32(x, h, l);
@@ -1017,10 +1020,12 @@ __device__ __forceinline__ void convert_operand(const uint8_t* raw, uint8_t* hi,
         // box j: K-row k (128 B) holds MN values 32j..32j+31, 16-byte chunk c
         // (MN values 4c..4c+3) at c ^ (k & 7).  Thread (mn = ct & 31,
         // q = ct >> 5) gathers K values 4q..4q+3 of one MN index.
-        const int m = ct & 31, q = ct >> 5;
+        // (the converter threads split the boxes: thread ct takes boxes
+        // ct / 128, ct / 128 + kConvThreads / 128, ...)
+        const int m = ct & 31, q = (ct >> 5) & 3;
         const uint32_t src = static_cast<uint32_t>((m & 3) * 4);
 #pragma unroll
-        for (int j = 0; j < ROWS / 32; ++j) {
+        for (int j = ct >> 7; j < ROWS / 32; j += kConvThreads / 128) {
             const uint8_t* box = raw + j * kMnBoxF;
             uint4 x;
             uint32_t* xv = reinterpret_cast<uint32_t*>(&x);
@@ -1071,10 +1076,10 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRawStages; ++s) {
             mbar_init(&bars->full[s], 1);
-            mbar_init(&bars->rempty[s], 4);  // the four converter warps
+            mbar_init(&bars->rempty[s], kConvWarps);
         }
         for (int s = 0; s < kConvStages; ++s) {
-            mbar_init(&bars->conv[s], 4);  // the four converter warps
+            mbar_init(&bars->conv[s], kConvWarps);
             mbar_init(&bars->empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -1083,7 +1088,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         }
         for (int s = 0; s < kSchedDepth; ++s) {
             mbar_init(&bars->sfull[s], 1);
-            mbar_init(&bars->sempty[s], 9);  // MMA + 4 epilogue + 4 converter warps
+            mbar_init(&bars->sempty[s], 5 + kConvWarps);  // MMA + 4 epilogue + converters
         }
         mbar_init(&bars->drain, 1);
         bars->abort = 0;
@@ -1194,7 +1199,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         }
     } else if (warp >= 6) {
         // ------------------------------------------------ hi / lo converters
-        const int ct = threadIdx.x - 6 * 32;  // 0..127
+        const int ct = threadIdx.x - 6 * 32;  // 0..kConvThreads - 1
         int rs = 0, cs = 0, sslot = 0;
         uint32_t rphase = 0, cphase = 0, sphase = 0;
         bool ok = true;

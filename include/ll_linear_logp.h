@@ -126,7 +126,7 @@ size_t ll_workspace_size(int64_t N, int64_t D, int64_t V, int dtype,
 /*
  * Forward.  Issue #261 "Current production path" (the linear_logp op) and
  * PR #495 "Summary" (logp of the selected token; lse is saved for backward).
- *   hidden  [N, D] dtype, device, 16-byte aligned, D * elemsize % 16 == 0
+ *   hidden  [N, D] dtype, device, 16-byte aligned; D a multiple of 8 (else LL_ERR_ALIGN)
  *   weight  [V, D] dtype, device, 16-byte aligned
  *   bias    [V]    dtype, device, or NULL
  *   targets [N]    int64, device

@@ -171,3 +171,43 @@ def test_options_are_validated_before_any_device_work(L):
                             ctypes.byref(o), None) == 1
     with pytest.raises(ValueError, match="temperature"):
         ll._opts(-2.0)
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include "ll_linear_logp.h"
+int main(void) {
+    /* host-only entry points: no device needed */
+    size_t ws = ll_workspace_size(4096, 2048, 32768, LL_BF16, 0, 1, 0);
+    ll_options opt = {1.0f, 0, {0, 0, 0, 0, 0, 0}};
+    (void)opt;
+    printf("%d %zu %s\n", ll_version(), ws, ll_status_string(LL_ERR_ALIGN));
+    return ws == 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(L, tmp_path):
+    """The header compiles as C99 (no C++ or torch types) and a C program
+    links against the shared library and calls its host-only entry points."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "use_abi"
+    lib_dir = os.path.dirname(B.LIB_PATH)
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER),
+                        str(src), "-o", str(exe), "-L", lib_dir,
+                        "-l:" + os.path.basename(B.LIB_PATH), "-Wl,-rpath," + lib_dir],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stderr
+    version, ws, name = r.stdout.split(maxsplit=2)
+    assert int(version) == L.ll_version()
+    assert int(ws) == L.ll_workspace_size(4096, 2048, 32768, ll.LL_BF16, 0, 1, 0)
+    assert name.strip() != ""

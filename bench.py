@@ -51,6 +51,10 @@ def parse():
     ap.add_argument("--dtype", default=None, choices=["bf16", "f16", "f32"],
                     help="operand dtype of the dtype sweep workload")
     ap.add_argument("--bias", action="store_true", help="dtype sweep workload with a bias")
+    ap.add_argument("--shards", type=int, default=0,
+                    help="also time the vocab-parallel composition with this many shards, "
+                         "run one after another on this GPU (the collectives replaced by "
+                         "their single-process equivalents)")
     ap.add_argument("--logits-rows", type=int, default=32768,
                     help="rows of the logits-input measurement (vocab 151936)")
     return ap.parse_args()
@@ -517,6 +521,8 @@ def run_ours(args, rank, world, local_rank):
                    "note": "one ll_forward + ll_backward allocating its outputs and "
                            "workspaces, max_memory_allocated above the resident inputs"},
     }
+    if args.shards > 1 and world == 1:
+        out["vocab_shards"] = shard_path(args, h, W, b, y, gl, ms, timed_loop, tdt, dw_dt)
     if not args.no_logits and args.workload == WORKLOAD:
         del ws_b, flush_buf
         torch.cuda.empty_cache()
@@ -524,6 +530,72 @@ def run_ours(args, rank, world, local_rank):
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(p)
     print(json.dumps(out), flush=True)
+
+
+def shard_path(args, h, W, b, y, gl, ms_whole, timed_loop, tdt, dw_dt):
+    """The vocab-parallel composition on one GPU: per step, each shard's
+    forward (segment partials), the ordered merge of all partials, each
+    shard's backward; the rank exchanges become a copy into the gathered
+    partials, a max over the shards' zy and a fixed-order sum of the
+    grad_hidden parts.  Compared with the whole-vocab step it shows what
+    sharding costs apart from the communication."""
+    import torch
+
+    import cross_entropy_rl_gb300 as ll
+    from cross_entropy_rl_gb300 import tp
+
+    K = args.shards
+    N, D = h.shape
+    V = W.shape[0]
+    dev = h.device
+    bounds = [(v0, v1) for v0, v1 in tp.shard_bounds(V, K) if v1 > v0]
+    segs = [ll.shard_segments(v1 - v0) for v0, v1 in bounds]
+    pm = torch.empty(sum(segs), N, dtype=torch.float32, device=dev)
+    ps = torch.empty_like(pm)
+    zys = [torch.empty(N, dtype=torch.float32, device=dev) for _ in bounds]
+    logp = torch.empty(N, dtype=torch.float32, device=dev)
+    lse = torch.empty_like(logp)
+    dh_parts = [torch.empty(N, D, dtype=torch.float32, device=dev) for _ in bounds]
+    dh = torch.empty(N, D, dtype=torch.float32, device=dev)
+    dW = torch.empty(V, D, dtype=dw_dt, device=dev)
+    db = torch.empty(V, dtype=dw_dt, device=dev) if b is not None else None
+    code = {torch.bfloat16: 2, torch.float16: 1, torch.float32: 0}[tdt]
+    L = ll.load()
+    ws_f = [torch.empty(max(256, L.ll_workspace_size_shard(N, D, v1 - v0, code, 0, 0, 0)),
+                        dtype=torch.uint8, device=dev) for v0, v1 in bounds]
+    ws_b = [torch.empty(max(256, L.ll_workspace_size_shard(N, D, v1 - v0, code, 0, 1,
+                                                           int(b is not None))),
+                        dtype=torch.uint8, device=dev) for v0, v1 in bounds]
+
+    def step():
+        s0 = 0
+        for i, (v0, v1) in enumerate(bounds):
+            bb = None if b is None else b[v0:v1]
+            ll.forward_shard(h, W[v0:v1], bb, y, v0, V, workspace=ws_f[i],
+                             out=(pm[s0:s0 + segs[i]], ps[s0:s0 + segs[i]], zys[i]))
+            s0 += segs[i]
+        zy = zys[0]
+        for z in zys[1:]:
+            zy = torch.maximum(zy, z)
+        ll.lse_merge(pm, ps, zy, y, V, out=(logp, lse))
+        for i, (v0, v1) in enumerate(bounds):
+            bb = None if b is None else b[v0:v1]
+            ll.backward_shard(gl, h, W[v0:v1], bb, y, lse, v0, V, workspace=ws_b[i],
+                              out=(dh_parts[i], dW[v0:v1], None if db is None else db[v0:v1]))
+        dh.copy_(dh_parts[0])
+        for part in dh_parts[1:]:
+            dh.add_(part)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert ll.check_status() == 0
+    ms = timed_loop(step, args.steps)
+    return {"shards": len(bounds), "ms_per_step": ms, "value": N / (ms * 1e-3),
+            "unit": "tokens/s", "ratio_to_whole_vocab": ms / ms_whole,
+            "note": "shards run one after another on one GPU; the rank exchanges "
+                    "(partials gather, zy max, grad_hidden sum) are single-process "
+                    "copies, max and adds; grad_hidden accumulated in FP32"}
 
 
 def logits_path(args, device, pk):

@@ -331,7 +331,7 @@ cudaError_t forward_gemm(const void* hidden, const void* weight, const void* bia
     G.dtype = dtype;
     G.nkinds = 1;
     G.kind[0] = EpiKind::Fwd;
-    G.op[0] = GemmOperands{hidden, D, 0, weight, D, 0, N, V, D};
+    G.op[0] = GemmOperands{hidden, D, 0, weight, D, 0, N, V, D, nullptr};
     G.shape[0] = sh;
     G.ea[0] = ea;
     Phase ph(dtype == LL_F32 ? "fwd_gemm_f32" : "fwd_gemm", s);
@@ -508,7 +508,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             G.dtype = dtype;
             G.nkinds = 1;
             G.kind[0] = EpiKind::Recomp;
-            G.op[0] = GemmOperands{h_c, D, 0, weight, D, 0, rows, V, D};
+            G.op[0] = GemmOperands{h_c, D, 0, weight, D, 0, rows, V, D, nullptr};
             GemmShape& sh = G.shape[0];
             sh.m_blocks = cdiv(rows, kBM);
             sh.n_tiles = cdiv(V, kBN);
@@ -542,7 +542,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             G.dtype = dtype;
             G.nkinds = 1;
             G.kind[0] = EpiKind::Fwd;
-            G.op[0] = GemmOperands{h_c, D, 0, weight, D, 0, rows, V, D};
+            G.op[0] = GemmOperands{h_c, D, 0, weight, D, 0, rows, V, D, nullptr};
             GemmShape& sh = G.shape[0];
             sh.m_blocks = cdiv(rows, kBM);
             sh.n_tiles = cdiv(V, kBN);

@@ -141,7 +141,6 @@ __device__ __forceinline__ Unit decode_unit(const KParams& P, int64_t u) {
 template <typename T, EpiKind E, bool A_MN, bool B_MN>
 struct Kind {
     using Epi = RowEpilogue<E, T>;
-    static constexpr EpiKind kEpi = E;
     static constexpr bool kAmn = A_MN, kBmn = B_MN;
     static constexpr int kFmt = std::is_same<T, __half>::value   ? 0
                                 : std::is_same<T, float>::value ? 2  // tf32

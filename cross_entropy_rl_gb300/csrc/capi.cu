@@ -179,9 +179,11 @@ BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need
     L.ldZ = round_up(V, 8);
     L.n_segs = cdiv(cdiv(V, kBN), kVocabTilesPerSeg);
     split = split && dtype != LL_F32;
-    const size_t row_bytes =
-        size_t(L.ldS) * esize(dtype) * (split ? 2 : 1) +
-        (fused ? size_t(L.ldZ) * 4 + size_t(L.n_segs) * 8 + 4 : 0);
+    // The automatic chunk count depends on the softmax part S alone, so the
+    // two calls, the single call and the hi / lo split choose the same chunks
+    // (and so give the same grad_weight bits); the single call's FP32 logits
+    // and the split's S_lo come on top of the budget.
+    const size_t row_bytes = size_t(L.ldS) * esize(dtype);
     const int64_t n1 = N > 0 ? N : 1;
     int64_t k = token_chunks;
     if (k <= 0) {

@@ -14,11 +14,13 @@
 // The array's name is only a host-side stand-in in host code, so its device
 // address is looked up with cudaGetSymbolAddress, once per device, with that
 // device current; the first call on a device does this set-up, so that first
-// call should come before any stream capture.  All calls on a device share
-// the one array and it keeps the last call's contents: the forward writes
-// every scratch entry it reads before reading it, so nothing needs clearing,
-// and calls that may overlap on the GPU (different streams, or host threads)
-// race on it.
+// call should come before any stream capture.  The address is kept for the
+// life of the process: do not call this entry point on a device after
+// cudaDeviceReset of that device (the library's module, and the array with it,
+// is reloaded at a new address).  All calls on a device share the one array
+// and it keeps the last call's contents: the forward writes every scratch
+// entry it reads before reading it, so nothing needs clearing, and calls that
+// may overlap on the GPU (different streams, or host threads) race on it.
 #include <stdio.h>
 
 #include <mutex>
@@ -61,7 +63,13 @@ extern "C" int ll_forward_noalloc(const void* hidden, const void* weight, const 
                                   const int64_t* targets, int64_t N, int64_t D, int64_t V,
                                   int dtype, float* logp, float* lse, void* stream) {
     using namespace ll;
-    if (!weight) return LL_ERR_INVALID_ARG;
+    // ll_forward's own argument checks, with no workspace: an invalid argument
+    // gives ll_forward's error, N == 0 gives LL_OK with nothing launched, and
+    // a valid problem that needs scratch gives LL_ERR_WORKSPACE.  Nothing
+    // runs on the device in any of these cases.
+    const int pre = ll_forward(hidden, weight, bias, targets, N, D, V, dtype, logp, lse,
+                               nullptr, 0, stream);
+    if (pre != LL_ERR_WORKSPACE) return pre;
     const size_t need = ll_workspace_size(N, D, V, dtype, 0, 0, 0);
     if (need > kNoAllocScratchBytes) {
         fprintf(stderr,
@@ -71,9 +79,10 @@ extern "C" int ll_forward_noalloc(const void* hidden, const void* weight, const 
                 kNoAllocScratchBytes);
         return LL_ERR_WORKSPACE;
     }
-    // the device that owns the weight, current while the address is looked up
+    // the device that owns the hidden states (ll_forward runs there), current
+    // while the address is looked up
     cudaPointerAttributes attr;
-    if (cudaPointerGetAttributes(&attr, weight) != cudaSuccess) {
+    if (cudaPointerGetAttributes(&attr, hidden) != cudaSuccess) {
         cudaGetLastError();
         return LL_ERR_INVALID_ARG;
     }

@@ -48,6 +48,9 @@
  * - Device-side waits are bounded.  A wait that runs out records
  *   LL_ERR_DEVICE_TIMEOUT in a per-device status word that ll_check_status()
  *   returns; the kernel then returns without hanging the device.
+ * - The library keeps per-device state for the life of the process (device
+ *   properties, the device address of its status word, kernel attributes).
+ *   Do not use it on a device after cudaDeviceReset of that device.
  */
 #ifndef LL_LINEAR_LOGP_H
 #define LL_LINEAR_LOGP_H
@@ -141,9 +144,11 @@ int ll_forward(const void* hidden, const void* weight, const void* bias,
 
 /*
  * Backward.  Issue #261 "Current accumulation" (FP32 grad_w table, per-chunk
- * accumulation) and "Static traffic model" (C = floor(2^24 / V) rows per
- * chunk); Liger-Kernel PR #1324 "Details" (accumulate each chunk's
- * contribution into grad_weight with no [V, D] temporary).
+ * accumulation; its "Static traffic model" prices the chunking); Liger-Kernel
+ * PR #1324 "Details" (accumulate each chunk's contribution into grad_weight
+ * with no [V, D] temporary).  The automatic chunk size is not #261's rule of
+ * C = floor(2^24 / V) rows: it is a 2 GiB budget on the chunk's softmax part
+ * (below).
  *   grad_logp [N] float, device.  hidden/weight/bias/targets as in ll_forward.
  *   lse       [N] float, device: the forward's lse for the same inputs.
  *   need_dh / need_dw / need_db: which gradients to produce (0 or 1).
@@ -153,9 +158,10 @@ int ll_forward(const void* hidden, const void* weight, const void* bias,
  *     accumulates each token chunk in FP32 and rounds the running table once
  *     per chunk (once in total when token_chunks == 1).
  *   grad_bias [V] of dw_dtype (written when need_db; requires a bias).
- *   token_chunks: 0 = automatic (one chunk when its softmax workspace is at
- *     most 2 GiB, otherwise the fewest chunks that fit), else the number of
- *     chunks N is split into, in order.  logp-independent outputs (dh) are
+ *   token_chunks: 0 = automatic (one chunk when its softmax part S,
+ *     [rows, round_up(V, 8)] in the operand dtype, is at most 2 GiB, otherwise
+ *     the fewest chunks of a multiple of 128 rows whose S fits), else the
+ *     number of chunks N is split into, in order.  logp-independent outputs (dh) are
  *     bitwise independent of token_chunks; dW/db differ by FP32 rounding.
  * N == 0: grad_weight / grad_bias (if requested) are filled with +0.
  */
@@ -173,10 +179,11 @@ int ll_backward(const float* grad_logp, const void* hidden, const void* weight,
  * forward (a fixed loss weighting such as a mean cross entropy, as in the
  * fused linear cross entropy of Liger-Kernel PR #1324, "Summary").  Same
  * arguments and results as ll_forward followed by ll_backward (logp and lse
- * are written as the forward's outputs), bitwise: each token chunk's forward
- * GEMM keeps its FP32 logits in the workspace (one chunk's worth, bounded by
- * the same 2 GiB automatic budget, never the whole [N, V] beyond it), and
- * the softmax part is formed from them instead of recomputing the logits.
+ * are written as the forward's outputs), bitwise, for the same token_chunks
+ * (token_chunks = 0 chooses the same chunks as ll_backward): each token
+ * chunk's forward GEMM keeps its FP32 logits in the workspace (one chunk's
+ * worth, never the whole [N, V] beyond it), and the softmax part is formed
+ * from them instead of recomputing the logits.
  * Workspace: ll_workspace_size(..., is_backward = 2, need_db).
  */
 int ll_forward_backward(const float* grad_logp, const void* hidden, const void* weight,
@@ -289,15 +296,19 @@ int ll_backward_shard(const float* grad_logp, const void* hidden, const void* we
  * it exists for callers that cannot allocate device memory (a framework
  * that forbids allocation during a step, plugin code without access to the
  * application's allocator).  Same arguments, results and errors as
- * ll_forward, minus the workspace: the scratch lives in a static 8 MiB
+ * ll_forward, minus the workspace (argument errors and N == 0 are answered
+ * exactly as ll_forward answers them): the scratch lives in a static 8 MiB
  * (8388608-byte) device array of the library, held on every GPU that loads
- * the library until the process exits.  Problems needing more scratch than
- * that, (2 * ceil(V / 1024) + 1) * N * 4 bytes with 256-byte padding (the
- * forward's ll_workspace_size), are rejected with LL_ERR_WORKSPACE before
- * anything runs.  The first call on a device looks up the array's device
- * address (cudaGetSymbolAddress with that device current); make that first
- * call before any stream capture.  It allocates nothing.  All calls on a
- * device share the one array, which keeps the last call's contents: calls
+ * the library until the process exits.  A problem whose forward workspace,
+ * ll_workspace_size(N, D, V, dtype, 0, 0) (three regions of
+ * ceil(V / 1024) * N, ceil(V / 1024) * N and N floats, each padded to 256
+ * bytes), exceeds that is rejected with LL_ERR_WORKSPACE before anything
+ * runs: N <= 32262 fits at V = 32768, N <= 7013 at V = 151936.  The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress
+ * with the device of `hidden` current) and keeps it for the process; make
+ * that first call before any stream capture, and do not call it on a device
+ * after cudaDeviceReset of that device.  It allocates nothing.  All calls on
+ * a device share the one array, which keeps the last call's contents: calls
  * that may overlap on the GPU (other streams, other host threads) race.
  */
 int ll_forward_noalloc(const void* hidden, const void* weight, const void* bias,

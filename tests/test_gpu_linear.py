@@ -356,6 +356,27 @@ def test_single_call_split_s_temperature_and_dw_only(lib):
             assert bits_equal(a, c), (k, need_dh)
 
 
+def test_single_call_automatic_chunks_bitwise_the_two_calls(lib):
+    """With token_chunks = 0 and a softmax part larger than the 2 GiB budget
+    (8192 x 151936 bf16 = 2.5 GB, so two chunks), the single call picks the
+    same chunks as the two calls: grad_weight too is bitwise theirs."""
+    N, D, V = 8192, 64, 151936
+    g = torch.Generator(device="cuda")
+    g.manual_seed(11)
+    h = torch.randn(N, D, generator=g, device="cuda").to(torch.bfloat16)
+    W = (torch.randn(V, D, generator=g, device="cuda") * D ** -0.5).to(torch.bfloat16)
+    y = torch.randint(0, V, (N,), generator=g, device="cuda")
+    gl = torch.randn(N, generator=g, device="cuda")
+    logp2, lse2 = lib.forward(h, W, None, y)
+    dh2, dW2, _ = lib.backward(gl, h, W, None, y, lse2, token_chunks=0)
+    logp1, lse1, dh1, dW1, _ = lib.forward_backward(gl, h, W, None, y, token_chunks=0)
+    torch.cuda.synchronize()
+    assert lib.check_status() == 0
+    for k, a, c in (("logp", logp1, logp2), ("lse", lse1, lse2), ("dh", dh1, dh2),
+                    ("dW", dW1, dW2)):
+        assert bits_equal(a, c), k
+
+
 @pytest.mark.slow
 def test_single_call_bf16_4k_2k_32k_matches_two_calls(lib):
     p = synth.linear_inputs(**synth.WORKLOADS["bf16_4k_2k_32k"], seed=0)

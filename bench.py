@@ -48,11 +48,18 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--token-chunks", type=int, default=0)
+    ap.add_argument("--split-s", default="auto", choices=["auto", "always", "never"],
+                    help="hi / lo split of the softmax part S (16-bit operands)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-logits", action="store_true",
                     help="skip the logits-input path measurement")
     ap.add_argument("--no-small", action="store_true",
                     help="skip the 4096 x 2048 x 32768 step measured beside the default one")
+    ap.add_argument("--no-single", action="store_true",
+                    help="skip the single-call (ll_forward_backward) measurement")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="override the workload's token count (a smaller case of the same "
+                         "shape, for profiling)")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["fp32_small", "bf16_4k_2k_32k", "sweep_16k_4k_32000",
                              "bf16_32k_4k_151936"],
@@ -66,6 +73,8 @@ def parse():
                          "their single-process equivalents)")
     ap.add_argument("--logits-rows", type=int, default=32768,
                     help="rows of the logits-input measurement (vocab 151936)")
+    ap.add_argument("--logits-only", action="store_true",
+                    help="time only the logits-input path (for profiling; prints its object)")
     return ap.parse_args()
 
 
@@ -332,7 +341,7 @@ def run_ours(args, rank, world, local_rank):
     import torch
 
     import cross_entropy_rl_gb300 as ll
-    from cross_entropy_rl_gb300 import synth
+    from cross_entropy_rl_gb300 import dp, synth
 
     dist = None
     if world > 1:
@@ -340,9 +349,15 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
     ll.load()
+    if args.logits_only:
+        if rank == 0:
+            print(json.dumps(logits_path(args, device, peaks()[0])), flush=True)
+        return
     wl = dict(synth.WORKLOADS[args.workload])
     if args.workload == "sweep_16k_4k_32000":
         wl.update(dtype=args.dtype or "bf16", bias=args.bias)
+    if args.rows > 0:
+        wl.update(N=args.rows)
     p = synth.linear_inputs(**wl, seed=rank)
     N, D, V, dt = p["N"], p["D"], p["V"], p["dtype"]
     tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[dt]
@@ -366,9 +381,10 @@ def run_ours(args, rank, world, local_rank):
     db = torch.empty(V, dtype=dw_dt, device=device) if has_bias else None
     ws_f = torch.empty(max(256, ll.workspace_size(N, D, V, tdt)), dtype=torch.uint8,
                        device=device)
-    ws_b = torch.empty(max(256, ll.workspace_size(N, D, V, tdt, args.token_chunks,
-                                                  backward=True, need_db=has_bias)),
-                       dtype=torch.uint8, device=device)
+    split_code = ll.SPLIT_MODES[args.split_s]
+    ws_b = torch.empty(max(256, ll.load().ll_workspace_size(
+        N, D, V, ll._code(tdt), args.token_chunks, 1, int(has_bias) | (split_code << 1))),
+        dtype=torch.uint8, device=device)
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
 
@@ -376,7 +392,14 @@ def run_ours(args, rank, world, local_rank):
         ll.forward(hh, W, b, yy, workspace=ws_f, out=(logp, lse))
         ll.backward(gg, hh, W, b, yy, lse, need_dh=True, need_dw=True, need_db=has_bias,
                     dh_dtype=tdt, dw_dtype=dw_dt, token_chunks=args.token_chunks,
-                    workspace=ws_b, out=(dh, dW, db))
+                    split_s=args.split_s, workspace=ws_b, out=(dh, dW, db))
+        if world > 1:
+            # the gradient exchange of token-sharded data parallelism: the
+            # ranks' grad_weight (and grad_bias) tables summed in ascending
+            # rank order, slice by slice, then gathered (dp.py)
+            dp.reduce_sum_fixed_order(dW)
+            if db is not None:
+                dp.reduce_sum_fixed_order(db)
 
     def barrier():
         if dist is not None:
@@ -412,7 +435,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.reset_peak_memory_stats(device)
     m_logp, m_lse = ll.forward(h, W, b, y)
     m_out = ll.backward(gl, h, W, b, y, m_lse, need_db=has_bias, dh_dtype=tdt, dw_dtype=dw_dt,
-                        token_chunks=args.token_chunks)
+                        token_chunks=args.token_chunks, split_s=args.split_s)
     torch.cuda.synchronize()
     mem_peak = torch.cuda.max_memory_allocated(device) - mem_base
     del m_logp, m_lse, m_out
@@ -494,28 +517,30 @@ def run_ours(args, rank, world, local_rank):
         ms_e2e = float(t.item())
 
     # single call (upstream gradient known before the forward): no logits recompute
-    ws_fb = torch.empty(max(256, ll.workspace_size(N, D, V, tdt, args.token_chunks,
-                                                   backward=2, need_db=has_bias)),
-                        dtype=torch.uint8, device=device)
+    ms_fb, prof_fb = None, {}
+    if not args.no_single:
+        ws_fb = torch.empty(max(256, ll.load().ll_workspace_size(
+            N, D, V, ll._code(tdt), args.token_chunks, 2, int(has_bias) | (split_code << 1))),
+            dtype=torch.uint8, device=device)
 
-    def fb_step():
-        ll.forward_backward(gl, h, W, b, y, need_dh=True, need_dw=True, need_db=has_bias,
-                            dh_dtype=tdt, dw_dtype=dw_dt, token_chunks=args.token_chunks,
-                            workspace=ws_fb, out=(logp, lse, dh, dW, db))
+        def fb_step():
+            ll.forward_backward(gl, h, W, b, y, need_dh=True, need_dw=True, need_db=has_bias,
+                                dh_dtype=tdt, dw_dtype=dw_dt, token_chunks=args.token_chunks,
+                                split_s=args.split_s, workspace=ws_fb, out=(logp, lse, dh, dW, db))
 
-    for _ in range(args.warmup):
-        fb_step()
-    ms_fb = timed_loop(fb_step, args.steps)
-    assert ll.check_status() == 0
-    ll.profile(True)
-    timed_loop(fb_step, args.steps)
-    prof_fb = ll.profile_summary()
-    ll.profile(False)
-    if dist is not None:
-        t = torch.tensor([ms_fb], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_fb = float(t.item())
-    del ws_fb
+        for _ in range(args.warmup):
+            fb_step()
+        ms_fb = timed_loop(fb_step, args.steps)
+        assert ll.check_status() == 0
+        ll.profile(True)
+        timed_loop(fb_step, args.steps)
+        prof_fb = ll.profile_summary()
+        ll.profile(False)
+        if dist is not None:
+            t = torch.tensor([ms_fb], device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_fb = float(t.item())
+        del ws_fb
 
     if rank != 0:
         return
@@ -564,8 +589,14 @@ def run_ours(args, rank, world, local_rank):
                    "grad_weight": str(dw_dt).replace("torch.", ""),
                    "grad_hidden": str(tdt).replace("torch.", ""),
                    "token_chunks": args.token_chunks or "auto",
+                   "split_s": args.split_s if dt != "f32" else None,
                    "l2": "flushed between steps (512 MiB write outside the timed events)",
-                   "parallelism": f"dp{world}"},
+                   "parallelism": f"dp{world}",
+                   "dp_sync": None if world == 1 else {
+                       "what": "grad_weight (+ grad_bias) summed over ranks in ascending rank "
+                               "order: all-to-all reduce-scatter + ll_sum_ordered + all-gather, "
+                               "inside the timed step",
+                       "bytes_per_rank": dp.slice_bytes(dW.numel(), dW.element_size(), world)}},
         "useful_tflops": useful, "useful_frac_of_bf16_peak": useful / pk["bf16_tflops"],
         "useful_frac_of_sustained_bf16_peak": useful / bf16_sus,
         "useful_frac_of_peak": useful / peak, "peak_tflops": peak,
@@ -590,13 +621,13 @@ def run_ours(args, rank, world, local_rank):
                      "flops_per_launch": launch_flops, "launches_per_step": cnt / args.steps},
         "kernels_ms_per_step": {k: v[1] / args.steps for k, v in prof.items()},
         "gpu_launches": launches,
-        "single_call": {"value": world * N / (ms_fb * 1e-3), "unit": "tokens/s",
-                        "ms_per_step": ms_fb,
-                        "useful_frac_of_bf16_peak": 6.0 * N * D * V / (ms_fb * 1e-3) / 1e12
-                        / pk["bf16_tflops"],
-                        "kernels_ms_per_step": {k: v[1] / args.steps for k, v in prof_fb.items()},
-                        "call": "ll_forward_backward (grad_logp known before the forward; "
-                                "bitwise the outputs of ll_forward + ll_backward)"},
+        "single_call": None if ms_fb is None else {
+            "value": world * N / (ms_fb * 1e-3), "unit": "tokens/s", "ms_per_step": ms_fb,
+            "useful_frac_of_bf16_peak": 6.0 * N * D * V / (ms_fb * 1e-3) / 1e12
+            / pk["bf16_tflops"],
+            "kernels_ms_per_step": {k: v[1] / args.steps for k, v in prof_fb.items()},
+            "call": "ll_forward_backward (grad_logp known before the forward; "
+                    "bitwise the outputs of ll_forward + ll_backward)"},
         "e2e": {"value": world * N / (ms_e2e * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h.numel() * h.element_size() + y.numel() * 8 + gl.numel() * 4,
                 "d2h_bytes_per_step": logp.numel() * 4, "ms_per_step": ms_e2e,

@@ -88,6 +88,7 @@ EXPORTS = {
     "ll_launch_count": (ctypes.c_longlong, []),
     "ll_profile_enable": (None, [_c_int]),
     "ll_profile_summary": (_c_int, [ctypes.c_char_p, _c_size]),
+    "ll_sum_ordered": (_c_int, [_c_p, _c_i64, _c_i64, _c_i64, _c_int, _c_p, _c_p]),
 }
 
 
@@ -97,14 +98,30 @@ class Options(ctypes.Structure):
                 ("reserved", ctypes.c_int * 6)]
 
 
-def _opts(temperature=1.0, split_s=False):
+SPLIT_MODES = {"auto": 0, "always": 1, "never": 2}
+
+
+def _split_code(split_s) -> int:
+    """ll_options.split_s of a binding argument: "auto" (or None, the
+    default), "always" (or True) or "never" (or False)."""
+    if split_s is None:
+        return 0
+    if isinstance(split_s, bool):
+        return 1 if split_s else 2
+    if split_s not in SPLIT_MODES:
+        raise ValueError(f"split_s must be one of {sorted(SPLIT_MODES)}, True, False or None")
+    return SPLIT_MODES[split_s]
+
+
+def _opts(temperature=1.0, split_s="auto"):
     """ll_options pointer for a call (None when every option is default)."""
     t = 1.0 if temperature is None else float(temperature)
     if not t > 0:
         raise ValueError("temperature must be > 0")
-    if t == 1.0 and not split_s:
+    code = _split_code(split_s)
+    if t == 1.0 and code == 0:
         return None
-    return ctypes.byref(Options(temperature=t, split_s=int(bool(split_s))))
+    return ctypes.byref(Options(temperature=t, split_s=code))
 
 
 class LLError(RuntimeError):
@@ -279,7 +296,7 @@ def forward(hidden, weight, bias, targets, *, temperature=1.0, workspace=None, o
 
 def backward(grad_logp, hidden, weight, bias, targets, lse, *, need_dh=True, need_dw=True,
              need_db=None, dh_dtype=None, dw_dtype=None, token_chunks=0, temperature=1.0,
-             split_s=False, workspace=None, out=None, stream=None):
+             split_s="auto", workspace=None, out=None, stream=None):
     """(grad_hidden, grad_weight, grad_bias); entries not requested are None.
 
     dw_dtype defaults to float32; grad_bias uses dw_dtype.
@@ -295,7 +312,7 @@ def backward(grad_logp, hidden, weight, bias, targets, lse, *, need_dh=True, nee
     dh, dW, db, dh_dtype, dw_dtype = _grad_outputs(out, need_dh, need_dw, need_db, N, D, V,
                                                    hidden.dtype, dh_dtype, dw_dtype, dev)
     ws_need = L.ll_workspace_size(N, D, V, code, token_chunks, 1,
-                                  int(bool(need_db)) | (int(bool(split_s)) << 1))
+                                  int(bool(need_db)) | (_split_code(split_s) << 1))
     if workspace is None:
         workspace = _workspace(ws_need, dev)
     _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
@@ -311,7 +328,7 @@ def backward(grad_logp, hidden, weight, bias, targets, lse, *, need_dh=True, nee
 
 def forward_backward(grad_logp, hidden, weight, bias, targets, *, need_dh=True, need_dw=True,
                      need_db=None, dh_dtype=None, dw_dtype=None, token_chunks=0,
-                     temperature=1.0, split_s=False, workspace=None, out=None, stream=None):
+                     temperature=1.0, split_s="auto", workspace=None, out=None, stream=None):
     """(logp, lse, grad_hidden, grad_weight, grad_bias) in one call, for a
     grad_logp known before the forward; bitwise equal to forward + backward."""
     torch = _torch()
@@ -333,7 +350,7 @@ def forward_backward(grad_logp, hidden, weight, bias, targets, *, need_dh=True, 
     dh, dW, db, dh_dtype, dw_dtype = _grad_outputs(grads, need_dh, need_dw, need_db, N, D, V,
                                                    hidden.dtype, dh_dtype, dw_dtype, dev)
     ws_need = L.ll_workspace_size(N, D, V, code, token_chunks, 2,
-                                  int(bool(need_db)) | (int(bool(split_s)) << 1))
+                                  int(bool(need_db)) | (_split_code(split_s) << 1))
     if workspace is None:
         workspace = _workspace(ws_need, dev)
     _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
@@ -446,6 +463,24 @@ def logits_fwd_bwd(grad_logp, logits, targets, V=None, *, temperature=1.0, out=N
     return logp, lse, g
 
 
+def sum_ordered(parts, out=None, stream=None):
+    """out[i] = parts[0, i] + parts[1, i] + ... in ascending order (FP32
+    accumulation, one rounding to the dtype): parts is a device tensor
+    [nparts, n] (contiguous rows), out [n]."""
+    torch = _torch()
+    L = load()
+    if parts.dim() != 2 or not parts.is_cuda or parts.stride(1) != 1:
+        raise ValueError("parts must be a CUDA tensor [nparts, n] with contiguous rows")
+    k, n = parts.shape
+    if out is None:
+        out = torch.empty(n, dtype=parts.dtype, device=parts.device)
+    _need(out, "out", (n,), parts.dtype, parts.device)
+    st = L.ll_sum_ordered(_ptr(parts), k, n, parts.stride(0), _code(parts.dtype), _ptr(out),
+                          _stream(stream))
+    _check("ll_sum_ordered", st)
+    return out
+
+
 def check_status(stream=None) -> int:
     """Synchronise and return (and clear) the device-side status word."""
     return int(load().ll_check_status(_stream(stream)))
@@ -517,7 +552,7 @@ def lse_merge(part_m, part_s, zy, targets, V, *, out=None, stream=None):
 
 def backward_shard(grad_logp, hidden, weight, bias, targets, lse, v0, V, *, need_dh=True,
                    need_dw=True, need_db=None, dh_dtype=None, dw_dtype=None, token_chunks=0,
-                   temperature=1.0, split_s=False, workspace=None, out=None, stream=None):
+                   temperature=1.0, split_s="auto", workspace=None, out=None, stream=None):
     """(grad_hidden part, grad_weight rows, grad_bias rows) of the vocab shard
     [v0, v0 + weight.shape[0]); lse is the merged whole-vocab lse.  The
     grad_hidden part defaults to float32 (the shards' parts are summed)."""
@@ -535,7 +570,7 @@ def backward_shard(grad_logp, hidden, weight, bias, targets, lse, v0, V, *, need
                                                    hidden.dtype, dh_dtype, dw_dtype, dev)
     if workspace is None:
         workspace = _workspace(L.ll_workspace_size_shard(
-            N, D, Vs, code, token_chunks, 1, int(bool(need_db)) | (int(bool(split_s)) << 1)), dev)
+            N, D, Vs, code, token_chunks, 1, int(bool(need_db)) | (_split_code(split_s) << 1)), dev)
     _need(workspace, "workspace", (workspace.numel(),), torch.uint8, dev)
     st = L.ll_backward_shard(_ptr(grad_logp), _ptr(hidden), _ptr(weight), _ptr(bias),
                              _ptr(targets), _ptr(lse), N, D, Vs, int(v0), int(V), code,

@@ -97,6 +97,35 @@ __global__ void __launch_bounds__(kSortThreads) bitonic_local_kernel(unsigned lo
     for (int t = threadIdx.x; t < kSortSeg; t += kSortThreads) keys[base + t] = s[t];
 }
 
+// The whole sort of n <= kSortSeg keys (n a power of two) in one block:
+// keys made from the targets (as make_keys_kernel), bitonic network in
+// shared memory, written back.  Same sorted keys as the multi-launch path.
+__global__ void __launch_bounds__(kSortThreads) sort_small_kernel(
+    const int64_t* __restrict__ targets, int64_t N, int64_t V, int n,
+    unsigned long long* __restrict__ keys) {
+    __shared__ unsigned long long s[kSortSeg];
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        unsigned long long k = ~0ull;
+        if (i < N) {
+            const int64_t y = targets[i];
+            if (y >= 0 && y < V)
+                k = (static_cast<unsigned long long>(y) << 32) | static_cast<unsigned long long>(i);
+        }
+        s[i] = k;
+    }
+    __syncthreads();
+    for (int k = 2; k <= n; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int p = threadIdx.x; p < n / 2; p += blockDim.x) {
+                const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
+                cmp_swap(s[i], s[i + j], (i & k) == 0);
+            }
+            __syncthreads();
+        }
+    }
+    for (int i = threadIdx.x; i < n; i += blockDim.x) keys[i] = s[i];
+}
+
 __global__ void bitonic_global_kernel(unsigned long long* keys, int64_t n, int64_t k, int64_t j) {
     const int64_t p = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
     if (p >= n / 2) return;
@@ -182,12 +211,13 @@ __host__ __device__ constexpr int brev5(int i) {
 // Loads in flight per warp and blocks per SM, from a sweep on GB300 (rows of
 // FP32 logits, 16-bit S): without the column sums 4 rows a batch at 6
 // blocks per SM (~6 TB/s), with them 8 rows at 3 (~5.5 TB/s).
-template <typename T, bool DB>
+template <typename T, bool DB, bool LO_ALL>
 __global__ void __launch_bounds__(256, DB ? 3 : 6) softmax_part_kernel(
     const float* __restrict__ Z, int64_t ldZ, int64_t rows, int64_t V,
     const int64_t* __restrict__ targets, const float* __restrict__ grad,
     const float* __restrict__ lse, T* __restrict__ S, int64_t ldS, float* __restrict__ tc,
-    float* __restrict__ db_part, float inv_temp, T* __restrict__ S_lo) {
+    float* __restrict__ db_part, float inv_temp, T* __restrict__ S_lo,
+    uint8_t* __restrict__ lo_flags) {
     constexpr int kAhead = DB ? 8 : 4;  // rows whose loads are in flight together
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -206,6 +236,7 @@ __global__ void __launch_bounds__(256, DB ? 3 : 6) softmax_part_kernel(
     for (int64_t c = (int64_t(blockIdx.y) * 8 + warp) * 128 + 4 * lane; c - 4 * lane < V;
          c += step) {
         float acc[5][4];  // pending subtree sums, one per binary-counter level
+        bool kept = false;  // automatic split: an entry of this lane's columns keeps its rest
 #pragma unroll
         for (int i0 = 0; i0 < 32; i0 += kAhead) {
             float z[kAhead][4];
@@ -244,16 +275,32 @@ __global__ void __launch_bounds__(256, DB ? 3 : 6) softmax_part_kernel(
                         for (int j = 0; j < 4; ++j)
                             if (j == off) v[j] = 0.f;
                     }
+                    if (!LO_ALL && lo_flags && coef != 0.f) {  // p >= kLoTau: flag below
+                        float pm = v[0];
+#pragma unroll
+                        for (int j = 1; j < 4; ++j)
+                            if (c + j < V) pm = fmaxf(pm, v[j]);
+                        kept |= pm >= kLoTau;
+                    }
 #pragma unroll
                     for (int j = 0; j < 4; ++j) v[j] = coef * v[j];
                     T* srow = S + (r0 + r) * ldS;
-                    T* lrow = S_lo ? S_lo + (r0 + r) * ldS : nullptr;
                     if constexpr (sizeof(T) == 4) {  // FP32 S, no split
                         if (c + 4 <= V) {
                             *reinterpret_cast<float4*>(srow + c) =
                                 make_float4(v[0], v[1], v[2], v[3]);
                         } else {
                             for (int j = 0; j < 4 && c + j < V; ++j) srow[c + j] = v[j];
+                        }
+                    } else if constexpr (!LO_ALL) {
+                        uint2 hu;  // S rounded to T
+                        T* hi = reinterpret_cast<T*>(&hu);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) hi[j] = Elem<T>::from_f(v[j]);
+                        if (c + 4 <= V) {
+                            *reinterpret_cast<uint2*>(srow + c) = hu;
+                        } else {
+                            for (int j = 0; j < 4 && c + j < V; ++j) srow[c + j] = hi[j];
                         }
                     } else {
                         uint2 hu, lu;  // S rounded to T; the rest S - S_hi rounded to T
@@ -264,13 +311,14 @@ __global__ void __launch_bounds__(256, DB ? 3 : 6) softmax_part_kernel(
                             hi[j] = Elem<T>::from_f(v[j]);
                             lo[j] = Elem<T>::from_f(v[j] - Elem<T>::to_f(hi[j]));
                         }
+                        T* lrow = S_lo + (r0 + r) * ldS;
                         if (c + 4 <= V) {
                             *reinterpret_cast<uint2*>(srow + c) = hu;
-                            if (lrow) *reinterpret_cast<uint2*>(lrow + c) = lu;
+                            *reinterpret_cast<uint2*>(lrow + c) = lu;
                         } else {
                             for (int j = 0; j < 4 && c + j < V; ++j) {
                                 srow[c + j] = hi[j];
-                                if (lrow) lrow[c + j] = lo[j];
+                                lrow[c + j] = lo[j];
                             }
                         }
                     }
@@ -295,6 +343,17 @@ __global__ void __launch_bounds__(256, DB ? 3 : 6) softmax_part_kernel(
                             if (c + j < V) db_part[blockIdx.x * V + c + j] = v[j];
                     }
                 }
+            }
+        }
+        if constexpr (sizeof(T) == 2 && !LO_ALL) {
+            // Automatic split: flag each 64-column piece of these 32 rows (a
+            // half warp's columns) holding an entry with p >= kLoTau; the
+            // pieces are written by lo_pieces_kernel.
+            if (lo_flags) {  // every piece gets its flag: 1 = to be written
+                const unsigned m = __ballot_sync(0xffffffffu, kept);
+                if ((lane & 15) == 0 && c < V)
+                    lo_flags[blockIdx.x * lo_flags_pitch(V) + c / kLoCols] =
+                        ((lane < 16 ? m : m >> 16) & 0xffffu) != 0;
             }
         }
     }
@@ -327,8 +386,43 @@ __global__ void unsatisfied_wait_kernel(int* flag, int* status, uint64_t wait_ns
     }
 }
 
+// out[i] = sum over k = 0, 1, ..., nparts - 1 (in that order) of
+// parts[k * ld + i], accumulated in FP32 and rounded once to T.  A thread
+// takes 4 consecutive elements (one 16-byte load per part for FP32 when the
+// rows are 16-byte aligned), grid-stride over the row.
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(256) sum_ordered_kernel(const T* __restrict__ parts,
+                                                          int64_t nparts, int64_t n, int64_t ld,
+                                                          T* __restrict__ out) {
+    for (int64_t i = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) * 4; i < n;
+         i += int64_t(gridDim.x) * blockDim.x * 4) {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (VEC && i + 4 <= n) {
+            for (int64_t k = 0; k < nparts; ++k) {
+                const float4 f = *reinterpret_cast<const float4*>(
+                    reinterpret_cast<const float*>(parts) + k * ld + i);
+                if (k == 0) {
+                    acc[0] = f.x, acc[1] = f.y, acc[2] = f.z, acc[3] = f.w;
+                } else {
+                    acc[0] += f.x, acc[1] += f.y, acc[2] += f.z, acc[3] += f.w;
+                }
+            }
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + i) =
+                make_float4(acc[0], acc[1], acc[2], acc[3]);
+        } else {
+            const int m = static_cast<int>(n - i < 4 ? n - i : 4);
+            for (int64_t k = 0; k < nparts; ++k)
+                for (int j = 0; j < m; ++j) {
+                    const float x = Elem<T>::to_f(parts[k * ld + i + j]);
+                    acc[j] = k == 0 ? x : acc[j] + x;
+                }
+            for (int j = 0; j < m; ++j) out[i + j] = Elem<T>::from_f(acc[j]);
+        }
+    }
+}
+
 int64_t pow2_at_least(int64_t n) {
-    int64_t p = kSortSeg;
+    int64_t p = 64;
     while (p < n) p <<= 1;
     return p;
 }
@@ -362,6 +456,14 @@ cudaError_t launch_token_sort(const int64_t* targets, int64_t N, int64_t V, int6
                               int* offs, cudaStream_t s) {
     unsigned long long* keys = reinterpret_cast<unsigned long long*>(keys_);
     const int64_t n = pow2_at_least(N);
+    if (n <= kSortSeg) {  // one block sorts all keys
+        note_launches(2);
+        const int threads = static_cast<int>(n / 2 < kSortThreads ? n / 2 : kSortThreads);
+        sort_small_kernel<<<1, threads, 0, s>>>(targets, N, V, static_cast<int>(n), keys);
+        offsets_kernel<<<static_cast<unsigned>((V + 1 + 255) / 256), 256, 0, s>>>(keys, n, V,
+                                                                                  offs);
+        return cudaGetLastError();
+    }
     note_launches(3);
     make_keys_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(targets, N, V, n,
                                                                             keys);
@@ -378,10 +480,165 @@ cudaError_t launch_token_sort(const int64_t* targets, int64_t N, int64_t V, int6
     return cudaGetLastError();
 }
 
+// Automatic split of the single call: the pieces of S_lo that the softmax
+// part flagged, each written whole (32 rows x 64 columns: the rest
+// S - S_hi of every entry with p >= kLoTau, zero elsewhere) from the stored
+// FP32 logits with the softmax part's arithmetic, so they are bitwise the
+// recompute epilogue's pieces.  One warp per 32-row group; a lane takes two
+// columns of a piece.
+template <typename T>
+__global__ void __launch_bounds__(256) lo_pieces_kernel(
+    const float* __restrict__ Z, int64_t ldZ, int64_t rows, int64_t V,
+    const int64_t* __restrict__ targets, const float* __restrict__ grad,
+    const float* __restrict__ lse, T* __restrict__ S_lo, int64_t ldS,
+    const uint8_t* __restrict__ lo_flags, float inv_temp) {
+    const int lane = threadIdx.x & 31;
+    const int64_t g = blockIdx.x * int64_t(8) + (threadIdx.x >> 5);
+    const int64_t r0 = g * 32;
+    if (r0 >= rows) return;
+    const int64_t my_row = r0 + lane;
+    const bool rvalid = my_row < rows;
+    const int64_t my_y = rvalid ? targets[my_row] : -1;
+    const float my_g = rvalid ? grad[my_row] : 0.f;
+    const bool live = rvalid && my_y >= 0 && my_y < V && my_g != 0.f;
+    const float my_coef = live ? -my_g * inv_temp : 0.f;
+    const float my_lse2 = rvalid ? lse[my_row] * kLog2e : 0.f;
+    const int nr = static_cast<int>(rows - r0 < 32 ? rows - r0 : 32);
+    const int64_t fld = (V + kLoCols - 1) / kLoCols;
+    const int64_t pitch = lo_flags_pitch(V);
+    for (int64_t kb0 = 0; kb0 < fld; kb0 += 32) {
+        const int64_t kb = kb0 + lane;
+        unsigned m = __ballot_sync(0xffffffffu, kb < fld && lo_flags[g * pitch + kb] != 0);
+        while (m) {
+            const int64_t c = (kb0 + __ffs(m) - 1) * kLoCols + 2 * lane;
+            m &= m - 1;
+#pragma unroll 1
+            for (int r = 0; r < nr; ++r) {
+                const float coef = __shfl_sync(0xffffffffu, my_coef, r);
+                const float lse2 = __shfl_sync(0xffffffffu, my_lse2, r);
+                const int64_t y = __shfl_sync(0xffffffffu, my_y, r);
+                if (c >= V) continue;
+                // c is even and ldZ a multiple of 8: an aligned pair in the row
+                const float2 f = *reinterpret_cast<const float2*>(Z + (r0 + r) * ldZ + c);
+                float v[2] = {ex2(fmaf(f.x, kLog2e, -lse2)), ex2(fmaf(f.y, kLog2e, -lse2))};
+                const int64_t off = y - c;
+                if (off == 0) v[0] = 0.f;
+                if (off == 1) v[1] = 0.f;
+                T lo[2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const bool keep = coef != 0.f && c + j < V && v[j] >= kLoTau;
+                    const float s = coef * v[j];
+                    lo[j] = Elem<T>::from_f(keep ? s - Elem<T>::to_f(Elem<T>::from_f(s)) : 0.f);
+                }
+                T* lrow = S_lo + (r0 + r) * ldS;
+                if (c + 2 <= V) {
+                    *reinterpret_cast<uint32_t*>(lrow + c) = *reinterpret_cast<uint32_t*>(lo);
+                } else {
+                    lrow[c] = lo[0];
+                }
+            }
+        }
+    }
+}
+
+// One warp per block of the plan: first the grad_hidden row blocks, then
+// the grad_weight vocab blocks.  The flags are read 16 bytes at a time; a
+// lane's listed K blocks go to its place in the warp's ascending list (a
+// prefix count over the lanes).
+__device__ __forceinline__ int warp_excl_prefix(int x, int lane, int* total) {
+    int v = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+    }
+    *total = __shfl_sync(0xffffffffu, v, 31);
+    return v - x;
+}
+
+__global__ void lo_plan_kernel(const uint8_t* __restrict__ F, int64_t rows, int64_t V, int R,
+                               int C, int* __restrict__ dh_cnt, int64_t* __restrict__ dh_idx,
+                               int* __restrict__ dw_cnt, int64_t* __restrict__ dw_idx) {
+    const int lane = threadIdx.x & 31;
+    const int64_t item = blockIdx.x * int64_t(blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int64_t fld = (V + kLoCols - 1) / kLoCols;
+    const int64_t pitch = lo_flags_pitch(V);
+    const int64_t groups = (rows + kLoRows - 1) / kLoRows;
+    const int64_t n_dh = (rows + R - 1) / R;
+    const int64_t n_dw = (V + C - 1) / C;
+    if (item < n_dh) {
+        // K blocks kb of the row block: lane takes 16 consecutive kb per step
+        const int64_t mb = item;
+        const int64_t g0 = mb * (R / kLoRows);
+        const int ng = static_cast<int>(min(int64_t(R / kLoRows), groups - g0));
+        int cnt = 0;
+        for (int64_t kb0 = 0; kb0 < fld; kb0 += 32 * 16) {
+            const int64_t kb = kb0 + 16 * lane;
+            uint32_t bits[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) bits[j] = 0;
+            if (kb < fld) {
+                for (int i = 0; i < ng; ++i) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(F + (g0 + i) * pitch + kb);
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if ((ws[j >> 2] >> (8 * (j & 3))) & 0xffu) bits[j] |= 1u << i;
+                }
+            }
+            int n = 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) n += (bits[j] != 0 && kb + j < fld);
+            int total;
+            int at = cnt + warp_excl_prefix(n, lane, &total);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (bits[j] != 0 && kb + j < fld) dh_idx[mb * fld + at++] = ((kb + j) << 8) | bits[j];
+            cnt += total;
+        }
+        if (lane == 0) dh_cnt[mb] = cnt;
+    } else if (item < n_dh + n_dw) {
+        // K blocks kb (64 tokens = row groups 2 kb, 2 kb + 1) of the vocab block
+        const int64_t vb = item - n_dh;
+        const int64_t c0 = vb * (C / kLoCols);
+        const int nc = static_cast<int>(min(int64_t(C / kLoCols), fld - c0));
+        const int64_t kbs = (rows + 63) / 64;
+        int cnt = 0;
+        for (int64_t kb0 = 0; kb0 < kbs; kb0 += 32) {
+            const int64_t kb = kb0 + lane;
+            uint32_t bits = 0;
+            if (kb < kbs)
+                for (int i = 0; i < 2; ++i) {
+                    const int64_t g = 2 * kb + i;
+                    if (g >= groups) break;
+                    for (int c = 0; c < nc; ++c)
+                        if (F[g * pitch + c0 + c]) bits |= 1u << (2 * c + i);
+                }
+            const unsigned m = __ballot_sync(0xffffffffu, bits != 0);
+            if (bits) dw_idx[vb * kbs + cnt + __popc(m & ((1u << lane) - 1))] = (kb << 8) | bits;
+            cnt += __popc(m);
+        }
+        if (lane == 0) dw_cnt[vb] = cnt;
+    }
+}
+
+cudaError_t launch_lo_plan(const uint8_t* F, int64_t rows, int64_t V, int R, int C,
+                           int* dh_cnt, int64_t* dh_idx, int* dw_cnt, int64_t* dw_idx,
+                           cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    const int64_t items = (rows + R - 1) / R + (V + C - 1) / C;
+    note_launches(1);
+    lo_plan_kernel<<<static_cast<unsigned>((items + 7) / 8), 256, 0, s>>>(F, rows, V, R, C,
+                                                                          dh_cnt, dh_idx,
+                                                                          dw_cnt, dw_idx);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_softmax_part(const float* Z, int64_t ldZ, int64_t rows, int64_t V,
                                 const int64_t* targets, const float* grad, const float* lse,
                                 void* S, int64_t ldS, int s_dtype, float* tc, float* db_part,
-                                float inv_temp, void* S_lo, cudaStream_t s) {
+                                float inv_temp, void* S_lo, uint8_t* lo_flags, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
     note_launches(1);
     // a block: 32 rows x (8 warps x 128 columns) per step of its column loop
@@ -389,32 +646,63 @@ cudaError_t launch_softmax_part(const float* Z, int64_t ldZ, int64_t rows, int64
     if (gy > 65535) gy = 65535;
     const dim3 grid(static_cast<unsigned>((rows + 31) / 32), static_cast<unsigned>(gy));
     const bool db = db_part != nullptr;
+    // S_lo without flags: every entry's rest, written by the softmax part
+    const bool all = S_lo != nullptr && lo_flags == nullptr;
     if (s_dtype == LL_BF16) {
         auto* Sp = static_cast<__nv_bfloat16*>(S);
         auto* Lp = static_cast<__nv_bfloat16*>(S_lo);
-        if (db)
-            softmax_part_kernel<__nv_bfloat16, true><<<grid, 256, 0, s>>>(
-                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, db_part, inv_temp, Lp);
+        if (db && all)
+            softmax_part_kernel<__nv_bfloat16, true, true><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, db_part, inv_temp, Lp, nullptr);
+        else if (db)
+            softmax_part_kernel<__nv_bfloat16, true, false><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, db_part, inv_temp, Lp, lo_flags);
+        else if (all)
+            softmax_part_kernel<__nv_bfloat16, false, true><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, nullptr, inv_temp, Lp, nullptr);
         else
-            softmax_part_kernel<__nv_bfloat16, false><<<grid, 256, 0, s>>>(
-                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, nullptr, inv_temp, Lp);
+            softmax_part_kernel<__nv_bfloat16, false, false><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, nullptr, inv_temp, Lp, lo_flags);
     } else if (s_dtype == LL_F16) {
         auto* Sp = static_cast<__half*>(S);
         auto* Lp = static_cast<__half*>(S_lo);
-        if (db)
-            softmax_part_kernel<__half, true><<<grid, 256, 0, s>>>(
-                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, db_part, inv_temp, Lp);
+        if (db && all)
+            softmax_part_kernel<__half, true, true><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, db_part, inv_temp, Lp, nullptr);
+        else if (db)
+            softmax_part_kernel<__half, true, false><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, db_part, inv_temp, Lp, lo_flags);
+        else if (all)
+            softmax_part_kernel<__half, false, true><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, nullptr, inv_temp, Lp, nullptr);
         else
-            softmax_part_kernel<__half, false><<<grid, 256, 0, s>>>(
-                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, nullptr, inv_temp, Lp);
+            softmax_part_kernel<__half, false, false><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, nullptr, inv_temp, Lp, lo_flags);
     } else {
         auto* Sp = static_cast<float*>(S);
+        lo_flags = nullptr;  // FP32 S: no split
         if (db)
-            softmax_part_kernel<float, true><<<grid, 256, 0, s>>>(
-                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, db_part, inv_temp, nullptr);
+            softmax_part_kernel<float, true, false><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, db_part, inv_temp, nullptr,
+                nullptr);
         else
-            softmax_part_kernel<float, false><<<grid, 256, 0, s>>>(
-                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, nullptr, inv_temp, nullptr);
+            softmax_part_kernel<float, false, false><<<grid, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, Sp, ldS, tc, nullptr, inv_temp, nullptr,
+                nullptr);
+    }
+    if (lo_flags && S_lo) {  // the flagged pieces of S_lo
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        note_launches(1);
+        const unsigned gb = static_cast<unsigned>(((rows + 31) / 32 + 7) / 8);
+        if (s_dtype == LL_BF16)
+            lo_pieces_kernel<__nv_bfloat16><<<gb, 256, 0, s>>>(
+                Z, ldZ, rows, V, targets, grad, lse, static_cast<__nv_bfloat16*>(S_lo), ldS,
+                lo_flags, inv_temp);
+        else
+            lo_pieces_kernel<__half><<<gb, 256, 0, s>>>(Z, ldZ, rows, V, targets, grad, lse,
+                                                        static_cast<__half*>(S_lo), ldS,
+                                                        lo_flags, inv_temp);
     }
     return cudaGetLastError();
 }
@@ -435,6 +723,35 @@ cudaError_t launch_db_finish(const float* partial, int64_t groups, int64_t V, fl
         db_finish_kernel<__nv_bfloat16><<<fb, 256, 0, s>>>(
             partial, groups, V, db_acc, first, last, offs, k, tc_all,
             static_cast<__nv_bfloat16*>(grad_bias));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sum_ordered(const void* parts, int64_t nparts, int64_t n, int64_t ld,
+                               int dtype, void* out, int num_sms, cudaStream_t s) {
+    if (n <= 0 || nparts <= 0) return cudaSuccess;
+    note_launches(1);
+    const int64_t threads = (n + 3) / 4;
+    int64_t blocks = (threads + 255) / 256;
+    const int64_t cap = int64_t(num_sms) * 8;  // 8 resident blocks of 256 per SM
+    if (blocks > cap) blocks = cap;
+    const unsigned gb = static_cast<unsigned>(blocks < 1 ? 1 : blocks);
+    if (dtype == LL_F32) {
+        const bool vec = ld % 4 == 0 && reinterpret_cast<uintptr_t>(parts) % 16 == 0 &&
+                         reinterpret_cast<uintptr_t>(out) % 16 == 0;
+        if (vec)
+            sum_ordered_kernel<float, true><<<gb, 256, 0, s>>>(
+                static_cast<const float*>(parts), nparts, n, ld, static_cast<float*>(out));
+        else
+            sum_ordered_kernel<float, false><<<gb, 256, 0, s>>>(
+                static_cast<const float*>(parts), nparts, n, ld, static_cast<float*>(out));
+    } else if (dtype == LL_BF16) {
+        sum_ordered_kernel<__nv_bfloat16, false><<<gb, 256, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(parts), nparts, n, ld,
+            static_cast<__nv_bfloat16*>(out));
+    } else {
+        sum_ordered_kernel<__half, false><<<gb, 256, 0, s>>>(
+            static_cast<const __half*>(parts), nparts, n, ld, static_cast<__half*>(out));
+    }
     return cudaGetLastError();
 }
 

@@ -165,20 +165,27 @@ constexpr size_t kAutoChunkBytes = size_t(2) << 30;  // softmax workspace budget
 // Rows of grad_bias partials a chunk of Nc tokens writes: one per 32 rows.
 int64_t db_groups(int64_t Nc) { return Nc > 32 ? cdiv(Nc, 32) : 1; }
 
+// Hi / lo split of the softmax part S (ll_options.split_s; 16-bit operands).
+enum SplitMode { kSplitAuto = 0, kSplitAll = 1, kSplitNone = 2 };
+
 struct BwdLayout {
-    int64_t chunks, Nc, ldS, ldZ, n_segs;
+    int64_t chunks, Nc, ldS, ldZ, n_segs, lo_fld;
     size_t S, S_lo, Z, part_m, part_s, zy, tc, keys, offs, ctr, db, total;
+    size_t lo_flags, dh_cnt, dh_idx, dw_cnt, dw_idx;  // automatic split
 };
 // fused = 1: the single fwd+bwd call, which also keeps the chunk's FP32
 // logits Z and the forward partials.
-// split = 1: the softmax part is kept as a hi / lo pair (16-bit dtypes).
+// split_mode (SplitMode): all / automatic keep an S_lo buffer (16-bit
+// dtypes); automatic also the piece flags and the second pass's plan.
 BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need_db,
-                     int fused = 0, int split = 0) {
+                     int fused = 0, int split_mode = kSplitNone) {
     BwdLayout L;
     L.ldS = round_up(V, 8);
     L.ldZ = round_up(V, 8);
     L.n_segs = cdiv(cdiv(V, kBN), kVocabTilesPerSeg);
-    split = split && dtype != LL_F32;
+    L.lo_fld = cdiv(V, kLoCols);
+    const bool split = dtype != LL_F32 && split_mode != kSplitNone;
+    const bool lo_auto = split && split_mode == kSplitAuto;
     // The automatic chunk count depends on the softmax part S alone, so the
     // two calls, the single call and the hi / lo split choose the same chunks
     // (and so give the same grad_weight bits); the single call's FP32 logits
@@ -199,6 +206,18 @@ BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need
     off = align_up(off + size_t(L.Nc) * size_t(L.ldS) * esize(dtype));
     L.S_lo = off;
     if (split) off = align_up(off + size_t(L.Nc) * size_t(L.ldS) * esize(dtype));
+    L.lo_flags = L.dh_cnt = L.dh_idx = L.dw_cnt = L.dw_idx = off;
+    if (lo_auto) {  // plan sized for single-CTA blocks (128 rows / vocab rows)
+        off = align_up(off + size_t(cdiv(L.Nc, kLoRows)) * size_t(lo_flags_pitch(V)));
+        L.dh_cnt = off;
+        off = align_up(off + size_t(cdiv(L.Nc, kBM)) * 4);
+        L.dh_idx = off;
+        off = align_up(off + size_t(cdiv(L.Nc, kBM)) * size_t(L.lo_fld) * 8);
+        L.dw_cnt = off;
+        off = align_up(off + size_t(cdiv(V, kBM)) * 4);
+        L.dw_idx = off;
+        off = align_up(off + size_t(cdiv(V, kBM)) * size_t(cdiv(L.Nc, 64)) * 8);
+    }
     L.Z = L.part_m = L.part_s = L.zy = off;
     if (fused) {
         L.Z = off;
@@ -240,15 +259,15 @@ int check_shard(int64_t Vs, int64_t v0, int64_t V) {
     return LL_OK;
 }
 
-// Options of a call: *inv_temp = 1 / temperature, *split = hi / lo S.
+// Options of a call: *inv_temp = 1 / temperature, *split = SplitMode of S.
 // NULL = defaults.
 int read_options(const ll_options* o, float* inv_temp, int* split = nullptr) {
     *inv_temp = 1.f;
-    if (split) *split = 0;
+    if (split) *split = kSplitAuto;
     if (!o) return LL_OK;
     for (int r : o->reserved)
         if (r != 0) return LL_ERR_INVALID_ARG;
-    if (o->split_s != 0 && o->split_s != 1) return LL_ERR_INVALID_ARG;
+    if (o->split_s < kSplitAuto || o->split_s > kSplitNone) return LL_ERR_INVALID_ARG;
     if (split) *split = o->split_s;
     const float T = o->temperature;
     if (!(T > 0.f) || !(T < INFINITY)) return LL_ERR_INVALID_ARG;
@@ -290,8 +309,9 @@ size_t ll_workspace_size(int64_t N, int64_t D, int64_t V, int dtype, int token_c
     (void)D;
     if (N < 0 || V < 1 || !dtype_ok(dtype)) return 0;
     if (!is_backward) return fwd_layout(N, V).total;
-    return bwd_layout(N, V, dtype, token_chunks, flags & 1, is_backward == 2, (flags >> 1) & 1)
-        .total;
+    const int mode = (flags >> 1) & 3;
+    if (mode > kSplitNone) return 0;
+    return bwd_layout(N, V, dtype, token_chunks, flags & 1, is_backward == 2, mode).total;
 }
 
 void ll_set_wait_limit_ns(int64_t ns) { g_wait_limit_ns = ns > 0 ? uint64_t(ns) : 2000000000ull; }
@@ -333,7 +353,7 @@ cudaError_t forward_gemm(const void* hidden, const void* weight, const void* bia
     G.dtype = dtype;
     G.nkinds = 1;
     G.kind[0] = EpiKind::Fwd;
-    G.op[0] = GemmOperands{hidden, D, 0, weight, D, 0, N, V, D, nullptr};
+    G.op[0] = GemmOperands{hidden, D, 0, weight, D, 0, N, V, D, nullptr, nullptr, nullptr, 0};
     G.shape[0] = sh;
     G.ea[0] = ea;
     Phase ph(dtype == LL_F32 ? "fwd_gemm_f32" : "fwd_gemm", s);
@@ -409,7 +429,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
                   void* grad_hidden, int dh_dtype, void* grad_weight, int dw_dtype,
                   void* grad_bias, int token_chunks, void* workspace, size_t ws_bytes,
                   void* stream, int fused, float* logp_out, float* lse_out, int shard = 0,
-                  float inv_temp = 1.f, int split = 0) {
+                  float inv_temp = 1.f, int split = kSplitAuto) {
     int st = check_sizes(N, D, V);
     if (st) return st;
     if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
@@ -440,14 +460,21 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
     }
     if (!grad_logp || !hidden || !targets || (!fused && !lse)) return LL_ERR_INVALID_ARG;
     if (!aligned16(hidden) || (need_dh && !aligned16(grad_hidden))) return LL_ERR_ALIGN;
-    split = split && dtype != LL_F32;  // FP32 keeps S in FP32: nothing to split
     const BwdLayout L = bwd_layout(N, V, dtype, token_chunks, need_db, fused, split);
     if (!workspace || ws_bytes < L.total) return LL_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return LL_ERR_WORKSPACE;
 
     char* ws = static_cast<char*>(workspace);
     void* S = ws + L.S;
-    void* S_lo = split ? static_cast<void*>(ws + L.S_lo) : nullptr;
+    // FP32 keeps S in FP32: nothing to split
+    const bool has_lo = dtype != LL_F32 && split != kSplitNone;
+    const bool lo_auto = has_lo && split == kSplitAuto;
+    void* S_lo = has_lo ? static_cast<void*>(ws + L.S_lo) : nullptr;
+    uint8_t* lo_flags = lo_auto ? reinterpret_cast<uint8_t*>(ws + L.lo_flags) : nullptr;
+    int* dh_cnt = reinterpret_cast<int*>(ws + L.dh_cnt);
+    int64_t* dh_idx = reinterpret_cast<int64_t*>(ws + L.dh_idx);
+    int* dw_cnt = reinterpret_cast<int*>(ws + L.dw_cnt);
+    int64_t* dw_idx = reinterpret_cast<int64_t*>(ws + L.dw_idx);
     float* tc = reinterpret_cast<float*>(ws + L.tc);
     int64_t* keys = reinterpret_cast<int64_t*>(ws + L.keys);
     int* offs = reinterpret_cast<int*>(ws + L.offs);
@@ -510,7 +537,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             G.dtype = dtype;
             G.nkinds = 1;
             G.kind[0] = EpiKind::Recomp;
-            G.op[0] = GemmOperands{h_c, D, 0, weight, D, 0, rows, V, D, nullptr};
+            G.op[0] = GemmOperands{h_c, D, 0, weight, D, 0, rows, V, D, nullptr, nullptr, nullptr, 0};
             GemmShape& sh = G.shape[0];
             sh.m_blocks = cdiv(rows, kBM);
             sh.n_tiles = cdiv(V, kBN);
@@ -527,6 +554,9 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             ea.grad = grad_logp + r0;
             ea.S = S;
             ea.S_lo = S_lo;
+            ea.lo_flags = lo_flags;
+            ea.lo_flags_ld = lo_flags_pitch(V);
+            ea.lo_flags_cols = L.lo_fld;
             ea.ldS = L.ldS;
             ea.tc = tc + r0;
             ea.db_part = need_db ? db_part : nullptr;
@@ -544,7 +574,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             G.dtype = dtype;
             G.nkinds = 1;
             G.kind[0] = EpiKind::Fwd;
-            G.op[0] = GemmOperands{h_c, D, 0, weight, D, 0, rows, V, D, nullptr};
+            G.op[0] = GemmOperands{h_c, D, 0, weight, D, 0, rows, V, D, nullptr, nullptr, nullptr, 0};
             GemmShape& sh = G.shape[0];
             sh.m_blocks = cdiv(rows, kBM);
             sh.n_tiles = cdiv(V, kBN);
@@ -581,7 +611,8 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
                 Phase ph("softmax_part", s);
                 e = launch_softmax_part(Z, L.ldZ, rows, V, targets + r0, grad_logp + r0,
                                         lse_out + r0, S, L.ldS, dtype, tc + r0,
-                                        need_db ? db_part : nullptr, inv_temp, S_lo, s);
+                                        need_db ? db_part : nullptr, inv_temp, S_lo, lo_flags,
+                                        s);
             }
             if (e != cudaSuccess) return cuda_status(e);
         }
@@ -593,6 +624,18 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
         // (2)+(3) grad_hidden rows of the chunk (S . W + c * W[y]) and
         // grad_weight += S^T . h (+ the target part on the last chunk), in
         // one launch: grad_hidden tiles (K = V) first, grad_weight tiles after
+        if ((need_dh || need_dw) && lo_auto) {
+            // the automatic split's second pass: which K blocks of which
+            // blocks have written pieces of S_lo, at the launch's block size
+            int64_t Ms[2];
+            int nk = 0;
+            if (need_dh) Ms[nk++] = rows;
+            if (need_dw) Ms[nk++] = V;
+            const int blk = gemm_uses_pairs(dtype, Ms, nk) ? 2 * kBM : kBM;
+            Phase ph("lo_plan", s);
+            e = launch_lo_plan(lo_flags, rows, V, blk, blk, dh_cnt, dh_idx, dw_cnt, dw_idx, s);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
         if (need_dh || need_dw) {
             GemmLaunch G;
             memset(&G, 0, sizeof(G));
@@ -600,7 +643,8 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             int k = 0;
             if (need_dh) {
                 G.kind[k] = EpiKind::Dh;
-                G.op[k] = GemmOperands{S, L.ldS, 0, weight, D, 1, rows, D, V, S_lo};
+                G.op[k] = GemmOperands{S, L.ldS, 0, weight, D, 1, rows, D, V, S_lo,
+                                       lo_auto ? dh_cnt : nullptr, dh_idx, L.lo_fld};
                 GemmShape& sh = G.shape[k];
                 sh.m_blocks = cdiv(rows, kBM);
                 sh.n_tiles = cdiv(D, kBN);
@@ -625,7 +669,8 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             }
             if (need_dw) {
                 G.kind[k] = EpiKind::Dw;
-                G.op[k] = GemmOperands{S, L.ldS, 1, h_c, D, 1, V, D, rows, S_lo};
+                G.op[k] = GemmOperands{S, L.ldS, 1, h_c, D, 1, V, D, rows, S_lo,
+                                       lo_auto ? dw_cnt : nullptr, dw_idx, cdiv(rows, 64)};
                 GemmShape& sh = G.shape[k];
                 sh.m_blocks = cdiv(V, kBM);
                 sh.n_tiles = cdiv(D, kBN);
@@ -741,7 +786,9 @@ size_t ll_workspace_size_shard(int64_t N, int64_t D, int64_t Vs, int dtype, int 
     if (N < 0 || Vs < 1 || !dtype_ok(dtype)) return 0;
     if (N == 0) return 0;
     if (!is_backward) return local_targets_bytes(N);
-    return bwd_layout(N, Vs, dtype, token_chunks, flags & 1, 0, (flags >> 1) & 1).total +
+    const int mode = (flags >> 1) & 3;
+    if (mode > kSplitNone) return 0;
+    return bwd_layout(N, Vs, dtype, token_chunks, flags & 1, 0, mode).total +
            local_targets_bytes(N);
 }
 
@@ -924,6 +971,27 @@ int logits_logp_fwd_bwd_ex(const float* grad_logp, const void* logits, int64_t l
     Phase ph("logits_fused", s);
     return cuda_status(launch_logits_fused(grad_logp, logits, ld, dtype, targets, N, V, logp, lse,
                                            grad_logits, it, dev, s));
+}
+
+int ll_sum_ordered(const void* parts, int64_t nparts, int64_t n, int64_t ld, int dtype,
+                   void* out, void* stream) {
+    if (!dtype_ok(dtype)) return LL_ERR_DTYPE;
+    if (nparts < 0 || n < 0 || ld < n) return LL_ERR_SHAPE;
+    if (n == 0) return LL_OK;
+    if (nparts == 0 || !parts || !out) return LL_ERR_INVALID_ARG;
+    const char* p0 = static_cast<const char*>(parts);
+    const char* p1 = p0 + size_t(nparts) * size_t(ld) * esize(dtype);
+    const char* o0 = static_cast<const char*>(out);
+    const char* o1 = o0 + size_t(n) * esize(dtype);
+    if (o0 < p1 && p0 < o1) return LL_ERR_INVALID_ARG;  // out may not overlap the parts
+    DeviceGuard guard(parts);
+    if (guard.err) return guard.err;
+    DevInfo dev;
+    int st = device_info(guard.dev, &dev);
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Phase ph("sum_ordered", s);
+    return cuda_status(launch_sum_ordered(parts, nparts, n, ld, dtype, out, dev.num_sms, s));
 }
 
 int ll_check_status(void* stream) {

@@ -90,6 +90,9 @@ struct RowEpilogue {
     float zyv;
     bool found;
     int oh_beg, oh_end;  // Dw: one-hot token range in the sorted key list
+    float lo_prev[32];   // Recomp, automatic split: the rest of the even chunk of a piece
+    bool lo_any_prev;
+    uint32_t lo_keep;    // Recomp, automatic split: entries of the chunk with p >= kLoTau
 
     __device__ __forceinline__ void begin_unit(const EpiArgs& ea, int64_t row_) {
         row = row_;
@@ -160,6 +163,7 @@ struct RowEpilogue {
                     s += acc;
                 }
             } else {  // Recomp: S = -grad * exp(z - lse), target entry apart
+                lo_keep = 0;
                 if (!rvalid) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 0.f;
@@ -178,6 +182,13 @@ struct RowEpilogue {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         if (j == off) v[j] = 0.f;
+                }
+                if (ea.lo_flags && coef != 0.f) {  // automatic split: which rests to keep
+                    if (max32(v) >= kLoTau) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (col0 + j < V && v[j] >= kLoTau) lo_keep |= 1u << j;
+                    }
                 }
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = coef * v[j];
@@ -254,14 +265,66 @@ struct RowEpilogue {
     // Recomp with a hi / lo split of S: S_lo = S - S_hi, S_hi being S rounded
     // to T (what the tile store writes), in direct row stores.  The two 16-bit
     // parts carry S to ~2^-17 relative instead of 2^-9.
+    // Automatic split (ea.lo_flags): only entries with p >= kLoTau (marked by
+    // chunk()) keep their rest, the others count 0, so a row's S_lo depends
+    // on that row alone.  The rests are written in pieces of 32 rows (this
+    // warp) x 64 columns (an even and the following odd chunk): a piece
+    // holding any kept entry is written whole (zeros included), and every
+    // piece's flag is set to whether it was written (no clearing needed).
+    // All 32 lanes of the warp call it for every chunk of the tile in order.
     __device__ __forceinline__ void store_lo(const EpiArgs& ea, const float (&v)[32],
                                              int64_t col0) {
         if constexpr (E == EpiKind::Recomp && sizeof(T) == 2) {
-            if (!ea.S_lo || !rvalid) return;
-            float lo[32];
+            if (!ea.S_lo) return;
+            if (!ea.lo_flags) {
+                if (!rvalid) return;
+                float lo[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) lo[j] = v[j] - Elem<T>::to_f(Elem<T>::from_f(v[j]));
-            store_row32<T>(ea.S_lo, row * ea.ldS + col0, lo, col0, ea.Ncols, own_tag<T>());
+                for (int j = 0; j < 32; ++j) lo[j] = v[j] - Elem<T>::to_f(Elem<T>::from_f(v[j]));
+                store_row32<T>(ea.S_lo, row * ea.ldS + col0, lo, col0, ea.Ncols, own_tag<T>());
+                return;
+            }
+            const bool any = __any_sync(0xffffffffu, lo_keep != 0);
+            const bool even = ((col0 / 32) & 1) == 0;
+            if (any) {  // the kept entries' rests, zeros elsewhere
+                float* dst = even ? lo_prev : nullptr;
+                float lo[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    lo[j] = ((lo_keep >> j) & 1) ? v[j] - Elem<T>::to_f(Elem<T>::from_f(v[j]))
+                                                 : 0.f;
+                if (dst) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) lo_prev[j] = lo[j];
+                } else if (rvalid) {
+                    store_row32<T>(ea.S_lo, row * ea.ldS + col0, lo, col0, ea.Ncols,
+                                   own_tag<T>());
+                }
+            }
+            if (even) {
+                lo_any_prev = any;
+                return;
+            }
+            // odd chunk: the piece [col0 - 32, col0 + 32) is complete
+            const bool written = any || lo_any_prev;
+            if (written && rvalid) {
+                float z[32];
+                if (!lo_any_prev) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) z[j] = 0.f;
+                }
+                store_row32<T>(ea.S_lo, row * ea.ldS + col0 - 32, lo_any_prev ? lo_prev : z,
+                               col0 - 32, ea.Ncols, own_tag<T>());
+                if (!any) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) z[j] = 0.f;
+                    store_row32<T>(ea.S_lo, row * ea.ldS + col0, z, col0, ea.Ncols,
+                                   own_tag<T>());
+                }
+            }
+            const int64_t piece = (col0 - 32) / kLoCols;
+            if ((threadIdx.x & 31) == 0 && rvalid && piece < ea.lo_flags_cols)
+                ea.lo_flags[(row / kLoRows) * ea.lo_flags_ld + piece] = written ? 1 : 0;
         }
     }
 

@@ -59,6 +59,7 @@ struct Bars {
     uint64_t sempty[kSchedDepth];
     uint64_t drain;
     int sched[kSchedDepth];
+    int sched_lo[kSchedDepth];  // second-pass K blocks of the unit in sched
     uint32_t tmem_base;
     int abort;
 };
@@ -76,6 +77,12 @@ struct KParams {
     int64_t out_rows[2], out_cols[2];
     int64_t k_split[2];  // 16-bit: K blocks from the first A map; later blocks read the
                          // second A map (A_lo) at K block kb - k_split (0 = one A)
+    // planned second pass (automatic split): lo_cnt[kind][mb] K blocks of A_lo
+    // after the first pass, the j-th being lo_idx[kind][mb * lo_ld + j] =
+    // (K block << 8 | bits of the written pieces); nullptr = whole second pass
+    const int* lo_cnt[2];
+    const int64_t* lo_idx[2];
+    int64_t lo_ld[2];
 };
 
 // ----------------------------------------------------------- bulk stores
@@ -113,7 +120,9 @@ struct Unit {
     int64_t mb, seg, t0, t1, k_blocks;
 };
 
-__device__ __forceinline__ Unit decode_unit(const KParams& P, int64_t u) {
+// n_lo: K blocks of the unit's planned second pass (0 without a plan); the
+// scheduler reads it once from the plan and publishes it with the unit id.
+__device__ __forceinline__ Unit decode_unit(const KParams& P, int64_t u, int n_lo = 0) {
     Unit r;
     r.kind = u < P.n_units[0] ? 0 : 1;
     const GemmShape& sh = P.sh[r.kind];
@@ -134,8 +143,46 @@ __device__ __forceinline__ Unit decode_unit(const KParams& P, int64_t u) {
     }
     r.t0 = r.seg * sh.tiles_per_unit;
     r.t1 = min(r.t0 + sh.tiles_per_unit, sh.n_tiles);
-    r.k_blocks = sh.k_blocks;
+    r.k_blocks = sh.k_blocks + n_lo;
     return r;
+}
+
+// The planned second pass's K-block count of unit u (scheduler side).
+__device__ __forceinline__ int unit_lo_count(const KParams& P, int64_t u) {
+    if (u < 0) return 0;
+    const Unit r = decode_unit(P, u);
+    return P.lo_cnt[r.kind] ? P.lo_cnt[r.kind][r.mb] : 0;
+}
+
+// The planned second pass's K block (scaled to elements) and piece bits.
+__device__ __forceinline__ void lo_block(const KParams& P, const Unit& un, int64_t j,
+                                         int32_t* k0, uint32_t* bits) {
+    const int64_t e = P.lo_idx[un.kind][un.mb * P.lo_ld[un.kind] + j];
+    *k0 = static_cast<int32_t>((e >> 8) * kBK);
+    *bits = static_cast<uint32_t>(e & 0xff);
+}
+
+// A_lo of the planned second pass in pieces of 32 rows (K-major A: 4 per
+// 128-row tile) or of 32 K rows (MN-major A: 2 in each 64-wide box): a piece
+// whose bit is set is read from A_lo, any other from rows [-32, 0), outside
+// the tensor, which the copy fills with zeros.  Same bytes and shared-memory
+// layout as the whole-tile load (a 32-row piece is 4 KB, a multiple of the
+// 1 KB swizzle pattern).  `load(dst, x, y)` issues one piece.
+template <bool A_MN, class Load>
+__device__ __forceinline__ void load_a_pieces(uint8_t* sa, int32_t k0, int32_t m0,
+                                              uint32_t bits, Load load) {
+    if constexpr (!A_MN) {
+#pragma unroll
+        for (int i = 0; i < kBM / 32; ++i)
+            load(sa + i * 32 * 128, k0, ((bits >> i) & 1) ? m0 + 32 * i : -32);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kBM / 64; ++j)
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                load(sa + j * kMnBoxBytes + i * 32 * 128, m0 + 64 * j,
+                     ((bits >> (2 * j + i)) & 1) ? k0 + 32 * i : -32);
+    }
 }
 
 template <typename T, EpiKind E, bool A_MN, bool B_MN>
@@ -161,6 +208,23 @@ __device__ __forceinline__ void load_stage(uint8_t* sa, const CUtensorMap* tmA,
 #pragma unroll
         for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sa + j * kMnBoxBytes, tmA, fb, m0 + 64 * j, k0);
     }
+    if constexpr (!B_MN) {
+        tma_load_2d(sb, tmB, fb, k0, n0);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sb + j * kMnBoxBytes, tmB, fb, n0 + 64 * j, k0);
+    }
+}
+
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void load_stage_lo(uint8_t* sa, const CUtensorMap* tmL,
+                                              const CUtensorMap* tmB, uint64_t* fb, int32_t k0,
+                                              int32_t m0, int32_t n0, uint32_t bits) {
+    uint8_t* sb = sa + kABytes;
+    mbar_arrive_expect_tx(fb, kStageBytes);
+    load_a_pieces<A_MN>(sa, k0, m0, bits, [&](uint8_t* d, int32_t x, int32_t y) {
+        tma_load_2d(d, tmL, fb, x, y);
+    });
     if constexpr (!B_MN) {
         tma_load_2d(sb, tmB, fb, k0, n0);
     } else {
@@ -280,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 next_static += gridDim.x;
             }
             if (u >= total) u = -1;
+            const int n_lo = unit_lo_count(P, u);
             if (!__all_sync(0xffffffffu,
                             mbar_wait(&bars->sempty[sslot], sphase ^ 1, wait_ns, abort))) {
                 ok = false;
@@ -287,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (lane == 0) {
                 bars->sched[sslot] = static_cast<int>(u);
+                bars->sched_lo[sslot] = n_lo;
                 mbar_arrive(&bars->sfull[sslot]);
             }
             __syncwarp();
@@ -295,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sphase ^= 1;
             }
             if (u < 0) break;
-            const Unit un = decode_unit(P, u);
+            const Unit un = decode_unit(P, u, n_lo);
             for (int64_t t = un.t0; t < un.t1 && ok; ++t) {
                 for (int64_t kb = 0; kb < un.k_blocks; ++kb) {
                     if (!__all_sync(0xffffffffu,
@@ -308,15 +374,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // a hi / lo split runs K twice: A, then A_lo, against the same B
                         const int64_t ks = P.k_split[un.kind];
                         const bool lo = ks > 0 && kb >= ks;
-                        const int32_t k0 = static_cast<int32_t>((lo ? kb - ks : kb) * kBK);
                         const int32_t m0 = static_cast<int32_t>(un.mb * kBM);
                         const int32_t n0 = static_cast<int32_t>(t * kBN);
-                        if (NK == 1 || un.kind == 0)
-                            load_stage<K0::kAmn, K0::kBmn>(sa, lo ? &tmL0 : &tmA0, &tmB0,
-                                                           &bars->full[stage], k0, m0, n0);
-                        else
-                            load_stage<K1::kAmn, K1::kBmn>(sa, lo ? &tmL1 : &tmA1, &tmB1,
-                                                           &bars->full[stage], k0, m0, n0);
+                        if (lo && P.lo_cnt[un.kind]) {  // planned second pass
+                            int32_t k0;
+                            uint32_t bits;
+                            lo_block(P, un, kb - ks, &k0, &bits);
+                            if (NK == 1 || un.kind == 0)
+                                load_stage_lo<K0::kAmn, K0::kBmn>(sa, &tmL0, &tmB0,
+                                                                  &bars->full[stage], k0, m0, n0,
+                                                                  bits);
+                            else
+                                load_stage_lo<K1::kAmn, K1::kBmn>(sa, &tmL1, &tmB1,
+                                                                  &bars->full[stage], k0, m0, n0,
+                                                                  bits);
+                        } else {
+                            const int32_t k0 = static_cast<int32_t>((lo ? kb - ks : kb) * kBK);
+                            if (NK == 1 || un.kind == 0)
+                                load_stage<K0::kAmn, K0::kBmn>(sa, lo ? &tmL0 : &tmA0, &tmB0,
+                                                               &bars->full[stage], k0, m0, n0);
+                            else
+                                load_stage<K1::kAmn, K1::kBmn>(sa, lo ? &tmL1 : &tmA1, &tmB1,
+                                                               &bars->full[stage], k0, m0, n0);
+                        }
                     }
                     __syncwarp();
                     issued[stage] = true;
@@ -346,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             const int u = *reinterpret_cast<volatile int*>(&bars->sched[sslot]);
+            const int n_lo = *reinterpret_cast<volatile int*>(&bars->sched_lo[sslot]);
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->sempty[sslot]);
             if (++sslot == kSchedDepth) {
@@ -353,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sphase ^= 1;
             }
             if (u < 0) break;
-            const Unit un = decode_unit(P, u);
+            const Unit un = decode_unit(P, u, n_lo);
             for (int64_t t = un.t0; t < un.t1 && ok; ++t) {
                 if (!__all_sync(0xffffffffu,
                                 mbar_wait(&bars->tempty[buf], bphase ^ 1, wait_ns, abort))) {
@@ -415,6 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             const int u = *reinterpret_cast<volatile int*>(&bars->sched[sslot]);
+            const int n_lo = *reinterpret_cast<volatile int*>(&bars->sched_lo[sslot]);
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->sempty[sslot]);
             if (++sslot == kSchedDepth) {
@@ -422,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sphase ^= 1;
             }
             if (u < 0) break;
-            const Unit un = decode_unit(P, u);
+            const Unit un = decode_unit(P, u, n_lo);
             const int kind = (NK == 1) ? 0 : un.kind;
             const EpiArgs& ea = kind == 0 ? ea0 : ea1;
             const CUtensorMap* tmO = kind == 0 ? &tmO0 : &tmO1;
@@ -545,6 +627,7 @@ struct BarsPair {
     uint64_t sempty[kSchedDepth]; // leader: every consumer of the pair read it
     uint64_t drain;
     int sched[kSchedDepth];
+    int sched_lo[kSchedDepth];  // second-pass K blocks of the unit in sched
     uint32_t tmem_base;
     int abort;
 };
@@ -562,6 +645,24 @@ __device__ __forceinline__ void load_stage_pair(uint8_t* sa, const CUtensorMap* 
         for (int j = 0; j < kBM / 64; ++j)
             tma_load_2d_pair(sa + j * kMnBoxBytes, tmA, bar_cl, m0 + 64 * j, k0);
     }
+    if constexpr (!B_MN) {
+        tma_load_2d_pair(sb, tmB, bar_cl, k0, n0);
+    } else {
+#pragma unroll
+        for (int j = 0; j < kBHalf / 64; ++j)
+            tma_load_2d_pair(sb + j * kMnBoxBytes, tmB, bar_cl, n0 + 64 * j, k0);
+    }
+}
+
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ void load_stage_pair_lo(uint8_t* sa, const CUtensorMap* tmL,
+                                                   const CUtensorMap* tmB, uint32_t bar_cl,
+                                                   int32_t k0, int32_t m0, int32_t n0,
+                                                   uint32_t bits) {
+    uint8_t* sb = sa + kABytes;
+    load_a_pieces<A_MN>(sa, k0, m0, bits, [&](uint8_t* d, int32_t x, int32_t y) {
+        tma_load_2d_pair(d, tmL, bar_cl, x, y);
+    });
     if constexpr (!B_MN) {
         tma_load_2d_pair(sb, tmB, bar_cl, k0, n0);
     } else {
@@ -647,12 +748,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t tmem = bars->tmem_base;
 
     // every consumer of the unit ring arrives on the leader's slot barrier
-    auto next_unit = [&](int& sslot, uint32_t& sphase, bool& ok) -> int {
+    auto next_unit = [&](int& sslot, uint32_t& sphase, bool& ok, int& n_lo) -> int {
         if (!__all_sync(0xffffffffu, mbar_wait_cl(&bars->sfull[sslot], sphase, wait_ns, abort))) {
             ok = false;
             return -1;
         }
         const int u = *reinterpret_cast<volatile int*>(&bars->sched[sslot]);
+        n_lo = *reinterpret_cast<volatile int*>(&bars->sched_lo[sslot]);
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(cluster_addr(&bars->sempty[sslot], 0));
         if (++sslot == kSchedDepth) {
@@ -670,6 +772,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int64_t next_static = pair;
         while (ok) {
             int64_t u;
+            int n_lo = 0;
             if (leader) {
                 if (P.dynamic) {
                     int got = 0;
@@ -680,6 +783,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     next_static += n_pairs;
                 }
                 if (u >= total) u = -1;
+                n_lo = unit_lo_count(P, u);
                 if (!__all_sync(0xffffffffu,
                                 mbar_wait_cl(&bars->sempty[sslot], sphase ^ 1, wait_ns, abort))) {
                     ok = false;
@@ -687,7 +791,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (lane == 0) {  // the slot in both CTAs, then its barrier in both
                     bars->sched[sslot] = static_cast<int>(u);
+                    bars->sched_lo[sslot] = n_lo;
                     st_cluster_u32(cluster_addr(&bars->sched[sslot], 1), static_cast<uint32_t>(u));
+                    st_cluster_u32(cluster_addr(&bars->sched_lo[sslot], 1),
+                                   static_cast<uint32_t>(n_lo));
                     mbar_arrive(&bars->sfull[sslot]);
                     mbar_arrive_cluster(cluster_addr(&bars->sfull[sslot], 1));
                 }
@@ -697,11 +804,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     sphase ^= 1;
                 }
             } else {
-                u = next_unit(sslot, sphase, ok);
+                u = next_unit(sslot, sphase, ok, n_lo);
                 if (!ok) break;
             }
             if (u < 0) break;
-            const Unit un = decode_unit(P, u);
+            const Unit un = decode_unit(P, u, n_lo);
             const uint32_t full_cl0 = cluster_addr(&bars->full[0], 0);
             for (int64_t t = un.t0; t < un.t1 && ok; ++t) {
                 for (int64_t kb = 0; kb < un.k_blocks; ++kb) {
@@ -717,15 +824,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (leader) mbar_arrive_expect_tx(&bars->full[stage], 2 * kPairStageBytes);
                         const int64_t ks = P.k_split[un.kind];
                         const bool lo = ks > 0 && kb >= ks;
-                        const int32_t k0 = static_cast<int32_t>((lo ? kb - ks : kb) * kBK);
                         const int32_t m0 = static_cast<int32_t>(un.mb * 2 * kBM + rank * kBM);
                         const int32_t n0 = static_cast<int32_t>(t * kBN + rank * kBHalf);
-                        if (NK == 1 || un.kind == 0)
-                            load_stage_pair<K0::kAmn, K0::kBmn>(sa, lo ? &tmL0 : &tmA0, &tmB0,
-                                                                bar_cl, k0, m0, n0);
-                        else
-                            load_stage_pair<K1::kAmn, K1::kBmn>(sa, lo ? &tmL1 : &tmA1, &tmB1,
-                                                                bar_cl, k0, m0, n0);
+                        if (lo && P.lo_cnt[un.kind]) {  // planned second pass
+                            int32_t k0;
+                            uint32_t bits;
+                            lo_block(P, un, kb - ks, &k0, &bits);
+                            bits >>= 4 * rank;  // this CTA's half of the pair's pieces
+                            if (NK == 1 || un.kind == 0)
+                                load_stage_pair_lo<K0::kAmn, K0::kBmn>(sa, &tmL0, &tmB0, bar_cl,
+                                                                       k0, m0, n0, bits);
+                            else
+                                load_stage_pair_lo<K1::kAmn, K1::kBmn>(sa, &tmL1, &tmB1, bar_cl,
+                                                                       k0, m0, n0, bits);
+                        } else {
+                            const int32_t k0 = static_cast<int32_t>((lo ? kb - ks : kb) * kBK);
+                            if (NK == 1 || un.kind == 0)
+                                load_stage_pair<K0::kAmn, K0::kBmn>(sa, lo ? &tmL0 : &tmA0,
+                                                                    &tmB0, bar_cl, k0, m0, n0);
+                            else
+                                load_stage_pair<K1::kAmn, K1::kBmn>(sa, lo ? &tmL1 : &tmA1,
+                                                                    &tmB1, bar_cl, k0, m0, n0);
+                        }
                     }
                     __syncwarp();
                     if (++stage == kPairStages) {
@@ -747,9 +867,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool ok = true;
             const uint32_t sbase = smem_u32(smem);
             while (ok) {
-                const int u = next_unit(sslot, sphase, ok);
+                int n_lo = 0;
+                const int u = next_unit(sslot, sphase, ok, n_lo);
                 if (!ok || u < 0) break;
-                const Unit un = decode_unit(P, u);
+                const Unit un = decode_unit(P, u, n_lo);
                 for (int64_t t = un.t0; t < un.t1 && ok; ++t) {
                     if (!__all_sync(0xffffffffu,
                                     mbar_wait_cl(&bars->tempty[buf], bphase ^ 1, wait_ns, abort))) {
@@ -809,9 +930,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         typename K0::Epi epi0;
         typename K1::Epi epi1;
         while (ok) {
-            const int u = next_unit(sslot, sphase, ok);
+            int n_lo = 0;
+            const int u = next_unit(sslot, sphase, ok, n_lo);
             if (!ok || u < 0) break;
-            const Unit un = decode_unit(P, u);
+            const Unit un = decode_unit(P, u, n_lo);
             const int kind = (NK == 1) ? 0 : un.kind;
             const EpiArgs& ea = kind == 0 ? ea0 : ea1;
             const CUtensorMap* tmO = kind == 0 ? &tmO0 : &tmO1;
@@ -1587,6 +1709,12 @@ cudaError_t dispatch_f32(const GemmLaunch& L, const CUtensorMap* m, const KParam
 
 }  // namespace
 
+bool gemm_uses_pairs(int dtype, const int64_t* Ms, int nkinds) {
+    bool pair = dtype != LL_F32 && kUsePairs;
+    for (int k = 0; k < nkinds; ++k) pair = pair && Ms[k] >= 2 * kBM;
+    return pair;
+}
+
 cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s) {
     CUtensorMap m[8];  // A, B, out of kind 0; of kind 1; A_lo of kind 0, 1
     memset(m, 0, sizeof(m));
@@ -1595,8 +1723,8 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
     GemmLaunch G = L;
     // 16-bit operands run on CTA pairs (256 x 256 tiles) when every kind has
     // at least 256 rows; smaller problems keep the single-CTA kernel
-    bool pair = G.dtype != LL_F32 && kUsePairs;
-    for (int k = 0; k < G.nkinds; ++k) pair = pair && G.op[k].M >= 2 * kBM;
+    int64_t Ms[2] = {G.op[0].M, G.nkinds > 1 ? G.op[1].M : 0};
+    const bool pair = gemm_uses_pairs(G.dtype, Ms, G.nkinds);
     for (int k = 0; k < G.nkinds; ++k) {
         const bool okm = G.dtype == LL_F32
                              ? operand_maps_f32(G.op[k], &m[3 * k], &m[3 * k + 1])
@@ -1610,12 +1738,26 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
         if (G.dtype == LL_F32) P.sh[k].k_blocks = (G.op[k].K + kBKf - 1) / kBKf;
         if (G.op[k].A_lo) {  // hi / lo split: A_lo after A along K
             if (G.dtype == LL_F32) return cudaErrorInvalidValue;
-            GemmOperands lo = G.op[k];
-            lo.A = lo.A_lo;
-            CUtensorMap unused;
-            if (!operand_maps(lo, G.dtype, &m[6 + k], &unused, pair)) return cudaErrorInvalidValue;
+            const GemmOperands& g = G.op[k];
             P.k_split[k] = P.sh[k].k_blocks;
-            P.sh[k].k_blocks *= 2;
+            if (g.lo_cnt) {
+                // planned second pass: A_lo read in 32-row pieces
+                const bool ok = g.a_mn ? make_map(&m[6 + k], g.A_lo, G.dtype, g.M, g.K, g.lda,
+                                                  64, 32)
+                                       : make_map(&m[6 + k], g.A_lo, G.dtype, g.K, g.M, g.lda,
+                                                  kBK, 32);
+                if (!ok) return cudaErrorInvalidValue;
+                P.lo_cnt[k] = g.lo_cnt;
+                P.lo_idx[k] = g.lo_idx;
+                P.lo_ld[k] = g.lo_ld;
+            } else {
+                GemmOperands lo = g;
+                lo.A = lo.A_lo;
+                CUtensorMap unused;
+                if (!operand_maps(lo, G.dtype, &m[6 + k], &unused, pair))
+                    return cudaErrorInvalidValue;
+                P.sh[k].k_blocks *= 2;
+            }
         }
         P.n_units[k] = P.sh[k].m_blocks * P.sh[k].n_segs;
         P.out16[k] = G.out[k].dtype != LL_F32;
@@ -1634,6 +1776,9 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
         m[5] = m[2];
         m[7] = m[6];
         P.k_split[1] = P.k_split[0];
+        P.lo_cnt[1] = P.lo_cnt[0];
+        P.lo_idx[1] = P.lo_idx[0];
+        P.lo_ld[1] = P.lo_ld[0];
     }
     P.dynamic = G.counter != nullptr;
     P.counter = G.counter;

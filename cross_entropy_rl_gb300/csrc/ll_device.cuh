@@ -215,6 +215,24 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Maximum of 32 values by a tree of three-input maxima (16 instructions).
+__device__ __forceinline__ float max32(const float (&v)[32]) {
+    float a[11];
+#pragma unroll
+    for (int i = 0; i < 10; ++i) a[i] = max3f(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+    a[10] = fmaxf(v[30], v[31]);
+    const float b0 = max3f(a[0], a[1], a[2]), b1 = max3f(a[3], a[4], a[5]);
+    const float b2 = max3f(a[6], a[7], a[8]), b3 = fmaxf(a[9], a[10]);
+    return fmaxf(max3f(b0, b1, b2), b3);
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

@@ -102,7 +102,27 @@ struct EpiArgs {
     float inv_temp;          // Fwd / Recomp: logits scaled by 1 / temperature (1 = none)
     void* S_lo;              // Recomp, 16-bit: S - S_hi (the rounding rest of S) [M, ldS],
                              //   or nullptr (no hi / lo split)
+    uint8_t* lo_flags;       // Recomp, automatic split: [ceil(M / 32), lo_flags_ld] bytes, one
+                             //   per piece of 32 rows x 64 columns: 1 if its S_lo was
+                             //   written, else 0 (every piece in the chunk gets one);
+                             //   nullptr = S_lo written in full (split of every entry)
+    int64_t lo_flags_ld;     // row pitch of the flags: lo_flags_cols rounded up to 16
+    int64_t lo_flags_cols;   // pieces per row group: ceil(V / 64)
 };
+
+// Row pitch of the automatic split's piece flags: ceil(V / 64) rounded up to
+// 16 bytes, so that the plan reads them 16 at a time.
+__host__ __device__ inline int64_t lo_flags_pitch(int64_t V) { return ((V + 63) / 64 + 15) / 16 * 16; }
+
+// Automatic hi / lo split of S: an off-target entry keeps its rounding rest
+// S - S_hi when its probability p = S / (-grad / T) is at least this.
+// Smaller ones store S_hi alone (their rounding error is below 2^-9 * tau *
+// |grad / T| each).
+constexpr float kLoTau = 1.0f / 256.0f;
+
+// Pieces of the flag grid of the automatic split.
+constexpr int kLoRows = 32;
+constexpr int kLoCols = 64;
 
 struct GemmShape {
     int64_t m_blocks;        // M / 128, rounded up
@@ -131,7 +151,17 @@ struct GemmOperands {
     int64_t M, N, K;
     const void* A_lo;  // 16-bit only: a second A of A's layout; the contraction then
                        // runs over K twice, A then A_lo, against the same B (nullptr: no)
+    // planned second pass (automatic split): only the K blocks of each m block
+    // listed by launch_lo_plan run over A_lo, with the pieces of A_lo not
+    // written read as zeros (lo_cnt == nullptr: the whole second pass)
+    const int* lo_cnt;
+    const int64_t* lo_idx;
+    int64_t lo_ld;
 };
+
+// Whether launch_gemm runs these kinds (M of each) on CTA pairs: 16-bit
+// operands and every kind with at least 256 rows.
+bool gemm_uses_pairs(int dtype, const int64_t* Ms, int nkinds);
 
 // Tile output written by the epilogue ([rows, cols], row stride ld).
 struct OutDesc {
@@ -179,16 +209,39 @@ cudaError_t launch_db_finish(const float* partial, int64_t groups, int64_t V, fl
                              int first, int last, const int* offs, const int64_t* keys,
                              const float* tc_all, void* grad_bias, int out_dtype, cudaStream_t s);
 cudaError_t launch_fill_zero(void* p, int64_t n_elems, int dtype, cudaStream_t s);
+// out[i] = parts[0 * ld + i] + parts[1 * ld + i] + ... (ascending part
+// order, FP32 accumulation, one rounding to dtype), i < n.
+cudaError_t launch_sum_ordered(const void* parts, int64_t nparts, int64_t n, int64_t ld,
+                               int dtype, void* out, int num_sms, cudaStream_t s);
+// Plan of the second (S_lo) pass of the automatic hi / lo split, from the
+// recompute's piece flags F [ceil(rows / 32), ceil(V / 64)], row pitch
+// lo_flags_pitch(V) (1 = that piece of 32 rows x 64 columns of S_lo was
+// written):
+//  grad_hidden, per block of R rows (R = 128, or 256 on CTA pairs): the
+//   64-column K blocks kb with a written piece in the block, ascending, as
+//   (kb << 8 | bits) where bit i is row group i of the block (32 rows);
+//   dh_cnt[mb] entries at dh_idx[mb * ceil(V / 64)].
+//  grad_weight, per block of C vocab rows (C = 128 or 256): the 64-token K
+//   blocks kb with a written piece in the block, ascending, as (kb << 8 |
+//   bits), bit 2c + i being 64-column group c of the block and row group
+//   2 kb + i; dw_cnt[vb] entries at dw_idx[vb * ceil(rows / 64)].
+// A block with no entry runs no second pass.
+cudaError_t launch_lo_plan(const uint8_t* F, int64_t rows, int64_t V, int R, int C,
+                           int* dh_cnt, int64_t* dh_idx, int* dw_cnt, int64_t* dw_idx,
+                           cudaStream_t s);
 // Softmax part from stored FP32 logits Z [rows, ldZ] (bias included):
 // S = -grad * exp(z - lse) off target (S dtype s_dtype), S = 0 and
 // tc = grad * (1 - p) at the target, +0 rows when the target is invalid or
 // the gradient zero.  Same arithmetic as the recompute epilogue.
 // With db_part (not null) it also writes the grad_bias partials per 32 rows,
-// as the recompute epilogue does.
+// as the recompute epilogue does.  S_lo (16-bit): the rests S - S_hi, all of
+// them, or with lo_flags the automatic split's pieces and flags, as the
+// recompute epilogue writes them.
 cudaError_t launch_softmax_part(const float* Z, int64_t ldZ, int64_t rows, int64_t V,
                                 const int64_t* targets, const float* grad, const float* lse,
                                 void* S, int64_t ldS, int s_dtype, float* tc, float* db_part,
-                                float inv_temp, void* S_lo, cudaStream_t s);
+                                float inv_temp, void* S_lo, uint8_t* lo_flags,
+                                cudaStream_t s);
 cudaError_t launch_unsatisfied_wait(int* flag, int* status, uint64_t wait_ns, cudaStream_t s);
 
 }  // namespace ll

@@ -87,18 +87,29 @@ typedef enum { LL_F32 = 0, LL_F16 = 1, LL_BF16 = 2 } ll_dtype;
  *                RL-Kernel PR #495, the vLLM provider evidence at
  *                temperatures 1.0 and 0.7).  T = 1 gives bitwise the
  *                results of the calls without options.
- *   split_s      0 or 1; backward with 16-bit operands: the off-target part
- *                S = -grad_logp * p / T of g is stored as a hi / lo pair of
- *                the operand dtype (S_hi = S rounded, S_lo = S - S_hi
- *                rounded) and the grad_hidden / grad_weight contractions run
- *                over both, twice their work: S is then carried to ~2^-17
- *                relative instead of 2^-9, which matters for peaked
- *                distributions whose large off-target probabilities would
- *                otherwise lose 2^-9 * |grad| at that entry.  The workspace
- *                grows by one more S buffer (flags bit 1 of
- *                ll_workspace_size).  Ignored for FP32 operands (S is FP32).
+ *   split_s      backward with 16-bit operands: how the off-target part
+ *                S = -grad_logp * p / T of g is stored before the
+ *                grad_hidden / grad_weight contractions, whose operands are
+ *                16-bit.  One 16-bit part loses up to 2^-9 of an entry, which
+ *                matters where off-target probabilities are large (peaked
+ *                rows, small vocabularies).
+ *                0 (default) automatic: S_hi = S rounded, and the rounding
+ *                  rest S_lo = S - S_hi (rounded) is kept for the entries
+ *                  with p >= 2^-8 only, in pieces of 32 rows x 64 columns;
+ *                  the contractions run a second pass over the pieces that
+ *                  hold such an entry.  A row's results depend on that row
+ *                  alone (batch invariance holds).  Flat distributions,
+ *                  such as a freshly initialised head, write few or no
+ *                  pieces (none at all where every p < 2^-8) and cost
+ *                  little more than mode 2.
+ *                1 every entry keeps its rest; the contractions run over S_hi
+ *                  and S_lo, twice their work: S carried to ~2^-17 relative.
+ *                2 never: S in one 16-bit part (no S_lo buffer needed).
+ *                Modes 0 and 1 take one more S-sized buffer in the workspace
+ *                (bits 1-2 of ll_workspace_size's flags give the mode).
+ *                Ignored for FP32 operands (S is FP32).
  *   reserved     must be 0.
- * A bad temperature, split_s not 0 / 1 or a non-zero reserved field is
+ * A bad temperature, split_s not 0 / 1 / 2 or a non-zero reserved field is
  * LL_ERR_INVALID_ARG.
  */
 typedef struct {
@@ -117,8 +128,9 @@ int ll_version(void);
  * Workspace bytes needed by ll_forward (is_backward = 0), ll_backward
  * (is_backward = 1) or ll_forward_backward (is_backward = 2) for these
  * sizes; `flags` bit 0 is the need_db flag of the backward (bias gradient
- * partials), bit 1 the split_s option (ll_options); both are ignored for
- * the forward.
+ * partials), bits 1-2 the split_s option of ll_options (0 = automatic, the
+ * default, 1 = always, 2 = never); both are ignored for the forward.
+ * Returns 0 for a split_s field above 2.
  * token_chunks: number of token chunks the backward splits N into (0 =
  * automatic, see ll_backward).  Returns 0 only for N == 0 in the forward.
  * The workspace pointer must be 256-byte aligned.
@@ -371,11 +383,28 @@ int logits_logp_fwd_bwd_ex(const float* grad_logp, const void* logits, int64_t l
 int ll_check_status(void* stream);
 
 /*
+ * Fixed-order sum of partial tables, the data-parallel exchange of
+ * grad_weight / grad_bias.  Each rank computes its token shard's tables and
+ * they must be added (issue #261, "Current accumulation": the FP32 gradient
+ * table is a sum over tokens); adding them in ascending rank order on one
+ * rank, for each slice of the table it owns, gives the same bits whatever
+ * the transport and on every rank that receives the result.
+ *   parts [nparts, ld] of dtype, device: part k at parts + k * ld elements.
+ *   out   [n] of dtype, device (written): out[i] = parts[0][i] + parts[1][i]
+ *         + ... + parts[nparts - 1][i], in that order, accumulated in FP32
+ *         and rounded once to dtype.  n <= ld.  out may not overlap parts.
+ * n == 0 launches nothing.  Asynchronous on `stream`.
+ */
+int ll_sum_ordered(const void* parts, int64_t nparts, int64_t n, int64_t ld, int dtype,
+                   void* out, void* stream);
+
+/*
  * Tracing.  ll_launch_count(): number of kernels this library has launched
  * in the process.  ll_profile_enable(1) clears earlier records and brackets
  * every phase of later calls (fwd_gemm, lse_merge, token_sort,
- * recompute_gemm, softmax_part, grad_gemm (grad_hidden and grad_weight
- * tiles), db_sums, logits_fwd, logits_bwd, logits_fused; an _f32 suffix
+ * recompute_gemm, softmax_part, lo_plan, grad_gemm (grad_hidden and
+ * grad_weight tiles), db_sums, logits_fwd, logits_bwd, logits_fused,
+ * sum_ordered; an _f32 suffix
  * marks the GEMMs of FP32 operands, 3 x TF32 on the tensor cores) with CUDA
  * events on the call's
  * stream; ll_profile_enable(0) stops recording.  ll_profile_summary()

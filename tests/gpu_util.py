@@ -10,13 +10,14 @@ Tolerances (|got - ref| <= atol + rtol * |ref| (+ one output ulp)):
                              rounding is up to half an ulp)
 
 For 16-bit operands the off-target entries S = -grad * p of g are stored in
-the operand dtype before the two gradient contractions.  Outside the
-benchmark shapes (small vocabularies, where p is large) that rounding alone
-can exceed 5e-4, so the small full-parity cases add its worst-case bound,
-u * (|S| . |W|) for grad_hidden, u * (|S|^T . |h|) for grad_weight and
-u * sum_n |S| for grad_bias (u = 2^-8 for bf16, 2^-11 for fp16), computed
-in float64 from the exact S.  At the benchmark shapes the term is below
-1e-5 and the bar is the plain 5e-4.
+the operand dtype before the two gradient contractions.  By default the
+library also keeps the rounding rest S - S_hi of every entry with p >= 2^-8
+(the automatic hi / lo split), and every parity test holds the plain bound
+above.  With the split switched off (split_s = "never") the 16-bit rounding
+of S alone can exceed 5e-4 outside the benchmark shapes; s_rounding_bounds
+gives its worst case, u * (|S| . |W|) for grad_hidden, u * (|S|^T . |h|) for
+grad_weight and u * sum_n |S| for grad_bias (u = 2^-8 for bf16, 2^-11 for
+fp16), used only by the test of that mode.
 """
 import math
 

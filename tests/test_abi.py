@@ -58,9 +58,18 @@ def test_workspace_size_rules(L):
     assert bwd1 >= N * V * 2
     bwd8 = L.ll_workspace_size(N, 2048, V, ll.LL_BF16, 8, 1, 0)
     assert bwd8 < bwd1 and bwd8 >= (N // 8) * V * 2
-    # automatic chunking keeps the softmax part within 2 GiB
-    big = L.ll_workspace_size(32768, 4096, 151936, ll.LL_BF16, 0, 1, 0)
+    # automatic chunking keeps the softmax part within 2 GiB (split_s =
+    # never: S alone); the default automatic split adds one S-sized buffer
+    # and its small piece flags and plan
+    big = L.ll_workspace_size(32768, 4096, 151936, ll.LL_BF16, 0, 1, 2 << 1)
     assert big <= (2 << 30) + (64 << 20)
+    auto = L.ll_workspace_size(32768, 4096, 151936, ll.LL_BF16, 0, 1, 0)
+    always = L.ll_workspace_size(32768, 4096, 151936, ll.LL_BF16, 0, 1, 1 << 1)
+    assert 2 * big - (64 << 20) <= always <= auto <= 2 * big + (64 << 20)
+    assert L.ll_workspace_size(32768, 4096, 151936, ll.LL_BF16, 0, 1, 3 << 1) == 0
+    # FP32 keeps S in FP32: the split mode changes nothing
+    f = [L.ll_workspace_size(4096, 2048, 32768, ll.LL_F32, 1, 1, m << 1) for m in range(3)]
+    assert f[0] == f[1] == f[2]
     assert L.ll_workspace_size(N, 2048, V, ll.LL_F32, 1, 1, 0) >= N * V * 4
     # grad_bias partials only when requested
     assert L.ll_workspace_size(N, 2048, V, ll.LL_BF16, 1, 1, 1) > bwd1
@@ -169,8 +178,19 @@ def test_options_are_validated_before_any_device_work(L):
     assert L.ll_backward_ex(None, None, None, None, None, None, 4, 8, 16, ll.LL_BF16, 1, 1, 0,
                             None, ll.LL_BF16, None, ll.LL_F32, None, 0, None, 0,
                             ctypes.byref(o), None) == 1
+    for bad in (-1, 3):  # split_s is 0 (automatic), 1 (always) or 2 (never)
+        o = ll.Options(temperature=1.0, split_s=bad)
+        assert L.ll_backward_ex(None, None, None, None, None, None, 4, 8, 16, ll.LL_BF16, 1, 1,
+                                0, None, ll.LL_BF16, None, ll.LL_F32, None, 0, None, 0,
+                                ctypes.byref(o), None) == 1
     with pytest.raises(ValueError, match="temperature"):
         ll._opts(-2.0)
+    # binding: the default is the automatic split (no options struct at all)
+    assert ll._opts(1.0) is None and ll._opts(1.0, "auto") is None
+    assert ll._split_code(True) == 1 and ll._split_code("always") == 1
+    assert ll._split_code(False) == 2 and ll._split_code("never") == 2
+    with pytest.raises(ValueError, match="split_s"):
+        ll._split_code("sometimes")
 
 
 C_PROGRAM = r"""

@@ -10,7 +10,7 @@ import torch
 
 import oracle as O
 from cross_entropy_rl_gb300 import synth, tp
-from gpu_util import TOL, assert_pos_zero, bits_equal, check, dev, s_rounding_bounds
+from gpu_util import TOL, assert_pos_zero, bits_equal, check, dev
 
 pytestmark = pytest.mark.gpu
 
@@ -61,7 +61,6 @@ def test_shards_reproduce_the_whole_vocab_run(lib, dt, V, world):
     gl = p["gl"].copy()
     gl[[5, 150]] = [0.0, -0.0]        # zero upstream rows
     y[10:20] = np.arange(10) * (V // 10)  # targets spread over the shards
-    q = dict(p, y=y, gl=gl)
     h, W, b = dev(p["h"], dt), dev(p["W"], dt), dev(p["b"], dt)
     yd, gd = dev(y), dev(gl)
     logp, lse = lib.forward(h, W, b, yd)
@@ -74,8 +73,7 @@ def test_shards_reproduce_the_whole_vocab_run(lib, dt, V, world):
     # grad_hidden: the shards' parts summed, against the oracle
     ref = O.linear_forward_backward(gl, p["h"], p["W"], p["b"], y, dt)
     ga, gr = TOL[dt]["grad"]
-    sb = s_rounding_bounds(q)
-    check("dh", got[2], ref["dh"], ga, gr, extra=sb.get("dh"))
+    check("dh", got[2], ref["dh"], ga, gr)
     for r in (3, 77, 5, 150):
         assert_pos_zero(f"dh[{r}]", got[2][r])
 

@@ -1,8 +1,9 @@
-"""Token-sharded data parallelism with CPU ranks (gloo, world_size 2):
+"""Token-sharded data parallelism with CPU ranks (gloo, world_size 2 and 3):
 per-rank shards through the FP64 oracle, the fixed-order grad_weight /
-grad_bias reduction reproduces the single-process gradients and is bitwise
-identical on every rank; a rank that fails is seen by the others as an
-error, not a hang."""
+grad_bias reduction (a reduce-scatter by all-to-all, each slice summed in
+ascending rank order by its owner, then an all-gather) reproduces the
+single-process gradients and is bitwise identical on every rank; a rank that
+fails is seen by the others as an error, not a hang."""
 import os
 import socket
 
@@ -43,6 +44,50 @@ def _worker(rank, world, port, out_dir, fail_rank):
         np.save(os.path.join(out_dir, f"logp{rank}.npy"), r["logp"])
     finally:
         dist.destroy_process_group()
+
+
+def _rs_worker(rank, world, port, out_dir, numel):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=__import__("datetime").timedelta(seconds=20))
+    try:
+        g = torch.Generator().manual_seed(100 + rank)
+        t = torch.randn(numel, generator=g, dtype=torch.float32)
+        mine = dp.reduce_scatter_fixed_order(t)
+        full = dp.reduce_sum_fixed_order(t.view(-1, 1))
+        np.save(os.path.join(out_dir, f"slice{rank}.npy"), mine.numpy())
+        np.save(os.path.join(out_dir, f"full{rank}.npy"), full.view(-1).numpy())
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,numel", [(2, 1000), (3, 1001), (3, 2)])
+def test_reduce_scatter_fixed_order(tmp_path, world, numel):
+    """Each rank's slice is the ascending-rank FP32 sum of that slice of
+    every rank's table (bitwise); the all-gathered sum is the same bits on
+    every rank, shape kept."""
+    port = _free_port()
+    mp.start_processes(_rs_worker, args=(world, port, str(tmp_path), numel), nprocs=world,
+                       join=True, start_method="spawn")
+    ts = [torch.randn(numel, generator=torch.Generator().manual_seed(100 + r),
+                      dtype=torch.float32) for r in range(world)]
+    want = ts[0].clone()
+    for t in ts[1:]:
+        want += t
+    for r in range(world):
+        b, e = dp.shard_rows(numel, world, r)
+        got = np.load(tmp_path / f"slice{r}.npy")
+        assert np.array_equal(got, want[b:e].numpy()), r
+        assert np.array_equal(np.load(tmp_path / f"full{r}.npy"), want.numpy()), r
+
+
+def test_exchange_bytes_per_rank():
+    """(world - 1) / world of the table leaves and enters each rank."""
+    d = dp.slice_bytes(151936 * 4096, 4, 8)
+    table = 151936 * 4096 * 4
+    assert d["reduce_scatter_send"] == table - table // 8
+    assert d["reduce_scatter_recv"] == table - table // 8
+    assert dp.slice_bytes(100, 4, 1)["reduce_scatter_send"] == 0
 
 
 def test_shard_rows_cover_exactly_once():

@@ -38,9 +38,8 @@ __device__ __forceinline__ MS ms_combine(MS a, MS b) {
 
 // Fold 8 values (natural units) into the running (m, s).
 __device__ __forceinline__ void ms_fold8(MS& st, const float (&f)[8]) {
-    float vmax = f[0];
-#pragma unroll
-    for (int j = 1; j < 8; ++j) vmax = fmaxf(vmax, f[j]);
+    const float vmax =
+        max3f(max3f(f[0], f[1], f[2]), max3f(f[3], f[4], f[5]), fmaxf(f[6], f[7]));
     const float mu = vmax * kLog2e;
     if (mu > st.m) {
         st.s = st.s * ex2(st.m - mu);
@@ -123,9 +122,31 @@ __device__ __forceinline__ void st8(T* p, const float (&f)[8], uint64_t pol) {
         store8(p, f);
 }
 
+// The tempered logits x / T (it = 1 / T); T = 1 skips the exact multiply.
 __device__ __forceinline__ void scale8(float (&f)[8], float it) {
+    if (it == 1.f) return;
 #pragma unroll
     for (int j = 0; j < 8; ++j) f[j] *= it;
+}
+
+// Gradient of 8 tempered logits z (columns c0 .. c0 + 7) of a live row:
+// g * (onehot - p), p = 2^(z log2e - lse2).  Off target onehot - p = -p
+// exactly (0 - p and -p differ only for p = +0, where either gives +0 after
+// the + 0), so only the target column takes the 1 - p form.
+__device__ __forceinline__ void grad8(float (&f)[8], int64_t c0, int64_t y, float g,
+                                      float lse2) {
+    float p[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        p[j] = ex2(fmaf(f[j], kLog2e, -lse2));
+        f[j] = fmaf(g, -p[j], 0.f);  // + 0 keeps empty results at +0
+    }
+    const int64_t off = y - c0;
+    if (off >= 0 && off < 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j == off) f[j] = fmaf(g, 1.f - p[j], 0.f);
+    }
 }
 
 // This thread's (max, sum-exp) of row x: 8-element vectors tid, tid + T,
@@ -203,7 +224,8 @@ __device__ __forceinline__ void row_grad(const T* x, T* o, int64_t V, int vec_ok
                     float f[8];
                     unpack(r[u], f);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) f[j] = grad_elem(f[j] * it, c0 + j, y, g, lse2);
+                    scale8(f, it);
+                    grad8(f, c0, y, g, lse2);
                     st8<T, HINT>(o + c0, f, pol_st);
                 }
             }
@@ -211,8 +233,8 @@ __device__ __forceinline__ void row_grad(const T* x, T* o, int64_t V, int vec_ok
                 float f[8];
                 const int64_t c0 = i * 8;
                 unpack(ld_raw<T, HINT>(x + c0, pol_ld), f);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) f[j] = grad_elem(f[j] * it, c0 + j, y, g, lse2);
+                scale8(f, it);
+                grad8(f, c0, y, g, lse2);
                 st8<T, HINT>(o + c0, f, pol_st);
             }
         }
@@ -402,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1) logits_fwd_bwd_onchip_kernel(
                     Raw8<T> r;
                     r.a = rr[k];
                     unpack(r, f);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) f[j] = grad_elem(f[j] * it, i * 8 + j, y, gi, lse2);
+                    scale8(f, it);
+                    grad8(f, i * 8, y, gi, lse2);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) f[j] = 0.f;
@@ -420,8 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1) logits_fwd_bwd_onchip_kernel(
                     Raw8<T> r;
                     r.a = sm[k * kThreads + t];
                     unpack(r, f);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) f[j] = grad_elem(f[j] * it, i * 8 + j, y, gi, lse2);
+                    scale8(f, it);
+                    grad8(f, i * 8, y, gi, lse2);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 8; ++j) f[j] = 0.f;

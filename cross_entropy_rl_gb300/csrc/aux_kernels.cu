@@ -755,6 +755,43 @@ cudaError_t launch_sum_ordered(const void* parts, int64_t nparts, int64_t n, int
     return cudaGetLastError();
 }
 
+// hT[d, n] = h[n, d] for 16-bit h [N, D] (row stride D, D % 8 == 0) into
+// hT [D, ldT] (ldT >= N, a multiple of 8): 64 x 64 tiles through shared
+// memory, 16-byte loads and stores.
+__global__ void __launch_bounds__(256) transpose16_kernel(const uint16_t* __restrict__ h,
+                                                          int64_t N, int64_t D,
+                                                          uint16_t* __restrict__ hT, int64_t ldT) {
+    __shared__ uint16_t tile[64][64 + 8];
+    const int64_t n0 = blockIdx.x * int64_t(64), d0 = blockIdx.y * int64_t(64);
+    const int c = (threadIdx.x & 7) * 8;
+    for (int r = threadIdx.x >> 3; r < 64; r += 32) {
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (n0 + r < N && d0 + c < D) v = *reinterpret_cast<const uint4*>(h + (n0 + r) * D + d0 + c);
+        const uint16_t* e = reinterpret_cast<const uint16_t*>(&v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) tile[r][c + j] = e[j];
+    }
+    __syncthreads();
+    for (int r = threadIdx.x >> 3; r < 64; r += 32) {
+        if (d0 + r >= D || n0 + c >= N) continue;
+        uint4 v;
+        uint16_t* e = reinterpret_cast<uint16_t*>(&v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) e[j] = tile[c + j][r];
+        *reinterpret_cast<uint4*>(hT + (d0 + r) * ldT + n0 + c) = v;
+    }
+}
+
+cudaError_t launch_transpose16(const void* h, int64_t N, int64_t D, void* hT, int64_t ldT,
+                               cudaStream_t s) {
+    if (N <= 0 || D <= 0) return cudaSuccess;
+    note_launches(1);
+    const dim3 grid(static_cast<unsigned>((N + 63) / 64), static_cast<unsigned>((D + 63) / 64));
+    transpose16_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(h), N, D,
+                                            static_cast<uint16_t*>(hT), ldT);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_fill_zero(void* p, int64_t n_elems, int dtype, cudaStream_t s) {
     if (n_elems <= 0) return cudaSuccess;
     note_launches(1);

@@ -172,12 +172,14 @@ struct BwdLayout {
     int64_t chunks, Nc, ldS, ldZ, n_segs, lo_fld;
     size_t S, S_lo, Z, part_m, part_s, zy, tc, keys, offs, ctr, db, total;
     size_t lo_flags, dh_cnt, dh_idx, dw_cnt, dw_idx;  // automatic split
+    size_t hT;      // 16-bit: h^T [D, ldT] (grad_weight's K-major B operand)
+    int64_t ldT;
 };
 // fused = 1: the single fwd+bwd call, which also keeps the chunk's FP32
 // logits Z and the forward partials.
 // split_mode (SplitMode): all / automatic keep an S_lo buffer (16-bit
 // dtypes); automatic also the piece flags and the second pass's plan.
-BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need_db,
+BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, int dtype, int token_chunks, int need_db,
                      int fused = 0, int split_mode = kSplitNone) {
     BwdLayout L;
     L.ldS = round_up(V, 8);
@@ -239,6 +241,9 @@ BwdLayout bwd_layout(int64_t N, int64_t V, int dtype, int token_chunks, int need
     off = align_up(off + 64);
     L.db = off;
     if (need_db) off = align_up(off + size_t(db_groups(L.Nc) + 1) * size_t(V) * 4);
+    L.hT = off;
+    L.ldT = round_up(L.Nc, 8);
+    if (dtype != LL_F32) off = align_up(off + size_t(D) * size_t(L.ldT) * 2);
     L.total = off;
     return L;
 }
@@ -311,7 +316,7 @@ size_t ll_workspace_size(int64_t N, int64_t D, int64_t V, int dtype, int token_c
     if (!is_backward) return fwd_layout(N, V).total;
     const int mode = (flags >> 1) & 3;
     if (mode > kSplitNone) return 0;
-    return bwd_layout(N, V, dtype, token_chunks, flags & 1, is_backward == 2, mode).total;
+    return bwd_layout(N, D, V, dtype, token_chunks, flags & 1, is_backward == 2, mode).total;
 }
 
 void ll_set_wait_limit_ns(int64_t ns) { g_wait_limit_ns = ns > 0 ? uint64_t(ns) : 2000000000ull; }
@@ -460,7 +465,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
     }
     if (!grad_logp || !hidden || !targets || (!fused && !lse)) return LL_ERR_INVALID_ARG;
     if (!aligned16(hidden) || (need_dh && !aligned16(grad_hidden))) return LL_ERR_ALIGN;
-    const BwdLayout L = bwd_layout(N, V, dtype, token_chunks, need_db, fused, split);
+    const BwdLayout L = bwd_layout(N, D, V, dtype, token_chunks, need_db, fused, split);
     if (!workspace || ws_bytes < L.total) return LL_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return LL_ERR_WORKSPACE;
 
@@ -515,6 +520,10 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
         }
         if (e != cudaSuccess) return cuda_status(e);
     }
+
+    // grad_weight's B operand, the chunk's h^T: K-major (tokens contiguous)
+    // for the tensor cores, so that only its A operand (S) is read MN-major
+    void* hT = dtype != LL_F32 ? static_cast<void*>(ws + L.hT) : nullptr;
 
     EpiArgs base;
     memset(&base, 0, sizeof(base));
@@ -636,6 +645,11 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             e = launch_lo_plan(lo_flags, rows, V, blk, blk, dh_cnt, dh_idx, dw_cnt, dw_idx, s);
             if (e != cudaSuccess) return cuda_status(e);
         }
+        if (need_dw && hT) {
+            Phase ph("transpose_h", s);
+            e = launch_transpose16(h_c, rows, D, hT, L.ldT, s);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
         if (need_dh || need_dw) {
             GemmLaunch G;
             memset(&G, 0, sizeof(G));
@@ -669,8 +683,12 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             }
             if (need_dw) {
                 G.kind[k] = EpiKind::Dw;
-                G.op[k] = GemmOperands{S, L.ldS, 1, h_c, D, 1, V, D, rows, S_lo,
-                                       lo_auto ? dw_cnt : nullptr, dw_idx, cdiv(rows, 64)};
+                if (hT)  // K-major B: the chunk's h^T [D, rows]
+                    G.op[k] = GemmOperands{S, L.ldS, 1, hT, L.ldT, 0, V, D, rows, S_lo,
+                                           lo_auto ? dw_cnt : nullptr, dw_idx, cdiv(rows, 64)};
+                else
+                    G.op[k] = GemmOperands{S, L.ldS, 1, h_c, D, 1, V, D, rows, S_lo,
+                                           lo_auto ? dw_cnt : nullptr, dw_idx, cdiv(rows, 64)};
                 GemmShape& sh = G.shape[k];
                 sh.m_blocks = cdiv(V, kBM);
                 sh.n_tiles = cdiv(D, kBN);
@@ -788,7 +806,7 @@ size_t ll_workspace_size_shard(int64_t N, int64_t D, int64_t Vs, int dtype, int 
     if (!is_backward) return local_targets_bytes(N);
     const int mode = (flags >> 1) & 3;
     if (mode > kSplitNone) return 0;
-    return bwd_layout(N, Vs, dtype, token_chunks, flags & 1, 0, mode).total +
+    return bwd_layout(N, D, Vs, dtype, token_chunks, flags & 1, 0, mode).total +
            local_targets_bytes(N);
 }
 
@@ -854,7 +872,7 @@ int ll_backward_shard(const float* grad_logp, const void* hidden, const void* we
     if (!workspace || ws_bytes < tail) return LL_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return LL_ERR_WORKSPACE;
     const size_t body = ws_bytes - tail;
-    const BwdLayout L = bwd_layout(N, Vs, dtype, token_chunks, need_db, 0, split);
+    const BwdLayout L = bwd_layout(N, D, Vs, dtype, token_chunks, need_db, 0, split);
     if (body < L.total) return LL_ERR_WORKSPACE;
     // checks of backward_impl that must pass before anything is launched
     if ((need_dh | need_dw | need_db) & ~1 || token_chunks < 0) return LL_ERR_INVALID_ARG;

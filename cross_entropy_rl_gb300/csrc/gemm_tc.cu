@@ -1628,7 +1628,7 @@ cudaError_t dispatch(const GemmLaunch& L, const CUtensorMap* m, const KParams& P
     using Fwd = Kind<T, EpiKind::Fwd, false, false>;
     using Rec = Kind<T, EpiKind::Recomp, false, false>;
     using Dh = Kind<T, EpiKind::Dh, false, true>;
-    using Dw = Kind<T, EpiKind::Dw, true, true>;
+    using Dw = Kind<T, EpiKind::Dw, true, false>;  // B = h^T, K-major
     const int mc = L.max_ctas;
     if (L.nkinds == 1) {
         switch (L.kind[0]) {

@@ -209,6 +209,9 @@ cudaError_t launch_db_finish(const float* partial, int64_t groups, int64_t V, fl
                              int first, int last, const int* offs, const int64_t* keys,
                              const float* tc_all, void* grad_bias, int out_dtype, cudaStream_t s);
 cudaError_t launch_fill_zero(void* p, int64_t n_elems, int dtype, cudaStream_t s);
+// hT [D, ldT] = h^T for 16-bit h [N, D] (D % 8 == 0; ldT >= N, a multiple of 8).
+cudaError_t launch_transpose16(const void* h, int64_t N, int64_t D, void* hT, int64_t ldT,
+                               cudaStream_t s);
 // out[i] = parts[0 * ld + i] + parts[1 * ld + i] + ... (ascending part
 // order, FP32 accumulation, one rounding to dtype), i < n.
 cudaError_t launch_sum_ordered(const void* parts, int64_t nparts, int64_t n, int64_t ld,

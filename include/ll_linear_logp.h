@@ -402,9 +402,9 @@ int ll_sum_ordered(const void* parts, int64_t nparts, int64_t n, int64_t ld, int
  * Tracing.  ll_launch_count(): number of kernels this library has launched
  * in the process.  ll_profile_enable(1) clears earlier records and brackets
  * every phase of later calls (fwd_gemm, lse_merge, token_sort,
- * recompute_gemm, softmax_part, lo_plan, grad_gemm (grad_hidden and
- * grad_weight tiles), db_sums, logits_fwd, logits_bwd, logits_fused,
- * sum_ordered; an _f32 suffix
+ * recompute_gemm, softmax_part, lo_plan, transpose_h, grad_gemm
+ * (grad_hidden and grad_weight tiles), db_sums, logits_fwd, logits_bwd,
+ * logits_fused, sum_ordered; an _f32 suffix
  * marks the GEMMs of FP32 operands, 3 x TF32 on the tensor cores) with CUDA
  * events on the call's
  * stream; ll_profile_enable(0) stops recording.  ll_profile_summary()

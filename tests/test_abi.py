@@ -59,13 +59,16 @@ def test_workspace_size_rules(L):
     bwd8 = L.ll_workspace_size(N, 2048, V, ll.LL_BF16, 8, 1, 0)
     assert bwd8 < bwd1 and bwd8 >= (N // 8) * V * 2
     # automatic chunking keeps the softmax part within 2 GiB (split_s =
-    # never: S alone); the default automatic split adds one S-sized buffer
-    # and its small piece flags and plan
+    # never: S alone, plus the transposed hidden states h^T of 16-bit
+    # operands); the default automatic split adds one S-sized buffer and its
+    # small piece flags and plan
+    hT = 4096 * 6656 * 2  # one chunk's h^T (5 chunks of 6656 rows)
     big = L.ll_workspace_size(32768, 4096, 151936, ll.LL_BF16, 0, 1, 2 << 1)
-    assert big <= (2 << 30) + (64 << 20)
+    assert hT <= big <= (2 << 30) + hT + (64 << 20)
     auto = L.ll_workspace_size(32768, 4096, 151936, ll.LL_BF16, 0, 1, 0)
     always = L.ll_workspace_size(32768, 4096, 151936, ll.LL_BF16, 0, 1, 1 << 1)
-    assert 2 * big - (64 << 20) <= always <= auto <= 2 * big + (64 << 20)
+    s_only = big - hT
+    assert 2 * s_only - (64 << 20) <= always - hT <= auto - hT <= 2 * s_only + (64 << 20)
     assert L.ll_workspace_size(32768, 4096, 151936, ll.LL_BF16, 0, 1, 3 << 1) == 0
     # FP32 keeps S in FP32: the split mode changes nothing
     f = [L.ll_workspace_size(4096, 2048, 32768, ll.LL_F32, 1, 1, m << 1) for m in range(3)]

@@ -873,6 +873,9 @@ def logits_path(args, device, pk):
             "logits_fwd": {"ms": fwd_ms, "gbs": fwd_b / (fwd_ms * 1e-3) / 1e9,
                            "frac": fwd_b / (fwd_ms * 1e-3) / 1e9 / peak},
             "single_pass": {"call": "logits_logp_fwd_bwd (grad_logp known before the forward)",
+                            "traffic": None if ncu_traffic("logits_fused", "logits_32k_151936")
+                            is None else ncu_traffic("logits_fused", "logits_32k_151936")
+                            * N / 32768,
                             "ms_per_step": ms_fused, "value": N / (ms_fused * 1e-3),
                             "unit": "tokens/s", "bytes_per_token": 4 * V,
                             "gbs": 4.0 * N * V / (ms_fused * 1e-3) / 1e9,

@@ -134,12 +134,13 @@ __device__ __forceinline__ Unit decode_unit(const KParams& P, int64_t u, int n_l
         r.mb = v / sh.n_segs;
         r.seg = v % sh.n_segs;
     } else {
-        const int64_t per_group = kGroupM * sh.n_segs;
+        const int64_t G = sh.group_m;
+        const int64_t per_group = G * sh.n_segs;
         const int64_t g = v / per_group;
         const int64_t in_g = v % per_group;
-        const int64_t gm = min(kGroupM, sh.m_blocks - g * kGroupM);
+        const int64_t gm = min(G, sh.m_blocks - g * G);
         r.seg = in_g / gm;
-        r.mb = g * kGroupM + in_g % gm;
+        r.mb = g * G + in_g % gm;
     }
     r.t0 = r.seg * sh.tiles_per_unit;
     r.t1 = min(r.t0 + sh.tiles_per_unit, sh.n_tiles);
@@ -1733,6 +1734,11 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
         if (!out_map(&m[3 * k + 2], G.out[k])) return cudaErrorInvalidValue;
         P.sh[k] = G.shape[k];
         if (pair) P.sh[k].m_blocks = (G.op[k].M + 2 * kBM - 1) / (2 * kBM);
+        {   // grouped order: as many row blocks of A per group as fit kGroupBytes
+            const int64_t blk = (pair ? 2 * kBM : kBM) * G.op[k].K * (G.dtype == LL_F32 ? 4 : 2);
+            const int64_t gm = kGroupBytes / (blk > 0 ? blk : 1);
+            P.sh[k].group_m = gm < 4 ? 4 : (gm > kGroupM ? kGroupM : gm);
+        }
         // the host sizes K blocks for the 16-bit kernel (64 values); the
         // tf32 kernel takes 16 per stage
         if (G.dtype == LL_F32) P.sh[k].k_blocks = (G.op[k].K + kBKf - 1) / kBKf;

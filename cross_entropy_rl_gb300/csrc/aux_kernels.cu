@@ -755,6 +755,66 @@ cudaError_t launch_sum_ordered(const void* parts, int64_t nparts, int64_t n, int
     return cudaGetLastError();
 }
 
+// grad_hidden of an FP32 K-split contraction: the parts' partial sums of
+// S . W added in ascending part order, then the rules of the grad_hidden
+// epilogue: + c_n * W[y_n] where the target lies in this vocab, the softmax
+// part alone (+ 0) for a target in another vocab shard, exact +0 for a dead
+// row (invalid target or zero upstream gradient).  Four values per thread
+// (D % 8 == 0 and every row 16-byte aligned), grid-stride over the rows.
+__global__ void __launch_bounds__(256) dh_finish_kernel(
+    const float* __restrict__ parts, int ks, int64_t part_rows, int64_t rows, int64_t D,
+    const int64_t* __restrict__ targets, const float* __restrict__ grad,
+    const float* __restrict__ tc, int64_t V, int shard, const float* __restrict__ W,
+    float* __restrict__ dh) {
+    const int64_t n4 = rows * (D / 4);
+    const int64_t part_pitch = part_rows * D;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n4;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t r = i / (D / 4);
+        const int64_t d = (i - r * (D / 4)) * 4;
+        const int64_t y = targets[r];
+        const bool here = y >= 0 && y < V;
+        const bool live = (here || (shard && y == kTargetInOtherShard)) && grad[r] != 0.f;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live) {
+            const float* p = parts + r * D + d;
+            a = *reinterpret_cast<const float4*>(p);
+            for (int k = 1; k < ks; ++k) {
+                const float4 b = *reinterpret_cast<const float4*>(p + k * part_pitch);
+                a.x += b.x, a.y += b.y, a.z += b.z, a.w += b.w;
+            }
+            if (here) {
+                const float c = tc[r];
+                const float4 w = *reinterpret_cast<const float4*>(W + y * D + d);
+                a.x = fmaf(c, w.x, a.x) + 0.f;
+                a.y = fmaf(c, w.y, a.y) + 0.f;
+                a.z = fmaf(c, w.z, a.z) + 0.f;
+                a.w = fmaf(c, w.w, a.w) + 0.f;
+            } else {
+                a.x += 0.f, a.y += 0.f, a.z += 0.f, a.w += 0.f;
+            }
+        }
+        *reinterpret_cast<float4*>(dh + r * D + d) = a;
+    }
+}
+
+cudaError_t launch_dh_finish(const float* parts, int ks, int64_t part_rows, int64_t rows,
+                             int64_t D, const int64_t* targets, const float* grad,
+                             const float* tc, int64_t V, int shard, const float* W,
+                             float* dh, int num_sms, cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    if (D % 4 != 0 || reinterpret_cast<uintptr_t>(parts) % 16 ||
+        reinterpret_cast<uintptr_t>(W) % 16 || reinterpret_cast<uintptr_t>(dh) % 16)
+        return cudaErrorInvalidValue;
+    note_launches(1);
+    int64_t blocks = (rows * (D / 4) + 255) / 256;
+    const int64_t cap = int64_t(num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    dh_finish_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        parts, ks, part_rows, rows, D, targets, grad, tc, V, shard, W, dh);
+    return cudaGetLastError();
+}
+
 // hT[d, n] = h[n, d] for 16-bit h [N, D] (row stride D, D % 8 == 0) into
 // hT [D, ldT] (ldT >= N, a multiple of 8): 64 x 64 tiles through shared
 // memory, 16-byte loads and stores.

@@ -168,8 +168,21 @@ int64_t db_groups(int64_t Nc) { return Nc > 32 ? cdiv(Nc, 32) : 1; }
 // Hi / lo split of the softmax part S (ll_options.split_s; 16-bit operands).
 enum SplitMode { kSplitAuto = 0, kSplitAll = 1, kSplitNone = 2 };
 
+// FP32 grad_hidden over a narrow hidden size (D <= 512: one or two column
+// tiles per row block): the K = V contraction is cut into ks parts of at least
+// 16 K blocks, one unit each, whose FP32 partial sums a finishing pass adds in
+// ascending part order.  A few row blocks then spread over many SMs.  ks
+// depends on (D, V) alone, so a row's grad_hidden stays independent of the
+// batch and of the token chunks.
+int64_t dh_k_splits(int dtype, int64_t D, int64_t V) {
+    if (dtype != LL_F32 || D > 512) return 1;
+    const int64_t ks = cdiv(V, 16) / 16;  // 16 K values per TF32 K block
+    return ks < 2 ? 1 : (ks > 16 ? 16 : ks);
+}
+
 struct BwdLayout {
-    int64_t chunks, Nc, ldS, ldZ, n_segs, lo_fld;
+    int64_t chunks, Nc, ldS, ldZ, n_segs, lo_fld, dh_ks;
+    size_t dh_parts;  // FP32 K-split grad_hidden: ks x round_up(Nc, 128) x D partial sums
     size_t S, S_lo, Z, part_m, part_s, zy, tc, keys, offs, ctr, db, total;
     size_t lo_flags, dh_cnt, dh_idx, dw_cnt, dw_idx;  // automatic split
     size_t hT;      // 16-bit: h^T [D, ldT] (grad_weight's K-major B operand)
@@ -244,6 +257,10 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, int dtype, int token_chunk
     L.hT = off;
     L.ldT = round_up(L.Nc, 8);
     if (dtype != LL_F32) off = align_up(off + size_t(D) * size_t(L.ldT) * 2);
+    L.dh_ks = dh_k_splits(dtype, D, V);
+    L.dh_parts = off;
+    if (L.dh_ks > 1) off = align_up(off + size_t(L.dh_ks) * size_t(round_up(L.Nc, kBM)) *
+                                              size_t(D) * 4);
     L.total = off;
     return L;
 }
@@ -332,6 +349,7 @@ cudaError_t forward_gemm(const void* hidden, const void* weight, const void* bia
                          float* part_m, float* part_s, float* zy, int shard, float inv_temp,
                          const DevInfo& dev, cudaStream_t s) {
     GemmShape sh;
+    memset(&sh, 0, sizeof(sh));
     sh.m_blocks = cdiv(N, kBM);
     sh.n_tiles = cdiv(V, kBN);
     sh.tiles_per_unit = kVocabTilesPerSeg;
@@ -550,7 +568,12 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             GemmShape& sh = G.shape[0];
             sh.m_blocks = cdiv(rows, kBM);
             sh.n_tiles = cdiv(V, kBN);
-            sh.tiles_per_unit = kVocabTilesPerSeg;
+            // the recompute's tiles are independent (no running state across a
+            // segment): a small problem takes one tile per unit, so that its few
+            // tiles spread over the SMs
+            const bool few = sh.m_blocks * cdiv(sh.n_tiles, kVocabTilesPerSeg) <
+                             int64_t(2) * dev.num_sms;
+            sh.tiles_per_unit = few ? 1 : kVocabTilesPerSeg;
             sh.n_segs = cdiv(sh.n_tiles, sh.tiles_per_unit);
             sh.k_blocks = cdiv(D, 64);
             sh.unit_order = 2;
@@ -679,6 +702,12 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
                 ea.ld_out = D;
                 ea.out_dtype = dh_dtype;
                 G.out[k] = OutDesc{ea.out, dh_dtype, rows, D, D};
+                if (L.dh_ks > 1) {  // K parts: raw partial sums, finished below
+                    sh.k_splits = L.dh_ks;
+                    ea.dh_part = 1;
+                    G.out[k] = OutDesc{ws + L.dh_parts, LL_F32, L.dh_ks * round_up(rows, kBM), D,
+                                       D};
+                }
                 ++k;
             }
             if (need_dw) {
@@ -716,9 +745,20 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             G.nkinds = k;
             G.counter = k == 2 ? counter : nullptr;
             const char* label = dtype == LL_F32 ? "grad_gemm_f32" : "grad_gemm";
-            Phase ph(label, s);
-            e = launch_gemm(G, dev, s);
+            {
+                Phase ph(label, s);
+                e = launch_gemm(G, dev, s);
+            }
             if (e != cudaSuccess) return cuda_status(e);
+            if (need_dh && L.dh_ks > 1) {
+                Phase ph("dh_finish", s);
+                e = launch_dh_finish(reinterpret_cast<const float*>(ws + L.dh_parts),
+                                     static_cast<int>(L.dh_ks), round_up(rows, kBM), rows, D,
+                                     targets + r0, grad_logp + r0, tc + r0, V, shard,
+                                     static_cast<const float*>(weight),
+                                     static_cast<float*>(grad_hidden) + r0 * D, dev.num_sms, s);
+                if (e != cudaSuccess) return cuda_status(e);
+            }
         }
         // (4) grad_bias: fixed-order column sums of S (+ one-hot part at the end)
         if (need_db) {

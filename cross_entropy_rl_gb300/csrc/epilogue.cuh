@@ -194,7 +194,7 @@ struct RowEpilogue {
                 for (int j = 0; j < 32; ++j) v[j] = coef * v[j];
             }
         } else if constexpr (E == EpiKind::Dh) {
-            if (!rvalid) return;
+            if (!rvalid || ea.dh_part) return;  // a K part: stored as summed
             const int64_t D = ea.Ncols;
             if (onehot) {
                 float w[32];

@@ -83,6 +83,7 @@ struct KParams {
     const int* lo_cnt[2];
     const int64_t* lo_idx[2];
     int64_t lo_ld[2];
+    int64_t part_rows[2];  // K split: rows between two parts' partial sums
 };
 
 // ----------------------------------------------------------- bulk stores
@@ -118,6 +119,7 @@ __device__ __forceinline__ void bulk_wait_all() {
 struct Unit {
     int kind;
     int64_t mb, seg, t0, t1, k_blocks;
+    int64_t k_begin, kpart;  // K split: first K block and part index of the unit
 };
 
 // n_lo: K blocks of the unit's planned second pass (0 without a plan); the
@@ -142,9 +144,19 @@ __device__ __forceinline__ Unit decode_unit(const KParams& P, int64_t u, int n_l
         r.seg = in_g / gm;
         r.mb = g * G + in_g % gm;
     }
+    r.k_begin = 0;
+    r.kpart = 0;
+    int64_t kb_total = sh.k_blocks;
+    if (sh.k_splits > 1) {  // seg = tile * k_splits + part
+        r.kpart = r.seg % sh.k_splits;
+        r.seg /= sh.k_splits;
+        const int64_t per = (kb_total + sh.k_splits - 1) / sh.k_splits;
+        r.k_begin = r.kpart * per;
+        kb_total = min(per, kb_total - r.k_begin);
+    }
     r.t0 = r.seg * sh.tiles_per_unit;
     r.t1 = min(r.t0 + sh.tiles_per_unit, sh.n_tiles);
-    r.k_blocks = sh.k_blocks + n_lo;
+    r.k_blocks = kb_total + n_lo;
     return r;
 }
 
@@ -1293,7 +1305,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                     }
                     if (lane == 0) {
                         uint8_t* st = smem + stage * kRawBytes;
-                        const int32_t k0 = static_cast<int32_t>(kb * kBKf);
+                        const int32_t k0 = static_cast<int32_t>((un.k_begin + kb) * kBKf);
                         const int32_t m0 = static_cast<int32_t>(un.mb * kBM);
                         const int32_t n0 = static_cast<int32_t>(t * kBN);
                         if (NK == 1 || un.kind == 0)
@@ -1434,7 +1446,8 @@ __global__ void __launch_bounds__(kThreadsF, 1)
             const CUtensorMap* tmO = kind == 0 ? &tmO0 : &tmO1;
             const bool reduce = P.reduce[kind] != 0;
             const bool stores = P.out_rows[kind] > 0;
-            const int64_t row0 = un.mb * kBM + q * 32;
+            // a K part of grad_hidden stores its partial sum at rows part * M
+            const int64_t row0 = un.mb * kBM + q * 32 + un.kpart * P.part_rows[kind];
             if (kind == 0)
                 epi0.begin_unit(ea, un.mb * kBM + r_in_tile);
             else
@@ -1765,6 +1778,13 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
                 P.sh[k].k_blocks *= 2;
             }
         }
+        if (P.sh[k].k_splits > 1) {  // FP32 grad_hidden only: units per K part
+            if (G.dtype != LL_F32 || G.kind[k] != EpiKind::Dh || P.sh[k].tiles_per_unit != 1 ||
+                !G.ea[k].dh_part || G.out[k].rows != P.sh[k].k_splits * P.sh[k].m_blocks * kBM)
+                return cudaErrorInvalidValue;
+            P.sh[k].n_segs = P.sh[k].n_tiles * P.sh[k].k_splits;
+            P.part_rows[k] = P.sh[k].m_blocks * kBM;
+        }
         P.n_units[k] = P.sh[k].m_blocks * P.sh[k].n_segs;
         P.out16[k] = G.out[k].dtype != LL_F32;
         P.out_rows[k] = G.out[k].rows;
@@ -1785,6 +1805,7 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
         P.lo_cnt[1] = P.lo_cnt[0];
         P.lo_idx[1] = P.lo_idx[0];
         P.lo_ld[1] = P.lo_ld[0];
+        P.part_rows[1] = P.part_rows[0];
     }
     P.dynamic = G.counter != nullptr;
     P.counter = G.counter;

@@ -108,6 +108,8 @@ struct EpiArgs {
                              //   nullptr = S_lo written in full (split of every entry)
     int64_t lo_flags_ld;     // row pitch of the flags: lo_flags_cols rounded up to 16
     int64_t lo_flags_cols;   // pieces per row group: ceil(V / 64)
+    int dh_part;             // Dh, K split: store the raw partial sum (no target column,
+                             //   no zero rules); dh_finish_kernel completes the rows
 };
 
 // Row pitch of the automatic split's piece flags: ceil(V / 64) rounded up to
@@ -133,6 +135,8 @@ struct GemmShape {
     int unit_order;          // 0: segment-major, 1: m-major, 2: segment-major within
                              //    groups of group_m row blocks (L2 rasterisation)
     int64_t group_m;         // row blocks per group of order 2 (set by launch_gemm)
+    int64_t k_splits;        // FP32 grad_hidden: K cut into this many parts, one unit
+                             //   each, written as FP32 partial sums (0 or 1 = whole K)
 };
 
 // Row blocks per group of the grouped unit order: the units in flight then
@@ -214,6 +218,14 @@ cudaError_t launch_db_finish(const float* partial, int64_t groups, int64_t V, fl
                              int first, int last, const int* offs, const int64_t* keys,
                              const float* tc_all, void* grad_bias, int out_dtype, cudaStream_t s);
 cudaError_t launch_fill_zero(void* p, int64_t n_elems, int dtype, cudaStream_t s);
+// grad_hidden of a K-split contraction: dh[n, :] = the parts P[k][n, :]
+// (k = 0 .. ks - 1, row pitch D, part pitch part_rows rows) added in
+// ascending k, then the Dh epilogue's target column and zero rules (exact +0
+// for dead rows, + c[n] * W[y_n] where the target lies in the vocab).
+cudaError_t launch_dh_finish(const float* parts, int ks, int64_t part_rows, int64_t rows,
+                             int64_t D, const int64_t* targets, const float* grad,
+                             const float* tc, int64_t V, int shard, const float* W,
+                             float* dh, int num_sms, cudaStream_t s);
 // hT [D, ldT] = h^T for 16-bit h [N, D] (D % 8 == 0; ldT >= N, a multiple of 8).
 cudaError_t launch_transpose16(const void* h, int64_t N, int64_t D, void* hT, int64_t ldT,
                                cudaStream_t s);

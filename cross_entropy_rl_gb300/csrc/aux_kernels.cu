@@ -34,6 +34,85 @@ __global__ void lse_merge_kernel(const float* __restrict__ pm, const float* __re
     lse_out[r] = lse;
 }
 
+// The forward epilogue's fold from stored logits (small problems, whose
+// forward GEMM runs one vocab tile per unit and stores Z instead): one warp
+// per (row, 1024-column segment), lane c holding the segment's 32-column
+// chunk c.  The epilogue thread that owns the row folds the chunks in
+// ascending order: columns past V read as -inf; mu = chunk max * log2(e);
+// when mu exceeds the running max m2 the running sum s is rescaled by
+// 2^(m2 - mu) and m2 = mu; then, unless m2 is still -inf, the chunk's 32
+// terms 2^(z * log2(e) - m2) are added one after another in column order and
+// their sum is added to s.  Here m2 after chunk c is the prefix max of mu
+// (exact in any order), so every lane forms its chunk's sum with the same
+// steps at once, and one pass over the lanes replays the rescales and adds
+// of s in chunk order: the same bits as the epilogue.  Chunks wholly past V
+// change nothing there (their terms are +0) and are not visited here.
+__global__ void __launch_bounds__(256) fwd_fold_kernel(
+    const float* __restrict__ Z, int64_t ldZ, int64_t rows, int64_t V,
+    const int64_t* __restrict__ targets, float* __restrict__ part_m,
+    float* __restrict__ part_s, float* __restrict__ zy, int64_t part_ld) {
+    const int lane = threadIdx.x & 31;
+    const int64_t n_segs = (V + kSegCols - 1) / kSegCols;
+    const int64_t w = blockIdx.x * int64_t(blockDim.x / 32) + (threadIdx.x >> 5);
+    if (w >= rows * n_segs) return;
+    const int64_t seg = w / rows, row = w - seg * rows;
+    const int64_t y = targets[row];
+    const int64_t seg0 = seg * kSegCols;
+    const int n_chunks = static_cast<int>(min(int64_t(32), (V - seg0 + 31) / 32));
+    const int64_t col0 = seg0 + 32 * lane;
+    const bool mine = lane < n_chunks;
+    float v[32];
+    const float* z = Z + row * ldZ + col0;
+    if (mine && col0 + 32 <= V) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 f = *reinterpret_cast<const float4*>(z + 4 * q);
+            v[4 * q] = f.x, v[4 * q + 1] = f.y, v[4 * q + 2] = f.z, v[4 * q + 3] = f.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = (mine && col0 + j < V) ? z[j] : -INFINITY;
+    }
+    const int64_t off = y - col0;
+    if (mine && off >= 0 && off < 32) {
+        float t = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j == off) t = v[j];
+        zy[row] = t;
+    }
+    float cmax = v[0];
+#pragma unroll
+    for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, v[j]);
+    const float mu = mine ? cmax * kLog2e : -INFINITY;
+    float m2 = mu;  // prefix max over the lanes: the running max after chunk `lane`
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, m2, o);
+        if (lane >= o) m2 = fmaxf(m2, t);
+    }
+    float acc = 0.f;
+    if (mine && m2 != -INFINITY) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc += ex2(fmaf(v[j], kLog2e, -m2));
+    }
+    // the running sum, chunk by chunk as the epilogue forms it
+    float rm = -INFINITY, s = 0.f;
+    for (int c = 0; c < n_chunks; ++c) {
+        const float mc = __shfl_sync(0xffffffffu, mu, c);
+        const float ac = __shfl_sync(0xffffffffu, acc, c);
+        if (mc > rm) {
+            s = s * ex2(rm - mc);
+            rm = mc;
+        }
+        if (rm != -INFINITY) s += ac;
+    }
+    if (lane == 0) {
+        part_m[seg * part_ld + row] = rm;
+        part_s[seg * part_ld + row] = s;
+    }
+}
+
 // Targets of one vocab shard [v0, v0 + Vs) of a vocab of V entries.
 __global__ void localize_targets_kernel(const int64_t* __restrict__ targets, int64_t N,
                                         int64_t v0, int64_t Vs, int64_t V,
@@ -429,6 +508,17 @@ int64_t pow2_at_least(int64_t n) {
 
 }  // namespace
 
+cudaError_t launch_fwd_fold(const float* Z, int64_t ldZ, int64_t rows, int64_t V,
+                            const int64_t* targets, float* part_m, float* part_s, float* zy,
+                            int64_t part_ld, cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    note_launches(1);
+    const int64_t warps = rows * ((V + kSegCols - 1) / kSegCols);
+    fwd_fold_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, s>>>(
+        Z, ldZ, rows, V, targets, part_m, part_s, zy, part_ld);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_lse_merge(const float* part_m, const float* part_s, const float* zy,
                              int64_t part_ld, int64_t n_segs, const int64_t* targets, int64_t N,
                              int64_t V, float* logp, float* lse, cudaStream_t s) {
@@ -777,12 +867,16 @@ __global__ void __launch_bounds__(256) dh_finish_kernel(
         const bool live = (here || (shard && y == kTargetInOtherShard)) && grad[r] != 0.f;
         float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
         if (live) {
+            // all parts' loads in flight first, then the ascending sum
             const float* p = parts + r * D + d;
-            a = *reinterpret_cast<const float4*>(p);
-            for (int k = 1; k < ks; ++k) {
-                const float4 b = *reinterpret_cast<const float4*>(p + k * part_pitch);
-                a.x += b.x, a.y += b.y, a.z += b.z, a.w += b.w;
-            }
+            float4 b[kMaxDhParts];
+#pragma unroll
+            for (int k = 0; k < kMaxDhParts; ++k)
+                if (k < ks) b[k] = *reinterpret_cast<const float4*>(p + k * part_pitch);
+            a = b[0];
+#pragma unroll
+            for (int k = 1; k < kMaxDhParts; ++k)
+                if (k < ks) a.x += b[k].x, a.y += b[k].y, a.z += b[k].z, a.w += b[k].w;
             if (here) {
                 const float c = tc[r];
                 const float4 w = *reinterpret_cast<const float4*>(W + y * D + d);
@@ -803,7 +897,7 @@ cudaError_t launch_dh_finish(const float* parts, int ks, int64_t part_rows, int6
                              const float* tc, int64_t V, int shard, const float* W,
                              float* dh, int num_sms, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
-    if (D % 4 != 0 || reinterpret_cast<uintptr_t>(parts) % 16 ||
+    if (ks < 1 || ks > kMaxDhParts || D % 4 != 0 || reinterpret_cast<uintptr_t>(parts) % 16 ||
         reinterpret_cast<uintptr_t>(W) % 16 || reinterpret_cast<uintptr_t>(dh) % 16)
         return cudaErrorInvalidValue;
     note_launches(1);

@@ -142,13 +142,26 @@ int cuda_status(cudaError_t e) {
 }
 
 // ---------------------------------------------------------------- layouts
+// A small forward (fewer than 128 units of 128 rows x one 1024-column
+// segment, its FP32 logits within 4 MiB) runs its GEMM one vocab tile per
+// unit, so that its few segments spread over 4x as many SMs, and stores the
+// logits; fwd_fold_kernel then forms the partials with the epilogue's own
+// arithmetic (bitwise the fused epilogue's).  Depends on (N, V) only.
+bool fwd_z_only(int64_t N, int64_t V) {
+    const int64_t units = cdiv(N, kBM) * cdiv(cdiv(V, kBN), kVocabTilesPerSeg);
+    return N > 0 && units < 128 && size_t(N) * size_t(round_up(V, 8)) * 4 <= (size_t(4) << 20);
+}
+
 struct FwdLayout {
-    int64_t n_segs;
-    size_t part_m, part_s, zy, total;
+    int64_t n_segs, ldZ;
+    bool z_only;
+    size_t part_m, part_s, zy, Z, total;
 };
 FwdLayout fwd_layout(int64_t N, int64_t V) {
     FwdLayout L;
     L.n_segs = cdiv(cdiv(V, kBN), kVocabTilesPerSeg);
+    L.ldZ = round_up(V, 8);
+    L.z_only = fwd_z_only(N, V);
     size_t off = 0;
     L.part_m = off;
     off = align_up(off + size_t(L.n_segs) * size_t(N) * 4);
@@ -156,6 +169,8 @@ FwdLayout fwd_layout(int64_t N, int64_t V) {
     off = align_up(off + size_t(L.n_segs) * size_t(N) * 4);
     L.zy = off;
     off = align_up(off + size_t(N) * 4);
+    L.Z = off;
+    if (L.z_only) off = align_up(off + size_t(N) * size_t(L.ldZ) * 4);
     L.total = N == 0 ? 0 : off;
     return L;
 }
@@ -177,7 +192,7 @@ enum SplitMode { kSplitAuto = 0, kSplitAll = 1, kSplitNone = 2 };
 int64_t dh_k_splits(int dtype, int64_t D, int64_t V) {
     if (dtype != LL_F32 || D > 512) return 1;
     const int64_t ks = cdiv(V, 16) / 16;  // 16 K values per TF32 K block
-    return ks < 2 ? 1 : (ks > 16 ? 16 : ks);
+    return ks < 2 ? 1 : (ks > kMaxDhParts ? kMaxDhParts : ks);
 }
 
 struct BwdLayout {
@@ -347,13 +362,16 @@ namespace {
 cudaError_t forward_gemm(const void* hidden, const void* weight, const void* bias,
                          const int64_t* targets, int64_t N, int64_t D, int64_t V, int dtype,
                          float* part_m, float* part_s, float* zy, int shard, float inv_temp,
-                         const DevInfo& dev, cudaStream_t s) {
+                         const DevInfo& dev, cudaStream_t s, float* Z = nullptr,
+                         int64_t ldZ = 0) {
+    // Z: store the logits there, one vocab tile per unit, and leave the
+    // partials to fwd_fold_kernel
     GemmShape sh;
     memset(&sh, 0, sizeof(sh));
     sh.m_blocks = cdiv(N, kBM);
     sh.n_tiles = cdiv(V, kBN);
-    sh.tiles_per_unit = kVocabTilesPerSeg;
-    sh.n_segs = cdiv(sh.n_tiles, kVocabTilesPerSeg);
+    sh.tiles_per_unit = Z ? 1 : kVocabTilesPerSeg;
+    sh.n_segs = cdiv(sh.n_tiles, sh.tiles_per_unit);
     sh.k_blocks = cdiv(D, 64);
     sh.unit_order = 2;
     EpiArgs ea;
@@ -371,6 +389,7 @@ cudaError_t forward_gemm(const void* hidden, const void* weight, const void* bia
     ea.wait_ns = wait_limit_ns();
     ea.shard = shard;
     ea.inv_temp = inv_temp;
+    ea.z_only = Z != nullptr;
     GemmLaunch G;
     memset(&G, 0, sizeof(G));
     G.dtype = dtype;
@@ -379,6 +398,7 @@ cudaError_t forward_gemm(const void* hidden, const void* weight, const void* bia
     G.op[0] = GemmOperands{hidden, D, 0, weight, D, 0, N, V, D, nullptr, nullptr, nullptr, 0};
     G.shape[0] = sh;
     G.ea[0] = ea;
+    if (Z) G.out[0] = OutDesc{Z, LL_F32, N, V, ldZ};
     Phase ph(dtype == LL_F32 ? "fwd_gemm_f32" : "fwd_gemm", s);
     return launch_gemm(G, dev, s);
 }
@@ -429,9 +449,15 @@ int ll_forward_ex(const void* hidden, const void* weight, const void* bias,
     float* part_m = reinterpret_cast<float*>(ws + L.part_m);
     float* part_s = reinterpret_cast<float*>(ws + L.part_s);
     float* zy = reinterpret_cast<float*>(ws + L.zy);
+    float* Z = L.z_only ? reinterpret_cast<float*>(ws + L.Z) : nullptr;
     cudaError_t e = forward_gemm(hidden, weight, bias, targets, N, D, V, dtype, part_m, part_s,
-                                 zy, 0, it, dev, s);
+                                 zy, 0, it, dev, s, Z, L.ldZ);
     if (e != cudaSuccess) return cuda_status(e);
+    if (Z) {
+        Phase ph("fwd_fold", s);
+        e = launch_fwd_fold(Z, L.ldZ, N, V, targets, part_m, part_s, zy, N, s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
     {
         Phase ph("lse_merge", s);
         e = launch_lse_merge(part_m, part_s, zy, N, L.n_segs, targets, N, V, logp, lse, s);
@@ -610,8 +636,11 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             GemmShape& sh = G.shape[0];
             sh.m_blocks = cdiv(rows, kBM);
             sh.n_tiles = cdiv(V, kBN);
-            sh.tiles_per_unit = kVocabTilesPerSeg;
-            sh.n_segs = L.n_segs;
+            // few units: one vocab tile per unit and the fold as its own
+            // kernel (the same bits; the logits are stored either way)
+            const bool fold = sh.m_blocks * L.n_segs < int64_t(2) * dev.num_sms;
+            sh.tiles_per_unit = fold ? 1 : kVocabTilesPerSeg;
+            sh.n_segs = fold ? sh.n_tiles : L.n_segs;
             sh.k_blocks = cdiv(D, 64);
             sh.unit_order = 2;
             EpiArgs& ea = G.ea[0];
@@ -625,6 +654,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             ea.part_ld = L.Nc;
             ea.Z = Z;
             ea.ldZ = L.ldZ;
+            ea.z_only = fold;
             G.out[0] = OutDesc{Z, LL_F32, rows, V, L.ldZ};
             G.zero_counter = counter;
             if (overlap && c == 0) G.max_ctas = dev.num_sms - kSideSms;
@@ -633,6 +663,11 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
                 e = launch_gemm(G, dev, s);
             }
             if (e != cudaSuccess) return cuda_status(e);
+            if (ea.z_only) {
+                Phase ph("fwd_fold", s);
+                e = launch_fwd_fold(Z, L.ldZ, rows, V, targets + r0, part_m, part_s, zy, L.Nc, s);
+                if (e != cudaSuccess) return cuda_status(e);
+            }
             {
                 Phase ph("lse_merge", s);
                 e = launch_lse_merge(part_m, part_s, zy, L.Nc, L.n_segs, targets + r0, rows, V,

@@ -136,6 +136,7 @@ struct RowEpilogue {
                 for (int j = 0; j < 32; ++j) v[j] *= ea.inv_temp;
             }
             if constexpr (E == EpiKind::Fwd) {
+                if (ea.z_only) return;  // logits stored; the fold runs as its own kernel
                 if (col0 + 32 > V) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
@@ -330,7 +331,7 @@ struct RowEpilogue {
 
     __device__ __forceinline__ void end_unit(const EpiArgs& ea, int64_t seg) {
         if constexpr (E == EpiKind::Fwd) {
-            if (!rvalid) return;
+            if (!rvalid || ea.z_only) return;
             ea.part_m[seg * ea.part_ld + row] = m2;
             ea.part_s[seg * ea.part_ld + row] = s;
             if (found) ea.zy[row] = zyv;

@@ -110,6 +110,8 @@ struct EpiArgs {
     int64_t lo_flags_cols;   // pieces per row group: ceil(V / 64)
     int dh_part;             // Dh, K split: store the raw partial sum (no target column,
                              //   no zero rules); dh_finish_kernel completes the rows
+    int z_only;              // Fwd: store the logits (bias, temperature applied) and
+                             //   nothing else; fwd_fold_kernel forms the partials
 };
 
 // Row pitch of the automatic split's piece flags: ceil(V / 64) rounded up to
@@ -201,6 +203,14 @@ cudaError_t launch_gemm(const GemmLaunch& L, const DevInfo& dev, cudaStream_t s)
 // for other valid y in [0, V), -1 for invalid ones; zy (if given) = -inf.
 cudaError_t launch_localize_targets(const int64_t* targets, int64_t N, int64_t v0, int64_t Vs,
                                     int64_t V, int64_t* local, float* zy, cudaStream_t s);
+// The forward's per-(segment, row) partials from stored FP32 logits Z
+// [rows, ldZ] (bias and temperature applied): the forward epilogue's fold,
+// 32 columns at a time in ascending order, with the same arithmetic, so the
+// partials are bitwise those of the fused epilogue; also the target logit
+// zy[n] of rows whose target lies in [0, V).
+cudaError_t launch_fwd_fold(const float* Z, int64_t ldZ, int64_t rows, int64_t V,
+                            const int64_t* targets, float* part_m, float* part_s, float* zy,
+                            int64_t part_ld, cudaStream_t s);
 cudaError_t launch_lse_merge(const float* part_m, const float* part_s, const float* zy,
                              int64_t part_ld, int64_t n_segs, const int64_t* targets, int64_t N,
                              int64_t V, float* logp, float* lse, cudaStream_t s);
@@ -218,6 +228,7 @@ cudaError_t launch_db_finish(const float* partial, int64_t groups, int64_t V, fl
                              int first, int last, const int* offs, const int64_t* keys,
                              const float* tc_all, void* grad_bias, int out_dtype, cudaStream_t s);
 cudaError_t launch_fill_zero(void* p, int64_t n_elems, int dtype, cudaStream_t s);
+constexpr int kMaxDhParts = 16;  // FP32 grad_hidden K split: most parts
 // grad_hidden of a K-split contraction: dh[n, :] = the parts P[k][n, :]
 // (k = 0 .. ks - 1, row pitch D, part pitch part_rows rows) added in
 // ascending k, then the Dh epilogue's target column and zero rules (exact +0

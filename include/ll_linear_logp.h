@@ -148,6 +148,11 @@ size_t ll_workspace_size(int64_t N, int64_t D, int64_t V, int dtype,
  *   logp    [N]    float, device (written)
  *   lse     [N]    float, device (written; pass it to ll_backward)
  * N == 0 launches nothing.  D >= 1, V >= 1.
+ * A small problem (fewer than 128 blocks of 128 rows x 1024 vocab columns,
+ * N * round_up(V, 8) FP32 logits within 4 MiB) keeps its logits in the
+ * workspace and forms the per-segment partials in a second kernel with the
+ * same arithmetic: the same bits as the one-kernel path of larger problems,
+ * with 4x as many SMs busy.
  */
 int ll_forward(const void* hidden, const void* weight, const void* bias,
                const int64_t* targets, int64_t N, int64_t D, int64_t V, int dtype,
@@ -314,7 +319,8 @@ int ll_backward_shard(const float* grad_logp, const void* hidden, const void* we
  * the library until the process exits.  A problem whose forward workspace,
  * ll_workspace_size(N, D, V, dtype, 0, 0) (three regions of
  * ceil(V / 1024) * N, ceil(V / 1024) * N and N floats, each padded to 256
- * bytes), exceeds that is rejected with LL_ERR_WORKSPACE before anything
+ * bytes, plus at most 4 MiB of logits for a small problem, see ll_forward),
+ * exceeds that is rejected with LL_ERR_WORKSPACE before anything
  * runs: N <= 32262 fits at V = 32768, N <= 7013 at V = 151936.  The first
  * call on a device looks up the array's device address (cudaGetSymbolAddress
  * with the device of `hidden` current) and keeps it for the process; make

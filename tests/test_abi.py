@@ -53,6 +53,14 @@ def test_workspace_size_rules(L):
     fwd = L.ll_workspace_size(N, 2048, V, ll.LL_BF16, 0, 0, 0)
     assert fwd >= (2 * n_segs + 1) * N * 4
     assert L.ll_workspace_size(0, 2048, V, ll.LL_BF16, 0, 0, 0) == 0
+    assert fwd < N * V  # partials only: not the logits
+    # a small forward (few 128-row x 1024-column blocks) also keeps its FP32
+    # logits, N x round_up(V, 8), for the second kernel that folds them
+    small = L.ll_workspace_size(128, 256, 4096, ll.LL_F32, 0, 0, 0)
+    assert 128 * 4096 * 4 <= small <= 128 * 4096 * 4 + 64 * 1024
+    assert L.ll_workspace_size(2, 64, 3001, ll.LL_BF16, 0, 0, 0) >= 2 * 3008 * 4
+    big_v = L.ll_workspace_size(128, 256, 300000, ll.LL_F32, 0, 0, 0)  # logits > 4 MiB
+    assert big_v < 128 * 300000 * 4
     # backward, one chunk: [N, round_up(V, 8)] 16-bit softmax part
     bwd1 = L.ll_workspace_size(N, 2048, V, ll.LL_BF16, 1, 1, 0)
     assert bwd1 >= N * V * 2

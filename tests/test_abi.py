@@ -82,6 +82,14 @@ def test_workspace_size_rules(L):
     f = [L.ll_workspace_size(4096, 2048, 32768, ll.LL_F32, 1, 1, m << 1) for m in range(3)]
     assert f[0] == f[1] == f[2]
     assert L.ll_workspace_size(N, 2048, V, ll.LL_F32, 1, 1, 0) >= N * V * 4
+    # FP32 grad_hidden over D <= 512 is cut along K = V into min(16, ceil(V / 16) / 16)
+    # parts whose FP32 partial sums take [parts, round_up(N, 128), D] of the workspace
+    narrow = L.ll_workspace_size(128, 512, 4096, ll.LL_F32, 1, 1, 0)
+    wide = L.ll_workspace_size(128, 520, 4096, ll.LL_F32, 1, 1, 0)
+    assert 16 * 128 * 512 * 4 <= narrow - wide <= 16 * 128 * 512 * 4 + 64 * 1024
+    two = L.ll_workspace_size(100, 512, 520, ll.LL_F32, 1, 1, 0)  # ceil(520/16)/16 = 2 parts
+    one = L.ll_workspace_size(100, 512, 496, ll.LL_F32, 1, 1, 0)  # ceil(496/16) = 31: one part
+    assert 2 * 128 * 512 * 4 <= two - one <= 2 * 128 * 512 * 4 + 64 * 1024
     # grad_bias partials only when requested
     assert L.ll_workspace_size(N, 2048, V, ll.LL_BF16, 1, 1, 1) > bwd1
 

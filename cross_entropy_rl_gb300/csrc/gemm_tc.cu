@@ -1050,7 +1050,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // (64-byte swizzle), MN-major operands in 32-wide 128-byte boxes.  Eight
 // converter warps write the hi and lo parts of both into a converted stage,
 // always K-major with 64-byte rows: kind::tf32 takes no MN-major operand, so
-// the converters transpose MN-major tiles on the way.
+// the converters transpose MN-major tiles on the way.  When every operand of
+// a launch is K-major (forward, recompute) the raw stage is already in that
+// layout and serves as hi itself, so the converters write lo alone.  This
+// relies on kind::tf32 ignoring the 13 low mantissa bits of its FP32 inputs:
+// measured on GB300, the unmasked values give bitwise the same results.
 constexpr int kBKf = 16;                       // K values per stage
 constexpr int kAfBytes = kBM * kBKf * 4;       // 8 KB
 constexpr int kBfBytes = kBN * kBKf * 4;       // 16 KB
@@ -1058,6 +1062,17 @@ constexpr int kRawBytes = kAfBytes + kBfBytes; // 24 KB (one raw stage)
 constexpr int kConvBytes = 2 * kRawBytes;      // hi A, hi B, lo A, lo B
 constexpr int kRawStages = 4;
 constexpr int kConvStages = 2;
+// Launches whose operands are all K-major (forward, recompute): the raw
+// stage itself serves as hi and the converters write lo alone, so a
+// converted stage is half as large and the memory goes to a deeper raw ring
+// (TMA lookahead): 6 x 24 KB raw + 2 x 24 KB lo (measured best of 4 + 4,
+// 5 + 3 and 6 + 2).  A raw stage is freed by the MMA commit.
+constexpr int kRawStagesKK = 6;
+constexpr int kLoStagesKK = 2;
+constexpr int kMaxRaw = kRawStagesKK > kRawStages ? kRawStagesKK : kRawStages;
+constexpr int kMaxConv = kLoStagesKK > kConvStages ? kLoStagesKK : kConvStages;
+static_assert(kRawStagesKK * kRawBytes + kLoStagesKK * kRawBytes == kStages * kStageBytes,
+              "tf32 rings (all K-major) fill the 16-bit kernel's stage memory");
 constexpr int kMnBoxF = 32 * kBKf * 4;         // one 32(MN) x 16(K) box, 2 KB
 constexpr int kConvWarps = 8;                  // hi / lo converter warps
 constexpr int kConvThreads = kConvWarps * 32;
@@ -1067,10 +1082,10 @@ static_assert(kRawStages * kRawBytes + kConvStages * kConvBytes == kStages * kSt
               "tf32 rings fill the 16-bit kernel's stage memory");
 
 struct BarsF {
-    uint64_t full[kRawStages];     // TMA landed in the raw stage
-    uint64_t rempty[kRawStages];   // converters done reading the raw stage
-    uint64_t conv[kConvStages];    // hi / lo written
-    uint64_t empty[kConvStages];   // MMAs done with the converted stage
+    uint64_t full[kMaxRaw];        // TMA landed in the raw stage
+    uint64_t rempty[kMaxRaw];      // raw stage free (converters done; all K-major: MMAs done)
+    uint64_t conv[kMaxConv];       // hi / lo (all K-major: lo) written
+    uint64_t empty[kMaxConv];      // MMAs done with the converted stage
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t sfull[kSchedDepth];
@@ -1111,9 +1126,12 @@ __device__ __forceinline__ uint64_t desc_f(uint32_t base, int kk) {
 
 constexpr uint32_t kIdescF = instr_desc(2 /*tf32*/, 0, 0, kBM, kBN);
 
-__device__ __forceinline__ void mma_stage_f(uint32_t d_tmem, uint32_t st, bool first) {
-    const uint32_t a_hi = st, b_hi = st + kAfBytes;
-    const uint32_t a_lo = st + kRawBytes, b_lo = st + kRawBytes + kAfBytes;
+// hi: A at hi, B at hi + 8 KB; lo likewise (a converted stage holds hi then
+// lo; all K-major: hi is the raw stage, lo a stage of its own).
+__device__ __forceinline__ void mma_stage_f(uint32_t d_tmem, uint32_t hi, uint32_t lo,
+                                            bool first) {
+    const uint32_t a_hi = hi, b_hi = hi + kAfBytes;
+    const uint32_t a_lo = lo, b_lo = lo + kAfBytes;
 #pragma unroll
     for (int kk = 0; kk < kBKf / 8; ++kk) {
         tc_mma<1>(d_tmem, desc_f(a_hi, kk), desc_f(b_hi, kk), kIdescF,
@@ -1179,6 +1197,18 @@ __device__ __forceinline__ void convert_operand(const uint8_t* raw, uint8_t* hi,
     }
 }
 
+// All K-major: lo = x - (x with its 13 low mantissa bits cleared) of both
+// operands, at the raw stage's offsets.
+__device__ __forceinline__ void convert_stage_lo(const uint8_t* raw, uint8_t* lo, int ct) {
+#pragma unroll
+    for (int e = ct; e < (kBM + kBN) * 4; e += kConvThreads) {
+        const uint4 x = *reinterpret_cast<const uint4*>(raw + e * 16);
+        uint4 h, l;
+        split_tf32(x, h, l);
+        *reinterpret_cast<uint4*>(lo + e * 16) = l;
+    }
+}
+
 template <bool A_MN, bool B_MN>
 __device__ __forceinline__ void convert_stage(const uint8_t* raw, uint8_t* cv, int ct) {
     convert_operand<A_MN, kBM>(raw, cv, cv + kRawBytes, ct);
@@ -1195,6 +1225,11 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                      const __grid_constant__ CUtensorMap tmO1, const KParams P,
                      const EpiArgs ea0, const EpiArgs ea1) {
     using T = float;
+    // all operands K-major: the raw stage is the hi operand (see kRawStagesKK)
+    constexpr bool KK = !K0::kAmn && !K0::kBmn && (NK == 1 || (!K1::kAmn && !K1::kBmn));
+    constexpr int kR = KK ? kRawStagesKK : kRawStages;  // raw ring
+    constexpr int kC = KK ? kLoStagesKK : kConvStages;  // converted ring
+    constexpr int kCB = KK ? kRawBytes : kConvBytes;    // converted stage bytes
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1208,11 +1243,11 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     volatile int* abort = &bars->abort;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kRawStages; ++s) {
+        for (int s = 0; s < kR; ++s) {
             mbar_init(&bars->full[s], 1);
-            mbar_init(&bars->rempty[s], kConvWarps);
+            mbar_init(&bars->rempty[s], KK ? 1 : kConvWarps);  // MMA commit, or converters
         }
-        for (int s = 0; s < kConvStages; ++s) {
+        for (int s = 0; s < kC; ++s) {
             mbar_init(&bars->conv[s], kConvWarps);
             mbar_init(&bars->empty[s], 1);
         }
@@ -1264,9 +1299,9 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         // ------------------------------------------- scheduler + TMA producer
         int stage = 0, sslot = 0;
         uint32_t phase = 0, sphase = 0;
-        uint32_t issued_phase[kRawStages];
-        bool issued[kRawStages];
-        for (int s = 0; s < kRawStages; ++s) issued[s] = false;
+        uint32_t issued_phase[kR];
+        bool issued[kR];
+        for (int s = 0; s < kR; ++s) issued[s] = false;
         bool ok = true;
         int64_t next_static = blockIdx.x;
         while (ok) {
@@ -1318,7 +1353,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                     __syncwarp();
                     issued[stage] = true;
                     issued_phase[stage] = phase;
-                    if (++stage == kRawStages) {
+                    if (++stage == kR) {
                         stage = 0;
                         phase ^= 1;
                     }
@@ -1328,7 +1363,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         if (!ok) {
             if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
             bars->abort = 1;
-            for (int s = 0; s < kRawStages; ++s)
+            for (int s = 0; s < kR; ++s)
                 if (issued[s]) mbar_wait(&bars->full[s], issued_phase[s], wait_ns, nullptr);
         }
     } else if (warp >= 6) {
@@ -1337,7 +1372,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         int rs = 0, cs = 0, sslot = 0;
         uint32_t rphase = 0, cphase = 0, sphase = 0;
         bool ok = true;
-        uint8_t* conv_base = smem + kRawStages * kRawBytes;
+        uint8_t* conv_base = smem + kR * kRawBytes;
         while (ok) {
             const int u = next_unit(sslot, sphase, ok);
             if (!ok || u < 0) break;
@@ -1351,22 +1386,24 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                     break;
                 }
                 const uint8_t* raw = smem + rs * kRawBytes;
-                uint8_t* cv = conv_base + cs * kConvBytes;
-                if (NK == 1 || un.kind == 0)
+                uint8_t* cv = conv_base + cs * kCB;
+                if constexpr (KK)
+                    convert_stage_lo(raw, cv, ct);
+                else if (NK == 1 || un.kind == 0)
                     convert_stage<K0::kAmn, K0::kBmn>(raw, cv, ct);
                 else
                     convert_stage<K1::kAmn, K1::kBmn>(raw, cv, ct);
                 fence_proxy_async_shared_cta();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&bars->rempty[rs]);
+                    if (!KK) mbar_arrive(&bars->rempty[rs]);  // all K-major: the MMAs free it
                     mbar_arrive(&bars->conv[cs]);
                 }
-                if (++rs == kRawStages) {
+                if (++rs == kR) {
                     rs = 0;
                     rphase ^= 1;
                 }
-                if (++cs == kConvStages) {
+                if (++cs == kC) {
                     cs = 0;
                     cphase ^= 1;
                 }
@@ -1378,10 +1415,11 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        int stage = 0, sslot = 0, buf = 0;
-        uint32_t phase = 0, sphase = 0, bphase = 0;
+        int stage = 0, sslot = 0, buf = 0, rs = 0;
+        uint32_t phase = 0, sphase = 0, bphase = 0, rphase = 0;
         bool ok = true;
-        const uint32_t sbase = smem_u32(smem) + kRawStages * kRawBytes;
+        const uint32_t rbase = smem_u32(smem);
+        const uint32_t sbase = rbase + kR * kRawBytes;
         while (ok) {
             const int u = next_unit(sslot, sphase, ok);
             if (!ok || u < 0) break;
@@ -1395,20 +1433,33 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem + buf * kBN;
                 for (int64_t kb = 0; kb < un.k_blocks; ++kb) {
+                    // all K-major: the raw stage (hi) too, which its converters
+                    // have seen land already
                     if (!__all_sync(0xffffffffu,
-                                    mbar_wait(&bars->conv[stage], phase, wait_ns, abort))) {
+                                    (!KK || mbar_wait(&bars->full[rs], rphase, wait_ns, abort)) &&
+                                        mbar_wait(&bars->conv[stage], phase, wait_ns, abort))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     if (lane == 0) {
-                        mma_stage_f(d_tmem, sbase + stage * kConvBytes, kb == 0);
+                        const uint32_t cvs = sbase + stage * kCB;
+                        if constexpr (KK) {
+                            mma_stage_f(d_tmem, rbase + rs * kRawBytes, cvs, kb == 0);
+                            tc_commit(&bars->rempty[rs]);
+                        } else {
+                            mma_stage_f(d_tmem, cvs, cvs + kRawBytes, kb == 0);
+                        }
                         tc_commit(&bars->empty[stage]);
                     }
                     __syncwarp();
-                    if (++stage == kConvStages) {
+                    if (++stage == kC) {
                         stage = 0;
                         phase ^= 1;
+                    }
+                    if (++rs == kR) {
+                        rs = 0;
+                        rphase ^= 1;
                     }
                 }
                 if (!ok) break;

@@ -230,12 +230,15 @@ class Clocks:
 # source files each timed kernel is built from (a change to any of them
 # invalidates a stored ncu traffic figure for that kernel)
 KERNEL_SOURCES = {
-    "gemm": ["gemm_tc.cu", "epilogue.cuh", "ll_device.cuh", "ll_internal.h", "capi.cu"],
+    "gemm": ["gemm_tc.cu", "gemm_common.cuh", "epilogue.cuh", "ll_device.cuh", "ll_internal.h",
+             "capi.cu"],
+    "gemm_f32": ["gemm_tf32.cu", "gemm_tc.cu", "gemm_common.cuh", "epilogue.cuh", "ll_device.cuh",
+                 "ll_internal.h", "capi.cu"],
     "logits": ["logits_kernels.cu", "ll_device.cuh", "ll_internal.h"],
 }
 PHASE_SOURCES = {"fwd_gemm": "gemm", "recompute_gemm": "gemm", "grad_gemm": "gemm",
-                 "fwd_gemm_f32": "gemm", "recompute_gemm_f32": "gemm",
-                 "grad_gemm_f32": "gemm", "logits_fwd": "logits", "logits_bwd": "logits",
+                 "fwd_gemm_f32": "gemm_f32", "recompute_gemm_f32": "gemm_f32",
+                 "grad_gemm_f32": "gemm_f32", "logits_fwd": "logits", "logits_bwd": "logits",
                  "logits_fused": "logits"}
 
 

@@ -21,9 +21,9 @@ OUT_DIR = os.path.join(PKG, "_lib")
 LIB_NAME = "libll_gb300.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 
-SOURCES = ["capi.cu", "logits_kernels.cu", "gemm_tc.cu",
+SOURCES = ["capi.cu", "logits_kernels.cu", "gemm_tc.cu", "gemm_tf32.cu",
            "aux_kernels.cu", "noalloc.cu"]
-HEADERS = ["ll_device.cuh", "ll_internal.h", "epilogue.cuh"]
+HEADERS = ["ll_device.cuh", "ll_internal.h", "epilogue.cuh", "gemm_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -27,263 +27,10 @@
 // of one tile overlap the MMAs of the next.  Which SM computes a tile never
 // changes any result: every output element is one MMA accumulation over K
 // in a fixed order.
-#include <string.h>
-
-#include <mutex>
-#include <type_traits>
-
-#include "epilogue.cuh"
+#include "gemm_common.cuh"
 
 namespace ll {
 namespace {
-
-constexpr int kBK = 64;  // K elements per stage (128 bytes of 16-bit values)
-constexpr int kStages = 4;
-constexpr int kABytes = kBM * kBK * 2;
-constexpr int kBBytes = kBN * kBK * 2;
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kMnBoxBytes = 64 * kBK * 2;  // one 64(MN) x 64(K) box, 8 KB
-constexpr int kThreads = 192;
-constexpr int kTmemCols = 512;
-constexpr int kSchedDepth = 4;
-constexpr int kOutBufBytes = 32 * 128;  // one warp's 32 rows x 128 bytes
-constexpr int kOutBytes = 4 * 2 * kOutBufBytes;
-constexpr int kSmemBytes = kStages * kStageBytes + kOutBytes + 1024 /*align*/ + 512 /*bars*/;
-
-struct Bars {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
-    uint64_t sfull[kSchedDepth];
-    uint64_t sempty[kSchedDepth];
-    uint64_t drain;
-    int sched[kSchedDepth];
-    int sched_lo[kSchedDepth];  // second-pass K blocks of the unit in sched
-    uint32_t tmem_base;
-    int abort;
-};
-static_assert(sizeof(Bars) <= 512, "barrier block");
-
-// Launch-wide parameters (by value).
-struct KParams {
-    GemmShape sh[2];
-    int64_t n_units[2];  // units of kind 0, then kind 1
-    int dynamic;         // 1: units handed out by an atomic counter
-    int* counter;        // zero before the launch when dynamic
-    int* zero_counter;   // if set, CTA 0 zeroes it (for the next launch)
-    int out16[2];        // output element of the kind is 16-bit
-    int reduce[2];       // TMA reduce-add instead of store
-    int64_t out_rows[2], out_cols[2];
-    int64_t k_split[2];  // 16-bit: K blocks from the first A map; later blocks read the
-                         // second A map (A_lo) at K block kb - k_split (0 = one A)
-    // planned second pass (automatic split): lo_cnt[kind][mb] K blocks of A_lo
-    // after the first pass, the j-th being lo_idx[kind][mb * lo_ld + j] =
-    // (K block << 8 | bits of the written pieces); nullptr = whole second pass
-    const int* lo_cnt[2];
-    const int64_t* lo_idx[2];
-    int64_t lo_ld[2];
-    int64_t part_rows[2];  // K split: rows between two parts' partial sums
-};
-
-// ----------------------------------------------------------- bulk stores
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x,
-                                             int32_t y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(smem_u32(src)), "r"(x), "r"(y)
-        : "memory");
-}
-__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src,
-                                                  int32_t x, int32_t y) {
-    asm volatile(
-        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group"
-        " [%0, {%2, %3}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
-        "r"(smem_u32(src)), "r"(x), "r"(y)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_read_1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-struct Unit {
-    int kind;
-    int64_t mb, seg, t0, t1, k_blocks;
-    int64_t k_begin, kpart;  // K split: first K block and part index of the unit
-};
-
-// n_lo: K blocks of the unit's planned second pass (0 without a plan); the
-// scheduler reads it once from the plan and publishes it with the unit id.
-__device__ __forceinline__ Unit decode_unit(const KParams& P, int64_t u, int n_lo = 0) {
-    Unit r;
-    r.kind = u < P.n_units[0] ? 0 : 1;
-    const GemmShape& sh = P.sh[r.kind];
-    const int64_t v = r.kind ? u - P.n_units[0] : u;
-    if (sh.unit_order == 0) {
-        r.seg = v / sh.m_blocks;
-        r.mb = v % sh.m_blocks;
-    } else if (sh.unit_order == 1) {
-        r.mb = v / sh.n_segs;
-        r.seg = v % sh.n_segs;
-    } else {
-        const int64_t G = sh.group_m;
-        const int64_t per_group = G * sh.n_segs;
-        const int64_t g = v / per_group;
-        const int64_t in_g = v % per_group;
-        const int64_t gm = min(G, sh.m_blocks - g * G);
-        r.seg = in_g / gm;
-        r.mb = g * G + in_g % gm;
-    }
-    r.k_begin = 0;
-    r.kpart = 0;
-    int64_t kb_total = sh.k_blocks;
-    if (sh.k_splits > 1) {  // seg = tile * k_splits + part
-        r.kpart = r.seg % sh.k_splits;
-        r.seg /= sh.k_splits;
-        const int64_t per = (kb_total + sh.k_splits - 1) / sh.k_splits;
-        r.k_begin = r.kpart * per;
-        kb_total = min(per, kb_total - r.k_begin);
-    }
-    r.t0 = r.seg * sh.tiles_per_unit;
-    r.t1 = min(r.t0 + sh.tiles_per_unit, sh.n_tiles);
-    r.k_blocks = kb_total + n_lo;
-    return r;
-}
-
-// The planned second pass's K-block count of unit u (scheduler side).
-__device__ __forceinline__ int unit_lo_count(const KParams& P, int64_t u) {
-    if (u < 0) return 0;
-    const Unit r = decode_unit(P, u);
-    return P.lo_cnt[r.kind] ? P.lo_cnt[r.kind][r.mb] : 0;
-}
-
-// The planned second pass's K block (scaled to elements) and piece bits.
-__device__ __forceinline__ void lo_block(const KParams& P, const Unit& un, int64_t j,
-                                         int32_t* k0, uint32_t* bits) {
-    const int64_t e = P.lo_idx[un.kind][un.mb * P.lo_ld[un.kind] + j];
-    *k0 = static_cast<int32_t>((e >> 8) * kBK);
-    *bits = static_cast<uint32_t>(e & 0xff);
-}
-
-// A_lo of the planned second pass in pieces of 32 rows (K-major A: 4 per
-// 128-row tile) or of 32 K rows (MN-major A: 2 in each 64-wide box): a piece
-// whose bit is set is read from A_lo, any other from rows [-32, 0), outside
-// the tensor, which the copy fills with zeros.  Same bytes and shared-memory
-// layout as the whole-tile load (a 32-row piece is 4 KB, a multiple of the
-// 1 KB swizzle pattern).  `load(dst, x, y)` issues one piece.
-template <bool A_MN, class Load>
-__device__ __forceinline__ void load_a_pieces(uint8_t* sa, int32_t k0, int32_t m0,
-                                              uint32_t bits, Load load) {
-    if constexpr (!A_MN) {
-#pragma unroll
-        for (int i = 0; i < kBM / 32; ++i)
-            load(sa + i * 32 * 128, k0, ((bits >> i) & 1) ? m0 + 32 * i : -32);
-    } else {
-#pragma unroll
-        for (int j = 0; j < kBM / 64; ++j)
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-                load(sa + j * kMnBoxBytes + i * 32 * 128, m0 + 64 * j,
-                     ((bits >> (2 * j + i)) & 1) ? k0 + 32 * i : -32);
-    }
-}
-
-template <typename T, EpiKind E, bool A_MN, bool B_MN>
-struct Kind {
-    using Epi = RowEpilogue<E, T>;
-    static constexpr bool kAmn = A_MN, kBmn = B_MN;
-    static constexpr int kFmt = std::is_same<T, __half>::value   ? 0
-                                : std::is_same<T, float>::value ? 2  // tf32
-                                                                : 1;
-    static constexpr uint32_t kIdesc = instr_desc(kFmt, A_MN, B_MN, kBM, kBN);
-    static constexpr uint32_t kIdescPair = instr_desc(kFmt, A_MN, B_MN, 2 * kBM, kBN);
-};
-
-template <bool A_MN, bool B_MN>
-__device__ __forceinline__ void load_stage(uint8_t* sa, const CUtensorMap* tmA,
-                                           const CUtensorMap* tmB, uint64_t* fb, int32_t k0,
-                                           int32_t m0, int32_t n0) {
-    uint8_t* sb = sa + kABytes;
-    mbar_arrive_expect_tx(fb, kStageBytes);
-    if constexpr (!A_MN) {
-        tma_load_2d(sa, tmA, fb, k0, m0);
-    } else {
-#pragma unroll
-        for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sa + j * kMnBoxBytes, tmA, fb, m0 + 64 * j, k0);
-    }
-    if constexpr (!B_MN) {
-        tma_load_2d(sb, tmB, fb, k0, n0);
-    } else {
-#pragma unroll
-        for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sb + j * kMnBoxBytes, tmB, fb, n0 + 64 * j, k0);
-    }
-}
-
-template <bool A_MN, bool B_MN>
-__device__ __forceinline__ void load_stage_lo(uint8_t* sa, const CUtensorMap* tmL,
-                                              const CUtensorMap* tmB, uint64_t* fb, int32_t k0,
-                                              int32_t m0, int32_t n0, uint32_t bits) {
-    uint8_t* sb = sa + kABytes;
-    mbar_arrive_expect_tx(fb, kStageBytes);
-    load_a_pieces<A_MN>(sa, k0, m0, bits, [&](uint8_t* d, int32_t x, int32_t y) {
-        tma_load_2d(d, tmL, fb, x, y);
-    });
-    if constexpr (!B_MN) {
-        tma_load_2d(sb, tmB, fb, k0, n0);
-    } else {
-#pragma unroll
-        for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sb + j * kMnBoxBytes, tmB, fb, n0 + 64 * j, k0);
-    }
-}
-
-template <bool A_MN, bool B_MN, uint32_t IDESC>
-__device__ __forceinline__ void mma_stage(uint32_t d_tmem, uint32_t sa, bool first) {
-    const uint32_t sb = sa + kABytes;
-#pragma unroll
-    for (int kk = 0; kk < kBK / 16; ++kk) {
-        const uint64_t ad = A_MN ? smem_desc_sw128(sa + kk * 2048, kMnBoxBytes, 1024)
-                                 : smem_desc_sw128(sa + kk * 32, 16, 1024);
-        const uint64_t bd = B_MN ? smem_desc_sw128(sb + kk * 2048, kMnBoxBytes, 1024)
-                                 : smem_desc_sw128(sb + kk * 32, 16, 1024);
-        tc_mma<0>(d_tmem, ad, bd, IDESC, (!first || kk > 0) ? 1u : 0u);
-    }
-}
-
-// Stage 32 values of this thread's row into the warp's swizzled buffer
-// (32 rows x 128 bytes, 16-byte chunk c of row r at chunk c ^ (r & 7), the
-// layout of a 128-byte-swizzled TMA box): fp32 fills the whole row; 16-bit
-// fills half `h` of it.
-template <typename T>
-__device__ __forceinline__ void stage_row(uint8_t* buf, int lane, const float (&v)[32], bool out16,
-                                          int h) {
-    uint8_t* rowp = buf + lane * 128;
-    const int sw = lane & 7;
-    if (!out16) {
-#pragma unroll
-        for (int sl = 0; sl < 8; ++sl)
-            *reinterpret_cast<float4*>(rowp + ((sl ^ sw) << 4)) =
-                make_float4(v[4 * sl], v[4 * sl + 1], v[4 * sl + 2], v[4 * sl + 3]);
-    } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            uint4 u;
-            T* e = reinterpret_cast<T*>(&u);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) e[j] = Elem<T>::from_f(v[8 * k + j]);
-            *reinterpret_cast<uint4*>(rowp + (((4 * h + k) ^ sw) << 4)) = u;
-        }
-    }
-}
 
 template <typename T, class K0, class K1, int NK>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -341,9 +88,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------- scheduler + TMA producer
         int stage = 0, sslot = 0;
         uint32_t phase = 0, sphase = 0;
-        uint32_t issued_phase[kStages];
-        bool issued[kStages];
-        for (int s = 0; s < kStages; ++s) issued[s] = false;
+        // stages with a load issued, and the phase it completes (bit per stage)
+        uint32_t issued = 0, issued_phase = 0;
         bool ok = true;
         int64_t next_static = blockIdx.x;
         while (ok) {
@@ -412,8 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     __syncwarp();
-                    issued[stage] = true;
-                    issued_phase[stage] = phase;
+                    issued |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
@@ -425,7 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
             bars->abort = 1;
             for (int s = 0; s < kStages; ++s)
-                if (issued[s]) mbar_wait(&bars->full[s], issued_phase[s], wait_ns, nullptr);
+                if ((issued >> s) & 1u)
+                    mbar_wait(&bars->full[s], (issued_phase >> s) & 1u, wait_ns, nullptr);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
@@ -1040,543 +787,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc_pair(tmem, kTmemCols);
 }
 
-// ------------------------------------------------------ FP32 (3 x TF32)
-// FP32 operands on the tensor cores: each operand x is split exactly into
-// hi = x with its 13 low mantissa bits cleared (a TF32 value) and
-// lo = x - hi, and every K step runs three kind::tf32 MMAs,
-// hi*hi + hi*lo + lo*hi (the lo*lo term, ~2^-22 of the product, is
-// dropped).  TMA lands 16 K-values of A [128 x 16] and B [256 x 16] in a
-// raw stage as they lie in memory: K-major operands in 64-byte rows
-// (64-byte swizzle), MN-major operands in 32-wide 128-byte boxes.  Eight
-// converter warps write the hi and lo parts of both into a converted stage,
-// always K-major with 64-byte rows: kind::tf32 takes no MN-major operand, so
-// the converters transpose MN-major tiles on the way.  When every operand of
-// a launch is K-major (forward, recompute) the raw stage is already in that
-// layout and serves as hi itself, so the converters write lo alone.  This
-// relies on kind::tf32 ignoring the 13 low mantissa bits of its FP32 inputs:
-// measured on GB300, the unmasked values give bitwise the same results.
-constexpr int kBKf = 16;                       // K values per stage
-constexpr int kAfBytes = kBM * kBKf * 4;       // 8 KB
-constexpr int kBfBytes = kBN * kBKf * 4;       // 16 KB
-constexpr int kRawBytes = kAfBytes + kBfBytes; // 24 KB (one raw stage)
-constexpr int kConvBytes = 2 * kRawBytes;      // hi A, hi B, lo A, lo B
-constexpr int kRawStages = 4;
-constexpr int kConvStages = 2;
-// Launches whose operands are all K-major (forward, recompute): the raw
-// stage itself serves as hi and the converters write lo alone, so a
-// converted stage is half as large and the memory goes to a deeper raw ring
-// (TMA lookahead): 6 x 24 KB raw + 2 x 24 KB lo (measured best of 4 + 4,
-// 5 + 3 and 6 + 2).  A raw stage is freed by the MMA commit.
-constexpr int kRawStagesKK = 6;
-constexpr int kLoStagesKK = 2;
-constexpr int kMaxRaw = kRawStagesKK > kRawStages ? kRawStagesKK : kRawStages;
-constexpr int kMaxConv = kLoStagesKK > kConvStages ? kLoStagesKK : kConvStages;
-static_assert(kRawStagesKK * kRawBytes + kLoStagesKK * kRawBytes == kStages * kStageBytes,
-              "tf32 rings (all K-major) fill the 16-bit kernel's stage memory");
-constexpr int kMnBoxF = 32 * kBKf * 4;         // one 32(MN) x 16(K) box, 2 KB
-constexpr int kConvWarps = 8;                  // hi / lo converter warps
-constexpr int kConvThreads = kConvWarps * 32;
-constexpr int kThreadsF = 192 + kConvThreads;  // producer, MMA, 4 epilogue, converters
-static_assert(kConvThreads % 128 == 0, "converters split whole 128-thread groups");
-static_assert(kRawStages * kRawBytes + kConvStages * kConvBytes == kStages * kStageBytes,
-              "tf32 rings fill the 16-bit kernel's stage memory");
-
-struct BarsF {
-    uint64_t full[kMaxRaw];        // TMA landed in the raw stage
-    uint64_t rempty[kMaxRaw];      // raw stage free (converters done; all K-major: MMAs done)
-    uint64_t conv[kMaxConv];       // hi / lo (all K-major: lo) written
-    uint64_t empty[kMaxConv];      // MMAs done with the converted stage
-    uint64_t tfull[2];
-    uint64_t tempty[2];
-    uint64_t sfull[kSchedDepth];
-    uint64_t sempty[kSchedDepth];
-    uint64_t drain;
-    int sched[kSchedDepth];
-    uint32_t tmem_base;
-    int abort;
-};
-static_assert(sizeof(BarsF) <= 512, "barrier block");
-
-template <bool A_MN, bool B_MN>
-__device__ __forceinline__ void load_stage_f(uint8_t* st, const CUtensorMap* tmA,
-                                             const CUtensorMap* tmB, uint64_t* fb, int32_t k0,
-                                             int32_t m0, int32_t n0) {
-    uint8_t* sa = st;
-    uint8_t* sb = st + kAfBytes;
-    mbar_arrive_expect_tx(fb, kRawBytes);
-    if constexpr (!A_MN) {
-        tma_load_2d(sa, tmA, fb, k0, m0);
-    } else {
-#pragma unroll
-        for (int j = 0; j < kBM / 32; ++j) tma_load_2d(sa + j * kMnBoxF, tmA, fb, m0 + 32 * j, k0);
-    }
-    if constexpr (!B_MN) {
-        tma_load_2d(sb, tmB, fb, k0, n0);
-    } else {
-#pragma unroll
-        for (int j = 0; j < kBN / 32; ++j) tma_load_2d(sb + j * kMnBoxF, tmB, fb, n0 + 32 * j, k0);
-    }
-}
-
-// K-major operand with 64-byte rows: 8-row groups of 512 B, a K step of
-// 8 values is 32 B along the row.
-__device__ __forceinline__ uint64_t desc_f(uint32_t base, int kk) {
-    return smem_desc_sw64(base + kk * 32, 16, 512);
-}
-
-constexpr uint32_t kIdescF = instr_desc(2 /*tf32*/, 0, 0, kBM, kBN);
-
-// hi: A at hi, B at hi + 8 KB; lo likewise (a converted stage holds hi then
-// lo; all K-major: hi is the raw stage, lo a stage of its own).
-__device__ __forceinline__ void mma_stage_f(uint32_t d_tmem, uint32_t hi, uint32_t lo,
-                                            bool first) {
-    const uint32_t a_hi = hi, b_hi = hi + kAfBytes;
-    const uint32_t a_lo = lo, b_lo = lo + kAfBytes;
-#pragma unroll
-    for (int kk = 0; kk < kBKf / 8; ++kk) {
-        tc_mma<1>(d_tmem, desc_f(a_hi, kk), desc_f(b_hi, kk), kIdescF,
-                  (!first || kk > 0) ? 1u : 0u);
-        tc_mma<1>(d_tmem, desc_f(a_hi, kk), desc_f(b_lo, kk), kIdescF, 1u);
-        tc_mma<1>(d_tmem, desc_f(a_lo, kk), desc_f(b_hi, kk), kIdescF, 1u);
-    }
-}
-
-__device__ __forceinline__ void split_tf32(const uint4& x, uint4& hi, uint4& lo) {
-    hi.x = x.x & 0xFFFFE000u;
-    hi.y = x.y & 0xFFFFE000u;
-    hi.z = x.z & 0xFFFFE000u;
-    hi.w = x.w & 0xFFFFE000u;
-    lo.x = __float_as_uint(__uint_as_float(x.x) - __uint_as_float(hi.x));
-    lo.y = __float_as_uint(__uint_as_float(x.y) - __uint_as_float(hi.y));
-    lo.z = __float_as_uint(__uint_as_float(x.z) - __uint_as_float(hi.z));
-    lo.w = __float_as_uint(__uint_as_float(x.w) - __uint_as_float(hi.w));
-}
-
-// One operand of ROWS rows x 16 K-values from its raw stage into hi / lo in
-// K-major 64-byte rows (row r at r * 64, 16-byte chunk c at c ^ ((r >> 1) & 3),
-// the 64-byte swizzle).  ct = converter thread 0..kConvThreads - 1.
-template <bool MN, int ROWS>
-__device__ __forceinline__ void convert_operand(const uint8_t* raw, uint8_t* hi, uint8_t* lo,
-                                                int ct) {
-    if constexpr (!MN) {
-        // already in that layout: split 16-byte vectors in place
-#pragma unroll
-        for (int e = ct; e < ROWS * 4; e += kConvThreads) {
-            const uint4 x = *reinterpret_cast<const uint4*>(raw + e * 16);
-            uint4 h, l;
-            split_tf32(x, h, l);
-            *reinterpret_cast<uint4*>(hi + e * 16) = h;
-            *reinterpret_cast<uint4*>(lo + e * 16) = l;
-        }
-    } else {
-        // box j: K-row k (128 B) holds MN values 32j..32j+31, 16-byte chunk c
-        // (MN values 4c..4c+3) at c ^ (k & 7).  Thread (mn = ct & 31,
-        // q = ct >> 5) gathers K values 4q..4q+3 of one MN index.
-        // (the converter threads split the boxes: thread ct takes boxes
-        // ct / 128, ct / 128 + kConvThreads / 128, ...)
-        const int m = ct & 31, q = (ct >> 5) & 3;
-        const uint32_t src = static_cast<uint32_t>((m & 3) * 4);
-#pragma unroll
-        for (int j = ct >> 7; j < ROWS / 32; j += kConvThreads / 128) {
-            const uint8_t* box = raw + j * kMnBoxF;
-            uint4 x;
-            uint32_t* xv = reinterpret_cast<uint32_t*>(&x);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int k = 4 * q + i;
-                xv[i] = *reinterpret_cast<const uint32_t*>(box + k * 128 +
-                                                           (((m >> 2) ^ (k & 7)) * 16) + src);
-            }
-            uint4 h, l;
-            split_tf32(x, h, l);
-            const int r = j * 32 + m;
-            const int off = r * 64 + ((q ^ ((r >> 1) & 3)) * 16);
-            *reinterpret_cast<uint4*>(hi + off) = h;
-            *reinterpret_cast<uint4*>(lo + off) = l;
-        }
-    }
-}
-
-// All K-major: lo = x - (x with its 13 low mantissa bits cleared) of both
-// operands, at the raw stage's offsets.
-__device__ __forceinline__ void convert_stage_lo(const uint8_t* raw, uint8_t* lo, int ct) {
-#pragma unroll
-    for (int e = ct; e < (kBM + kBN) * 4; e += kConvThreads) {
-        const uint4 x = *reinterpret_cast<const uint4*>(raw + e * 16);
-        uint4 h, l;
-        split_tf32(x, h, l);
-        *reinterpret_cast<uint4*>(lo + e * 16) = l;
-    }
-}
-
-template <bool A_MN, bool B_MN>
-__device__ __forceinline__ void convert_stage(const uint8_t* raw, uint8_t* cv, int ct) {
-    convert_operand<A_MN, kBM>(raw, cv, cv + kRawBytes, ct);
-    convert_operand<B_MN, kBN>(raw + kAfBytes, cv + kAfBytes, cv + kRawBytes + kAfBytes, ct);
-}
-
-template <class K0, class K1, int NK>
-__global__ void __launch_bounds__(kThreadsF, 1)
-    gemm_tf32_kernel(const __grid_constant__ CUtensorMap tmA0,
-                     const __grid_constant__ CUtensorMap tmB0,
-                     const __grid_constant__ CUtensorMap tmO0,
-                     const __grid_constant__ CUtensorMap tmA1,
-                     const __grid_constant__ CUtensorMap tmB1,
-                     const __grid_constant__ CUtensorMap tmO1, const KParams P,
-                     const EpiArgs ea0, const EpiArgs ea1) {
-    using T = float;
-    // all operands K-major: the raw stage is the hi operand (see kRawStagesKK)
-    constexpr bool KK = !K0::kAmn && !K0::kBmn && (NK == 1 || (!K1::kAmn && !K1::kBmn));
-    constexpr int kR = KK ? kRawStagesKK : kRawStages;  // raw ring
-    constexpr int kC = KK ? kLoStagesKK : kConvStages;  // converted ring
-    constexpr int kCB = KK ? kRawBytes : kConvBytes;    // converted stage bytes
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* outbuf = smem + kStages * kStageBytes;
-    BarsF* bars = reinterpret_cast<BarsF*>(outbuf + kOutBytes);
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int64_t total = P.n_units[0] + (NK > 1 ? P.n_units[1] : 0);
-    const uint64_t wait_ns = ea0.wait_ns;
-    int* status = ea0.status;
-    volatile int* abort = &bars->abort;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kR; ++s) {
-            mbar_init(&bars->full[s], 1);
-            mbar_init(&bars->rempty[s], KK ? 1 : kConvWarps);  // MMA commit, or converters
-        }
-        for (int s = 0; s < kC; ++s) {
-            mbar_init(&bars->conv[s], kConvWarps);
-            mbar_init(&bars->empty[s], 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&bars->tfull[b], 1);
-            mbar_init(&bars->tempty[b], 4);
-        }
-        for (int s = 0; s < kSchedDepth; ++s) {
-            mbar_init(&bars->sfull[s], 1);
-            mbar_init(&bars->sempty[s], 5 + kConvWarps);  // MMA + 4 epilogue + converters
-        }
-        mbar_init(&bars->drain, 1);
-        bars->abort = 0;
-        fence_mbar_init();
-        tma_prefetch_desc(&tmA0);
-        tma_prefetch_desc(&tmB0);
-        if (NK > 1) {
-            tma_prefetch_desc(&tmA1);
-            tma_prefetch_desc(&tmB1);
-        }
-        if (P.zero_counter && blockIdx.x == 0) *P.zero_counter = 0;
-    }
-    if (warp == 1) {
-        tmem_alloc(&bars->tmem_base, kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = bars->tmem_base;
-
-    // every role but the producer takes the unit sequence from the ring
-    auto next_unit = [&](int& sslot, uint32_t& sphase, bool& ok) -> int {
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->sfull[sslot], sphase, wait_ns, abort))) {
-            ok = false;
-            return -1;
-        }
-        const int u = *reinterpret_cast<volatile int*>(&bars->sched[sslot]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->sempty[sslot]);
-        if (++sslot == kSchedDepth) {
-            sslot = 0;
-            sphase ^= 1;
-        }
-        return u;
-    };
-
-    if (warp == 0) {
-        // ------------------------------------------- scheduler + TMA producer
-        int stage = 0, sslot = 0;
-        uint32_t phase = 0, sphase = 0;
-        uint32_t issued_phase[kR];
-        bool issued[kR];
-        for (int s = 0; s < kR; ++s) issued[s] = false;
-        bool ok = true;
-        int64_t next_static = blockIdx.x;
-        while (ok) {
-            int64_t u;
-            if (P.dynamic) {
-                int got = 0;
-                if (lane == 0) got = atomicAdd(P.counter, 1);
-                u = __shfl_sync(0xffffffffu, got, 0);
-            } else {
-                u = next_static;
-                next_static += gridDim.x;
-            }
-            if (u >= total) u = -1;
-            if (!__all_sync(0xffffffffu,
-                            mbar_wait(&bars->sempty[sslot], sphase ^ 1, wait_ns, abort))) {
-                ok = false;
-                break;
-            }
-            if (lane == 0) {
-                bars->sched[sslot] = static_cast<int>(u);
-                mbar_arrive(&bars->sfull[sslot]);
-            }
-            __syncwarp();
-            if (++sslot == kSchedDepth) {
-                sslot = 0;
-                sphase ^= 1;
-            }
-            if (u < 0) break;
-            const Unit un = decode_unit(P, u);
-            for (int64_t t = un.t0; t < un.t1 && ok; ++t) {
-                for (int64_t kb = 0; kb < un.k_blocks; ++kb) {
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait(&bars->rempty[stage], phase ^ 1, wait_ns, abort))) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) {
-                        uint8_t* st = smem + stage * kRawBytes;
-                        const int32_t k0 = static_cast<int32_t>((un.k_begin + kb) * kBKf);
-                        const int32_t m0 = static_cast<int32_t>(un.mb * kBM);
-                        const int32_t n0 = static_cast<int32_t>(t * kBN);
-                        if (NK == 1 || un.kind == 0)
-                            load_stage_f<K0::kAmn, K0::kBmn>(st, &tmA0, &tmB0,
-                                                             &bars->full[stage], k0, m0, n0);
-                        else
-                            load_stage_f<K1::kAmn, K1::kBmn>(st, &tmA1, &tmB1,
-                                                             &bars->full[stage], k0, m0, n0);
-                    }
-                    __syncwarp();
-                    issued[stage] = true;
-                    issued_phase[stage] = phase;
-                    if (++stage == kR) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-            }
-        }
-        if (!ok) {
-            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
-            bars->abort = 1;
-            for (int s = 0; s < kR; ++s)
-                if (issued[s]) mbar_wait(&bars->full[s], issued_phase[s], wait_ns, nullptr);
-        }
-    } else if (warp >= 6) {
-        // ------------------------------------------------ hi / lo converters
-        const int ct = threadIdx.x - 6 * 32;  // 0..kConvThreads - 1
-        int rs = 0, cs = 0, sslot = 0;
-        uint32_t rphase = 0, cphase = 0, sphase = 0;
-        bool ok = true;
-        uint8_t* conv_base = smem + kR * kRawBytes;
-        while (ok) {
-            const int u = next_unit(sslot, sphase, ok);
-            if (!ok || u < 0) break;
-            const Unit un = decode_unit(P, u);
-            const int64_t steps = (un.t1 - un.t0) * un.k_blocks;
-            for (int64_t i = 0; i < steps; ++i) {
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(&bars->full[rs], rphase, wait_ns, abort) &&
-                                    mbar_wait(&bars->empty[cs], cphase ^ 1, wait_ns, abort))) {
-                    ok = false;
-                    break;
-                }
-                const uint8_t* raw = smem + rs * kRawBytes;
-                uint8_t* cv = conv_base + cs * kCB;
-                if constexpr (KK)
-                    convert_stage_lo(raw, cv, ct);
-                else if (NK == 1 || un.kind == 0)
-                    convert_stage<K0::kAmn, K0::kBmn>(raw, cv, ct);
-                else
-                    convert_stage<K1::kAmn, K1::kBmn>(raw, cv, ct);
-                fence_proxy_async_shared_cta();
-                __syncwarp();
-                if (lane == 0) {
-                    if (!KK) mbar_arrive(&bars->rempty[rs]);  // all K-major: the MMAs free it
-                    mbar_arrive(&bars->conv[cs]);
-                }
-                if (++rs == kR) {
-                    rs = 0;
-                    rphase ^= 1;
-                }
-                if (++cs == kC) {
-                    cs = 0;
-                    cphase ^= 1;
-                }
-            }
-        }
-        if (!ok) {
-            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
-            bars->abort = 1;
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
-        int stage = 0, sslot = 0, buf = 0, rs = 0;
-        uint32_t phase = 0, sphase = 0, bphase = 0, rphase = 0;
-        bool ok = true;
-        const uint32_t rbase = smem_u32(smem);
-        const uint32_t sbase = rbase + kR * kRawBytes;
-        while (ok) {
-            const int u = next_unit(sslot, sphase, ok);
-            if (!ok || u < 0) break;
-            const Unit un = decode_unit(P, u);
-            for (int64_t t = un.t0; t < un.t1 && ok; ++t) {
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(&bars->tempty[buf], bphase ^ 1, wait_ns, abort))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + buf * kBN;
-                for (int64_t kb = 0; kb < un.k_blocks; ++kb) {
-                    // all K-major: the raw stage (hi) too, which its converters
-                    // have seen land already
-                    if (!__all_sync(0xffffffffu,
-                                    (!KK || mbar_wait(&bars->full[rs], rphase, wait_ns, abort)) &&
-                                        mbar_wait(&bars->conv[stage], phase, wait_ns, abort))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t cvs = sbase + stage * kCB;
-                        if constexpr (KK) {
-                            mma_stage_f(d_tmem, rbase + rs * kRawBytes, cvs, kb == 0);
-                            tc_commit(&bars->rempty[rs]);
-                        } else {
-                            mma_stage_f(d_tmem, cvs, cvs + kRawBytes, kb == 0);
-                        }
-                        tc_commit(&bars->empty[stage]);
-                    }
-                    __syncwarp();
-                    if (++stage == kC) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                    if (++rs == kR) {
-                        rs = 0;
-                        rphase ^= 1;
-                    }
-                }
-                if (!ok) break;
-                if (lane == 0) tc_commit(&bars->tfull[buf]);
-                __syncwarp();
-                if (++buf == 2) {
-                    buf = 0;
-                    bphase ^= 1;
-                }
-            }
-        }
-        if (!ok) {
-            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
-            bars->abort = 1;
-        }
-        if (lane == 0) tc_commit(&bars->drain);
-        __syncwarp();
-        mbar_wait(&bars->drain, 0, wait_ns, nullptr);
-    } else {
-        // ------------------------------------------------------- epilogue
-        const int q = warp & 3;
-        const int r_in_tile = q * 32 + lane;
-        uint8_t* wbuf = outbuf + q * 2 * kOutBufBytes;
-        int sslot = 0, buf = 0, sidx = 0;
-        uint32_t sphase = 0, bphase = 0;
-        bool ok = true;
-        typename K0::Epi epi0;
-        typename K1::Epi epi1;
-        while (ok) {
-            const int u = next_unit(sslot, sphase, ok);
-            if (!ok || u < 0) break;
-            const Unit un = decode_unit(P, u);
-            const int kind = (NK == 1) ? 0 : un.kind;
-            const EpiArgs& ea = kind == 0 ? ea0 : ea1;
-            const CUtensorMap* tmO = kind == 0 ? &tmO0 : &tmO1;
-            const bool reduce = P.reduce[kind] != 0;
-            const bool stores = P.out_rows[kind] > 0;
-            // a K part of grad_hidden stores its partial sum at rows part * M
-            const int64_t row0 = un.mb * kBM + q * 32 + un.kpart * P.part_rows[kind];
-            if (kind == 0)
-                epi0.begin_unit(ea, un.mb * kBM + r_in_tile);
-            else
-                epi1.begin_unit(ea, un.mb * kBM + r_in_tile);
-            for (int64_t t = un.t0; t < un.t1; ++t) {
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait(&bars->tfull[buf], bphase, wait_ns, abort))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t taddr = tmem + buf * kBN + (static_cast<uint32_t>(q * 32) << 16);
-#pragma unroll 1
-                for (int c = 0; c < kBN / 32; ++c) {
-                    uint32_t r[32];
-                    __syncwarp();
-                    tmem_ld32(taddr + c * 32, r);
-                    tmem_ld_wait(r);
-                    float v[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    const int64_t col0 = t * kBN + c * 32;
-                    if (kind == 0)
-                        epi0.chunk(ea, v, col0);
-                    else
-                        epi1.chunk(ea, v, col0);
-                    if (!stores) continue;
-                    // a box past the output is neither staged nor stored (each
-                    // staging buffer holds exactly one store in flight)
-                    const bool put = row0 < P.out_rows[kind] && col0 < P.out_cols[kind];
-                    uint8_t* sb = wbuf + (sidx & 1) * kOutBufBytes;
-                    if (put) {
-                        if (lane == 0) bulk_wait_read_1();
-                        __syncwarp();
-                        stage_row<T>(sb, lane, v, false, 0);
-                    }
-                    if (kind == 0) epi0.db_partials(ea, v, col0);
-                    if (!put) continue;
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (reduce)
-                            tma_reduce_add_2d(tmO, sb, static_cast<int32_t>(col0),
-                                              static_cast<int32_t>(row0));
-                        else
-                            tma_store_2d(tmO, sb, static_cast<int32_t>(col0),
-                                         static_cast<int32_t>(row0));
-                        bulk_commit();
-                    }
-                    ++sidx;
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->tempty[buf]);
-                if (++buf == 2) {
-                    buf = 0;
-                    bphase ^= 1;
-                }
-            }
-            if (!ok) break;
-            if (kind == 0)
-                epi0.end_unit(ea, un.seg);
-            else
-                epi1.end_unit(ea, un.seg);
-        }
-        if (lane == 0) bulk_wait_all();
-        if (!ok) {
-            if (lane == 0) set_status(status, LL_ERR_DEVICE_TIMEOUT);
-            bars->abort = 1;
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
-}
-
 // ---------------------------------------------------------------- host side
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1720,26 +930,6 @@ cudaError_t dispatch(const GemmLaunch& L, const CUtensorMap* m, const KParams& P
 // 16-bit operands on CTA pairs (gemm_pair_kernel) for problems of >= 256 rows.
 constexpr bool kUsePairs = true;
 
-template <class K0, class K1, int NK>
-cudaError_t launch_f(const CUtensorMap* m, const KParams& P, const EpiArgs& ea0,
-                     const EpiArgs& ea1, const DevInfo& dev, int max_ctas, cudaStream_t s) {
-    auto kern = gemm_tf32_kernel<K0, K1, NK>;
-    static int configured[64] = {0};
-    if (dev.device < 64 && !configured[dev.device]) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        configured[dev.device] = 1;
-    }
-    const int64_t units = P.n_units[0] + (NK > 1 ? P.n_units[1] : 0);
-    const int cap = (max_ctas > 0 && max_ctas < dev.num_sms) ? max_ctas : dev.num_sms;
-    int grid = static_cast<int>(units < cap ? units : cap);
-    if (grid < 1) grid = 1;
-    note_launches(1);
-    kern<<<grid, kThreadsF, kSmemBytes, s>>>(m[0], m[1], m[2], m[3], m[4], m[5], P, ea0, ea1);
-    return cudaGetLastError();
-}
-
 // FP32 operand maps: K-major [rows, K] box 16(K) x rows, 64-byte swizzle;
 // MN-major [K, MN] box 32 x 16, 128-byte swizzle.
 bool operand_maps_f32(const GemmOperands& g, CUtensorMap* ma, CUtensorMap* mb) {
@@ -1750,26 +940,6 @@ bool operand_maps_f32(const GemmOperands& g, CUtensorMap* ma, CUtensorMap* mb) {
                             : make_map(mb, g.B, LL_F32, g.K, g.N, g.ldb, kBKf, kBN,
                                        CU_TENSOR_MAP_SWIZZLE_64B);
     return oka && okb;
-}
-
-cudaError_t dispatch_f32(const GemmLaunch& L, const CUtensorMap* m, const KParams& P,
-                         const DevInfo& dev, cudaStream_t s) {
-    using Fwd = Kind<float, EpiKind::Fwd, false, false>;
-    using Rec = Kind<float, EpiKind::Recomp, false, false>;
-    using Dh = Kind<float, EpiKind::Dh, false, true>;
-    using Dw = Kind<float, EpiKind::Dw, true, true>;
-    const int mc = L.max_ctas;
-    if (L.nkinds == 1) {
-        switch (L.kind[0]) {
-            case EpiKind::Fwd: return launch_f<Fwd, Fwd, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
-            case EpiKind::Recomp: return launch_f<Rec, Rec, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
-            case EpiKind::Dh: return launch_f<Dh, Dh, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
-            case EpiKind::Dw: return launch_f<Dw, Dw, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
-        }
-    } else if (L.kind[0] == EpiKind::Dh && L.kind[1] == EpiKind::Dw) {
-        return launch_f<Dh, Dw, 2>(m, P, L.ea[0], L.ea[1], dev, mc, s);
-    }
-    return cudaErrorInvalidValue;
 }
 
 }  // namespace

@@ -946,6 +946,40 @@ cudaError_t launch_transpose16(const void* h, int64_t N, int64_t D, void* hT, in
     return cudaGetLastError();
 }
 
+// dst[c, r] = src[r, c] for FP32 src [R, C] (row stride lds, a multiple of 4
+// with lds >= round_up(C, 4)) into dst [C, ldd] (ldd a multiple of 4, >=
+// round_up(R, 4)): 32 x 32 tiles through shared memory, 16-byte loads and
+// stores.  A row's last vector may read src padding past C and write dst
+// padding past R; neither is read as data.
+__global__ void __launch_bounds__(256) transpose32_kernel(const float* __restrict__ src,
+                                                          int64_t R, int64_t C, int64_t lds,
+                                                          float* __restrict__ dst, int64_t ldd) {
+    __shared__ float tile[32][32 + 1];
+    const int64_t r0 = blockIdx.x * int64_t(32), c0 = blockIdx.y * int64_t(32);
+    const int q = (threadIdx.x & 7) * 4, t = threadIdx.x >> 3;  // t: 0..31
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r0 + t < R && c0 + q < C)
+        v = *reinterpret_cast<const float4*>(src + (r0 + t) * lds + c0 + q);
+    tile[t][q] = v.x, tile[t][q + 1] = v.y, tile[t][q + 2] = v.z, tile[t][q + 3] = v.w;
+    __syncthreads();
+    if (c0 + t < C && r0 + q < R) {
+        const float4 w = make_float4(tile[q][t], tile[q + 1][t], tile[q + 2][t], tile[q + 3][t]);
+        *reinterpret_cast<float4*>(dst + (c0 + t) * ldd + r0 + q) = w;
+    }
+}
+
+cudaError_t launch_transpose32(const float* src, int64_t R, int64_t C, int64_t lds, float* dst,
+                               int64_t ldd, cudaStream_t s) {
+    if (R <= 0 || C <= 0) return cudaSuccess;
+    if (lds % 4 || ldd % 4 || lds < ((C + 3) / 4) * 4 || ldd < ((R + 3) / 4) * 4 ||
+        reinterpret_cast<uintptr_t>(src) % 16 || reinterpret_cast<uintptr_t>(dst) % 16)
+        return cudaErrorInvalidValue;
+    note_launches(1);
+    const dim3 grid(static_cast<unsigned>((R + 31) / 32), static_cast<unsigned>((C + 31) / 32));
+    transpose32_kernel<<<grid, 256, 0, s>>>(src, R, C, lds, dst, ldd);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_fill_zero(void* p, int64_t n_elems, int dtype, cudaStream_t s) {
     if (n_elems <= 0) return cudaSuccess;
     note_launches(1);

@@ -195,13 +195,27 @@ int64_t dh_k_splits(int dtype, int64_t D, int64_t V) {
     return ks < 2 ? 1 : (ks > kMaxDhParts ? kMaxDhParts : ks);
 }
 
+// FP32 gradient operands transposed to K-major (W^T once per call, the
+// chunk's S^T and h^T), so that the tf32 kernel's converters only split and
+// never transpose: the same bits as the MN-major operands, faster from a few
+// GFLOP of gradient work on; below that the transposes cost more than they
+// save (128 x 256 x 4096: 2 launches, +16 us against -2 us).
+bool f32_kmajor_grads(int dtype, int64_t N, int64_t D, int64_t V) {
+    return dtype == LL_F32 && double(N) * double(D) * double(V) >= 4294967296.0;
+}
+
 struct BwdLayout {
     int64_t chunks, Nc, ldS, ldZ, n_segs, lo_fld, dh_ks;
     size_t dh_parts;  // FP32 K-split grad_hidden: ks x round_up(Nc, 128) x D partial sums
     size_t S, S_lo, Z, part_m, part_s, zy, tc, keys, offs, ctr, db, total;
     size_t lo_flags, dh_cnt, dh_idx, dw_cnt, dw_idx;  // automatic split
-    size_t hT;      // 16-bit: h^T [D, ldT] (grad_weight's K-major B operand)
+    size_t hT;      // h^T [D, ldT] in the operand dtype (grad_weight's K-major B operand)
     int64_t ldT;
+    // FP32: the other operands transposed to K-major for the tf32 kernel,
+    // whose converters then only split (no transposes): W^T [D, ldWT] (once
+    // per call) for grad_hidden, the chunk's S^T [V, ldST] for grad_weight
+    size_t WT, ST;
+    int64_t ldWT, ldST;
 };
 // fused = 1: the single fwd+bwd call, which also keeps the chunk's FP32
 // logits Z and the forward partials.
@@ -271,7 +285,15 @@ BwdLayout bwd_layout(int64_t N, int64_t D, int64_t V, int dtype, int token_chunk
     if (need_db) off = align_up(off + size_t(db_groups(L.Nc) + 1) * size_t(V) * 4);
     L.hT = off;
     L.ldT = round_up(L.Nc, 8);
-    if (dtype != LL_F32) off = align_up(off + size_t(D) * size_t(L.ldT) * 2);
+    off = align_up(off + size_t(D) * size_t(L.ldT) * esize(dtype));
+    L.WT = L.ST = off;
+    L.ldWT = round_up(V, 4);
+    L.ldST = round_up(L.Nc, 4);
+    if (f32_kmajor_grads(dtype, N, D, V)) {
+        off = align_up(off + size_t(D) * size_t(L.ldWT) * 4);
+        L.ST = off;
+        off = align_up(off + size_t(V) * size_t(L.ldST) * 4);
+    }
     L.dh_ks = dh_k_splits(dtype, D, V);
     L.dh_parts = off;
     if (L.dh_ks > 1) off = align_up(off + size_t(L.dh_ks) * size_t(round_up(L.Nc, kBM)) *
@@ -567,7 +589,15 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
 
     // grad_weight's B operand, the chunk's h^T: K-major (tokens contiguous)
     // for the tensor cores, so that only its A operand (S) is read MN-major
-    void* hT = dtype != LL_F32 ? static_cast<void*>(ws + L.hT) : nullptr;
+    void* hT = ws + L.hT;
+    float* WT = reinterpret_cast<float*>(ws + L.WT);
+    float* ST = reinterpret_cast<float*>(ws + L.ST);
+    const bool f32_t = f32_kmajor_grads(dtype, N, D, V);
+    if (f32_t && need_dh) {  // W^T: grad_hidden's B operand, K-major
+        Phase ph("transpose_w", s);
+        e = launch_transpose32(static_cast<const float*>(weight), V, D, D, WT, L.ldWT, s);
+        if (e != cudaSuccess) return cuda_status(e);
+    }
 
     EpiArgs base;
     memset(&base, 0, sizeof(base));
@@ -703,9 +733,17 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             e = launch_lo_plan(lo_flags, rows, V, blk, blk, dh_cnt, dh_idx, dw_cnt, dw_idx, s);
             if (e != cudaSuccess) return cuda_status(e);
         }
-        if (need_dw && hT) {
+        if (need_dw && (f32_t || dtype != LL_F32)) {
             Phase ph("transpose_h", s);
-            e = launch_transpose16(h_c, rows, D, hT, L.ldT, s);
+            if (f32_t) {  // h^T and S^T: grad_weight's operands, K-major
+                e = launch_transpose32(reinterpret_cast<const float*>(h_c), rows, D, D,
+                                       static_cast<float*>(hT), L.ldT, s);
+                if (e == cudaSuccess)
+                    e = launch_transpose32(static_cast<const float*>(S), rows, V, L.ldS, ST,
+                                           L.ldST, s);
+            } else {
+                e = launch_transpose16(h_c, rows, D, hT, L.ldT, s);
+            }
             if (e != cudaSuccess) return cuda_status(e);
         }
         if (need_dh || need_dw) {
@@ -715,8 +753,15 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             int k = 0;
             if (need_dh) {
                 G.kind[k] = EpiKind::Dh;
-                G.op[k] = GemmOperands{S, L.ldS, 0, weight, D, 1, rows, D, V, S_lo,
-                                       lo_auto ? dh_cnt : nullptr, dh_idx, L.lo_fld};
+                if (f32_t)  // K-major B: W^T [D, V]
+                    G.op[k] = GemmOperands{S, L.ldS, 0, WT, L.ldWT, 0, rows, D, V, nullptr,
+                                           nullptr, nullptr, 0};
+                else if (dtype == LL_F32)  // MN-major B: W itself
+                    G.op[k] = GemmOperands{S, L.ldS, 0, weight, D, 1, rows, D, V, nullptr,
+                                           nullptr, nullptr, 0};
+                else
+                    G.op[k] = GemmOperands{S, L.ldS, 0, weight, D, 1, rows, D, V, S_lo,
+                                           lo_auto ? dh_cnt : nullptr, dh_idx, L.lo_fld};
                 GemmShape& sh = G.shape[k];
                 sh.m_blocks = cdiv(rows, kBM);
                 sh.n_tiles = cdiv(D, kBN);
@@ -747,11 +792,14 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             }
             if (need_dw) {
                 G.kind[k] = EpiKind::Dw;
-                if (hT)  // K-major B: the chunk's h^T [D, rows]
+                if (f32_t)  // K-major A and B: S^T [V, rows], h^T [D, rows]
+                    G.op[k] = GemmOperands{ST, L.ldST, 0, hT, L.ldT, 0, V, D, rows, nullptr,
+                                           nullptr, nullptr, 0};
+                else if (dtype == LL_F32)  // MN-major A and B: S and the chunk's h
+                    G.op[k] = GemmOperands{S, L.ldS, 1, h_c, D, 1, V, D, rows, nullptr,
+                                           nullptr, nullptr, 0};
+                else  // K-major B: the chunk's h^T [D, rows]; A = S read MN-major
                     G.op[k] = GemmOperands{S, L.ldS, 1, hT, L.ldT, 0, V, D, rows, S_lo,
-                                           lo_auto ? dw_cnt : nullptr, dw_idx, cdiv(rows, 64)};
-                else
-                    G.op[k] = GemmOperands{S, L.ldS, 1, h_c, D, 1, V, D, rows, S_lo,
                                            lo_auto ? dw_cnt : nullptr, dw_idx, cdiv(rows, 64)};
                 GemmShape& sh = G.shape[k];
                 sh.m_blocks = cdiv(V, kBM);

@@ -565,18 +565,39 @@ cudaError_t dispatch_f32(const GemmLaunch& L, const CUtensorMap* m, const KParam
                          const DevInfo& dev, cudaStream_t s) {
     using Fwd = Kind<float, EpiKind::Fwd, false, false>;
     using Rec = Kind<float, EpiKind::Recomp, false, false>;
-    using Dh = Kind<float, EpiKind::Dh, false, true>;
-    using Dw = Kind<float, EpiKind::Dw, true, true>;
+    // gradient operands as the backward passes them: K-major copies (W^T,
+    // S^T, h^T: the converters only split), or W, S and h themselves (the
+    // converters transpose)
+    using DhT = Kind<float, EpiKind::Dh, false, false>;
+    using DwT = Kind<float, EpiKind::Dw, false, false>;
+    using DhM = Kind<float, EpiKind::Dh, false, true>;
+    using DwM = Kind<float, EpiKind::Dw, true, true>;
     const int mc = L.max_ctas;
+    auto is = [&](int k, int a_mn, int b_mn) {
+        return L.op[k].a_mn == a_mn && L.op[k].b_mn == b_mn;
+    };
     if (L.nkinds == 1) {
         switch (L.kind[0]) {
-            case EpiKind::Fwd: return launch_f<Fwd, Fwd, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
-            case EpiKind::Recomp: return launch_f<Rec, Rec, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
-            case EpiKind::Dh: return launch_f<Dh, Dh, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
-            case EpiKind::Dw: return launch_f<Dw, Dw, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
+            case EpiKind::Fwd:
+                if (!is(0, 0, 0)) break;
+                return launch_f<Fwd, Fwd, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
+            case EpiKind::Recomp:
+                if (!is(0, 0, 0)) break;
+                return launch_f<Rec, Rec, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
+            case EpiKind::Dh:
+                if (is(0, 0, 0)) return launch_f<DhT, DhT, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
+                if (is(0, 0, 1)) return launch_f<DhM, DhM, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
+                break;
+            case EpiKind::Dw:
+                if (is(0, 0, 0)) return launch_f<DwT, DwT, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
+                if (is(0, 1, 1)) return launch_f<DwM, DwM, 1>(m, P, L.ea[0], L.ea[0], dev, mc, s);
+                break;
         }
     } else if (L.kind[0] == EpiKind::Dh && L.kind[1] == EpiKind::Dw) {
-        return launch_f<Dh, Dw, 2>(m, P, L.ea[0], L.ea[1], dev, mc, s);
+        if (is(0, 0, 0) && is(1, 0, 0))
+            return launch_f<DhT, DwT, 2>(m, P, L.ea[0], L.ea[1], dev, mc, s);
+        if (is(0, 0, 1) && is(1, 1, 1))
+            return launch_f<DhM, DwM, 2>(m, P, L.ea[0], L.ea[1], dev, mc, s);
     }
     return cudaErrorInvalidValue;
 }

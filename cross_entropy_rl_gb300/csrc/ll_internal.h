@@ -237,6 +237,10 @@ cudaError_t launch_dh_finish(const float* parts, int ks, int64_t part_rows, int6
                              int64_t D, const int64_t* targets, const float* grad,
                              const float* tc, int64_t V, int shard, const float* W,
                              float* dh, int num_sms, cudaStream_t s);
+// dst [C, ldd] = src^T for FP32 src [R, C] with row stride lds (both strides
+// multiples of 4 floats, lds >= round_up(C, 4), ldd >= round_up(R, 4)).
+cudaError_t launch_transpose32(const float* src, int64_t R, int64_t C, int64_t lds, float* dst,
+                               int64_t ldd, cudaStream_t s);
 // hT [D, ldT] = h^T for 16-bit h [N, D] (D % 8 == 0; ldT >= N, a multiple of 8).
 cudaError_t launch_transpose16(const void* h, int64_t N, int64_t D, void* hT, int64_t ldT,
                                cudaStream_t s);

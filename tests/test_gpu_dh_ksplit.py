@@ -1,11 +1,14 @@
-"""FP32 grad_hidden over a narrow hidden size (D <= 512): the K = V
+"""The FP32 gradient launch.  First, grad_hidden over a narrow hidden size
+(D <= 512): the K = V
 contraction is cut into parts of at least 16 K blocks (up to 16 parts), each
 its own unit of the gradient launch, and a finishing pass adds the parts'
 FP32 partial sums in ascending part order before the target column and the
 zero rules.  The part count depends on (D, V) alone: a row's grad_hidden is
 bitwise independent of the batch it is in, of the token chunks and of the
 grad_weight tiles launched beside it, and it meets the FP32 tolerance against
-the FP64 oracle (including vocab sizes that leave a short last part)."""
+the FP64 oracle (including vocab sizes that leave a short last part).
+Second, the K-major operand copies of large problems give the bits of the
+MN-major operands."""
 import numpy as np
 import pytest
 import torch
@@ -78,3 +81,26 @@ def test_wide_hidden_keeps_one_part(lib):
     ga, gr = TOL["f32"]["grad"]
     check("dh", got["dh"], ref["dh"], ga, gr, out_dtype=got["dh"].dtype)
     assert np.isfinite(ref["dh"]).all()
+
+
+def test_kmajor_gradient_operands_bitwise_the_mn_major_ones(lib):
+    """From 2^32 multiply-adds (N * D * V) on, the FP32 backward passes its
+    gradient launch K-major copies (W^T, S^T, h^T) instead of W, S and h, so
+    the converters need not transpose.  The products and their order are the
+    same: rows of a 1024-row batch (copies) equal the same rows of a 1023-row
+    batch (no copies) bitwise, grad_hidden included."""
+    D, V = 1024, 4096
+    L = lib.load()
+    ws_t = L.ll_workspace_size(1024, D, V, lib.LL_F32, 0, 1, 0)
+    ws_m = L.ll_workspace_size(1023, D, V, lib.LL_F32, 0, 1, 0)
+    assert ws_t - ws_m >= D * V * 4  # W^T (and S^T, h^T) only for the larger batch
+    p = synth.linear_inputs(1024, D, V, dtype="f32", bias=True, seed=83)
+    big = run(lib, p)
+    q = dict(p, h=p["h"][:1023], y=p["y"][:1023], gl=p["gl"][:1023], N=1023)
+    small = run(lib, q)
+    for k in ("logp", "lse", "dh"):
+        assert bits_equal(small[k], big[k][:1023]), k
+    ref = O.linear_forward_backward(p["gl"], p["h"], p["W"], p["b"], p["y"], "f32")
+    ga, gr = TOL["f32"]["grad"]
+    for k in ("dh", "dW", "db"):
+        check(k, big[k], ref[k], ga, gr, out_dtype=big[k].dtype)

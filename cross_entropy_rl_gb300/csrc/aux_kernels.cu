@@ -955,16 +955,21 @@ __global__ void __launch_bounds__(256) transpose32_kernel(const float* __restric
                                                           int64_t R, int64_t C, int64_t lds,
                                                           float* __restrict__ dst, int64_t ldd) {
     __shared__ float tile[32][32 + 1];
-    const int64_t r0 = blockIdx.x * int64_t(32), c0 = blockIdx.y * int64_t(32);
     const int q = (threadIdx.x & 7) * 4, t = threadIdx.x >> 3;  // t: 0..31
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r0 + t < R && c0 + q < C)
-        v = *reinterpret_cast<const float4*>(src + (r0 + t) * lds + c0 + q);
-    tile[t][q] = v.x, tile[t][q + 1] = v.y, tile[t][q + 2] = v.z, tile[t][q + 3] = v.w;
-    __syncthreads();
-    if (c0 + t < C && r0 + q < R) {
-        const float4 w = make_float4(tile[q][t], tile[q + 1][t], tile[q + 2][t], tile[q + 3][t]);
-        *reinterpret_cast<float4*>(dst + (c0 + t) * ldd + r0 + q) = w;
+    const int64_t tr = (R + 31) / 32, n_tiles = tr * ((C + 31) / 32);
+    for (int64_t i = blockIdx.x; i < n_tiles; i += gridDim.x) {  // any R, C
+        const int64_t r0 = (i % tr) * 32, c0 = (i / tr) * 32;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r0 + t < R && c0 + q < C)
+            v = *reinterpret_cast<const float4*>(src + (r0 + t) * lds + c0 + q);
+        __syncthreads();  // the previous tile's reads of `tile` are done
+        tile[t][q] = v.x, tile[t][q + 1] = v.y, tile[t][q + 2] = v.z, tile[t][q + 3] = v.w;
+        __syncthreads();
+        if (c0 + t < C && r0 + q < R) {
+            const float4 w =
+                make_float4(tile[q][t], tile[q + 1][t], tile[q + 2][t], tile[q + 3][t]);
+            *reinterpret_cast<float4*>(dst + (c0 + t) * ldd + r0 + q) = w;
+        }
     }
 }
 
@@ -975,8 +980,10 @@ cudaError_t launch_transpose32(const float* src, int64_t R, int64_t C, int64_t l
         reinterpret_cast<uintptr_t>(src) % 16 || reinterpret_cast<uintptr_t>(dst) % 16)
         return cudaErrorInvalidValue;
     note_launches(1);
-    const dim3 grid(static_cast<unsigned>((R + 31) / 32), static_cast<unsigned>((C + 31) / 32));
-    transpose32_kernel<<<grid, 256, 0, s>>>(src, R, C, lds, dst, ldd);
+    const int64_t n_tiles = ((R + 31) / 32) * ((C + 31) / 32);
+    const int64_t cap = int64_t(1) << 20;  // blocks; more tiles are visited grid-stride
+    transpose32_kernel<<<static_cast<unsigned>(n_tiles < cap ? n_tiles : cap), 256, 0, s>>>(
+        src, R, C, lds, dst, ldd);
     return cudaGetLastError();
 }
 

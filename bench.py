@@ -314,7 +314,10 @@ def run_reference(args, rank):
         wl.update(dtype=args.dtype or "bf16", bias=args.bias)
     p = synth.linear_inputs(**wl, seed=0)
     q = decoded(p)
-    rows = 16
+    # tokens per step: a step also pays a fixed cost (the sample's grad_weight
+    # contribution touches all of [V, D]), so too small a sample understates the
+    # oracle's rate; 128 tokens keep a step near 2 s at the large workload
+    rows = 128
     for i in range(args.warmup):
         oracle.linear_rows(q["gl"], q["h"], q["W"], q["b"], q["y"], "f64",
                            np.arange(rows) % p["N"])

@@ -104,3 +104,20 @@ def test_kmajor_gradient_operands_bitwise_the_mn_major_ones(lib):
     ga, gr = TOL["f32"]["grad"]
     for k in ("dh", "dW", "db"):
         check(k, big[k], ref[k], ga, gr, out_dtype=big[k].dtype)
+
+
+def test_kmajor_gradient_operands_ragged_shapes(lib):
+    """K-major copies with ragged sizes (rows, hidden and vocab not multiples
+    of the 32 x 32 transpose tile, vocab not a multiple of 4, two token
+    chunks): every gradient meets the FP32 tolerance against the oracle."""
+    N, D, V = 1031, 1032, 4099
+    assert N * D * V >= 2 ** 32
+    p = synth.linear_inputs(N, D, V, dtype="f32", bias=True, seed=89)
+    p["y"][[4, 1030]] = [-100, V]
+    got = run(lib, p, token_chunks=2)
+    ref = O.linear_forward_backward(p["gl"], p["h"], p["W"], p["b"], p["y"], "f32")
+    ga, gr = TOL["f32"]["grad"]
+    for k in ("dh", "dW", "db"):
+        check(k, got[k], ref[k], ga, gr, out_dtype=got[k].dtype)
+    for r in (4, 1030):
+        assert_pos_zero(f"dh[{r}]", got["dh"][r])

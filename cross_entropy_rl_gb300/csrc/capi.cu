@@ -608,10 +608,24 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
     base.shard = shard;
     base.inv_temp = inv_temp;
 
+    // grad_bias is finished on the side stream, beside the gradient launch: it
+    // needs the chunk's partials (step 1) and, at the last chunk, the token
+    // sort, which runs earlier on that stream.  The next chunk's step 1
+    // rewrites the partials, so it first waits for this chunk's finishing.
+    cudaEvent_t db_fork = nullptr, db_done = nullptr;
+    bool db_side = need_db && dev.side != nullptr &&
+                   cudaEventCreateWithFlags(&db_fork, cudaEventDisableTiming) == cudaSuccess &&
+                   cudaEventCreateWithFlags(&db_done, cudaEventDisableTiming) == cudaSuccess;
+    if (!db_side) {
+        if (db_fork) cudaEventDestroy(db_fork);
+        if (db_done) cudaEventDestroy(db_done);
+    }
+
     for (int64_t c = 0; c < L.chunks; ++c) {
         const int64_t r0 = c * L.Nc;
         const int64_t rows = (N - r0) < L.Nc ? (N - r0) : L.Nc;
         const char* h_c = static_cast<const char*>(hidden) + size_t(r0) * size_t(D) * es;
+        if (db_side && c > 0) cudaStreamWaitEvent(s, db_done, 0);
 
         // (1) recompute z for the chunk, store S = -grad * p off target and c
         if (!fused) {
@@ -712,6 +726,18 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
                                         s);
             }
             if (e != cudaSuccess) return cuda_status(e);
+        }
+        if (db_side) {  // (4) grad_bias, beside what follows
+            cudaEventRecord(db_fork, s);
+            cudaStreamWaitEvent(dev.side, db_fork, 0);
+            {
+                Phase ph("db_sums", dev.side);
+                e = launch_db_finish(db_part, cdiv(rows, 32), V, db_acc, c == 0,
+                                     c == L.chunks - 1, offs, keys, tc, grad_bias, dw_dtype,
+                                     dev.side);
+            }
+            if (e != cudaSuccess) return cuda_status(e);
+            cudaEventRecord(db_done, dev.side);
         }
         if (overlap && c == L.chunks - 1) {  // the last chunk's epilogues read the sort
             cudaStreamWaitEvent(s, sort_done, 0);
@@ -844,7 +870,7 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
             }
         }
         // (4) grad_bias: fixed-order column sums of S (+ one-hot part at the end)
-        if (need_db) {
+        if (need_db && !db_side) {
             Phase ph("db_sums", s);
             // partials per 32 rows from the recompute epilogue (or, in the
             // single call, from the softmax-part kernel with the same sums)
@@ -856,6 +882,11 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
     if (overlap) {  // nothing read the sort (no chunk needed it): still join it
         cudaStreamWaitEvent(s, sort_done, 0);
         cudaEventDestroy(sort_done);
+    }
+    if (db_side) {  // the call ends when grad_bias is done
+        cudaStreamWaitEvent(s, db_done, 0);
+        cudaEventDestroy(db_fork);
+        cudaEventDestroy(db_done);
     }
     return LL_OK;
 }

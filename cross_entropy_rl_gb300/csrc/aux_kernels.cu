@@ -15,23 +15,36 @@
 namespace ll {
 namespace {
 
+// lse and logp of row r from its per-segment partials, in ascending segment
+// order (one thread; shared by every kernel that merges, so that they give the
+// same bits).
+__device__ __forceinline__ void merge_row(const float* __restrict__ pm,
+                                          const float* __restrict__ ps,
+                                          const float* __restrict__ zy, int64_t ld,
+                                          int64_t n_segs, const int64_t* __restrict__ targets,
+                                          int64_t r, int64_t V, float* __restrict__ logp,
+                                          float* __restrict__ lse_out) {
+    float M = -INFINITY;
+    for (int64_t j = 0; j < n_segs; ++j) M = fmaxf(M, pm[j * ld + r]);
+    float lse = -INFINITY;
+    if (M != -INFINITY) {
+        float S = 0.f;
+        for (int64_t j = 0; j < n_segs; ++j)
+            S = fmaf(ps[j * ld + r], ex2(pm[j * ld + r] - M), S);
+        lse = fmaf(M, kLn2, logf(S));
+    }
+    const int64_t y = targets[r];
+    logp[r] = (y >= 0 && y < V) ? zy[r] - lse : 0.f;
+    lse_out[r] = lse;
+}
+
 __global__ void lse_merge_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
                                  const float* __restrict__ zy, int64_t ld, int64_t n_segs,
                                  const int64_t* __restrict__ targets, int64_t N, int64_t V,
                                  float* __restrict__ logp, float* __restrict__ lse_out) {
     const int64_t r = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
     if (r >= N) return;
-    float M = -INFINITY;
-    for (int64_t j = 0; j < n_segs; ++j) M = fmaxf(M, pm[j * ld + r]);
-    float lse = -INFINITY;
-    if (M != -INFINITY) {
-        float S = 0.f;
-        for (int64_t j = 0; j < n_segs; ++j) S += ps[j * ld + r] * ex2(pm[j * ld + r] - M);
-        lse = M * kLn2 + logf(S);
-    }
-    const int64_t y = targets[r];
-    logp[r] = (y >= 0 && y < V) ? zy[r] - lse : 0.f;
-    lse_out[r] = lse;
+    merge_row(pm, ps, zy, ld, n_segs, targets, r, V, logp, lse_out);
 }
 
 // The forward epilogue's fold from stored logits (small problems, whose
@@ -47,16 +60,13 @@ __global__ void lse_merge_kernel(const float* __restrict__ pm, const float* __re
 // steps at once, and one pass over the lanes replays the rescales and adds
 // of s in chunk order: the same bits as the epilogue.  Chunks wholly past V
 // change nothing there (their terms are +0) and are not visited here.
-__global__ void __launch_bounds__(256) fwd_fold_kernel(
-    const float* __restrict__ Z, int64_t ldZ, int64_t rows, int64_t V,
-    const int64_t* __restrict__ targets, float* __restrict__ part_m,
-    float* __restrict__ part_s, float* __restrict__ zy, int64_t part_ld) {
-    const int lane = threadIdx.x & 31;
-    const int64_t n_segs = (V + kSegCols - 1) / kSegCols;
-    const int64_t w = blockIdx.x * int64_t(blockDim.x / 32) + (threadIdx.x >> 5);
-    if (w >= rows * n_segs) return;
-    const int64_t seg = w / rows, row = w - seg * rows;
-    const int64_t y = targets[row];
+// The fold of one (row, segment) by one warp; writes part_m / part_s (lane 0)
+// and zy[row] (the lane whose chunk holds the target).
+__device__ __forceinline__ void fold_segment(const float* __restrict__ Z, int64_t ldZ,
+                                             int64_t V, int64_t seg, int64_t row, int64_t y,
+                                             float* __restrict__ part_m,
+                                             float* __restrict__ part_s,
+                                             float* __restrict__ zy, int64_t part_ld, int lane) {
     const int64_t seg0 = seg * kSegCols;
     const int n_chunks = static_cast<int>(min(int64_t(32), (V - seg0 + 31) / 32));
     const int64_t col0 = seg0 + 32 * lane;
@@ -111,6 +121,36 @@ __global__ void __launch_bounds__(256) fwd_fold_kernel(
         part_m[seg * part_ld + row] = rm;
         part_s[seg * part_ld + row] = s;
     }
+}
+
+__global__ void __launch_bounds__(256) fwd_fold_kernel(
+    const float* __restrict__ Z, int64_t ldZ, int64_t rows, int64_t V,
+    const int64_t* __restrict__ targets, float* __restrict__ part_m,
+    float* __restrict__ part_s, float* __restrict__ zy, int64_t part_ld) {
+    const int lane = threadIdx.x & 31;
+    const int64_t n_segs = (V + kSegCols - 1) / kSegCols;
+    const int64_t w = blockIdx.x * int64_t(blockDim.x / 32) + (threadIdx.x >> 5);
+    if (w >= rows * n_segs) return;
+    const int64_t seg = w / rows, row = w - seg * rows;
+    fold_segment(Z, ldZ, V, seg, row, targets[row], part_m, part_s, zy, part_ld, lane);
+}
+
+// Rows with few segments: a block per row, warp w folding segment w, then
+// thread 0 merges them (lse, logp) with merge_row: one launch instead of two,
+// the same bits.
+__global__ void __launch_bounds__(256) fwd_fold_merge_kernel(
+    const float* __restrict__ Z, int64_t ldZ, int64_t rows, int64_t V,
+    const int64_t* __restrict__ targets, float* __restrict__ part_m,
+    float* __restrict__ part_s, float* __restrict__ zy, int64_t part_ld,
+    float* __restrict__ logp, float* __restrict__ lse) {
+    const int lane = threadIdx.x & 31;
+    const int64_t n_segs = (V + kSegCols - 1) / kSegCols;  // the block's warp count
+    const int64_t row = blockIdx.x;
+    fold_segment(Z, ldZ, V, threadIdx.x >> 5, row, targets[row], part_m, part_s, zy, part_ld,
+                 lane);
+    __syncthreads();  // the row's partials and zy, written by the block's warps
+    if (threadIdx.x == 0)
+        merge_row(part_m, part_s, zy, part_ld, n_segs, targets, row, V, logp, lse);
 }
 
 // Targets of one vocab shard [v0, v0 + Vs) of a vocab of V entries.
@@ -516,6 +556,20 @@ cudaError_t launch_fwd_fold(const float* Z, int64_t ldZ, int64_t rows, int64_t V
     const int64_t warps = rows * ((V + kSegCols - 1) / kSegCols);
     fwd_fold_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, s>>>(
         Z, ldZ, rows, V, targets, part_m, part_s, zy, part_ld);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_fold_merge(const float* Z, int64_t ldZ, int64_t rows, int64_t V,
+                                  const int64_t* targets, float* part_m, float* part_s,
+                                  float* zy, int64_t part_ld, float* logp, float* lse,
+                                  cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    const int64_t n_segs = (V + kSegCols - 1) / kSegCols;
+    if (n_segs > kFoldMergeSegs || rows > int64_t(1) << 31) return cudaErrorInvalidValue;
+    note_launches(1);
+    fwd_fold_merge_kernel<<<static_cast<unsigned>(rows), static_cast<unsigned>(32 * n_segs), 0,
+                            s>>>(Z, ldZ, rows, V, targets, part_m, part_s, zy, part_ld, logp,
+                                 lse);
     return cudaGetLastError();
 }
 

@@ -475,6 +475,11 @@ int ll_forward_ex(const void* hidden, const void* weight, const void* bias,
     cudaError_t e = forward_gemm(hidden, weight, bias, targets, N, D, V, dtype, part_m, part_s,
                                  zy, 0, it, dev, s, Z, L.ldZ);
     if (e != cudaSuccess) return cuda_status(e);
+    if (Z && L.n_segs <= kFoldMergeSegs) {  // fold and merge in one launch
+        Phase ph("fwd_fold", s);
+        return cuda_status(
+            launch_fwd_fold_merge(Z, L.ldZ, N, V, targets, part_m, part_s, zy, N, logp, lse, s));
+    }
     if (Z) {
         Phase ph("fwd_fold", s);
         e = launch_fwd_fold(Z, L.ldZ, N, V, targets, part_m, part_s, zy, N, s);
@@ -707,12 +712,17 @@ int backward_impl(const float* grad_logp, const void* hidden, const void* weight
                 e = launch_gemm(G, dev, s);
             }
             if (e != cudaSuccess) return cuda_status(e);
-            if (ea.z_only) {
+            if (ea.z_only && L.n_segs <= kFoldMergeSegs) {  // fold and merge in one launch
                 Phase ph("fwd_fold", s);
-                e = launch_fwd_fold(Z, L.ldZ, rows, V, targets + r0, part_m, part_s, zy, L.Nc, s);
-                if (e != cudaSuccess) return cuda_status(e);
-            }
-            {
+                e = launch_fwd_fold_merge(Z, L.ldZ, rows, V, targets + r0, part_m, part_s, zy,
+                                          L.Nc, logp_out + r0, lse_out + r0, s);
+            } else {
+                if (ea.z_only) {
+                    Phase ph("fwd_fold", s);
+                    e = launch_fwd_fold(Z, L.ldZ, rows, V, targets + r0, part_m, part_s, zy,
+                                        L.Nc, s);
+                    if (e != cudaSuccess) return cuda_status(e);
+                }
                 Phase ph("lse_merge", s);
                 e = launch_lse_merge(part_m, part_s, zy, L.Nc, L.n_segs, targets + r0, rows, V,
                                      logp_out + r0, lse_out + r0, s);

@@ -211,6 +211,13 @@ cudaError_t launch_localize_targets(const int64_t* targets, int64_t N, int64_t v
 cudaError_t launch_fwd_fold(const float* Z, int64_t ldZ, int64_t rows, int64_t V,
                             const int64_t* targets, float* part_m, float* part_s, float* zy,
                             int64_t part_ld, cudaStream_t s);
+// The fold and then the merge of each row (logp, lse) in one launch, a warp
+// per row: for rows of few segments (kFoldMergeSegs or fewer).
+constexpr int64_t kFoldMergeSegs = 8;
+cudaError_t launch_fwd_fold_merge(const float* Z, int64_t ldZ, int64_t rows, int64_t V,
+                                  const int64_t* targets, float* part_m, float* part_s,
+                                  float* zy, int64_t part_ld, float* logp, float* lse,
+                                  cudaStream_t s);
 cudaError_t launch_lse_merge(const float* part_m, const float* part_s, const float* zy,
                              int64_t part_ld, int64_t n_segs, const int64_t* targets, int64_t N,
                              int64_t V, float* logp, float* lse, cudaStream_t s);
